@@ -1,0 +1,120 @@
+// chunk.cu — chunked verification with early pruning, and the status strings.
+//
+// Source: [FASER] "FASER의 세 가지 메커니즘", mechanism 2 (early token
+// pruning: verification is cut into chunks and, at every chunk boundary, the
+// tokens behind an already rejected prefix are dropped, so no cycles are
+// spent on them) and the operations notes (the verification attention kernel
+// has to run on a part of the rows).
+//
+// The whole step is enqueued on one stream with no host synchronisation: a
+// tiny kernel turns `done` into the next chunk's windows (requests that are
+// done get an empty window, which every later kernel skips), then the
+// attention and accept calls run on those windows.
+
+#include "sv_internal.cuh"
+
+namespace sv {
+namespace chk {
+
+__global__ void __launch_bounds__(256) windows_kernel(sv_batch bt, int c, int cs,
+                                                      const int32_t* done, int32_t* rb,
+                                                      int32_t* re, int32_t* dev_status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= bt.n_req) return;
+  bt.row_begin = nullptr;
+  bt.row_end = nullptr;
+  const Window w = window_of(bt, i);
+  int b = c * cs, e = min(b + cs, w.lim);
+  const bool running = (c == 0) || (done && done[i] == 0);
+  if (!w.ok) {
+    if (c == 0) flag(dev_status, SV_DEV_BAD_WINDOW);
+    b = e = 0;
+  } else if (!running || b >= e) {
+    b = e = min(b, w.rows);
+  }
+  rb[i] = b;
+  re[i] = e;
+}
+
+inline size_t windows_bytes(int R) { return align256(sizeof(int32_t) * (size_t)R) * 2; }
+
+}  // namespace chk
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" const char* sv_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "ok";
+    case SV_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case SV_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case SV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case SV_ERR_CUDA: return "CUDA launch failed";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* sv_version(void) { return "libspecverify 0.1 (sm_103a)"; }
+
+extern "C" sv_status sv_chunk_windows(const sv_batch* bt, int32_t chunk_index, int32_t chunk_size,
+                                      const int32_t* done, int32_t* row_begin, int32_t* row_end,
+                                      void* stream) {
+  if (!bt || chunk_index < 0 || chunk_size < 1 || !row_begin || !row_end || bt->n_req < 0)
+    return SV_ERR_INVALID_ARGUMENT;
+  if (chunk_index > 0 && !done) return SV_ERR_INVALID_ARGUMENT;
+  if (bt->n_req == 0) return SV_OK;
+  if (!bt->cu_rows) return SV_ERR_INVALID_ARGUMENT;
+  chk::windows_kernel<<<(bt->n_req + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      *bt, chunk_index, chunk_size, done, row_begin, row_end, nullptr);
+  SV_LAUNCH_CHECK();
+  return SV_OK;
+}
+
+extern "C" size_t sv_verify_chunked_workspace(const sv_batch* bt, const sv_paged_kv* kv,
+                                              int32_t n_q_heads, int32_t vocab) {
+  if (!bt || !kv) return 0;
+  const size_t wa = sv_tree_attend_workspace(bt, kv, n_q_heads);
+  const size_t wb = sv_accept_workspace(bt, vocab);
+  if (!wa || !wb) return 0;
+  return chk::windows_bytes(bt->n_req) + (wa > wb ? wa : wb);
+}
+
+extern "C" sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* bt, const void* q,
+                                       int32_t n_q_heads, float softmax_scale, void* out,
+                                       const float* target_logits, const float* draft_logits,
+                                       int32_t vocab, float temperature, uint64_t seed,
+                                       int32_t chunk_size, int32_t* accepted_len,
+                                       int32_t* accepted_nodes, int32_t* next_token,
+                                       uint8_t* ambiguous, int32_t* done, void* ws,
+                                       size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (!kv || !bt || chunk_size < 1 || !done) return SV_ERR_INVALID_ARGUMENT;
+  if (bt->n_req < 0 || bt->max_rows_per_req < 1) return SV_ERR_INVALID_ARGUMENT;
+  if (bt->n_req == 0 || bt->total_rows == 0) return SV_OK;
+  const size_t need = sv_verify_chunked_workspace(bt, kv, n_q_heads, vocab);
+  if (!need) return SV_ERR_INVALID_ARGUMENT;
+  if (!ws || ((uintptr_t)ws & 255)) return SV_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < need) return SV_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* rb = reinterpret_cast<int32_t*>(w);
+  int32_t* re = reinterpret_cast<int32_t*>(w + align256(sizeof(int32_t) * (size_t)bt->n_req));
+  uint8_t* inner = w + chk::windows_bytes(bt->n_req);
+  const size_t inner_bytes = ws_bytes - chk::windows_bytes(bt->n_req);
+  sv_batch b2 = *bt;
+  b2.row_begin = rb;
+  b2.row_end = re;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int n_chunks = (bt->max_rows_per_req + chunk_size - 1) / chunk_size;
+  for (int c = 0; c < n_chunks; ++c) {
+    chk::windows_kernel<<<(bt->n_req + 255) / 256, 256, 0, s>>>(*bt, c, chunk_size, done, rb, re,
+                                                                 dev_status);
+    SV_LAUNCH_CHECK();
+    sv_status st = sv_tree_attend(kv, &b2, q, n_q_heads, softmax_scale, out, inner, inner_bytes,
+                                  dev_status, stream);
+    if (st != SV_OK) return st;
+    st = sv_accept(&b2, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
+                   accepted_nodes, next_token, ambiguous, done, nullptr, inner, inner_bytes,
+                   dev_status, stream);
+    if (st != SV_OK) return st;
+  }
+  return SV_OK;
+}

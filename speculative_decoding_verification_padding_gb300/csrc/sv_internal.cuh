@@ -1,0 +1,163 @@
+// sv_internal.cuh — device helpers shared by the libspecverify kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "libspecverify.h"
+
+namespace sv {
+
+constexpr int kBlockSize = 16;   // tokens per KV page
+constexpr int kMaxRows = 128;    // rows per request (ancestor masks are 128 bits)
+constexpr int kNumSMs = 152;     // GB300
+
+// Device findings are OR-ed into the caller's status word; a null word drops
+// them (the affected request is still skipped).
+__device__ __forceinline__ void flag(int32_t* st, int bits) {
+  if (st) atomicOr(st, bits);
+}
+
+// Index of the request owning packed position x, given an exclusive prefix
+// `cu` of length n + 1 (cu[0] = 0): the largest i with cu[i] <= x.
+__device__ __forceinline__ int find_segment(const int32_t* cu, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Rows of request i handled by this call: [b, e) inside the chain end lim.
+struct Window {
+  int rows, lim, b, e;
+  bool ok;
+};
+
+__device__ __forceinline__ Window window_of(const sv_batch& bt, int i) {
+  Window w;
+  w.rows = bt.cu_rows[i + 1] - bt.cu_rows[i];
+  w.ok = w.rows >= 1 && w.rows <= bt.max_rows_per_req && w.rows <= kMaxRows;
+  w.lim = w.rows;
+  if (bt.verify_len) {
+    int L = bt.verify_len[i];
+    if (L < 0) w.ok = false;
+    if (L + 1 < w.lim) w.lim = L + 1;
+  }
+  w.b = bt.row_begin ? bt.row_begin[i] : 0;
+  w.e = bt.row_end ? bt.row_end[i] : w.lim;
+  if (w.b < 0 || w.b > w.e || w.e > w.rows) w.ok = false;
+  if (w.e > w.lim) w.e = w.lim;
+  return w;
+}
+
+// ------------------------------------------------------------- Philox ----
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of
+// (c0, c1, c2, c3) -> (hi(B*c2) ^ c1 ^ k0, lo(B*c2), hi(A*c0) ^ c3 ^ k1,
+// lo(A*c0)) with A = 0xD2511F53, B = 0xCD9E8D57 and the key advanced by the
+// Weyl increments 0x9E3779B9, 0xBB67AE85 between rounds.
+struct U4 {
+  uint32_t a, b, c, d;
+};
+
+__device__ __forceinline__ U4 philox10(U4 x, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t A = 0xD2511F53u, B = 0xCD9E8D57u;
+    uint32_t pa_lo = A * x.a, pa_hi = __umulhi(A, x.a);
+    uint32_t pb_lo = B * x.c, pb_hi = __umulhi(B, x.c);
+    U4 y;
+    y.a = pb_hi ^ x.b ^ k0;
+    y.b = pb_lo;
+    y.c = pa_hi ^ x.d ^ k1;
+    y.d = pa_lo;
+    x = y;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return x;
+}
+
+// Accept uniform of draft j of request i: counter (j, i, 0, 0), word 0,
+// top 24 bits.
+__device__ __forceinline__ float accept_u(uint64_t seed, int i, int j) {
+  U4 c{(uint32_t)j, (uint32_t)i, 0u, 0u};
+  U4 o = philox10(c, (uint32_t)seed, (uint32_t)(seed >> 32));
+  return (float)(o.a >> 8) * 5.9604644775390625e-08f;  // 2^-24
+}
+
+// Race uniforms for vocabulary entries 4k .. 4k+3 of the draw at position
+// pos: counter (k, i, 1, pos), ((bits >> 9) + 0.5) * 2^-23 in (0, 1).
+__device__ __forceinline__ U4 race_bits(uint64_t seed, int i, int pos, int k) {
+  U4 c{(uint32_t)k, (uint32_t)i, 1u, (uint32_t)pos};
+  return philox10(c, (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+__device__ __forceinline__ float race_u(uint32_t bits) {
+  return ((float)(bits >> 9) + 0.5f) * 1.1920928955078125e-07f;  // 2^-23
+}
+
+// ---------------------------------------------------------- warp utils ----
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// --------------------------------------------------- tensor-core / copies --
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 zero-fills.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------ host side --
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace sv
+
+#define SV_LAUNCH_CHECK()                                  \
+  do {                                                     \
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA; \
+  } while (0)

@@ -1,0 +1,134 @@
+"""One verification step on the GPU through the C ABI.
+
+``DeviceStep`` uploads a workload (``workloads.Workload``) once, allocates the
+outputs and workspaces with torch, and enqueues the library calls of a step:
+
+  onepass   sv_tree_attend -> sv_accept -> sv_commit_kv
+  chunked   sv_verify_chunked (windows -> attend -> accept per chunk, early
+            pruning) -> sv_commit_kv
+  budget    sv_select_budget -> sv_tree_attend -> sv_accept -> sv_commit_kv,
+            with the selected verify_len feeding the batch
+
+Nothing here computes any part of the step; it only moves memory and calls.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import api
+from .workloads import Workload
+
+
+class DeviceStep:
+    def __init__(self, w: Workload, device="cuda", mode: str | None = None, chunk: int | None = None):
+        self.w = w
+        self.device = device
+        cfg = w.cfg
+        self.mode = mode or ("budget" if cfg.budget else "chunked" if cfg.chunk else "onepass")
+        self.chunk = chunk or cfg.chunk or 2
+        self.T = float(cfg.temperature)
+        self.Hq = cfg.n_q_heads
+        self.V = w.target_logits.shape[1]
+        self.scale = w.softmax_scale
+        dev = device
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+        bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16)).view(torch.bfloat16).to(dev)
+        f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+
+        self.batch = api.Batch(i32(w.cu_rows), i32(w.parent), i32(w.tokens), w.max_rows)
+        self.kv = api.PagedKV(bf16(w.k_cache), bf16(w.v_cache), i32(w.block_tables), i32(w.cache_lens))
+        self.pool = api.BlockPool(i32(w.free_list), i32(np.array([w.free_count])))
+        # pristine copies of the mutable cache state, restored before each step
+        self._tables0 = self.kv.block_tables.clone()
+        self._lens0 = self.kv.cache_lens.clone()
+        self._free0 = self.pool.free_list.clone()
+        self._fc0 = self.pool.free_count.clone()
+        self.q = bf16(w.q)
+        self.target = f32(w.target_logits)
+        self.draft = f32(w.draft_logits) if self.T > 0 else None
+        R, rows, maxr = w.n_req, w.total_rows, w.max_rows
+        self.out = torch.zeros((rows, self.Hq, cfg.head_dim), dtype=torch.bfloat16, device=dev)
+        self.accepted_len = torch.zeros(R, dtype=torch.int32, device=dev)
+        self.accepted_nodes = torch.zeros((R, maxr), dtype=torch.int32, device=dev)
+        self.next_token = torch.zeros(R, dtype=torch.int32, device=dev)
+        self.ambiguous = torch.zeros(R, dtype=torch.uint8, device=dev)
+        self.done = torch.zeros(R, dtype=torch.int32, device=dev)
+        self.row_stats = None
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if cfg.budget:
+            self.cond = f32(w.cond_survival)
+            self.gamma = i32(w.gamma)
+            self.sps = f32(w.sps)
+            self.verify_len = torch.zeros(R, dtype=torch.int32, device=dev)
+            self.best_B = torch.zeros(1, dtype=torch.int32, device=dev)
+            self.best_theta = torch.zeros(1, dtype=torch.float64, device=dev)
+            self.batch_sel = api.Batch(self.batch.cu_rows, self.batch.parent, self.batch.tokens,
+                                       maxr, verify_len=self.verify_len)
+        ws = max(api.sv_tree_attend_workspace(self.batch, self.kv, self.Hq),
+                 api.sv_accept_workspace(self.batch, self.V),
+                 api.sv_verify_chunked_workspace(self.batch, self.kv, self.Hq, self.V))
+        self.ws = api.workspace(ws, dev)
+
+    # ---------------------------------------------------------------------
+    def restore_cache_state(self):
+        self.kv.block_tables.copy_(self._tables0)
+        self.kv.cache_lens.copy_(self._lens0)
+        self.pool.free_list.copy_(self._free0)
+        self.pool.free_count.copy_(self._fc0)
+
+    def attend(self, batch=None):
+        api.sv_tree_attend(self.kv, batch or self.batch, self.q, self.Hq, self.scale, self.out,
+                           self.ws, self.dev_status)
+
+    def accept(self, batch=None, row_stats=None):
+        api.sv_accept(batch or self.batch, self.target, self.draft, self.V, self.T, self.w.seed,
+                      self.accepted_len, self.accepted_nodes, self.next_token, self.ambiguous,
+                      self.done, row_stats, self.ws, self.dev_status)
+
+    def chunked(self):
+        api.sv_verify_chunked(self.kv, self.batch, self.q, self.Hq, self.scale, self.out,
+                              self.target, self.draft, self.V, self.T, self.w.seed, self.chunk,
+                              self.accepted_len, self.accepted_nodes, self.next_token,
+                              self.ambiguous, self.done, self.ws, self.dev_status)
+
+    def select(self):
+        api.sv_select_budget(self.cond, self.gamma, self.sps, self.verify_len, self.best_B,
+                             self.best_theta, None, self.dev_status)
+
+    def commit(self, batch=None):
+        api.sv_commit_kv(self.kv, batch or self.batch, self.accepted_len, self.accepted_nodes,
+                         self.pool, self.dev_status)
+
+    def run(self, commit: bool = True, restore: bool = True):
+        """Enqueue one whole step of this workload's mode on the current stream."""
+        if restore:
+            self.restore_cache_state()
+        if self.mode == "onepass":
+            self.attend()
+            self.accept()
+            b = self.batch
+        elif self.mode == "chunked":
+            self.chunked()
+            b = self.batch
+        elif self.mode == "budget":
+            self.select()
+            self.attend(self.batch_sel)
+            self.accept(self.batch_sel)
+            b = self.batch_sel
+        else:
+            raise ValueError(self.mode)
+        if commit:
+            self.commit(b)
+
+    def results(self):
+        torch.cuda.synchronize()
+        return {
+            "accepted_len": self.accepted_len.cpu().numpy(),
+            "accepted_nodes": self.accepted_nodes.cpu().numpy(),
+            "next_token": self.next_token.cpu().numpy(),
+            "ambiguous": self.ambiguous.cpu().numpy(),
+            "done": self.done.cpu().numpy(),
+            "dev_status": int(self.dev_status.item()),
+        }

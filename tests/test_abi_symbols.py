@@ -1,0 +1,65 @@
+"""The C-ABI library loads and exports every function include/libspecverify.h
+declares, and the ctypes binding covers the same set (no GPU needed)."""
+
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "libspecverify.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(sv_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_padding_gb300 import build, _native
+    build.build()
+    return _native.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("sv_tree_attend", "sv_accept", "sv_commit_kv", "sv_select_budget",
+              "sv_verify_chunked", "sv_chunk_windows"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_the_header():
+    from speculative_decoding_verification_padding_gb300 import _native
+    assert sorted(_native.PROTOTYPES) == _declared()
+
+
+def test_host_side_validation_without_gpu(lib):
+    # Argument errors are returned before anything is enqueued, so they can
+    # be exercised without a device.
+    from speculative_decoding_verification_padding_gb300 import _native as N
+    assert lib.sv_status_string(N.SV_ERR_WORKSPACE_TOO_SMALL) == b"workspace too small"
+    assert lib.sv_tree_attend(None, None, None, 8, 0.1, None, None, 0, None, None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_select_budget(0, 4, None, None, None, 10, None, None, None, None, 0, None, None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_select_budget(100, 100, 1, None, 1, 200, 1, 1, 1, None, 0, None, None) == N.SV_ERR_UNSUPPORTED_SHAPE
+    import ctypes
+    b = N.SvBatch(1, 2, 200, 1, 1, 1, None, None, None)
+    assert lib.sv_accept(ctypes.byref(b), 1, None, 16, 0.0, 0, 1, 1, 1, 1, None, None, 1, 1 << 20,
+                         None, None) == N.SV_ERR_UNSUPPORTED_SHAPE
+    b = N.SvBatch(1, 2, 2, 1, 1, 1, None, None, None)
+    assert lib.sv_accept(ctypes.byref(b), 1, None, 16, 1.0, 0, 1, 1, 1, 1, None, None, 256, 1 << 20,
+                         None, None) == N.SV_ERR_INVALID_ARGUMENT  # T > 0 needs draft logits
+    kv = N.SvPagedKV(256, 256, 10, 16, 2, 96, 1, 4, 1)
+    assert lib.sv_tree_attend_workspace(ctypes.byref(b), ctypes.byref(kv), 8) == 0  # head_dim 96
+    kv = N.SvPagedKV(256, 256, 10, 16, 2, 64, 1, 4, 1)
+    need = lib.sv_tree_attend_workspace(ctypes.byref(b), ctypes.byref(kv), 8)
+    assert need > 0
+    assert lib.sv_tree_attend(ctypes.byref(kv), ctypes.byref(b), 256, 8, 0.125, 256, 256, need - 1,
+                              None, None) == N.SV_ERR_WORKSPACE_TOO_SMALL

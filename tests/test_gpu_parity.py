@@ -1,0 +1,432 @@
+"""GPU parity: every call of libspecverify, through the C ABI, against the
+CPU oracle on the same seeded inputs.
+
+Bars: token ids, accepted lengths and paths, block tables, free lists,
+cache lengths and budget selections bit-exact (sampling decisions the oracle
+or the device flags as ambiguous, |u - min(1, p/q)| < 1e-6 or a race too
+close to call in fp32, are reported and excluded); attention within 1e-2
+absolute and 1e-2 relative of the fp64 oracle (bf16 output, fp32
+accumulation); probabilities within 1e-5 absolute.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verification_padding_gb300 import api, build
+from speculative_decoding_verification_padding_gb300 import workloads as wl
+from speculative_decoding_verification_padding_gb300.step import DeviceStep
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+PROB_ATOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    oracle.build()
+
+
+def _bf16_to_f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _check_attention(gpu_out, ref64, rows):
+    g = _bf16_to_f64(gpu_out)[rows]
+    r = ref64[rows]
+    assert np.isfinite(g).all()
+    np.testing.assert_allclose(g, r, atol=ATOL, rtol=RTOL)
+
+
+def _compare_accept(res, st, w, label=""):
+    """Bit-exact comparison of the accept state, ambiguous requests excluded."""
+    amb = (st.ambiguous != 0) | (res["ambiguous"] != 0)
+    n_amb = int(amb.sum())
+    ok = ~amb
+    assert np.array_equal(res["accepted_len"][ok], st.accepted_len[ok]), label
+    assert np.array_equal(res["next_token"][ok], st.next_token[ok]), label
+    assert np.array_equal(res["done"][ok], st.done[ok]), label
+    for i in np.nonzero(ok)[0]:
+        a = st.accepted_len[i]
+        assert np.array_equal(res["accepted_nodes"][i, : a + 1], st.accepted_nodes[i, : a + 1]), (label, i)
+        assert (res["accepted_nodes"][i, a + 1:] == -1).all()
+    assert n_amb <= max(1, len(amb) // 100), f"{label}: {n_amb} ambiguous decisions"
+    return n_amb
+
+
+# ---------------------------------------------------------------- attention --
+
+ATTN_CASES = {
+    "tiny": dict(),
+    "chain8b": dict(),
+    "tree70b": dict(),
+    "batch64_small": dict(name="batch64", n_req=64, ctx_scale=0.05, vocab=256),
+    "batch256_small": dict(name="batch256", n_req=96, ctx_scale=0.02, vocab=256),
+    "ragged_ctx": dict(name="batch64", n_req=9, ctx_scale=0.0007, vocab=64),  # contexts of a few tokens
+}
+
+
+def _make(case, **extra):
+    kw = dict(ATTN_CASES[case]) if case in ATTN_CASES else {}
+    name = kw.pop("name", case)
+    kw.setdefault("vocab", 1024 if name != "tiny" else None)
+    if kw["vocab"] is None:
+        kw.pop("vocab")
+    kw.update(extra)
+    return wl.make_workload(wl.config(name), **kw)
+
+
+@pytest.mark.parametrize("case", list(ATTN_CASES))
+def test_tree_attend_matches_oracle(case):
+    w = _make(case)
+    s = DeviceStep(w, mode="onepass")
+    s.out.fill_(float("nan"))
+    s.attend()
+    torch.cuda.synchronize()
+    assert s.dev_status.item() == 0
+    err, _, ref64 = oracle.tree_attend(w.batch(), w.kv(), w.q, w.cfg.n_q_heads, w.softmax_scale)
+    assert err == 0
+    _check_attention(s.out, ref64, np.arange(w.total_rows))
+
+
+def test_tree_attend_windows_touch_only_window_rows():
+    w = _make("batch64_small")
+    s = DeviceStep(w, mode="onepass")
+    rows = np.diff(w.cu_rows)
+    rng = np.random.default_rng(1)
+    rb = np.array([rng.integers(0, r) for r in rows], dtype=np.int32)
+    re = np.array([rng.integers(b, r + 1) for b, r in zip(rb, rows)], dtype=np.int32)
+    b = api.Batch(s.batch.cu_rows, s.batch.parent, s.batch.tokens, w.max_rows,
+                  row_begin=torch.from_numpy(rb).cuda(), row_end=torch.from_numpy(re).cuda())
+    s.out.fill_(float("nan"))
+    s.attend(b)
+    torch.cuda.synchronize()
+    err, _, ref64 = oracle.tree_attend(w.batch(), w.kv(), w.q, w.cfg.n_q_heads, w.softmax_scale,
+                                       row_begin=rb, row_end=re)
+    inside = np.zeros(w.total_rows, bool)
+    for i in range(w.n_req):
+        inside[w.cu_rows[i] + rb[i]: w.cu_rows[i] + re[i]] = True
+    _check_attention(s.out, ref64, np.nonzero(inside)[0])
+    assert torch.isnan(s.out[torch.from_numpy(~inside).cuda()].float()).all()
+
+
+# ------------------------------------------------------------------- accept --
+
+ACCEPT_CASES = [
+    ("tiny", 0.0, None), ("tiny", 1.0, None),
+    ("chain8b", 1.0, 0.3), ("chain8b", 1.0, 1.0), ("chain8b", 1.0, 3.0),
+    ("tree70b", 0.0, 1.0), ("tree70b", 0.0, 0.2),
+    ("batch64", 0.7, 1.0), ("batch64", 0.0, 1.0),
+    ("batch256", 1.0, 1.0),
+]
+
+
+@pytest.mark.parametrize("name,T,sigma", ACCEPT_CASES)
+def test_accept_matches_oracle(name, T, sigma):
+    kw = dict(temperature=T, ctx_scale=0.01)
+    if sigma is not None:
+        kw["draft_sigma"] = sigma
+    w = wl.make_workload(wl.config(name), **kw)
+    s = DeviceStep(w, mode="onepass")
+    rs = torch.full((w.total_rows, 4), float("nan"), dtype=torch.float32, device="cuda")
+    s.accept(row_stats=rs)
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits if T > 0 else None, T, w.seed)
+    assert err == 0
+    _compare_accept(res, st, w, f"{name} T={T} sigma={sigma}")
+    g = rs.cpu().numpy().astype(np.float64)
+    o = st.row_stats
+    if T > 0:
+        for i in range(w.n_req):
+            if st.ambiguous[i] or res["ambiguous"][i]:
+                continue
+            cu, a = w.cu_rows[i], st.accepted_len[i]
+            rows = w.cu_rows[i + 1] - cu
+            np.testing.assert_allclose(g[cu: cu + rows, 0], o[cu: cu + rows, 0], rtol=2e-6, atol=2e-5)
+            dec = np.arange(cu + 1, cu + min(a + 2, rows))  # decided children
+            np.testing.assert_allclose(g[dec, 2], o[dec, 2], atol=PROB_ATOL, rtol=0)
+            np.testing.assert_allclose(g[dec, 3], o[dec, 3], atol=PROB_ATOL, rtol=0)
+    else:
+        assert np.array_equal(g[:, 1], o[:, 1])  # argmax
+        assert np.array_equal(g[:, 0], o[:, 0])  # max logit
+
+
+def test_accept_verify_len_truncation():
+    w = wl.make_workload(wl.config("batch256"), n_req=64, ctx_scale=0.01, vocab=4096, draft_sigma=0.3)
+    vl = np.random.default_rng(2).integers(0, 5, w.n_req).astype(np.int32)
+    s = DeviceStep(w, mode="onepass")
+    b = api.Batch(s.batch.cu_rows, s.batch.parent, s.batch.tokens, w.max_rows,
+                  verify_len=torch.from_numpy(vl).cuda())
+    s.accept(b)
+    res = s.results()
+    err, st = oracle.accept(w.batch(verify_len=vl), w.target_logits, w.draft_logits, 1.0, w.seed)
+    assert err == 0
+    _compare_accept(res, st, w, "verify_len")
+
+
+# ------------------------------------------------------------------- commit --
+
+@pytest.mark.parametrize("name,T,kw", [
+    ("tree70b", 0.0, dict(ctx_scale=0.01, vocab=512, draft_sigma=0.05)),
+    ("batch64", 0.7, dict(ctx_scale=0.01, vocab=512, draft_sigma=0.5)),
+    ("tiny", 1.0, dict(vocab=64)),
+])
+def test_commit_matches_oracle(name, T, kw):
+    w = wl.make_workload(wl.config(name), temperature=T, **kw)
+    err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits if T > 0 else None, T, w.seed)
+    assert err == 0
+    if name == "tree70b":
+        assert st.accepted_len.max() >= 2  # a path that moves slots
+    s = DeviceStep(w, mode="onepass")
+    s.accepted_len.copy_(torch.from_numpy(st.accepted_len))
+    nodes = np.where(st.accepted_nodes < 0, -1, st.accepted_nodes).astype(np.int32)
+    s.accepted_nodes.copy_(torch.from_numpy(nodes))
+    s.commit()
+    torch.cuda.synchronize()
+    assert s.dev_status.item() == 0
+    kv = w.kv_copy()
+    fl = w.free_list.copy()
+    fc = np.array([w.free_count], dtype=np.int32)
+    assert oracle.commit_kv(w.batch(), kv, st.accepted_len, nodes, fl, fc) == 0
+    assert np.array_equal(s.kv.block_tables.cpu().numpy(), kv["block_tables"])
+    assert np.array_equal(s.kv.cache_lens.cpu().numpy(), kv["cache_lens"])
+    assert s.pool.free_count.item() == fc[0]
+    assert np.array_equal(s.pool.free_list.cpu().numpy()[: fc[0]], fl[: fc[0]])
+    assert np.array_equal(s.kv.k_cache.view(torch.int16).cpu().numpy().view(np.uint16), kv["k_cache"])
+    assert np.array_equal(s.kv.v_cache.view(torch.int16).cpu().numpy().view(np.uint16), kv["v_cache"])
+
+
+def test_commit_pool_overflow_is_flagged_not_faulted():
+    w = wl.make_workload(wl.config("batch64"), n_req=16, ctx_scale=0.01, vocab=256,
+                         temperature=0.0, draft_sigma=3.0)
+    err, st = oracle.accept(w.batch(), w.target_logits, None, 0.0, w.seed)
+    nodes = np.where(st.accepted_nodes < 0, -1, st.accepted_nodes).astype(np.int32)
+    # the oracle, given the same full free list, must also overflow
+    fl = w.free_list[: w.free_count].copy()
+    fc = np.array([w.free_count], dtype=np.int32)
+    assert oracle.commit_kv(w.batch(), w.kv_copy(), st.accepted_len, nodes, fl, fc) & oracle.ORC_POOL_OVERFLOW
+    s = DeviceStep(w, mode="onepass")
+    s.accepted_len.copy_(torch.from_numpy(st.accepted_len))
+    s.accepted_nodes.copy_(torch.from_numpy(nodes))
+    pool = api.BlockPool(s.pool.free_list[: w.free_count].clone(), s.pool.free_count)
+    api.sv_commit_kv(s.kv, s.batch, s.accepted_len, s.accepted_nodes, pool, s.dev_status)
+    torch.cuda.synchronize()
+    assert s.dev_status.item() & api.N.SV_DEV_POOL_OVERFLOW
+    assert pool.free_count.item() == w.free_count
+
+
+# ------------------------------------------------------------------- budget --
+
+def _budget_gpu(c, gamma, sps):
+    R = c.shape[0]
+    vl = torch.zeros(R, dtype=torch.int32, device="cuda")
+    bB = torch.zeros(1, dtype=torch.int32, device="cuda")
+    th = torch.zeros(1, dtype=torch.float64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.sv_select_budget(torch.from_numpy(c).cuda(), None if gamma is None else torch.from_numpy(gamma).cuda(),
+                         torch.from_numpy(sps).cuda(), vl, bB, th, None, st)
+    torch.cuda.synchronize()
+    return vl.cpu().numpy(), int(bB.item()), float(th.item()), int(st.item())
+
+
+def test_budget_full_size_matches_oracle():
+    w = wl.make_workload(wl.config("batch256"), vocab=64, ctx_scale=0.001)
+    vl, bB, th, st = _budget_gpu(w.cond_survival, w.gamma, w.sps)
+    err, vl_o, bB_o, th_o = oracle.select_budget(w.cond_survival, w.gamma, w.sps)
+    assert st == 0 and err == 0
+    assert np.array_equal(vl, vl_o) and bB == bB_o and th == th_o
+
+
+@pytest.mark.parametrize("trial", range(40))
+def test_budget_random_matches_oracle(trial):
+    rng = np.random.default_rng(1000 + trial)
+    R = int(rng.integers(1, 400))
+    gmax = int(rng.integers(1, 9))
+    gamma = rng.integers(0, gmax + 1, R).astype(np.int32)
+    c = rng.beta(4, 2, size=(R, gmax)).astype(np.float32)
+    if trial % 4 == 0:
+        c = np.round(c * 4) / 4  # many equal survivals: tie order matters
+        c = c.astype(np.float32)
+    b_max = R + int(rng.integers(0, R * gmax + 2))
+    B = np.arange(b_max + 1, dtype=np.float64)
+    sps = (1000.0 / (1.0 + B / rng.uniform(16, 2048))).astype(np.float32)
+    vl, bB, th, st = _budget_gpu(c, gamma, sps)
+    err, vl_o, bB_o, th_o = oracle.select_budget(c, gamma, sps)
+    assert st == 0 and err == 0
+    assert np.array_equal(vl, vl_o) and bB == bB_o and th == th_o
+
+
+# ------------------------------------------------------- chunked / budget step --
+
+@pytest.mark.parametrize("T", [0.7, 0.0])
+def test_chunked_step_matches_oracle(T):
+    w = wl.make_workload(wl.config("batch64"), ctx_scale=0.05, vocab=2048, temperature=T,
+                         draft_sigma=0.7)
+    s = DeviceStep(w, mode="chunked")
+    s.out.fill_(float("nan"))
+    s.chunked()
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st, _, ref64, attended = oracle.verify_chunked(
+        w.batch(), w.kv(), w.q, w.cfg.n_q_heads, w.softmax_scale, w.target_logits,
+        w.draft_logits if T > 0 else None, T, w.seed, chunk=2)
+    assert err == 0
+    _compare_accept(res, st, w, f"chunked T={T}")
+    att = ~np.isnan(ref64[:, 0, 0])
+    assert int(att.sum()) == attended < w.total_rows  # pruning happened
+    _check_attention(s.out, ref64, np.nonzero(att)[0])
+    assert torch.isnan(s.out[torch.from_numpy(~att).cuda()].float()).all()
+
+
+def test_budget_step_matches_oracle():
+    w = wl.make_workload(wl.config("batch256"), ctx_scale=0.02, vocab=2048)
+    s = DeviceStep(w, mode="budget")
+    s.out.fill_(float("nan"))
+    s.run(commit=False)
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, vl, bB, th = oracle.select_budget(w.cond_survival, w.gamma, w.sps)
+    assert np.array_equal(s.verify_len.cpu().numpy(), vl) and s.best_B.item() == bB
+    err, st = oracle.accept(w.batch(verify_len=vl), w.target_logits, w.draft_logits, 1.0, w.seed)
+    assert err == 0
+    _compare_accept(res, st, w, "budget step")
+    err, _, ref64 = oracle.tree_attend(w.batch(verify_len=vl), w.kv(), w.q, w.cfg.n_q_heads,
+                                       w.softmax_scale)
+    att = ~np.isnan(ref64[:, 0, 0])
+    assert att.sum() == w.n_req + vl.sum()
+    _check_attention(s.out, ref64, np.nonzero(att)[0])
+
+
+# ------------------------------------------------------------- losslessness --
+
+@pytest.mark.parametrize("gamma,T", [(3, 1.0), (1, 0.7)])
+def test_gpu_speculative_sampling_chi2(gamma, T):
+    from scipy import stats
+    N, V = 1_000_000, 16
+    rows = gamma + 1
+    rng = np.random.default_rng(77 + gamma)
+    lt = (rng.standard_normal((rows, V)) * 2.0).astype(np.float32)
+    ld = (lt + rng.standard_normal((rows, V))).astype(np.float32)
+
+    def sm(l):
+        x = (l / np.float32(T)).astype(np.float64)
+        e = np.exp(x - x.max())
+        return e / e.sum()
+    p0, q0 = sm(lt[0]), sm(ld[0])
+    tokens = np.zeros((N, rows), dtype=np.int32)
+    for j in range(1, rows):
+        tokens[:, j] = rng.choice(V, size=N, p=sm(ld[j - 1]))
+    cu = (np.arange(N + 1) * rows).astype(np.int32)
+    parent = np.tile(np.arange(-1, gamma, dtype=np.int32), N)
+    dev = "cuda"
+    b = api.Batch(torch.from_numpy(cu).to(dev), torch.from_numpy(parent).to(dev),
+                  torch.from_numpy(tokens.ravel()).to(dev), rows)
+    tgt = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(lt, (N, rows, V)).reshape(-1, V))).to(dev)
+    drf = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(ld, (N, rows, V)).reshape(-1, V))).to(dev)
+    al = torch.zeros(N, dtype=torch.int32, device=dev)
+    an = torch.zeros((N, rows), dtype=torch.int32, device=dev)
+    nt = torch.zeros(N, dtype=torch.int32, device=dev)
+    amb = torch.zeros(N, dtype=torch.uint8, device=dev)
+    ws = api.workspace(api.sv_accept_workspace(b, V))
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    api.sv_accept(b, tgt, drf, V, T, 4242, al, an, nt, amb, None, None, ws, st)
+    a, nxt = al.cpu().numpy(), nt.cpu().numpy()
+    assert st.item() == 0 and (nxt >= 0).all()
+    first = np.where(a >= 1, tokens[:, 1], nxt)
+    obs = np.bincount(first, minlength=V)
+    chi = ((obs - p0 * N) ** 2 / (p0 * N)).sum()
+    assert chi < stats.chi2.ppf(0.999, V - 1), chi
+    acc = np.minimum(p0, q0).sum()
+    z = ((a >= 1).mean() - acc) / np.sqrt(acc * (1 - acc) / N)
+    assert abs(z) < 4
+    # the first 20000 requests decide exactly as the oracle does
+    n = 20000
+    bo = {"cu_rows": cu[: n + 1], "parent": parent[: n * rows], "tokens": tokens[:n].ravel(),
+          "max_rows": rows}
+    err, so = oracle.accept(bo, np.broadcast_to(lt, (n, rows, V)).reshape(-1, V),
+                            np.broadcast_to(ld, (n, rows, V)).reshape(-1, V), T, 4242)
+    ok = (so.ambiguous == 0) & (amb.cpu().numpy()[:n] == 0)
+    assert np.array_equal(a[:n][ok], so.accepted_len[ok])
+    assert np.array_equal(nxt[:n][ok], so.next_token[ok])
+
+
+# ---------------------------------------------------------- device findings --
+
+def test_bad_block_id_and_bad_parent_are_flagged():
+    w = _make("tiny", vocab=64)
+    s = DeviceStep(w, mode="onepass")
+    tbl = s.kv.block_tables.clone()
+    s.kv.block_tables[0, 3] = w.k_cache.shape[0] + 5
+    s.attend()
+    torch.cuda.synchronize()
+    assert s.dev_status.item() & api.N.SV_DEV_BAD_BLOCK_ID
+    s.kv.block_tables.copy_(tbl)
+    s.dev_status.zero_()
+    par = s.batch.parent.clone()
+    par[2] = 5
+    b = api.Batch(s.batch.cu_rows, par, s.batch.tokens, w.max_rows)
+    s.attend(b)
+    s.accept(b)
+    torch.cuda.synchronize()
+    assert s.dev_status.item() & api.N.SV_DEV_BAD_PARENT
+
+
+def test_tree_with_temperature_is_flagged_unsupported():
+    w = wl.make_workload(wl.config("tree70b"), ctx_scale=0.01, vocab=256, temperature=1.0)
+    s = DeviceStep(w, mode="onepass")
+    s.accept()
+    torch.cuda.synchronize()
+    assert s.dev_status.item() & api.N.SV_DEV_UNSUPPORTED
+
+
+def test_small_workspace_is_refused_before_launch():
+    w = _make("tiny", vocab=64)
+    s = DeviceStep(w, mode="onepass")
+    need = api.sv_tree_attend_workspace(s.batch, s.kv, w.cfg.n_q_heads)
+    with pytest.raises(api.N.SpecVerifyError, match="workspace too small"):
+        api.sv_tree_attend(s.kv, s.batch, s.q, w.cfg.n_q_heads, w.softmax_scale, s.out,
+                           s.ws[: need - 1], s.dev_status)
+
+
+# ------------------------------------------------ full size, bench launch shape --
+
+@pytest.fixture(scope="module")
+def batch64_full():
+    return wl.make_workload(wl.config("batch64"))
+
+
+def test_batch64_full_size_chunked_step(batch64_full):
+    """The bench workload at full size, run as the bench runs it (chunked,
+    with commit): every accept output against the oracle, attention on a
+    sample of requests."""
+    w = batch64_full
+    s = DeviceStep(w)
+    assert s.mode == "chunked"
+    s.out.fill_(float("nan"))
+    s.run(commit=False)
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits, w.cfg.temperature, w.seed)
+    assert err == 0
+    _compare_accept(res, st, w, "batch64 full")
+    sample = np.array([0, 7, 21, 33, 50, 63])
+    rb = np.zeros(w.n_req, np.int32)
+    re = np.zeros(w.n_req, np.int32)
+    rows = np.diff(w.cu_rows)
+    for i in sample:
+        re[i] = min(rows[i], 2 * (st.accepted_len[i] // 2 + 1))  # rows the chunks reached
+    err, _, ref64 = oracle.tree_attend(w.batch(), w.kv(), w.q, w.cfg.n_q_heads, w.softmax_scale,
+                                       row_begin=rb, row_end=re)
+    att = ~np.isnan(ref64[:, 0, 0])
+    _check_attention(s.out, ref64, np.nonzero(att)[0])
+    # and the commit that follows
+    s.commit()
+    torch.cuda.synchronize()
+    assert s.dev_status.item() == 0
+    new_lens = s.kv.cache_lens.cpu().numpy()
+    assert np.array_equal(new_lens, w.cache_lens + 1 + res["accepted_len"])
