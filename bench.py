@@ -108,7 +108,7 @@ class ClockSampler:
 def chunk_schedule(w, accepted_len, chunk):
     """Windows each chunk launch processed, from the step's accepted lengths
     (a request runs through chunk accepted_len // chunk)."""
-    rows = np.diff(w.cu_rows)
+    rows = [int(r) for r in np.diff(w.cu_rows)]
     n_chunks = math.ceil(w.max_rows / chunk)
     sched = []
     for c in range(n_chunks):
@@ -116,7 +116,7 @@ def chunk_schedule(w, accepted_len, chunk):
         for i in range(w.n_req):
             b = c * chunk
             e = min(b + chunk, rows[i])
-            if b < e and c <= accepted_len[i] // chunk:
+            if b < e and c <= int(accepted_len[i]) // chunk:
                 act.append((i, b, e))
         sched.append(act)
     return sched
@@ -130,14 +130,14 @@ def attend_bytes(w, windows):
 
 
 def accept_bytes(w, windows, accepted_len, T):
-    V = w.target_logits.shape[1]
-    rows = np.diff(w.cu_rows)
+    V = int(w.target_logits.shape[1])
+    rows = [int(r) for r in np.diff(w.cu_rows)]
     tot = 0
     for i, b, e in windows:
         tot += (e - b) * V * 4                               # target rows
         if T > 0:
             tot += (min(e, rows[i] - 1) - b) * V * 4          # draft rows with a child
-            a = accepted_len[i]
+            a = int(accepted_len[i])
             if b <= a < e:                                    # decided in this window
                 tot += (V * 4 if a == rows[i] - 1 else 2 * V * 4)
     return tot
