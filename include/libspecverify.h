@@ -206,6 +206,35 @@ sv_status sv_accept(const sv_batch* batch, const float* target_logits, const flo
                     int32_t* done, float* row_stats, void* ws, size_t ws_bytes,
                     int32_t* dev_status, void* stream);
 
+/* ------------------------------------------------ accept without workspace --
+ * No counterpart in the paper: a convenience for callers that cannot
+ * allocate device memory -- for example a plugin inside another runtime that
+ * is handed only its input and output buffers, or a serving engine that has
+ * already reserved nearly all HBM for its KV-cache pool, or a latency-critical
+ * loop that cannot afford cudaMalloc's implicit device synchronisation.
+ * sv_accept_static computes exactly what sv_accept computes (same arguments,
+ * same outputs) but takes its scratch from a device array of
+ * SV_ACCEPT_STATIC_SCRATCH_BYTES inside the library instead of a caller
+ * workspace; it calls no allocator.  That array exists once per GPU that
+ * loads the library and is held until the process exits.
+ * Limits and behaviour:
+ *   - Problems whose sv_accept_workspace() exceeds
+ *     SV_ACCEPT_STATIC_SCRATCH_BYTES (4 MiB; any batch of up to 50,000
+ *     packed rows fits) are refused with SV_ERR_WORKSPACE_TOO_SMALL before
+ *     anything is enqueued; use sv_accept with a workspace beyond that.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture begins.
+ *   - Every call shares the one array: calls whose work overlaps on the GPU
+ *     (for instance on two streams) race on it and must be ordered by the
+ *     caller. */
+#define SV_ACCEPT_STATIC_SCRATCH_BYTES (4u << 20)
+sv_status sv_accept_static(const sv_batch* batch, const float* target_logits,
+                           const float* draft_logits, int32_t vocab, float temperature,
+                           uint64_t seed, int32_t* accepted_len, int32_t* accepted_nodes,
+                           int32_t* next_token, uint8_t* ambiguous, int32_t* done,
+                           float* row_stats, int32_t* dev_status, void* stream);
+
 /* ---------------------------------------------------------------- commit --
  * [SwiftSpec] mechanism 2: keep only the accepted path's KV, free rejected
  * paths.  For request i with a = accepted_len[i], path = accepted_nodes[i]:

@@ -33,6 +33,8 @@ SV_DEV_BAD_TOKEN = 32
 SV_DEV_UNSUPPORTED = 64
 SV_DEV_BAD_LENGTH = 128
 
+SV_ACCEPT_STATIC_SCRATCH_BYTES = 4 << 20
+
 
 class SvPagedKV(ctypes.Structure):
     _fields_ = [("k_cache", P), ("v_cache", P), ("num_blocks", I32), ("block_size", I32),
@@ -58,6 +60,7 @@ PROTOTYPES = {
     "sv_tree_attend": (ctypes.c_int, [P, P, P, I32, F32, P, P, SZ, P, P]),
     "sv_accept_workspace": (SZ, [P, I32]),
     "sv_accept": (ctypes.c_int, [P, P, P, I32, F32, U64, P, P, P, P, P, P, P, SZ, P, P]),
+    "sv_accept_static": (ctypes.c_int, [P, P, P, I32, F32, U64, P, P, P, P, P, P, P, P]),
     "sv_commit_kv": (ctypes.c_int, [P, P, P, P, P, P, P]),
     "sv_select_budget_workspace": (SZ, [I32, I32]),
     "sv_select_budget": (ctypes.c_int, [I32, I32, P, P, P, I32, P, P, P, P, SZ, P, P]),

@@ -142,6 +142,27 @@ def sv_accept(batch: Batch, target_logits: torch.Tensor, draft_logits: Optional[
                               _stream(stream)), "sv_accept")
 
 
+def sv_accept_static(batch: Batch, target_logits: torch.Tensor,
+                     draft_logits: Optional[torch.Tensor], vocab: int, temperature: float,
+                     seed: int, accepted_len: torch.Tensor, accepted_nodes: torch.Tensor,
+                     next_token: torch.Tensor, ambiguous: torch.Tensor,
+                     done: Optional[torch.Tensor], row_stats: Optional[torch.Tensor],
+                     dev_status: Optional[torch.Tensor] = None, stream=None):
+    """sv_accept for callers that cannot allocate a workspace: the scratch is
+    a fixed device array inside the library (see the header for its limit
+    and for why concurrent calls must not overlap)."""
+    _expect(target_logits, torch.float32, "target_logits")
+    _expect(draft_logits, torch.float32, "draft_logits")
+    _expect(ambiguous, torch.uint8, "ambiguous")
+    _expect(row_stats, torch.float32, "row_stats")
+    b = batch.c()
+    N.check(N.lib().sv_accept_static(ctypes.byref(b), _ptr(target_logits), _ptr(draft_logits),
+                                     vocab, temperature, seed & 0xFFFFFFFFFFFFFFFF,
+                                     _ptr(accepted_len), _ptr(accepted_nodes), _ptr(next_token),
+                                     _ptr(ambiguous), _ptr(done), _ptr(row_stats),
+                                     _ptr(dev_status), _stream(stream)), "sv_accept_static")
+
+
 def sv_commit_kv(kv: PagedKV, batch: Batch, accepted_len: torch.Tensor,
                  accepted_nodes: torch.Tensor, pool: BlockPool,
                  dev_status: Optional[torch.Tensor] = None, stream=None):

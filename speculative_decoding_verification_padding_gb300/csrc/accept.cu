@@ -590,3 +590,56 @@ extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
   }
   return SV_OK;
 }
+
+// ------------------------------------------------ no-allocation variant ----
+// sv_accept_static: sv_accept without a caller workspace.  Its scratch is the
+// file-scope device array below, which every GPU that loads the library keeps
+// until the process exits.  The address of that array on the current device
+// is looked up once per device (cudaGetSymbolAddress) on the first call made
+// with that device current; make that first call before any stream capture.
+// All calls share the array: two calls whose work overlaps on the GPU (for
+// example on two streams) race on it.  Nothing in it has to start at zero:
+// the accept kernels write every scratch word before they read it (the
+// decide kernel clears each request's sampling job and ticket itself).
+
+#include <mutex>
+
+namespace {
+
+static __device__ __align__(256) uint8_t g_accept_scratch[SV_ACCEPT_STATIC_SCRATCH_BYTES];
+
+std::mutex g_accept_scratch_mu;
+constexpr int kMaxDevices = 64;
+void* g_accept_scratch_addr[kMaxDevices] = {};
+
+sv_status accept_scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_accept_scratch_mu);
+  if (!g_accept_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || !p) return SV_ERR_CUDA;
+    g_accept_scratch_addr[dev] = p;
+  }
+  *out = g_accept_scratch_addr[dev];
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" sv_status sv_accept_static(const sv_batch* bt, const float* target_logits,
+                                      const float* draft_logits, int32_t vocab, float temperature,
+                                      uint64_t seed, int32_t* accepted_len,
+                                      int32_t* accepted_nodes, int32_t* next_token,
+                                      uint8_t* ambiguous, int32_t* done, float* row_stats,
+                                      int32_t* dev_status, void* stream) {
+  if (!bt || bt->n_req < 0 || bt->total_rows < 0 || vocab < 1) return SV_ERR_INVALID_ARGUMENT;
+  const size_t need = sv_accept_workspace(bt, vocab);
+  if (need > (size_t)SV_ACCEPT_STATIC_SCRATCH_BYTES) return SV_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  const sv_status st = accept_scratch_address(&scratch);
+  if (st != SV_OK) return st;
+  return sv_accept(bt, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
+                   accepted_nodes, next_token, ambiguous, done, row_stats, scratch,
+                   (size_t)SV_ACCEPT_STATIC_SCRATCH_BYTES, dev_status, stream);
+}
