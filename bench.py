@@ -231,6 +231,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="only run this many steps (for a profiler), no timing line")
+    ap.add_argument("--ctx-scale", type=float, default=1.0,
+                    help="with --profile-steps: shrink every context (smaller profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -255,7 +257,8 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device(dev))
 
-    w = wl.make_workload(wl.config(args.workload))
+    w = wl.make_workload(wl.config(args.workload),
+                         ctx_scale=args.ctx_scale if args.profile_steps else 1.0)
     s = DeviceStep(w, device=dev)
     chunk = s.chunk
     stream = torch.cuda.current_stream()
