@@ -411,7 +411,7 @@ def main():
         if tr.get("workload") == args.workload and tr.get("kernel_rev") == KERNEL_REV:
             traffic = tr.get("bytes_per_launch")
 
-    launches_per_step = n_chunks * 7 + 2
+    launches_per_step = n_chunks * 6 + 2
     value = world * rows_attended / t_step
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -451,7 +451,7 @@ def main():
 
 
 # Revision tag of the attention kernel the stored ncu traffic belongs to.
-KERNEL_REV = "attend-v1"
+KERNEL_REV = "attend-v2"
 
 if __name__ == "__main__":
     main()

@@ -6,36 +6,42 @@
 // draft tokens of a request); [FASER] operations notes (the attention kernel
 // must accept a chunk of the rows); [SSD] section details (PagedAttention).
 //
-// Three kernels on one stream:
-//   plan   (1 CTA)   ancestor-or-self bit mask of every row (walk of the
-//                    parent links), parent / window / length validation, and
-//                    a length-weighted split-KV work list: the keys of each
-//                    (request, KV head, 64-row query tile) are cut into
-//                    splits of P pages so that about kUnitTarget units exist.
-//   attend (1 CTA per unit, 4 warps)
-//                    the query rows of the whole GQA group (row x head
-//                    packed as "virtual rows", 16 per warp) share every KV
-//                    page; pages are streamed through a 4-stage cp.async ring
-//                    (16-byte copies, XOR-swizzled rows); QK^T and PV run on
-//                    mma.sync m16n8k16 bf16 -> fp32; online softmax in the
-//                    log2 domain; the ancestor mask is applied only on the
-//                    stages that hold staged draft slots.
-//   merge  (1 warp per row x head)
-//                    log-sum-exp merge of the splits; requests that needed a
-//                    single split were already written by the attend kernel.
+// Two kernels on one stream:
+//   plan   (1 CTA)   validates parents / windows / lengths (one warp per
+//                    request) and builds a length-weighted split-KV work list:
+//                    the keys of each (request, KV head, 64-row query tile)
+//                    are cut into splits of P pages so that about kUnitTarget
+//                    units exist; clears the per-group merge tickets.
+//   attend (1 CTA per unit, 4 warps, 2 CTAs per SM)
+//                    the query rows of the whole GQA group (row x head packed
+//                    as "virtual rows") share every KV page.  Pages stream
+//                    through a 3-stage ring of 64-token stages (16-byte
+//                    cp.async copies into XOR-swizzled rows).  A warp owns a
+//                    16-row m-tile and a slice of each stage's tokens: with
+//                    one m-tile the four warps take 16 tokens each, with two
+//                    they take 32, with three or four every warp sees the
+//                    whole stage.  QK^T and PV run on mma.sync m16n8k16 bf16
+//                    -> fp32 with an online softmax in the log2 domain; the
+//                    ancestor mask (built per CTA from the parent links held
+//                    in shared memory) is applied only where staged draft
+//                    slots lie.  Warps that shared an m-tile merge through
+//                    shared memory.  A unit that covers all keys of its rows
+//                    writes bf16 output directly; otherwise it writes (m, l, O)
+//                    partials and the last CTA of the group (atomic ticket)
+//                    merges all splits and writes the output.
 
 #include "sv_internal.cuh"
 
 namespace sv {
 namespace attn {
 
-constexpr int kTB = 32;          // tokens per pipeline stage (two pages)
-constexpr int kStages = 4;       // cp.async ring depth
+constexpr int kTB = 64;          // tokens per pipeline stage (four pages)
+constexpr int kStages = 3;       // cp.async ring depth
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTileRows = 64;    // virtual rows per unit (16 per warp)
-constexpr int kUnitTarget = kNumSMs * 16;
-constexpr int kMinPagesPerSplit = 4;
+constexpr int kTileRows = 64;    // virtual rows per unit
+constexpr int kUnitTarget = kNumSMs * 8;
+constexpr int kMinPagesPerSplit = 8;
 
 struct ReqInfo {
   int ubase, nsplit, nrt, b, e, ctx, nblk, valid;
@@ -48,7 +54,7 @@ struct Header {
 };
 
 struct Layout {
-  size_t header, info, ubase, masks, ml, o, total;
+  size_t header, info, ubase, tickets, ml, o, total;
   int ucap;
 };
 
@@ -64,7 +70,7 @@ inline Layout layout(int R, int total_rows, int group, int Hkv, int D) {
   L.header = off; off += align256(sizeof(Header));
   L.info = off; off += align256(sizeof(ReqInfo) * (size_t)R);
   L.ubase = off; off += align256(sizeof(int) * (size_t)(R + 1));
-  L.masks = off; off += align256(16 * (size_t)total_rows);
+  L.tickets = off; off += align256(sizeof(int) * (size_t)L.ucap);
   L.ml = off; off += align256((size_t)L.ucap * kTileRows * 2 * sizeof(float));
   L.o = off; off += align256((size_t)L.ucap * kTileRows * (size_t)D * sizeof(float));
   L.total = off;
@@ -117,11 +123,11 @@ __device__ __forceinline__ void block_excl_scan(int* s_warp, int v, int& excl, i
 
 __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   const int R = a.bt.n_req;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Header* hdr = reinterpret_cast<Header*>(a.ws + a.L.header);
   ReqInfo* info = reinterpret_cast<ReqInfo*>(a.ws + a.L.info);
   int* ubase = reinterpret_cast<int*>(a.ws + a.L.ubase);
-  unsigned long long* masks = reinterpret_cast<unsigned long long*>(a.ws + a.L.masks);
+  int* tickets = reinterpret_cast<int*>(a.ws + a.L.tickets);
   __shared__ int s_bad;
   __shared__ unsigned long long s_W;
   __shared__ int s_warp[32];
@@ -132,7 +138,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     s_W = 0ull;
     s_carry = 0;
   }
-  for (int i = tid; i < R; i += blockDim.x) info[i].valid = 1;
   __syncthreads();
   if (s_bad) {
     if (tid == 0) {
@@ -142,59 +147,45 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     }
     return;
   }
-  // Rows: ancestor-or-self masks and parent validation.
-  for (int r = tid; r < a.bt.total_rows; r += blockDim.x) {
-    const int i = find_segment(a.bt.cu_rows, R, r);
-    const int cu = a.bt.cu_rows[i];
-    const int j = r - cu;
-    unsigned long long lo = 0ull, hi = 0ull;
-    bool ok = j < kMaxRows;
-    int m = j;
-    for (int steps = 0; ok && steps <= kMaxRows; ++steps) {
-      if (m < 64) lo |= 1ull << m; else hi |= 1ull << (m - 64);
-      const int p = a.bt.parent[cu + m];
-      if (m == 0) {
-        if (p != -1) ok = false;
-        break;
-      }
-      if (p < 0 || p >= m) { ok = false; break; }
-      m = p;
-    }
-    masks[2 * (size_t)r] = lo;
-    masks[2 * (size_t)r + 1] = hi;
-    if (!ok) {
-      info[i].valid = 0;
-      if (j < kMaxRows) flag(a.dev_status, SV_DEV_BAD_PARENT);
-    }
-  }
-  __syncthreads();
-  // Requests: windows, lengths, total work.
+  // One warp per request: window, parents, length, work.
   unsigned long long myW = 0;
-  for (int i = tid; i < R; i += blockDim.x) {
-    Window w = window_of(a.bt, i);
-    bool valid = info[i].valid && w.ok;
-    if (!w.ok) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-    const int ctx = a.cache_lens[i];
-    if (valid && (ctx < 0 || (long)ctx + w.rows > (long)a.max_blocks * kBlockSize)) {
-      valid = false;
-      flag(a.dev_status, SV_DEV_BAD_LENGTH);
+  for (int i = warp; i < R; i += 32) {
+    const Window w = window_of(a.bt, i);
+    const int cu = a.bt.cu_rows[i];
+    bool badp = false;
+    if (w.ok) {
+      for (int j = lane; j < w.rows; j += 32) {
+        const int p = a.bt.parent[cu + j];
+        badp |= (j == 0) ? (p != -1) : (p < 0 || p >= j);
+      }
     }
-    const int nw = valid ? max(0, w.e - w.b) : 0;
-    const int nrt = (a.group * nw + kTileRows - 1) / kTileRows;
-    const int nblk = nw ? (ctx + w.e + kBlockSize - 1) / kBlockSize : 0;
-    myW += (unsigned long long)nrt * a.Hkv * nblk;
-    ReqInfo ri;
-    ri.valid = valid && nw > 0;
-    ri.b = w.b;
-    ri.e = w.e;
-    ri.ctx = ctx;
-    ri.nrt = nrt;
-    ri.nblk = nblk;
-    ri.nsplit = 0;
-    ri.ubase = 0;
-    info[i] = ri;
+    badp = __any_sync(0xffffffffu, badp);
+    if (lane == 0) {
+      bool valid = w.ok && !badp;
+      if (!w.ok) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+      if (badp) flag(a.dev_status, SV_DEV_BAD_PARENT);
+      const int ctx = a.cache_lens[i];
+      if (valid && (ctx < 0 || (long)ctx + w.rows > (long)a.max_blocks * kBlockSize)) {
+        valid = false;
+        flag(a.dev_status, SV_DEV_BAD_LENGTH);
+      }
+      const int nw = valid ? max(0, w.e - w.b) : 0;
+      const int nrt = (a.group * nw + kTileRows - 1) / kTileRows;
+      const int nblk = nw ? (ctx + w.e + kBlockSize - 1) / kBlockSize : 0;
+      myW += (unsigned long long)nrt * a.Hkv * nblk;
+      ReqInfo ri;
+      ri.valid = valid && nw > 0;
+      ri.b = w.b;
+      ri.e = w.e;
+      ri.ctx = ctx;
+      ri.nrt = nrt;
+      ri.nblk = nblk;
+      ri.nsplit = 0;
+      ri.ubase = 0;
+      info[i] = ri;
+    }
   }
-  atomicAdd(&s_W, myW);
+  if (lane == 0 && myW) atomicAdd(&s_W, myW);
   __syncthreads();
   const unsigned long long W = s_W;
   int P = (int)((W + kUnitTarget - 1) / kUnitTarget);
@@ -204,12 +195,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     const int i = base + tid;
     int units = 0;
     if (i < R) {
-      ReqInfo ri = info[i];
-      if (ri.valid) {
-        ri.nsplit = (ri.nblk + P - 1) / P;
-        units = ri.nrt * a.Hkv * ri.nsplit;
-      }
-      info[i].nsplit = ri.valid ? ri.nsplit : 0;
+      const ReqInfo ri = info[i];
+      const int nsplit = ri.valid ? (ri.nblk + P - 1) / P : 0;
+      units = ri.nrt * a.Hkv * nsplit;
+      info[i].nsplit = nsplit;
     }
     int excl, total;
     block_excl_scan(s_warp, units, excl, total);
@@ -221,12 +210,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     if (tid == 0) s_carry += total;
     __syncthreads();
   }
+  int U = s_carry;
+  if (U > a.L.ucap) {  // cannot happen with the bound used for the workspace
+    U = 0;
+    if (tid == 0) flag(a.dev_status, SV_DEV_BAD_LENGTH);
+  }
+  for (int u = tid; u < U; u += blockDim.x) tickets[u] = 0;
   if (tid == 0) {
-    int U = s_carry;
-    if (U > a.L.ucap) {  // cannot happen with the bound used for the workspace
-      U = 0;
-      flag(a.dev_status, SV_DEV_BAD_LENGTH);
-    }
     ubase[R] = U;
     hdr->U = U;
     hdr->P = P;
@@ -236,9 +226,115 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
 // ---------------------------------------------------------------- attend --
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 3) attend_kernel(Args a) {
+struct Frag {
+  float o[D / 8][4];
+  float m_a, m_b, l_a, l_b;
+};
+
+// One 64-token stage for a warp: its slice [slice0, slice0 + 64 / TS) of the
+// stage held at shared-memory addresses kbase (K) / vbase (V).
+template <int D, int TS>
+__device__ __forceinline__ void stage_compute(Frag<D>& f, const uint32_t (&qf)[D / 16][4],
+                                              uint32_t kbase, uint32_t vbase, int t0, int slice0,
+                                              int ctx, int tok_end, float scale_log2,
+                                              unsigned long long mk_a0, unsigned long long mk_a1,
+                                              unsigned long long mk_b0, unsigned long long mk_b1,
+                                              int lane) {
+  constexpr int NT = kTB / TS / 8;   // 8-token n-tiles of the slice
+  constexpr int KK = kTB / TS / 16;  // 16-token k-steps of PV
+  const int tq = lane & 3;
+  float sc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks += 2) {
+      const int trow = slice0 + nt * 8 + (lane & 7);
+      const int chunk = 2 * ks + (lane >> 3);
+      uint32_t r[4];
+      ldsm_x4(r, kbase + (uint32_t)(trow * D + ((chunk ^ (trow & 7)) << 3)) * 2u);
+      mma16816(sc[nt], qf[ks], r[0], r[1]);
+      mma16816(sc[nt], qf[ks + 1], r[2], r[3]);
+    }
+  }
+  const int tfirst = t0 + slice0;
+  const bool need_mask = (tfirst + kTB / TS > ctx) || (tfirst + kTB / TS > tok_end);
+  float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float v = sc[nt][e] * scale_log2;
+      if (need_mask) {
+        const int tok = tfirst + nt * 8 + 2 * tq + (e & 1);
+        bool ok = tok < tok_end;
+        if (ok && tok >= ctx) {
+          const int m = tok - ctx;
+          const unsigned long long w0 = (e < 2) ? mk_a0 : mk_b0;
+          const unsigned long long w1 = (e < 2) ? mk_a1 : mk_b1;
+          ok = ((m < 64 ? (w0 >> m) : (w1 >> (m - 64))) & 1ull) != 0ull;
+        }
+        if (!ok) v = -INFINITY;
+      }
+      sc[nt][e] = v;
+      if (e < 2) mx_a = fmaxf(mx_a, v); else mx_b = fmaxf(mx_b, v);
+    }
+  }
+  mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+  mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+  mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+  mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+  const float nm_a = fmaxf(f.m_a, mx_a), nm_b = fmaxf(f.m_b, mx_b);
+  const float base_a = nm_a == -INFINITY ? 0.f : nm_a;
+  const float base_b = nm_b == -INFINITY ? 0.f : nm_b;
+  const float al_a = exp2f(f.m_a - base_a), al_b = exp2f(f.m_b - base_b);
+  f.m_a = nm_a;
+  f.m_b = nm_b;
+  float ps_a = 0.f, ps_b = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    sc[nt][0] = exp2f(sc[nt][0] - base_a);
+    sc[nt][1] = exp2f(sc[nt][1] - base_a);
+    sc[nt][2] = exp2f(sc[nt][2] - base_b);
+    sc[nt][3] = exp2f(sc[nt][3] - base_b);
+    ps_a += sc[nt][0] + sc[nt][1];
+    ps_b += sc[nt][2] + sc[nt][3];
+  }
+  f.l_a = f.l_a * al_a + ps_a;
+  f.l_b = f.l_b * al_b + ps_b;
+#pragma unroll
+  for (int dn = 0; dn < D / 8; ++dn) {
+    f.o[dn][0] *= al_a;
+    f.o[dn][1] *= al_a;
+    f.o[dn][2] *= al_b;
+    f.o[dn][3] *= al_b;
+  }
+#pragma unroll
+  for (int kk = 0; kk < KK; ++kk) {
+    uint32_t pa[4];
+    pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+    pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+    pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+    pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+#pragma unroll
+    for (int dn = 0; dn < D / 8; dn += 2) {
+      const int trow = slice0 + 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int chunk = dn + (lane >> 4);
+      uint32_t r[4];
+      ldsm_x4_t(r, vbase + (uint32_t)(trow * D + ((chunk ^ (trow & 7)) << 3)) * 2u);
+      mma16816(f.o[dn], pa, r[0], r[1]);
+      mma16816(f.o[dn + 1], pa, r[2], r[3]);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2) attend_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __nv_bfloat16* smem = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  __shared__ int s_par[kMaxRows];
+  __shared__ unsigned long long s_mask[kTileRows][2];
+  __shared__ int s_last;
   const Header* hdr = reinterpret_cast<const Header*>(a.ws + a.L.header);
   const int U = hdr->U;
   const int u = blockIdx.x;
@@ -247,8 +343,6 @@ __global__ void __launch_bounds__(kThreads, 3) attend_kernel(Args a) {
   const int R = a.bt.n_req;
   const ReqInfo* infos = reinterpret_cast<const ReqInfo*>(a.ws + a.L.info);
   const int* ubase = reinterpret_cast<const int*>(a.ws + a.L.ubase);
-  const unsigned long long* masks =
-      reinterpret_cast<const unsigned long long*>(a.ws + a.L.masks);
 
   const int i = find_segment(ubase, R, u);
   const ReqInfo ri = infos[i];
@@ -257,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 3) attend_kernel(Args a) {
   const int rest = local / ri.nsplit;
   const int g = rest % a.Hkv;
   const int rt = rest / a.Hkv;
-  const int M = a.group * (ri.e - ri.b);
+  const int group = a.group;
+  const int M = group * (ri.e - ri.b);
   const int vr0 = rt * kTileRows;
   const int Mu = min(kTileRows, M - vr0);
   const int blk0 = s * P;
@@ -265,42 +360,20 @@ __global__ void __launch_bounds__(kThreads, 3) attend_kernel(Args a) {
   const int ctx = ri.ctx;
   const int tok_end = min(ctx + ri.e, blk1 * kBlockSize);
   const int cu = a.bt.cu_rows[i];
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const bool active = warp * 16 < Mu;
 
-  // The two virtual rows of this thread: (query row, head in group).
-  const int vl_a = warp * 16 + gq, vl_b = vl_a + 8;
-  const bool real_a = vl_a < Mu, real_b = vl_b < Mu;
-  const int va = vr0 + vl_a, vb = vr0 + vl_b;
-  const int prow_a = cu + ri.b + (real_a ? va / a.group : 0);
-  const int prow_b = cu + ri.b + (real_b ? vb / a.group : 0);
-  const int head_a = g * a.group + va % a.group;
-  const int head_b = g * a.group + vb % a.group;
+  // Warp roles: m-tile mt, token slice ts of TS per stage.
+  const int MT = (Mu + 15) >> 4;
+  const int TS = MT == 1 ? 4 : MT == 2 ? 2 : 1;
+  const int mt = MT == 3 ? warp : warp % MT;
+  const int ts = MT == 3 ? 0 : warp / MT;
+  const bool active = mt < MT;
 
-  // Q fragments (A operand), zero for padding rows.
-  uint32_t qf[D / 16][4];
-  {
-    const uint32_t* qa = reinterpret_cast<const uint32_t*>(
-        a.q + ((size_t)prow_a * a.Hq + head_a) * D);
-    const uint32_t* qb = reinterpret_cast<const uint32_t*>(
-        a.q + ((size_t)prow_b * a.Hq + head_b) * D);
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      qf[ks][0] = (active && real_a) ? __ldg(qa + ks * 8 + tq) : 0u;
-      qf[ks][1] = (active && real_b) ? __ldg(qb + ks * 8 + tq) : 0u;
-      qf[ks][2] = (active && real_a) ? __ldg(qa + ks * 8 + 4 + tq) : 0u;
-      qf[ks][3] = (active && real_b) ? __ldg(qb + ks * 8 + 4 + tq) : 0u;
-    }
-  }
-  unsigned long long mk_a0 = 0, mk_a1 = 0, mk_b0 = 0, mk_b1 = 0;
-  if (real_a) { mk_a0 = masks[2 * (size_t)prow_a]; mk_a1 = masks[2 * (size_t)prow_a + 1]; }
-  if (real_b) { mk_b0 = masks[2 * (size_t)prow_b]; mk_b1 = masks[2 * (size_t)prow_b + 1]; }
-
-  const int n_stage = (blk1 - blk0 + 1) / 2;
+  const int n_stage = (blk1 - blk0 + 3) / 4;
   const int32_t* table = a.tables + (size_t)i * a.max_blocks;
-  constexpr int kChunksPerRow = D / 8;                 // 16-byte chunks per token row
+  constexpr int kChunksPerRow = D / 8;
   constexpr int kChunksPerTensor = kTB * kChunksPerRow;
   constexpr int kCopiesPerThread = 2 * kChunksPerTensor / kThreads;
 
@@ -309,12 +382,12 @@ __global__ void __launch_bounds__(kThreads, 3) attend_kernel(Args a) {
       __nv_bfloat16* buf = smem + (size_t)(st % kStages) * 2 * kTB * D;
 #pragma unroll
       for (int k = 0; k < kCopiesPerThread; ++k) {
-        const int c = threadIdx.x + k * kThreads;
+        const int c = tid + k * kThreads;
         const int tensor = c / kChunksPerTensor;
         const int rem = c % kChunksPerTensor;
         const int row = rem / kChunksPerRow;
         const int col = rem % kChunksPerRow;
-        const int page = blk0 + 2 * st + (row >> 4);
+        const int page = blk0 + 4 * st + (row >> 4);
         const int tok = page * kBlockSize + (row & 15);
         const __nv_bfloat16* base = tensor ? a.v : a.k;
         const void* src = base;
@@ -335,200 +408,206 @@ __global__ void __launch_bounds__(kThreads, 3) attend_kernel(Args a) {
     cp_async_commit();
   };
 
-  float o[D / 8][4];
-#pragma unroll
-  for (int dn = 0; dn < D / 8; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-
 #pragma unroll
   for (int st = 0; st < kStages - 1; ++st) issue(st);
+
+  // Ancestor-or-self masks of the unit's rows, only if it reaches staged slots.
+  const int r_first = vr0 / group;
+  const int r_count = (vr0 + Mu - 1) / group - r_first + 1;
+  const bool unit_masked = blk1 * kBlockSize > ctx;
+  if (unit_masked) {
+    const int rows = a.bt.cu_rows[i + 1] - cu;
+    for (int j = tid; j < rows; j += kThreads) s_par[j] = a.bt.parent[cu + j];
+    __syncthreads();
+    for (int t = tid; t < r_count; t += kThreads) {
+      unsigned long long lo = 0ull, hi = 0ull;
+      int m = ri.b + r_first + t;
+      for (int steps = 0; m >= 0 && steps <= kMaxRows; ++steps) {  // parents validated by plan
+        if (m < 64) lo |= 1ull << m; else hi |= 1ull << (m - 64);
+        m = s_par[m];
+      }
+      s_mask[t][0] = lo;
+      s_mask[t][1] = hi;
+    }
+    __syncthreads();
+  }
+
+  // This thread's two virtual rows of m-tile mt.
+  const int vl_a = mt * 16 + gq, vl_b = vl_a + 8;
+  const bool real_a = active && vl_a < Mu, real_b = active && vl_b < Mu;
+  const int va = vr0 + vl_a, vb = vr0 + vl_b;
+  const int prow_a = cu + ri.b + (real_a ? va / group : 0);
+  const int prow_b = cu + ri.b + (real_b ? vb / group : 0);
+  const int head_a = g * group + va % group;
+  const int head_b = g * group + vb % group;
+  unsigned long long mk_a0 = 0, mk_a1 = 0, mk_b0 = 0, mk_b1 = 0;
+  if (unit_masked) {
+    if (real_a) { mk_a0 = s_mask[va / group - r_first][0]; mk_a1 = s_mask[va / group - r_first][1]; }
+    if (real_b) { mk_b0 = s_mask[vb / group - r_first][0]; mk_b1 = s_mask[vb / group - r_first][1]; }
+  }
+  uint32_t qf[D / 16][4];
+  {
+    const uint32_t* qa = reinterpret_cast<const uint32_t*>(a.q + ((size_t)prow_a * a.Hq + head_a) * D);
+    const uint32_t* qb = reinterpret_cast<const uint32_t*>(a.q + ((size_t)prow_b * a.Hq + head_b) * D);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      qf[ks][0] = real_a ? __ldg(qa + ks * 8 + tq) : 0u;
+      qf[ks][1] = real_b ? __ldg(qb + ks * 8 + tq) : 0u;
+      qf[ks][2] = real_a ? __ldg(qa + ks * 8 + 4 + tq) : 0u;
+      qf[ks][3] = real_b ? __ldg(qb + ks * 8 + 4 + tq) : 0u;
+    }
+  }
+
+  Frag<D> f;
+#pragma unroll
+  for (int dn = 0; dn < D / 8; ++dn) f.o[dn][0] = f.o[dn][1] = f.o[dn][2] = f.o[dn][3] = 0.f;
+  f.m_a = f.m_b = -INFINITY;
+  f.l_a = f.l_b = 0.f;
 
   for (int st = 0; st < n_stage; ++st) {
     issue(st + kStages - 1);
     cp_async_wait<kStages - 1>();
     __syncthreads();
     if (active) {
-      const __nv_bfloat16* Ks = smem + (size_t)(st % kStages) * 2 * kTB * D;
-      const uint32_t kbase = smem_u32(Ks);
+      const uint32_t kbase = smem_u32(smem + (size_t)(st % kStages) * 2 * kTB * D);
       const uint32_t vbase = kbase + kTB * D * 2;
-      const int t0 = (blk0 + 2 * st) * kBlockSize;
-      float sc[4][4];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ks += 2) {
-          const int trow = nt * 8 + (lane & 7);
-          const int chunk = 2 * ks + (lane >> 3);
-          uint32_t r[4];
-          ldsm_x4(r, kbase + (uint32_t)(trow * D + ((chunk ^ (trow & 7)) << 3)) * 2u);
-          mma16816(sc[nt], qf[ks], r[0], r[1]);
-          mma16816(sc[nt], qf[ks + 1], r[2], r[3]);
-        }
-      }
-      // scale, mask, running max
-      const bool need_mask = (t0 + kTB > ctx) || (t0 + kTB > tok_end);
-      float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float v = sc[nt][e] * a.scale_log2;
-          if (need_mask) {
-            const int tok = t0 + nt * 8 + 2 * tq + (e & 1);
-            bool ok = tok < tok_end;
-            if (ok && tok >= ctx) {
-              const int m = tok - ctx;
-              const unsigned long long w0 = (e < 2) ? mk_a0 : mk_b0;
-              const unsigned long long w1 = (e < 2) ? mk_a1 : mk_b1;
-              ok = ((m < 64 ? (w0 >> m) : (w1 >> (m - 64))) & 1ull) != 0ull;
-            }
-            if (!ok) v = -INFINITY;
-          }
-          sc[nt][e] = v;
-          if (e < 2) mx_a = fmaxf(mx_a, v); else mx_b = fmaxf(mx_b, v);
-        }
-      }
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-      const float nm_a = fmaxf(m_a, mx_a), nm_b = fmaxf(m_b, mx_b);
-      const float base_a = nm_a == -INFINITY ? 0.f : nm_a;
-      const float base_b = nm_b == -INFINITY ? 0.f : nm_b;
-      const float al_a = exp2f(m_a - base_a), al_b = exp2f(m_b - base_b);
-      m_a = nm_a;
-      m_b = nm_b;
-      float ps_a = 0.f, ps_b = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        sc[nt][0] = exp2f(sc[nt][0] - base_a);
-        sc[nt][1] = exp2f(sc[nt][1] - base_a);
-        sc[nt][2] = exp2f(sc[nt][2] - base_b);
-        sc[nt][3] = exp2f(sc[nt][3] - base_b);
-        ps_a += sc[nt][0] + sc[nt][1];
-        ps_b += sc[nt][2] + sc[nt][3];
-      }
-      l_a = l_a * al_a + ps_a;
-      l_b = l_b * al_b + ps_b;
-#pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn) {
-        o[dn][0] *= al_a;
-        o[dn][1] *= al_a;
-        o[dn][2] *= al_b;
-        o[dn][3] *= al_b;
-      }
-      // O += P V
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-        pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-        pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-        pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-#pragma unroll
-        for (int dn = 0; dn < D / 8; dn += 2) {
-          const int trow = 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int chunk = dn + (lane >> 4);
-          uint32_t r[4];
-          ldsm_x4_t(r, vbase + (uint32_t)(trow * D + ((chunk ^ (trow & 7)) << 3)) * 2u);
-          mma16816(o[dn], pa, r[0], r[1]);
-          mma16816(o[dn + 1], pa, r[2], r[3]);
-        }
-      }
+      const int t0 = (blk0 + 4 * st) * kBlockSize;
+      if (TS == 4)
+        stage_compute<D, 4>(f, qf, kbase, vbase, t0, ts * 16, ctx, tok_end, a.scale_log2, mk_a0,
+                            mk_a1, mk_b0, mk_b1, lane);
+      else if (TS == 2)
+        stage_compute<D, 2>(f, qf, kbase, vbase, t0, ts * 32, ctx, tok_end, a.scale_log2, mk_a0,
+                            mk_a1, mk_b0, mk_b1, lane);
+      else
+        stage_compute<D, 1>(f, qf, kbase, vbase, t0, 0, ctx, tok_end, a.scale_log2, mk_a0,
+                            mk_a1, mk_b0, mk_b1, lane);
     }
     __syncthreads();
   }
   cp_async_wait<0>();
+  __syncthreads();
 
-  if (!active) return;
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+  // Warps that split the tokens of one m-tile merge through shared memory
+  // (the stage ring is free now): every thread hands its fragment to the
+  // same lane of the ts = 0 warp.
+  float* xch = reinterpret_cast<float*>(smem_raw);
+  constexpr int kFragFloats = D / 2 + 4;  // o (D/8 * 4) + m_a, m_b, l_a, l_b
+  if (TS > 1) {
+    if (active && ts > 0) {
+      float* dst = xch + ((size_t)warp * kFragFloats) * 32 + lane;
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[(dn * 4 + e) * 32] = f.o[dn][e];
+      dst[(D / 2 + 0) * 32] = f.m_a;
+      dst[(D / 2 + 1) * 32] = f.m_b;
+      dst[(D / 2 + 2) * 32] = f.l_a;
+      dst[(D / 2 + 3) * 32] = f.l_b;
+    }
+    __syncthreads();
+    if (active && ts == 0) {
+      for (int t = 1; t < TS; ++t) {
+        const float* src = xch + ((size_t)(warp + t * MT) * kFragFloats) * 32 + lane;
+        const float m2a = src[(D / 2 + 0) * 32], m2b = src[(D / 2 + 1) * 32];
+        const float l2a = src[(D / 2 + 2) * 32], l2b = src[(D / 2 + 3) * 32];
+        const float na = fmaxf(f.m_a, m2a), nb = fmaxf(f.m_b, m2b);
+        const float ba = na == -INFINITY ? 0.f : na, bb = nb == -INFINITY ? 0.f : nb;
+        const float s1a = exp2f(f.m_a - ba), s2a = exp2f(m2a - ba);
+        const float s1b = exp2f(f.m_b - bb), s2b = exp2f(m2b - bb);
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+          f.o[dn][0] = f.o[dn][0] * s1a + src[(dn * 4 + 0) * 32] * s2a;
+          f.o[dn][1] = f.o[dn][1] * s1a + src[(dn * 4 + 1) * 32] * s2a;
+          f.o[dn][2] = f.o[dn][2] * s1b + src[(dn * 4 + 2) * 32] * s2b;
+          f.o[dn][3] = f.o[dn][3] * s1b + src[(dn * 4 + 3) * 32] * s2b;
+        }
+        f.l_a = f.l_a * s1a + l2a * s2a;
+        f.l_b = f.l_b * s1b + l2b * s2b;
+        f.m_a = na;
+        f.m_b = nb;
+      }
+    }
+  }
+  const bool owner = active && ts == 0;
+  if (owner) {
+    f.l_a += __shfl_xor_sync(0xffffffffu, f.l_a, 1);
+    f.l_a += __shfl_xor_sync(0xffffffffu, f.l_a, 2);
+    f.l_b += __shfl_xor_sync(0xffffffffu, f.l_b, 1);
+    f.l_b += __shfl_xor_sync(0xffffffffu, f.l_b, 2);
+  }
 
   if (ri.nsplit == 1) {
-    const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f;
-    const float inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
+    if (!owner) return;
+    const float inv_a = f.l_a > 0.f ? 1.f / f.l_a : 0.f;
+    const float inv_b = f.l_b > 0.f ? 1.f / f.l_b : 0.f;
     uint32_t* oa = reinterpret_cast<uint32_t*>(a.out + ((size_t)prow_a * a.Hq + head_a) * D);
     uint32_t* ob = reinterpret_cast<uint32_t*>(a.out + ((size_t)prow_b * a.Hq + head_b) * D);
 #pragma unroll
     for (int dn = 0; dn < D / 8; ++dn) {
-      if (real_a) oa[dn * 4 + tq] = pack_bf16(o[dn][0] * inv_a, o[dn][1] * inv_a);
-      if (real_b) ob[dn * 4 + tq] = pack_bf16(o[dn][2] * inv_b, o[dn][3] * inv_b);
+      if (real_a) oa[dn * 4 + tq] = pack_bf16(f.o[dn][0] * inv_a, f.o[dn][1] * inv_a);
+      if (real_b) ob[dn * 4 + tq] = pack_bf16(f.o[dn][2] * inv_b, f.o[dn][3] * inv_b);
     }
-  } else {
-    float* ml = reinterpret_cast<float*>(a.ws + a.L.ml) + (size_t)u * kTileRows * 2;
-    float* op = reinterpret_cast<float*>(a.ws + a.L.o) + (size_t)u * kTileRows * D;
+    return;
+  }
+
+  // Several splits: write this split's partials, then the group's last CTA merges.
+  float* ml_all = reinterpret_cast<float*>(a.ws + a.L.ml);
+  float* op_all = reinterpret_cast<float*>(a.ws + a.L.o);
+  if (owner) {
+    float* ml = ml_all + (size_t)u * kTileRows * 2;
+    float* op = op_all + (size_t)u * kTileRows * D;
     if (tq == 0) {
-      if (real_a) { ml[2 * vl_a] = m_a; ml[2 * vl_a + 1] = l_a; }
-      if (real_b) { ml[2 * vl_b] = m_b; ml[2 * vl_b + 1] = l_b; }
+      if (real_a) { ml[2 * vl_a] = f.m_a; ml[2 * vl_a + 1] = f.l_a; }
+      if (real_b) { ml[2 * vl_b] = f.m_b; ml[2 * vl_b + 1] = f.l_b; }
     }
 #pragma unroll
     for (int dn = 0; dn < D / 8; ++dn) {
       if (real_a)
-        *reinterpret_cast<float2*>(op + (size_t)vl_a * D + dn * 8 + 2 * tq) =
-            make_float2(o[dn][0], o[dn][1]);
+        *reinterpret_cast<float2*>(op + (size_t)vl_a * D + dn * 8 + 2 * tq) = make_float2(f.o[dn][0], f.o[dn][1]);
       if (real_b)
-        *reinterpret_cast<float2*>(op + (size_t)vl_b * D + dn * 8 + 2 * tq) =
-            make_float2(o[dn][2], o[dn][3]);
+        *reinterpret_cast<float2*>(op + (size_t)vl_b * D + dn * 8 + 2 * tq) = make_float2(f.o[dn][2], f.o[dn][3]);
     }
   }
-}
-
-// ----------------------------------------------------------------- merge --
-
-template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(Args a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long pair = (long)blockIdx.x * 8 + warp;
-  if (pair >= (long)a.bt.total_rows * a.Hq) return;
-  const int prow = (int)(pair / a.Hq), head = (int)(pair % a.Hq);
-  const int R = a.bt.n_req;
-  const int i = find_segment(a.bt.cu_rows, R, prow);
-  const ReqInfo ri = reinterpret_cast<const ReqInfo*>(a.ws + a.L.info)[i];
-  const int r = prow - a.bt.cu_rows[i];
-  if (!ri.valid || ri.nsplit <= 1 || r < ri.b || r >= ri.e) return;
-  const int g = head / a.group, hg = head % a.group;
-  const int vr = (r - ri.b) * a.group + hg;
-  const int rt = vr / kTileRows, vi = vr % kTileRows;
-  const int ub = ri.ubase + (rt * a.Hkv + g) * ri.nsplit;
-  const float* ml = reinterpret_cast<const float*>(a.ws + a.L.ml);
-  const float* op = reinterpret_cast<const float*>(a.ws + a.L.o);
-  float Mx = -INFINITY;
-  for (int s = lane; s < ri.nsplit; s += 32)
-    Mx = fmaxf(Mx, ml[((size_t)(ub + s) * kTileRows + vi) * 2]);
-  Mx = warp_max(Mx);
-  float L = 0.f;
-  for (int s = lane; s < ri.nsplit; s += 32) {
-    const size_t k = ((size_t)(ub + s) * kTileRows + vi) * 2;
-    L += ml[k + 1] * exp2f(ml[k] - Mx);
+  __threadfence();
+  __syncthreads();
+  const int gidx = ri.ubase + (rt * a.Hkv + g) * ri.nsplit;  // unit of split 0
+  if (tid == 0) {
+    int* tickets = reinterpret_cast<int*>(a.ws + a.L.tickets);
+    const int prev = atomicAdd(tickets + gidx, 1);
+    s_last = prev == ri.nsplit - 1;
+    if (s_last) tickets[gidx] = 0;
   }
-  L = warp_sum(L);
-  constexpr int kPer = D / 32;
-  float acc[kPer];
-#pragma unroll
-  for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
-  for (int s = 0; s < ri.nsplit; ++s) {
-    const size_t row = (size_t)(ub + s) * kTileRows + vi;
-    const float w = exp2f(ml[row * 2] - Mx);
-    const float* src = op + row * D + lane * kPer;
-    if (kPer == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(src);
-      acc[0] += w * x.x;
-      acc[1 % kPer] += w * x.y;
-      acc[2 % kPer] += w * x.z;
-      acc[3 % kPer] += w * x.w;
-    } else {
-#pragma unroll
-      for (int c = 0; c < kPer; ++c) acc[c] += w * src[c];
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // Merge: thread -> (virtual row, 4 consecutive columns).
+  constexpr int kQuads = D / 4;
+  for (int x = tid; x < Mu * kQuads; x += kThreads) {
+    const int vr = x / kQuads, c4 = x % kQuads;
+    float Mx = -INFINITY;
+    for (int sp = 0; sp < ri.nsplit; ++sp)
+      Mx = fmaxf(Mx, __ldcg(ml_all + ((size_t)(gidx + sp) * kTileRows + vr) * 2));
+    const float base = Mx == -INFINITY ? 0.f : Mx;
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < ri.nsplit; ++sp) {
+      const size_t row = (size_t)(gidx + sp) * kTileRows + vr;
+      const float wgt = exp2f(__ldcg(ml_all + row * 2) - base);
+      L += __ldcg(ml_all + row * 2 + 1) * wgt;
+      const float4 o4 = __ldcg(reinterpret_cast<const float4*>(op_all + row * D) + c4);
+      acc.x += wgt * o4.x;
+      acc.y += wgt * o4.y;
+      acc.z += wgt * o4.z;
+      acc.w += wgt * o4.w;
     }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int vgl = vr0 + vr;
+    const int prow = cu + ri.b + vgl / group;
+    const int head = g * group + vgl % group;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + ((size_t)prow * a.Hq + head) * D + c4 * 4);
+    dst[0] = pack_bf16(acc.x * inv, acc.y * inv);
+    dst[1] = pack_bf16(acc.z * inv, acc.w * inv);
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  __nv_bfloat16* dst = a.out + ((size_t)prow * a.Hq + head) * D + lane * kPer;
-#pragma unroll
-  for (int c = 0; c < kPer; c += 2)
-    *reinterpret_cast<uint32_t*>(dst + c) = pack_bf16(acc[c] * inv, acc[c + 1] * inv);
 }
 
 template <int D>
@@ -546,9 +625,6 @@ sv_status launch(const Args& a, cudaStream_t stream) {
   plan_kernel<<<1, 1024, 0, stream>>>(a);
   SV_LAUNCH_CHECK();
   attend_kernel<D><<<a.L.ucap, kThreads, smem, stream>>>(a);
-  SV_LAUNCH_CHECK();
-  const long pairs = (long)a.bt.total_rows * a.Hq;
-  merge_kernel<D><<<(unsigned)((pairs + 7) / 8), 256, 0, stream>>>(a);
   SV_LAUNCH_CHECK();
   return SV_OK;
 }
