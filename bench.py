@@ -411,7 +411,7 @@ def main():
         if tr.get("workload") == args.workload and tr.get("kernel_rev") == KERNEL_REV:
             traffic = tr.get("bytes_per_launch")
 
-    launches_per_step = n_chunks * 6 + 2
+    launches_per_step = n_chunks * 5 + 2
     value = world * rows_attended / t_step
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -8,21 +8,28 @@
 // the standard lossless speculative-sampling rule (not printed on the pages).
 //
 // Kernels, in stream order:
-//   stats  (grid: row x vocab chunk x {target, draft})
-//          one pass over the row with 128-bit loads: online max / sum of
-//          exp(x - max) of x = logit / T (T > 0), or max and lowest-index
-//          argmax of the raw logits (T = 0); one partial per chunk.
-//   decide (one warp per request)
-//          merges the partials of the rows it needs, then scans the chain
-//          (or runs the tree descent) with Philox uniforms; writes the path
-//          and, for T > 0, a sampling job for the emitted token.
-//   race   (grid: request x vocab chunk)
-//          the exponential race argmax_v w_v / E_v over the job's row(s),
-//          w = max(0, p - q) after a rejection or p for the bonus token; the
-//          last CTA of a request (atomic ticket) reduces the chunk winners.
+//   list   (1 CTA)   the requests whose window is not empty, in request
+//                    order, and a cleared ticket for each (in chunked
+//                    verification the window kernel does this instead).
+//   stats  (grid-stride over active request x window row x {target, draft}
+//                    x vocab chunk)
+//                    one pass over the row slice with 128-bit loads: online
+//                    max / sum of exp(x - max) of x = logit / T (T > 0), or
+//                    max and lowest-index argmax of the raw logits (T = 0);
+//                    one partial per slice.  The CTA that finishes a
+//                    request's last slice (atomic ticket) runs the decision
+//                    for it with one warp: the chain scan (or the tree
+//                    descent) with Philox uniforms; it writes the path and,
+//                    for T > 0, a sampling job for the emitted token.
+//   race   (grid-stride over active request x vocab chunk)
+//                    the exponential race argmax_v w_v / E_v over the job's
+//                    row(s), w = max(0, p - q) after a rejection or p for the
+//                    bonus token; the last CTA of a request (atomic ticket)
+//                    reduces the chunk winners.
 
 #include <math.h>
 
+#include "sv_accept_internal.h"
 #include "sv_internal.cuh"
 
 namespace sv {
@@ -50,11 +57,11 @@ struct RacePart {
 
 constexpr int kStatThreads = 256;
 constexpr int kRaceThreads = 256;
-constexpr int kDecideWarps = 4;
+constexpr float kLog2e = 1.4426950408889634f;
 
-inline int stats_chunks(int total_rows, int V) {
+inline int stats_chunks(int rows_bound, int V) {
   const int maxc = max(1, min(64, V / 1024));
-  const int want = (kNumSMs * 32 + 2 * total_rows - 1) / max(1, 2 * total_rows);
+  const int want = (kNumSMs * 32 + 2 * rows_bound - 1) / max(1, 2 * rows_bound);
   return max(1, min(want, maxc));
 }
 inline int race_chunks(int R, int V) {
@@ -64,14 +71,11 @@ inline int race_chunks(int R, int V) {
 }
 inline int chunk_len(int V, int nch) { return ((V + nch - 1) / nch + 3) & ~3; }
 
-struct Layout {
-  size_t parts, jobs, race, tickets, total;
-  int nch, nch_r, ch, ch_r;
-};
-
-inline Layout layout(int R, int total_rows, int V) {
+Layout layout(int R, int total_rows, int V, int maxw) {
   Layout L;
-  L.nch = stats_chunks(total_rows, V);
+  L.maxw = max(1, min(maxw, kMaxRows));
+  const long bound = min((long)total_rows, (long)R * L.maxw);
+  L.nch = stats_chunks((int)max(1L, bound), V);
   L.nch_r = race_chunks(R, V);
   L.ch = chunk_len(V, L.nch);
   L.ch_r = chunk_len(V, L.nch_r);
@@ -79,7 +83,9 @@ inline Layout layout(int R, int total_rows, int V) {
   L.parts = off; off += align256(sizeof(StatPart) * (size_t)total_rows * 2 * L.nch);
   L.jobs = off; off += align256(sizeof(Job) * (size_t)R);
   L.race = off; off += align256(sizeof(RacePart) * (size_t)R * L.nch_r);
-  L.tickets = off; off += align256(sizeof(int) * (size_t)R);
+  L.race_tickets = off; off += align256(sizeof(int) * (size_t)R);
+  L.stat_tickets = off; off += align256(sizeof(int) * (size_t)R);
+  L.act = off; off += align256(sizeof(int) * (size_t)(R + 1));  // act[R] = count
   L.total = off;
   return L;
 }
@@ -105,110 +111,96 @@ struct Args {
 __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2) {
   const float M = fmaxf(m, m2);
   if (M == -INFINITY) return;
-  l = l * expf(m - M) + l2 * expf(m2 - M);
+  l = l * ex2((m - M) * kLog2e) + l2 * ex2((m2 - M) * kLog2e);
   m = M;
 }
 __device__ __forceinline__ void merge_am(float& v, int& i, float v2, int i2) {
   if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
 }
 
-// ----------------------------------------------------------------- stats --
-template <bool VEC>
-__global__ void __launch_bounds__(kStatThreads) stats_kernel(Args a) {
-  const int nch = a.L.nch;
-  const int c = blockIdx.x % nch;
-  const int r = blockIdx.x / nch;
-  const int type = blockIdx.y;
-  if (r >= a.bt.total_rows) return;
+// ------------------------------------------------------------------ list --
+// Active requests: window not empty, and (for a continuation window) not
+// already decided.  Also used by the chunk driver, which first turns `done`
+// into the windows of chunk `chunk` (chunk >= 0) and writes them out.
+__global__ void __launch_bounds__(1024) list_kernel(Args a, int chunk, int cs, const int32_t* done,
+                                                    int32_t* rb_out, int32_t* re_out) {
   const int R = a.bt.n_req;
-  const int i = find_segment(a.bt.cu_rows, R, r);
-  const Window w = window_of(a.bt, i);
-  const int j = r - a.bt.cu_rows[i];
-  if (!w.ok || j < w.b || j >= w.e) return;
-  if (w.b > 0 && a.next_token[i] >= 0) return;      // decided in an earlier window
-  if (type == 1 && (a.T == 0.f || j + 1 > w.lim - 1)) return;
-  const float* row = (type ? a.draft : a.target) + (size_t)r * a.V;
-  const int lo = c * a.L.ch;
-  const int hi = min(a.V, lo + a.L.ch);
-  const float T = a.T;
-  float m = -INFINITY, l = 0.f;
-  int am = 0x7fffffff;
-  if (T > 0.f) {
-    if (VEC) {
-      const float4* p4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 4
-      for (int v = lo + 4 * threadIdx.x; v < hi; v += 4 * kStatThreads) {
-        const float4 x4 = __ldcs(p4 + (v >> 2));
-        const float x0 = x4.x / T, x1 = x4.y / T, x2 = x4.z / T, x3 = x4.w / T;
-        const float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-        if (mx > m) {
-          l *= expf(m - mx);
-          m = mx;
-        }
-        l += expf(x0 - m) + expf(x1 - m) + expf(x2 - m) + expf(x3 - m);
-      }
-    } else {
-      for (int v = lo + threadIdx.x; v < hi; v += kStatThreads) {
-        const float x = row[v] / T;
-        if (x > m) {
-          l *= expf(m - x);
-          m = x;
-        }
-        l += expf(x - m);
-      }
-    }
-  } else {
-    if (VEC) {
-      const float4* p4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 4
-      for (int v = lo + 4 * threadIdx.x; v < hi; v += 4 * kStatThreads) {
-        const float4 x4 = __ldcs(p4 + (v >> 2));
-        if (x4.x > m) { m = x4.x; am = v; }
-        if (x4.y > m) { m = x4.y; am = v + 1; }
-        if (x4.z > m) { m = x4.z; am = v + 2; }
-        if (x4.w > m) { m = x4.w; am = v + 3; }
-      }
-    } else {
-      for (int v = lo + threadIdx.x; v < hi; v += kStatThreads) {
-        const float x = row[v];
-        if (x > m) { m = x; am = v; }
-      }
-    }
-  }
-  // block reduction
-  __shared__ float s_m[kStatThreads / 32], s_l[kStatThreads / 32];
-  __shared__ int s_i[kStatThreads / 32];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, am, o);
-    if (T > 0.f) merge_ml(m, l, m2, l2); else merge_am(m, am, m2, i2);
-  }
-  if (lane == 0) { s_m[wid] = m; s_l[wid] = l; s_i[wid] = am; }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* act = reinterpret_cast<int*>(a.ws + a.L.act);
+  int* tickets = reinterpret_cast<int*>(a.ws + a.L.stat_tickets);
+  __shared__ int s_warp[32];
+  __shared__ int s_carry;
+  if (tid == 0) s_carry = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int k = 1; k < kStatThreads / 32; ++k) {
-      if (T > 0.f) merge_ml(m, l, s_m[k], s_l[k]); else merge_am(m, am, s_m[k], s_i[k]);
+  for (int base = 0; base < R; base += blockDim.x) {
+    const int i = base + tid;
+    int f = 0;
+    if (i < R) {
+      if (chunk >= 0) {
+        sv_batch b0 = a.bt;
+        b0.row_begin = nullptr;
+        b0.row_end = nullptr;
+        const Window w = window_of(b0, i);
+        int b = chunk * cs, e = min(b + cs, w.lim);
+        const bool running = chunk == 0 || (done && done[i] == 0);
+        if (!w.ok) {
+          if (chunk == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+          b = e = 0;
+        } else if (!running || b >= e) {
+          b = e = min(b, w.rows);
+        }
+        rb_out[i] = b;
+        re_out[i] = e;
+        f = (w.ok && b < e) ? 1 : 0;
+      } else {
+        const Window w = window_of(a.bt, i);
+        if (!w.ok) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+        else if (w.b < w.e && !(w.b > 0 && a.next_token[i] >= 0)) f = 1;
+      }
+      if (f) tickets[i] = 0;
     }
-    StatPart sp;
-    sp.m = m;
-    sp.l = l;
-    sp.amax = am;
-    sp.pad = 0;
-    reinterpret_cast<StatPart*>(a.ws + a.L.parts)[((size_t)r * 2 + type) * nch + c] = sp;
+    // exclusive scan of the flags
+    int x = f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int wv = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wv, o);
+        if (lane >= o) wv += y;
+      }
+      s_warp[lane] = wv;
+    }
+    __syncthreads();
+    const int excl = (warp ? s_warp[warp - 1] : 0) + x - f;
+    const int total = s_warp[(blockDim.x >> 5) - 1];
+    if (f) act[s_carry + excl] = i;
+    __syncthreads();
+    if (tid == 0) s_carry += total;
+    __syncthreads();
   }
+  if (tid == 0) act[R] = s_carry;
 }
 
 // ---------------------------------------------------------------- decide --
+struct DecideSmem {
+  float mp[kMaxRows], lp[kMaxRows], mq[kMaxRows], lq[kMaxRows];
+  int am[kMaxRows], len[kMaxRows], child[kMaxRows];
+};
+
 __device__ __forceinline__ void row_ml(const Args& a, int r, int type, float& m, float& l) {
   const StatPart* parts = reinterpret_cast<const StatPart*>(a.ws + a.L.parts) +
                           ((size_t)r * 2 + type) * a.L.nch;
   const int lane = threadIdx.x & 31;
   m = -INFINITY;
   l = 0.f;
-  for (int c = lane; c < a.L.nch; c += 32) merge_ml(m, l, parts[c].m, parts[c].l);
+  for (int c = lane; c < a.L.nch; c += 32) merge_ml(m, l, __ldcg(&parts[c].m), __ldcg(&parts[c].l));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -223,7 +215,7 @@ __device__ __forceinline__ void row_argmax(const Args& a, int r, float& v, int& 
   const int lane = threadIdx.x & 31;
   v = -INFINITY;
   idx = 0x7fffffff;
-  for (int c = lane; c < a.L.nch; c += 32) merge_am(v, idx, parts[c].m, parts[c].amax);
+  for (int c = lane; c < a.L.nch; c += 32) merge_am(v, idx, __ldcg(&parts[c].m), __ldcg(&parts[c].amax));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
@@ -232,26 +224,16 @@ __device__ __forceinline__ void row_argmax(const Args& a, int r, float& v, int& 
   }
 }
 
-__global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
-  __shared__ float s_mp[kDecideWarps][kMaxRows], s_lp[kDecideWarps][kMaxRows];
-  __shared__ float s_mq[kDecideWarps][kMaxRows], s_lq[kDecideWarps][kMaxRows];
-  __shared__ int s_am[kDecideWarps][kMaxRows];
-  __shared__ int s_len[kDecideWarps][kMaxRows], s_child[kDecideWarps][kMaxRows];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = blockIdx.x * kDecideWarps + warp;
-  if (i >= a.bt.n_req) return;
+// The decision for request i, by one warp, once all its row partials exist.
+__device__ void decide_request(const Args& a, int i, DecideSmem& sm) {
+  const int lane = threadIdx.x & 31;
   Job* job = reinterpret_cast<Job*>(a.ws + a.L.jobs) + i;
   if (a.T > 0.f && lane == 0) {
     // Only jobs created by this call may reach the race kernel.
     job->mode = 0;
-    reinterpret_cast<int*>(a.ws + a.L.tickets)[i] = 0;
+    reinterpret_cast<int*>(a.ws + a.L.race_tickets)[i] = 0;
   }
   const Window w = window_of(a.bt, i);
-  if (!w.ok) {
-    if (lane == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-    return;
-  }
-  if (w.b >= w.e) return;
   const int cu = a.bt.cu_rows[i];
   const int V = a.V;
   bool chain = true, badp = false, badt = false;
@@ -282,13 +264,9 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
   int32_t* nodes = a.accepted_nodes + (size_t)i * max_rows;
   if (w.b == 0) {
     for (int k = lane; k < max_rows; k += 32) nodes[k] = k == 0 ? 0 : -1;
-  } else {
-    const int nt = a.next_token[i], al = a.accepted_len[i];
-    if (nt >= 0) return;  // decided in an earlier window
-    if (al != w.b) {
-      if (lane == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-      return;
-    }
+  } else if (a.accepted_len[i] != w.b) {
+    if (lane == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+    return;
   }
   int len = w.b;   // accepted drafts so far
   int next = -1;
@@ -301,7 +279,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
       int idx;
       row_argmax(a, cu + r, v, idx);
       if (lane == 0) {
-        s_am[warp][r] = idx;
+        sm.am[r] = idx;
         if (rs) {
           rs[(size_t)(cu + r) * 4 + 0] = v;
           rs[(size_t)(cu + r) * 4 + 1] = (float)idx;
@@ -313,7 +291,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
       if (lane == 0) {
         const int jmax = min(w.e, w.lim - 1);
         for (int j = w.b + 1; j <= jmax; ++j) {
-          const int am = s_am[warp][j - 1];
+          const int am = sm.am[j - 1];
           if (a.bt.tokens[cu + j] == am) {
             len = j;
             nodes[j] = j;
@@ -322,15 +300,15 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
             break;
           }
         }
-        if (next < 0 && w.e == w.lim && len == w.lim - 1) next = s_am[warp][w.lim - 1];
+        if (next < 0 && w.e == w.lim && len == w.lim - 1) next = sm.am[w.lim - 1];
       }
     } else {
       // tree: longest valid path, lower node index on ties (bottom-up)
       for (int n = w.rows - 1; n >= 0; --n) {
         int best = 0, bc = -1;
         for (int c = n + 1 + lane; c < w.rows; c += 32) {
-          if (a.bt.parent[cu + c] == n && a.bt.tokens[cu + c] == s_am[warp][n]) {
-            const int cand = 1 + s_len[warp][c];
+          if (a.bt.parent[cu + c] == n && a.bt.tokens[cu + c] == sm.am[n]) {
+            const int cand = 1 + sm.len[c];
             if (cand > best || (cand == best && bc >= 0 && c < bc)) { best = cand; bc = c; }
           }
         }
@@ -341,19 +319,19 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
           if (b2 > best || (b2 == best && c2 >= 0 && (bc < 0 || c2 < bc))) { best = b2; bc = c2; }
         }
         if (lane == 0) {
-          s_len[warp][n] = best;
-          s_child[warp][n] = bc;
+          sm.len[n] = best;
+          sm.child[n] = bc;
         }
         __syncwarp();
       }
       if (lane == 0) {
         int n = 0, k = 0;
-        while (s_child[warp][n] >= 0) {
-          n = s_child[warp][n];
+        while (sm.child[n] >= 0) {
+          n = sm.child[n];
           nodes[++k] = n;
         }
         len = k;
-        next = s_am[warp][n];
+        next = sm.am[n];
       }
     }
     if (lane == 0) {
@@ -371,69 +349,209 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
     float m, l;
     row_ml(a, cu + r, 0, m, l);
     if (lane == 0) {
-      s_mp[warp][r] = m;
-      s_lp[warp][r] = l;
+      sm.mp[r] = m;
+      sm.lp[r] = l;
       if (rs) rs[(size_t)(cu + r) * 4 + 0] = m + logf(l);
     }
     if (r + 1 <= w.lim - 1) {
       row_ml(a, cu + r, 1, m, l);
       if (lane == 0) {
-        s_mq[warp][r] = m;
-        s_lq[warp][r] = l;
+        sm.mq[r] = m;
+        sm.lq[r] = l;
         if (rs) rs[(size_t)(cu + r) * 4 + 1] = m + logf(l);
       }
     }
   }
   __syncwarp();
-  if (lane != 0) return;
+  // Lane j - b - 1 evaluates draft j's ratio; lane 0 then scans them.
   const float T = a.T;
+  const int nd = jmax - w.b;  // drafts decided by this window
+  double ratio = 1.0;
+  {
+    const int j = w.b + 1 + lane;
+    if (lane < nd) {
+      const int x = a.bt.tokens[cu + j];
+      const size_t off = (size_t)(cu + j - 1) * V + x;
+      const float xp = a.target[off] / T;
+      const float xq = a.draft[off] / T;
+      const double p = exp((double)xp - (double)sm.mp[j - 1]) / (double)sm.lp[j - 1];
+      const double q = exp((double)xq - (double)sm.mq[j - 1]) / (double)sm.lq[j - 1];
+      ratio = q > 0.0 ? fmin(1.0, p / q) : 1.0;
+      if (rs) {
+        rs[(size_t)(cu + j) * 4 + 2] = (float)p;
+        rs[(size_t)(cu + j) * 4 + 3] = (float)q;
+      }
+    }
+  }
+  __syncwarp();
   Job jb;
   jb.mode = 0;
   jb.pad = 0;
-  for (int j = w.b + 1; j <= jmax; ++j) {
-    const int x = a.bt.tokens[cu + j];
-    const size_t off = (size_t)(cu + j - 1) * V + x;
-    const float xp = a.target[off] / T;
-    const float xq = a.draft[off] / T;
-    const double p = exp((double)xp - (double)s_mp[warp][j - 1]) / (double)s_lp[warp][j - 1];
-    const double q = exp((double)xq - (double)s_mq[warp][j - 1]) / (double)s_lq[warp][j - 1];
-    if (rs) {
-      rs[(size_t)(cu + j) * 4 + 2] = (float)p;
-      rs[(size_t)(cu + j) * 4 + 3] = (float)q;
+  for (int k = 0; k < nd; ++k) {
+    const int j = w.b + 1 + k;
+    const double rk = __shfl_sync(0xffffffffu, ratio, k & 31);
+    if (k >= 32) {  // windows longer than a warp: evaluate the rest serially
+      const int x = a.bt.tokens[cu + j];
+      const size_t off = (size_t)(cu + j - 1) * V + x;
+      const double p = exp((double)(a.target[off] / T) - (double)sm.mp[j - 1]) / (double)sm.lp[j - 1];
+      const double q = exp((double)(a.draft[off] / T) - (double)sm.mq[j - 1]) / (double)sm.lq[j - 1];
+      ratio = q > 0.0 ? fmin(1.0, p / q) : 1.0;
+      if (rs && lane == 0) {
+        rs[(size_t)(cu + j) * 4 + 2] = (float)p;
+        rs[(size_t)(cu + j) * 4 + 3] = (float)q;
+      }
     }
-    const double ratio = q > 0.0 ? fmin(1.0, p / q) : 1.0;
+    const double r_j = k >= 32 ? ratio : rk;
     const double u = (double)accept_u(a.seed, i, j);
-    if (fabs(u - ratio) < 1e-6) amb = true;
-    if (u < ratio) {
+    if (fabs(u - r_j) < 1e-6) amb = true;
+    if (u < r_j) {
       len = j;
-      nodes[j] = j;
+      if (lane == 0) nodes[j] = j;
     } else {
       jb.mode = 1;
       jb.row = cu + j - 1;
       jb.pos = j;
-      jb.mp = s_mp[warp][j - 1];
-      jb.lp = s_lp[warp][j - 1];
-      jb.mq = s_mq[warp][j - 1];
-      jb.lq = s_lq[warp][j - 1];
+      jb.mp = sm.mp[j - 1];
+      jb.lp = sm.lp[j - 1];
+      jb.mq = sm.mq[j - 1];
+      jb.lq = sm.lq[j - 1];
       break;
     }
   }
+  if (lane != 0) return;
   if (jb.mode == 0 && w.e == w.lim && len == w.lim - 1) {
     jb.mode = 2;
     jb.row = cu + w.lim - 1;
     jb.pos = w.lim;
-    jb.mp = s_mp[warp][w.lim - 1];
-    jb.lp = s_lp[warp][w.lim - 1];
+    jb.mp = sm.mp[w.lim - 1];
+    jb.lp = sm.lp[w.lim - 1];
     jb.mq = 0.f;
     jb.lq = 1.f;
   }
   *job = jb;
-  reinterpret_cast<int*>(a.ws + a.L.tickets)[i] = 0;
   a.accepted_len[i] = len;
   a.next_token[i] = -1;
   if (w.b == 0) a.ambiguous[i] = 0;
   if (amb) a.ambiguous[i] = 1;
   if (a.done) a.done[i] = jb.mode != 0 ? 1 : 0;
+}
+
+// ----------------------------------------------------------------- stats --
+template <bool VEC>
+__global__ void __launch_bounds__(kStatThreads) stats_kernel(Args a) {
+  __shared__ float s_m[kStatThreads / 32], s_l[kStatThreads / 32];
+  __shared__ int s_i[kStatThreads / 32];
+  __shared__ int s_last;
+  __shared__ DecideSmem s_dec;
+  const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
+  int* tickets = reinterpret_cast<int*>(a.ws + a.L.stat_tickets);
+  const int R = a.bt.n_req;
+  const int count = act[R];
+  const int nch = a.L.nch, maxw = a.L.maxw;
+  const float T = a.T;
+  const int ntypes = T > 0.f ? 2 : 1;
+  const long total = (long)count * maxw * ntypes * nch;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (long item = blockIdx.x; item < total; item += gridDim.x) {
+    const int c = (int)(item % nch);
+    const long rest = item / nch;
+    const int type = (int)(rest % ntypes);
+    const long ro = rest / ntypes;
+    const int off = (int)(ro % maxw);
+    const int ai = (int)(ro / maxw);
+    const int i = act[ai];
+    const Window w = window_of(a.bt, i);
+    const int j = w.b + off;
+    if (j >= w.e) continue;
+    const int ndraft = T > 0.f ? max(0, min(w.e, w.lim - 1) - w.b) : 0;
+    if (type == 1 && off >= ndraft) continue;
+    const int r = a.bt.cu_rows[i] + j;
+    const float* row = (type ? a.draft : a.target) + (size_t)r * a.V;
+    const int lo = c * a.L.ch;
+    const int hi = min(a.V, lo + a.L.ch);
+    float m = -INFINITY, l = 0.f;
+    int am = 0x7fffffff;
+    if (T > 0.f) {
+      // x = logit / T; exp(x - m) as 2^((x - m) log2 e).  These only build
+      // the normaliser: the decision recomputes its own x with an exact
+      // division and exp in fp64.
+      const bool unit = T == 1.f;
+      const float rT = 1.f / T;
+      if (VEC) {
+        const float4* p4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 4
+        for (int v = lo + 4 * threadIdx.x; v < hi; v += 4 * kStatThreads) {
+          const float4 x4 = __ldcs(p4 + (v >> 2));
+          const float x0 = unit ? x4.x : div_by(x4.x, T, rT), x1 = unit ? x4.y : div_by(x4.y, T, rT);
+          const float x2 = unit ? x4.z : div_by(x4.z, T, rT), x3 = unit ? x4.w : div_by(x4.w, T, rT);
+          const float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+          if (mx > m) {
+            l *= ex2((m - mx) * kLog2e);
+            m = mx;
+          }
+          const float mb = m * kLog2e;
+          l += (ex2(fmaf(x0, kLog2e, -mb)) + ex2(fmaf(x1, kLog2e, -mb))) +
+               (ex2(fmaf(x2, kLog2e, -mb)) + ex2(fmaf(x3, kLog2e, -mb)));
+        }
+      } else {
+        for (int v = lo + threadIdx.x; v < hi; v += kStatThreads) {
+          const float x = unit ? row[v] : div_by(row[v], T, rT);
+          if (x > m) {
+            l *= ex2((m - x) * kLog2e);
+            m = x;
+          }
+          l += ex2((x - m) * kLog2e);
+        }
+      }
+    } else {
+      if (VEC) {
+        const float4* p4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 4
+        for (int v = lo + 4 * threadIdx.x; v < hi; v += 4 * kStatThreads) {
+          const float4 x4 = __ldcs(p4 + (v >> 2));
+          if (x4.x > m) { m = x4.x; am = v; }
+          if (x4.y > m) { m = x4.y; am = v + 1; }
+          if (x4.z > m) { m = x4.z; am = v + 2; }
+          if (x4.w > m) { m = x4.w; am = v + 3; }
+        }
+      } else {
+        for (int v = lo + threadIdx.x; v < hi; v += kStatThreads) {
+          const float x = row[v];
+          if (x > m) { m = x; am = v; }
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, am, o);
+      if (T > 0.f) merge_ml(m, l, m2, l2); else merge_am(m, am, m2, i2);
+    }
+    if (lane == 0) { s_m[wid] = m; s_l[wid] = l; s_i[wid] = am; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int k = 1; k < kStatThreads / 32; ++k) {
+        if (T > 0.f) merge_ml(m, l, s_m[k], s_l[k]); else merge_am(m, am, s_m[k], s_i[k]);
+      }
+      StatPart sp;
+      sp.m = m;
+      sp.l = l;
+      sp.amax = am;
+      sp.pad = 0;
+      reinterpret_cast<StatPart*>(a.ws + a.L.parts)[((size_t)r * 2 + type) * nch + c] = sp;
+      __threadfence();
+      const int expected = nch * ((w.e - w.b) + ndraft);
+      const int prev = atomicAdd(tickets + i, 1);
+      s_last = prev == expected - 1;
+    }
+    __syncthreads();
+    if (s_last && wid == 0) {
+      __threadfence();
+      decide_request(a, i, s_dec);
+    }
+    __syncthreads();
+  }
 }
 
 // ------------------------------------------------------------------ race --
@@ -443,108 +561,121 @@ __device__ __forceinline__ void race_take(float& best, int& bi, float key, int v
 
 template <bool VEC>
 __global__ void __launch_bounds__(kRaceThreads) race_kernel(Args a) {
-  const int nch = a.L.nch_r;
-  const int c = blockIdx.x % nch;
-  const int i = blockIdx.x / nch;
-  // decide_kernel clears every request's job before it can return early,
-  // so a non-zero mode here was written by this call.
-  const Job jb = reinterpret_cast<const Job*>(a.ws + a.L.jobs)[i];
-  if (jb.mode == 0) return;
-  const float T = a.T;
-  const bool resid = jb.mode == 1;
-  const float* lp = a.target + (size_t)jb.row * a.V;
-  const float* lq = a.draft + (size_t)jb.row * a.V;
-  const float inv_lp = 1.f / jb.lp, inv_lq = 1.f / jb.lq;
-  const int lo = c * a.L.ch_r;
-  const int hi = min(a.V, lo + a.L.ch_r);
-  float best = -1.f;
-  int bi = 0x7fffffff;
-  if (VEC) {
-    for (int v = lo + 4 * threadIdx.x; v < hi; v += 4 * kRaceThreads) {
-      const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
-      const float4 xp = __ldcs(reinterpret_cast<const float4*>(lp) + (v >> 2));
-      float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (resid) xq = __ldcs(reinterpret_cast<const float4*>(lq) + (v >> 2));
-      const float pv[4] = {xp.x, xp.y, xp.z, xp.w};
-      const float qv[4] = {xq.x, xq.y, xq.z, xq.w};
-      const uint32_t bv[4] = {bits.a, bits.b, bits.c, bits.d};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p = expf(pv[e] / T - jb.mp) * inv_lp;
-        float wv = p;
-        if (resid) wv = fmaxf(p - expf(qv[e] / T - jb.mq) * inv_lq, 0.f);
-        const float E = -logf(race_u(bv[e]));
-        race_take(best, bi, wv / E, v + e);
-      }
-    }
-  } else {
-    for (int v = lo + threadIdx.x; v < hi; v += kRaceThreads) {
-      const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
-      const uint32_t bw = (v & 3) == 0 ? bits.a : (v & 3) == 1 ? bits.b : (v & 3) == 2 ? bits.c : bits.d;
-      const float p = expf(lp[v] / T - jb.mp) * inv_lp;
-      float wv = p;
-      if (resid) wv = fmaxf(p - expf(lq[v] / T - jb.mq) * inv_lq, 0.f);
-      const float E = -logf(race_u(bw));
-      race_take(best, bi, wv / E, v);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-    race_take(best, bi, b2, i2);
-  }
   __shared__ float s_b[kRaceThreads / 32];
   __shared__ int s_i[kRaceThreads / 32];
   __shared__ int s_last;
+  const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
+  const int R = a.bt.n_req;
+  const int count = act[R];
+  const int nch = a.L.nch_r;
+  const long total = (long)count * nch;
+  const float T = a.T;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (lane == 0) { s_b[wid] = best; s_i[wid] = bi; }
-  __syncthreads();
-  RacePart* parts = reinterpret_cast<RacePart*>(a.ws + a.L.race) + (size_t)i * nch;
-  int* ticket = reinterpret_cast<int*>(a.ws + a.L.tickets) + i;
-  if (threadIdx.x == 0) {
-    for (int k = 1; k < kRaceThreads / 32; ++k) race_take(best, bi, s_b[k], s_i[k]);
-    parts[c].key = best;
-    parts[c].idx = bi;
-    __threadfence();
-    s_last = atomicAdd(ticket, 1) == nch - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  // last CTA of request i: reduce the chunk winners
-  if (threadIdx.x < 32) {
-    float b = -1.f;
-    int x = 0x7fffffff;
-    for (int k = lane; k < nch; k += 32) race_take(b, x, __ldcg(&parts[k].key), __ldcg(&parts[k].idx));
+  for (long item = blockIdx.x; item < total; item += gridDim.x) {
+    const int c = (int)(item % nch);
+    const int i = act[item / nch];
+    // decide_request cleared every listed request's job before it could
+    // return early, so a non-zero mode here was written by this call.
+    const Job jb = reinterpret_cast<const Job*>(a.ws + a.L.jobs)[i];
+    if (jb.mode == 0) continue;
+    const bool resid = jb.mode == 1;
+    const float* lp = a.target + (size_t)jb.row * a.V;
+    const float* lq = a.draft + (size_t)jb.row * a.V;
+    const float inv_lp = 1.f / jb.lp, inv_lq = 1.f / jb.lq;
+    const float rT = 1.f / T;
+    const float mpb = jb.mp * kLog2e, mqb = jb.mq * kLog2e;
+    const int lo = c * a.L.ch_r;
+    const int hi = min(a.V, lo + a.L.ch_r);
+    // Running best of this thread as (w, E): v beats it iff w_v E_b > w_b E_v.
+    // E_v >= kEmin for every uniform the generator can produce, so an entry
+    // with w_v < w_b / E_b * kEmin can never win: groups of four such entries
+    // skip the generator and the logarithm.
+    const float kEmin = 5.9e-8f;  // -log(1 - 2^-24) = 5.96e-8, rounded down
+    float bw = -1.f, bE = 1.f, thr = -1.f;
+    int bi = 0x7fffffff;
+    auto take = [&](float wv, float E, int v) {
+      const float lhs = wv * bE, rhs = bw * E;
+      if (lhs > rhs || (lhs == rhs && v < bi)) {
+        bw = wv;
+        bE = E;
+        bi = v;
+        thr = wv / E * kEmin;
+      }
+    };
+    auto weight = [&](float lpv, float lqv) {
+      const float p = ex2(fmaf(div_by(lpv, T, rT), kLog2e, -mpb)) * inv_lp;
+      if (!resid) return p;
+      return fmaxf(p - ex2(fmaf(div_by(lqv, T, rT), kLog2e, -mqb)) * inv_lq, 0.f);
+    };
+    if (VEC) {
+      for (int v = lo + 4 * threadIdx.x; v < hi; v += 4 * kRaceThreads) {
+        const float4 xp = __ldcs(reinterpret_cast<const float4*>(lp) + (v >> 2));
+        float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (resid) xq = __ldcs(reinterpret_cast<const float4*>(lq) + (v >> 2));
+        const float w0 = weight(xp.x, xq.x), w1 = weight(xp.y, xq.y);
+        const float w2 = weight(xp.z, xq.z), w3 = weight(xp.w, xq.w);
+        if (fmaxf(fmaxf(w0, w1), fmaxf(w2, w3)) < thr) continue;
+        const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
+        take(w0, -logf(race_u(bits.a)), v);
+        take(w1, -logf(race_u(bits.b)), v + 1);
+        take(w2, -logf(race_u(bits.c)), v + 2);
+        take(w3, -logf(race_u(bits.d)), v + 3);
+      }
+    } else {
+      for (int v = lo + threadIdx.x; v < hi; v += kRaceThreads) {
+        const float wv = weight(lp[v], resid ? lq[v] : 0.f);
+        if (wv < thr) continue;
+        const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
+        const uint32_t bw4 = (v & 3) == 0 ? bits.a : (v & 3) == 1 ? bits.b : (v & 3) == 2 ? bits.c : bits.d;
+        take(wv, -logf(race_u(bw4)), v);
+      }
+    }
+    float best = bi == 0x7fffffff ? -1.f : bw / bE;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float b2 = __shfl_xor_sync(0xffffffffu, b, o);
-      const int i2 = __shfl_xor_sync(0xffffffffu, x, o);
-      race_take(b, x, b2, i2);
+      const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      race_take(best, bi, b2, i2);
     }
-    if (lane == 0) {
-      a.next_token[i] = x;
-      *ticket = 0;
+    if (lane == 0) { s_b[wid] = best; s_i[wid] = bi; }
+    __syncthreads();
+    RacePart* parts = reinterpret_cast<RacePart*>(a.ws + a.L.race) + (size_t)i * nch;
+    int* ticket = reinterpret_cast<int*>(a.ws + a.L.race_tickets) + i;
+    if (threadIdx.x == 0) {
+      for (int k = 1; k < kRaceThreads / 32; ++k) race_take(best, bi, s_b[k], s_i[k]);
+      parts[c].key = best;
+      parts[c].idx = bi;
+      __threadfence();
+      s_last = atomicAdd(ticket, 1) == nch - 1;
     }
+    __syncthreads();
+    if (s_last && wid == 0) {
+      // last CTA of request i: reduce the chunk winners
+      float b = -1.f;
+      int x = 0x7fffffff;
+      for (int k = lane; k < nch; k += 32) race_take(b, x, __ldcg(&parts[k].key), __ldcg(&parts[k].idx));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float b2 = __shfl_xor_sync(0xffffffffu, b, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, x, o);
+        race_take(b, x, b2, i2);
+      }
+      if (lane == 0) {
+        a.next_token[i] = x;
+        *ticket = 0;
+      }
+    }
+    __syncthreads();
   }
 }
 
-}  // namespace acc
-}  // namespace sv
+// ------------------------------------------------------------------ host --
 
-using namespace sv;
-
-extern "C" size_t sv_accept_workspace(const sv_batch* bt, int32_t vocab) {
-  if (!bt || bt->n_req < 0 || bt->total_rows < 0 || vocab < 1) return 0;
-  return acc::layout(bt->n_req, bt->total_rows, vocab).total;
-}
-
-extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
-                               const float* draft_logits, int32_t vocab, float temperature,
-                               uint64_t seed, int32_t* accepted_len, int32_t* accepted_nodes,
-                               int32_t* next_token, uint8_t* ambiguous, int32_t* done,
-                               float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status,
-                               void* stream) {
+static sv_status check_accept_args(const sv_batch* bt, const float* target_logits,
+                                   const float* draft_logits, int32_t vocab, float temperature,
+                                   const int32_t* accepted_len, const int32_t* accepted_nodes,
+                                   const int32_t* next_token, const uint8_t* ambiguous,
+                                   const void* ws) {
   if (!bt || bt->n_req < 0 || bt->total_rows < 0 || vocab < 1) return SV_ERR_INVALID_ARGUMENT;
   if (!(temperature >= 0.f) || isinf(temperature)) return SV_ERR_INVALID_ARGUMENT;
   if (bt->max_rows_per_req < 1) return SV_ERR_INVALID_ARGUMENT;
@@ -555,7 +686,36 @@ extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
     return SV_ERR_INVALID_ARGUMENT;
   if (temperature > 0.f && !draft_logits) return SV_ERR_INVALID_ARGUMENT;
   if ((uintptr_t)ws & 255) return SV_ERR_INVALID_ARGUMENT;
-  acc::Args a;
+  return SV_OK;
+}
+
+sv_status chunk_list(const sv_batch* bt, int chunk, int cs, const int32_t* done, int32_t* rb,
+                     int32_t* re, int32_t vocab, void* ws, int32_t* dev_status, cudaStream_t s) {
+  if (!bt || chunk < 0 || cs < 1 || !rb || !re || !ws) return SV_ERR_INVALID_ARGUMENT;
+  if (chunk > 0 && !done) return SV_ERR_INVALID_ARGUMENT;
+  if (bt->n_req == 0) return SV_OK;
+  Args a{};
+  a.bt = *bt;
+  a.V = vocab;
+  a.ws = static_cast<uint8_t*>(ws);
+  a.L = layout(bt->n_req, bt->total_rows, vocab, cs);
+  a.dev_status = dev_status;
+  list_kernel<<<1, 1024, 0, s>>>(a, chunk, cs, done, rb, re);
+  SV_LAUNCH_CHECK();
+  return SV_OK;
+}
+
+// Enqueue the list pass (unless prebuilt), the statistics with the fused
+// decision, and the race.
+sv_status run(const sv_batch* bt, const float* target_logits, const float* draft_logits,
+              int32_t vocab, float temperature, uint64_t seed, int32_t* accepted_len,
+              int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
+              float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s,
+              int maxw, bool prebuilt_list) {
+  sv_status st = check_accept_args(bt, target_logits, draft_logits, vocab, temperature,
+                                   accepted_len, accepted_nodes, next_token, ambiguous, ws);
+  if (st != SV_OK || bt->n_req == 0 || bt->total_rows == 0) return st;
+  Args a;
   a.bt = *bt;
   a.target = target_logits;
   a.draft = draft_logits;
@@ -569,26 +729,50 @@ extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
   a.done = done;
   a.row_stats = row_stats;
   a.ws = static_cast<uint8_t*>(ws);
-  a.L = acc::layout(bt->n_req, bt->total_rows, vocab);
+  a.L = layout(bt->n_req, bt->total_rows, vocab, maxw);
   a.dev_status = dev_status;
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   const bool vec = (vocab % 4 == 0) && ((((uintptr_t)target_logits) |
                                          ((uintptr_t)(draft_logits ? draft_logits : target_logits))) & 15) == 0;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 gs((unsigned)((long)bt->total_rows * a.L.nch), temperature > 0.f ? 2 : 1);
-  if (vec) acc::stats_kernel<true><<<gs, acc::kStatThreads, 0, s>>>(a);
-  else acc::stats_kernel<false><<<gs, acc::kStatThreads, 0, s>>>(a);
-  SV_LAUNCH_CHECK();
-  acc::decide_kernel<<<(bt->n_req + acc::kDecideWarps - 1) / acc::kDecideWarps,
-                       acc::kDecideWarps * 32, 0, s>>>(a);
+  if (!prebuilt_list) {
+    list_kernel<<<1, 1024, 0, s>>>(a, -1, 0, nullptr, nullptr, nullptr);
+    SV_LAUNCH_CHECK();
+  }
+  const long items = (long)bt->n_req * a.L.maxw * (temperature > 0.f ? 2 : 1) * a.L.nch;
+  const unsigned gs = (unsigned)max(1L, min(items, (long)kNumSMs * 8));
+  if (vec) stats_kernel<true><<<gs, kStatThreads, 0, s>>>(a);
+  else stats_kernel<false><<<gs, kStatThreads, 0, s>>>(a);
   SV_LAUNCH_CHECK();
   if (temperature > 0.f) {
-    const unsigned gr = (unsigned)((long)bt->n_req * a.L.nch_r);
-    if (vec) acc::race_kernel<true><<<gr, acc::kRaceThreads, 0, s>>>(a);
-    else acc::race_kernel<false><<<gr, acc::kRaceThreads, 0, s>>>(a);
+    const long ritems = (long)bt->n_req * a.L.nch_r;
+    const unsigned gr = (unsigned)max(1L, min(ritems, (long)kNumSMs * 8));
+    if (vec) race_kernel<true><<<gr, kRaceThreads, 0, s>>>(a);
+    else race_kernel<false><<<gr, kRaceThreads, 0, s>>>(a);
     SV_LAUNCH_CHECK();
   }
   return SV_OK;
+}
+
+}  // namespace acc
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t sv_accept_workspace(const sv_batch* bt, int32_t vocab) {
+  if (!bt || bt->n_req < 0 || bt->total_rows < 0 || vocab < 1) return 0;
+  return acc::layout(bt->n_req, bt->total_rows, vocab, bt->max_rows_per_req).total;
+}
+
+extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
+                               const float* draft_logits, int32_t vocab, float temperature,
+                               uint64_t seed, int32_t* accepted_len, int32_t* accepted_nodes,
+                               int32_t* next_token, uint8_t* ambiguous, int32_t* done,
+                               float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status,
+                               void* stream) {
+  if (!bt) return SV_ERR_INVALID_ARGUMENT;
+  return acc::run(bt, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
+                  accepted_nodes, next_token, ambiguous, done, row_stats, ws, ws_bytes, dev_status,
+                  static_cast<cudaStream_t>(stream), bt->max_rows_per_req, false);
 }
 
 // ------------------------------------------------ no-allocation variant ----
@@ -599,8 +783,9 @@ extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
 // with that device current; make that first call before any stream capture.
 // All calls share the array: two calls whose work overlaps on the GPU (for
 // example on two streams) race on it.  Nothing in it has to start at zero:
-// the accept kernels write every scratch word before they read it (the
-// decide kernel clears each request's sampling job and ticket itself).
+// the accept kernels write every scratch word before they read it (the list
+// pass clears each listed request's ticket, the decision clears its sampling
+// job and race ticket).
 
 #include <mutex>
 

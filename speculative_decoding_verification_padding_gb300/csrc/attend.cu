@@ -42,6 +42,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTileRows = 64;    // virtual rows per unit
 constexpr int kUnitTarget = kNumSMs * 8;
 constexpr int kMinPagesPerSplit = 8;
+constexpr int kMaxPagesPerSplit = 1024;  // block ids of a unit staged in shared memory
 
 struct ReqInfo {
   int ubase, nsplit, nrt, b, e, ctx, nblk, valid;
@@ -54,22 +55,26 @@ struct Header {
 };
 
 struct Layout {
-  size_t header, info, ubase, tickets, ml, o, total;
+  size_t header, info, ubase, ureq, tickets, ml, o, total;
   int ucap;
 };
 
-inline int unit_cap(int R, int total_rows, int group, int Hkv) {
+// Units are at most W / P + Hkv * (row tiles): P >= W / kUnitTarget unless it
+// is capped at kMaxPagesPerSplit, and W <= Hkv * (row tiles) * max_blocks.
+inline int unit_cap(int R, int total_rows, int group, int Hkv, int max_blocks) {
   long nrt = (long)group * total_rows / kTileRows + R + 1;
-  return (int)((long)Hkv * nrt + kUnitTarget);
+  long rt_units = (long)Hkv * nrt;
+  return (int)(rt_units + kUnitTarget + (rt_units * max_blocks + kMaxPagesPerSplit - 1) / kMaxPagesPerSplit);
 }
 
-inline Layout layout(int R, int total_rows, int group, int Hkv, int D) {
+inline Layout layout(int R, int total_rows, int group, int Hkv, int D, int max_blocks) {
   Layout L;
   size_t off = 0;
-  L.ucap = unit_cap(R, total_rows, group, Hkv);
+  L.ucap = unit_cap(R, total_rows, group, Hkv, max_blocks);
   L.header = off; off += align256(sizeof(Header));
   L.info = off; off += align256(sizeof(ReqInfo) * (size_t)R);
   L.ubase = off; off += align256(sizeof(int) * (size_t)(R + 1));
+  L.ureq = off; off += align256(sizeof(int) * (size_t)L.ucap);
   L.tickets = off; off += align256(sizeof(int) * (size_t)L.ucap);
   L.ml = off; off += align256((size_t)L.ucap * kTileRows * 2 * sizeof(float));
   L.o = off; off += align256((size_t)L.ucap * kTileRows * (size_t)D * sizeof(float));
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   if (lane == 0 && myW) atomicAdd(&s_W, myW);
   __syncthreads();
   const unsigned long long W = s_W;
-  int P = (int)((W + kUnitTarget - 1) / kUnitTarget);
+  int P = (int)min((unsigned long long)kMaxPagesPerSplit, (W + kUnitTarget - 1) / kUnitTarget);
   if (P < kMinPagesPerSplit) P = kMinPagesPerSplit;
   // Work list offsets (exclusive scan of units per request).
   for (int base = 0; base < R; base += blockDim.x) {
@@ -216,6 +221,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     if (tid == 0) flag(a.dev_status, SV_DEV_BAD_LENGTH);
   }
   for (int u = tid; u < U; u += blockDim.x) tickets[u] = 0;
+  int* ureq = reinterpret_cast<int*>(a.ws + a.L.ureq);
+  if (U > 0)
+    for (int i = warp; i < R; i += 32) {
+      const int end = i + 1 < R ? ubase[i + 1] : U;
+      for (int x = ubase[i] + lane; x < end; x += 32) ureq[x] = i;
+    }
   if (tid == 0) {
     ubase[R] = U;
     hdr->U = U;
@@ -333,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __nv_bfloat16* smem = reinterpret_cast<__nv_bfloat16*>(smem_raw);
   __shared__ int s_par[kMaxRows];
+  __shared__ int s_tbl[kMaxPagesPerSplit];
   __shared__ unsigned long long s_mask[kTileRows][2];
   __shared__ int s_last;
   const Header* hdr = reinterpret_cast<const Header*>(a.ws + a.L.header);
@@ -340,11 +352,8 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(Args a) {
   const int u = blockIdx.x;
   if (u >= U) return;
   const int P = hdr->P;
-  const int R = a.bt.n_req;
   const ReqInfo* infos = reinterpret_cast<const ReqInfo*>(a.ws + a.L.info);
-  const int* ubase = reinterpret_cast<const int*>(a.ws + a.L.ubase);
-
-  const int i = find_segment(ubase, R, u);
+  const int i = reinterpret_cast<const int*>(a.ws + a.L.ureq)[u];
   const ReqInfo ri = infos[i];
   const int local = u - ri.ubase;
   const int s = local % ri.nsplit;
@@ -393,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(Args a) {
         const void* src = base;
         int bytes = 0;
         if (page < blk1 && tok < tok_end) {
-          const int bid = __ldg(table + page);
+          const int bid = s_tbl[page - blk0];
           if (bid >= 0 && bid < a.num_blocks) {
             src = base + (((size_t)bid * a.Hkv + g) * kBlockSize + (row & 15)) * D + col * 8;
             bytes = 16;
@@ -408,17 +417,23 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(Args a) {
     cp_async_commit();
   };
 
+  // Block ids of this unit's pages (and the request's parent links, if the
+  // unit reaches staged slots) into shared memory with one round trip.
+  const int r_first = vr0 / group;
+  const int r_count = (vr0 + Mu - 1) / group - r_first + 1;
+  const bool unit_masked = blk1 * kBlockSize > ctx;
+  for (int p = tid; p < blk1 - blk0; p += kThreads) s_tbl[p] = __ldg(table + blk0 + p);
+  if (unit_masked) {
+    const int rows = a.bt.cu_rows[i + 1] - cu;
+    for (int j = tid; j < rows; j += kThreads) s_par[j] = a.bt.parent[cu + j];
+  }
+  __syncthreads();
+
 #pragma unroll
   for (int st = 0; st < kStages - 1; ++st) issue(st);
 
   // Ancestor-or-self masks of the unit's rows, only if it reaches staged slots.
-  const int r_first = vr0 / group;
-  const int r_count = (vr0 + Mu - 1) / group - r_first + 1;
-  const bool unit_masked = blk1 * kBlockSize > ctx;
   if (unit_masked) {
-    const int rows = a.bt.cu_rows[i + 1] - cu;
-    for (int j = tid; j < rows; j += kThreads) s_par[j] = a.bt.parent[cu + j];
-    __syncthreads();
     for (int t = tid; t < r_count; t += kThreads) {
       unsigned long long lo = 0ull, hi = 0ull;
       int m = ri.b + r_first + t;
@@ -654,7 +669,8 @@ extern "C" size_t sv_tree_attend_workspace(const sv_batch* bt, const sv_paged_kv
                                            int32_t n_q_heads) {
   if (check_attend_args(bt, kv, n_q_heads) != SV_OK) return 0;
   const int group = n_q_heads / kv->n_kv_heads;
-  return attn::layout(bt->n_req, bt->total_rows, group, kv->n_kv_heads, kv->head_dim).total;
+  return attn::layout(bt->n_req, bt->total_rows, group, kv->n_kv_heads, kv->head_dim,
+                      kv->max_blocks_per_req).total;
 }
 
 extern "C" sv_status sv_tree_attend(const sv_paged_kv* kv, const sv_batch* bt, const void* q,
@@ -683,7 +699,8 @@ extern "C" sv_status sv_tree_attend(const sv_paged_kv* kv, const sv_batch* bt, c
   a.group = group;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.ws = static_cast<uint8_t*>(ws);
-  a.L = attn::layout(bt->n_req, bt->total_rows, group, kv->n_kv_heads, kv->head_dim);
+  a.L = attn::layout(bt->n_req, bt->total_rows, group, kv->n_kv_heads, kv->head_dim,
+                      kv->max_blocks_per_req);
   a.dev_status = dev_status;
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -11,6 +11,7 @@
 // done get an empty window, which every later kernel skips), then the
 // attention and accept calls run on those windows.
 
+#include "sv_accept_internal.h"
 #include "sv_internal.cuh"
 
 namespace sv {
@@ -72,11 +73,14 @@ extern "C" sv_status sv_chunk_windows(const sv_batch* bt, int32_t chunk_index, i
 
 extern "C" size_t sv_verify_chunked_workspace(const sv_batch* bt, const sv_paged_kv* kv,
                                               int32_t n_q_heads, int32_t vocab) {
-  if (!bt || !kv) return 0;
+  if (!bt || !kv || vocab < 1) return 0;
   const size_t wa = sv_tree_attend_workspace(bt, kv, n_q_heads);
-  const size_t wb = sv_accept_workspace(bt, vocab);
-  if (!wa || !wb) return 0;
-  return chk::windows_bytes(bt->n_req) + (wa > wb ? wa : wb);
+  if (!wa) return 0;
+  // The chunk size is not an argument here: the accept part is sized for
+  // one-row windows, the largest of its layouts (fewer rows per window give
+  // more vocabulary slices per row), so it fits every chunk size.
+  const size_t wb = acc::layout(bt->n_req, bt->total_rows, vocab, 1).total;
+  return chk::windows_bytes(bt->n_req) + align256(wb) + wa;
 }
 
 extern "C" sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* bt, const void* q,
@@ -90,30 +94,30 @@ extern "C" sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* bt
   if (!kv || !bt || chunk_size < 1 || !done) return SV_ERR_INVALID_ARGUMENT;
   if (bt->n_req < 0 || bt->max_rows_per_req < 1) return SV_ERR_INVALID_ARGUMENT;
   if (bt->n_req == 0 || bt->total_rows == 0) return SV_OK;
-  const size_t need = sv_verify_chunked_workspace(bt, kv, n_q_heads, vocab);
-  if (!need) return SV_ERR_INVALID_ARGUMENT;
+  const size_t wa = sv_tree_attend_workspace(bt, kv, n_q_heads);
+  if (!wa || vocab < 1) return SV_ERR_INVALID_ARGUMENT;
+  const acc::Layout AL = acc::layout(bt->n_req, bt->total_rows, vocab, chunk_size);
+  const size_t need = chk::windows_bytes(bt->n_req) + align256(AL.total) + wa;
   if (!ws || ((uintptr_t)ws & 255)) return SV_ERR_INVALID_ARGUMENT;
   if (ws_bytes < need) return SV_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* rb = reinterpret_cast<int32_t*>(w);
   int32_t* re = reinterpret_cast<int32_t*>(w + align256(sizeof(int32_t) * (size_t)bt->n_req));
-  uint8_t* inner = w + chk::windows_bytes(bt->n_req);
-  const size_t inner_bytes = ws_bytes - chk::windows_bytes(bt->n_req);
+  uint8_t* acc_ws = w + chk::windows_bytes(bt->n_req);
+  uint8_t* att_ws = acc_ws + align256(AL.total);
   sv_batch b2 = *bt;
   b2.row_begin = rb;
   b2.row_end = re;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int n_chunks = (bt->max_rows_per_req + chunk_size - 1) / chunk_size;
   for (int c = 0; c < n_chunks; ++c) {
-    chk::windows_kernel<<<(bt->n_req + 255) / 256, 256, 0, s>>>(*bt, c, chunk_size, done, rb, re,
-                                                                 dev_status);
-    SV_LAUNCH_CHECK();
-    sv_status st = sv_tree_attend(kv, &b2, q, n_q_heads, softmax_scale, out, inner, inner_bytes,
-                                  dev_status, stream);
+    sv_status st = acc::chunk_list(bt, c, chunk_size, done, rb, re, vocab, acc_ws, dev_status, s);
     if (st != SV_OK) return st;
-    st = sv_accept(&b2, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
-                   accepted_nodes, next_token, ambiguous, done, nullptr, inner, inner_bytes,
-                   dev_status, stream);
+    st = sv_tree_attend(kv, &b2, q, n_q_heads, softmax_scale, out, att_ws, wa, dev_status, stream);
+    if (st != SV_OK) return st;
+    st = acc::run(&b2, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
+                  accepted_nodes, next_token, ambiguous, done, nullptr, acc_ws, AL.total,
+                  dev_status, s, chunk_size, true);
     if (st != SV_OK) return st;
   }
   return SV_OK;

@@ -1,0 +1,37 @@
+// sv_accept_internal.h — accept entry points shared by accept.cu and the
+// chunk driver (host-side; not part of the public C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "libspecverify.h"
+
+namespace sv {
+namespace acc {
+
+// Workspace of the accept kernels for a batch whose windows hold at most
+// `maxw` rows per request.
+struct Layout {
+  size_t parts, jobs, race, race_tickets, stat_tickets, act, total;
+  int nch, nch_r, ch, ch_r, maxw;
+};
+Layout layout(int R, int total_rows, int V, int maxw);
+
+// Windows of chunk `chunk` (chunk size cs) from `done`, written to rb / re,
+// plus the list of requests with a non-empty window, into the accept
+// workspace `ws` laid out for (batch, vocab, maxw = cs).
+sv_status chunk_list(const sv_batch* bt, int chunk, int cs, const int32_t* done, int32_t* rb,
+                     int32_t* re, int32_t vocab, void* ws, int32_t* dev_status, cudaStream_t s);
+
+// The accept kernels.  prebuilt_list: the active list of `ws` was written by
+// chunk_list for this batch's windows (otherwise a list pass runs first).
+sv_status run(const sv_batch* bt, const float* target_logits, const float* draft_logits,
+              int32_t vocab, float temperature, uint64_t seed, int32_t* accepted_len,
+              int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
+              float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s,
+              int maxw, bool prebuilt_list);
+
+}  // namespace acc
+}  // namespace sv

@@ -98,6 +98,27 @@ __device__ __forceinline__ float race_u(uint32_t bits) {
   return ((float)(bits >> 9) + 0.5f) * 1.1920928955078125e-07f;  // 2^-23
 }
 
+// ------------------------------------------------------ fast arithmetic ----
+// x / d for a divisor d shared by many x, with r = 1 / d: the product x * r
+// corrected once by the exact residual x - q * d (an fma), after Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor" (IBM J. Res. Dev. 34(1), 1990).  Equal to the correctly rounded
+// quotient except in rare cases where it is one ulp away; used only where the
+// result feeds a normaliser, never a decision.
+__device__ __forceinline__ float div_by(float x, float d, float r) {
+  const float q = x * r;
+  const float e = fmaf(-q, d, x);
+  return fmaf(e, r, q);
+}
+
+// 2^x by the hardware approximation (relative error below 2^-22; results
+// below 2^-126 flush to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------- warp utils ----
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

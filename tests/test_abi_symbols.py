@@ -63,3 +63,19 @@ def test_host_side_validation_without_gpu(lib):
     assert need > 0
     assert lib.sv_tree_attend(ctypes.byref(kv), ctypes.byref(b), 256, 8, 0.125, 256, 256, need - 1,
                               None, None) == N.SV_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_static_scratch_holds_the_documented_batch(lib):
+    # sv_accept_static promises that any batch of up to 45,000 packed rows fits
+    # its fixed scratch array; sv_accept_workspace is a host function.
+    import ctypes
+    from speculative_decoding_verification_padding_gb300 import _native as N
+    worst = 0
+    for rows in (1, 100, 2432, 10000, 30000, 45000):
+        for per in (1, 2, 5, 9, 128):
+            R = max(1, rows // per)
+            for maxr in {min(128, per), 128}:
+                for V in (16, 1024, 128256, 151936, 262144):
+                    b = N.SvBatch(R, rows, maxr, 1, 1, 1, None, None, None)
+                    worst = max(worst, lib.sv_accept_workspace(ctypes.byref(b), V))
+    assert worst <= N.SV_ACCEPT_STATIC_SCRATCH_BYTES
