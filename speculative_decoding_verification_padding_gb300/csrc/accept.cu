@@ -59,14 +59,16 @@ constexpr int kStatThreads = 256;
 constexpr int kRaceThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Slices per row (stats) and per request (race): about 32 warps per SM in
+// flight, slices of at least 2 KB.
 inline int stats_chunks(int rows_bound, int V) {
-  const int maxc = max(1, min(64, V / 1024));
+  const int maxc = max(1, min(256, V / 512));
   const int want = (kNumSMs * 32 + 2 * rows_bound - 1) / max(1, 2 * rows_bound);
   return max(1, min(want, maxc));
 }
 inline int race_chunks(int R, int V) {
-  const int maxc = max(1, min(256, V / 1024));
-  const int want = (kNumSMs * 16 + R - 1) / max(1, R);
+  const int maxc = max(1, min(1024, V / 512));
+  const int want = (kNumSMs * 32 + R - 1) / max(1, R);
   return max(1, min(want, maxc));
 }
 inline int chunk_len(int V, int nch) { return ((V + nch - 1) / nch + 3) & ~3; }
@@ -437,12 +439,13 @@ __device__ void decide_request(const Args& a, int i, DecideSmem& sm) {
 }
 
 // ----------------------------------------------------------------- stats --
+// Warp-granular: every warp owns one slice of one row at a time, reduces it
+// with shuffles and arrives on its request's ticket itself, so no warp waits
+// for another; the warp that brings the last slice of a request runs the
+// decision for it.
 template <bool VEC>
-__global__ void __launch_bounds__(kStatThreads) stats_kernel(Args a) {
-  __shared__ float s_m[kStatThreads / 32], s_l[kStatThreads / 32];
-  __shared__ int s_i[kStatThreads / 32];
-  __shared__ int s_last;
-  __shared__ DecideSmem s_dec;
+__global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
+  __shared__ DecideSmem s_dec[kStatThreads / 32];
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   int* tickets = reinterpret_cast<int*>(a.ws + a.L.stat_tickets);
   const int R = a.bt.n_req;
@@ -452,14 +455,16 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(Args a) {
   const int ntypes = T > 0.f ? 2 : 1;
   const long total = (long)count * maxw * ntypes * nch;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (long item = blockIdx.x; item < total; item += gridDim.x) {
+  const long stride = (long)gridDim.x * (kStatThreads / 32);
+  const bool unit = T == 1.f;
+  const float rT = T > 0.f ? 1.f / T : 1.f;
+  for (long item = (long)blockIdx.x * (kStatThreads / 32) + wid; item < total; item += stride) {
     const int c = (int)(item % nch);
     const long rest = item / nch;
     const int type = (int)(rest % ntypes);
     const long ro = rest / ntypes;
     const int off = (int)(ro % maxw);
-    const int ai = (int)(ro / maxw);
-    const int i = act[ai];
+    const int i = act[ro / maxw];
     const Window w = window_of(a.bt, i);
     const int j = w.b + off;
     if (j >= w.e) continue;
@@ -475,12 +480,10 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(Args a) {
       // x = logit / T; exp(x - m) as 2^((x - m) log2 e).  These only build
       // the normaliser: the decision recomputes its own x with an exact
       // division and exp in fp64.
-      const bool unit = T == 1.f;
-      const float rT = 1.f / T;
       if (VEC) {
         const float4* p4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 4
-        for (int v = lo + 4 * threadIdx.x; v < hi; v += 4 * kStatThreads) {
+#pragma unroll 8
+        for (int v = lo + 4 * lane; v < hi; v += 128) {
           const float4 x4 = __ldcs(p4 + (v >> 2));
           const float x0 = unit ? x4.x : div_by(x4.x, T, rT), x1 = unit ? x4.y : div_by(x4.y, T, rT);
           const float x2 = unit ? x4.z : div_by(x4.z, T, rT), x3 = unit ? x4.w : div_by(x4.w, T, rT);
@@ -494,7 +497,7 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(Args a) {
                (ex2(fmaf(x2, kLog2e, -mb)) + ex2(fmaf(x3, kLog2e, -mb)));
         }
       } else {
-        for (int v = lo + threadIdx.x; v < hi; v += kStatThreads) {
+        for (int v = lo + lane; v < hi; v += 32) {
           const float x = unit ? row[v] : div_by(row[v], T, rT);
           if (x > m) {
             l *= ex2((m - x) * kLog2e);
@@ -506,8 +509,8 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(Args a) {
     } else {
       if (VEC) {
         const float4* p4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 4
-        for (int v = lo + 4 * threadIdx.x; v < hi; v += 4 * kStatThreads) {
+#pragma unroll 8
+        for (int v = lo + 4 * lane; v < hi; v += 128) {
           const float4 x4 = __ldcs(p4 + (v >> 2));
           if (x4.x > m) { m = x4.x; am = v; }
           if (x4.y > m) { m = x4.y; am = v + 1; }
@@ -515,7 +518,7 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(Args a) {
           if (x4.w > m) { m = x4.w; am = v + 3; }
         }
       } else {
-        for (int v = lo + threadIdx.x; v < hi; v += kStatThreads) {
+        for (int v = lo + lane; v < hi; v += 32) {
           const float x = row[v];
           if (x > m) { m = x; am = v; }
         }
@@ -528,12 +531,8 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(Args a) {
       const int i2 = __shfl_xor_sync(0xffffffffu, am, o);
       if (T > 0.f) merge_ml(m, l, m2, l2); else merge_am(m, am, m2, i2);
     }
-    if (lane == 0) { s_m[wid] = m; s_l[wid] = l; s_i[wid] = am; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int k = 1; k < kStatThreads / 32; ++k) {
-        if (T > 0.f) merge_ml(m, l, s_m[k], s_l[k]); else merge_am(m, am, s_m[k], s_i[k]);
-      }
+    int last = 0;
+    if (lane == 0) {
       StatPart sp;
       sp.m = m;
       sp.l = l;
@@ -542,15 +541,13 @@ __global__ void __launch_bounds__(kStatThreads) stats_kernel(Args a) {
       reinterpret_cast<StatPart*>(a.ws + a.L.parts)[((size_t)r * 2 + type) * nch + c] = sp;
       __threadfence();
       const int expected = nch * ((w.e - w.b) + ndraft);
-      const int prev = atomicAdd(tickets + i, 1);
-      s_last = prev == expected - 1;
+      last = atomicAdd(tickets + i, 1) == expected - 1;
     }
-    __syncthreads();
-    if (s_last && wid == 0) {
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
       __threadfence();
-      decide_request(a, i, s_dec);
+      decide_request(a, i, s_dec[wid]);
     }
-    __syncthreads();
   }
 }
 
@@ -559,19 +556,20 @@ __device__ __forceinline__ void race_take(float& best, int& bi, float key, int v
   if (key > best || (key == best && v < bi)) { best = key; bi = v; }
 }
 
+// Warp-granular like the statistics: a warp scans one slice of a request's
+// row(s) and arrives on the request's ticket; the last one reduces.
 template <bool VEC>
-__global__ void __launch_bounds__(kRaceThreads) race_kernel(Args a) {
-  __shared__ float s_b[kRaceThreads / 32];
-  __shared__ int s_i[kRaceThreads / 32];
-  __shared__ int s_last;
+__global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   const int R = a.bt.n_req;
   const int count = act[R];
   const int nch = a.L.nch_r;
   const long total = (long)count * nch;
   const float T = a.T;
+  const float rT = 1.f / T;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (long item = blockIdx.x; item < total; item += gridDim.x) {
+  const long stride = (long)gridDim.x * (kRaceThreads / 32);
+  for (long item = (long)blockIdx.x * (kRaceThreads / 32) + wid; item < total; item += stride) {
     const int c = (int)(item % nch);
     const int i = act[item / nch];
     // decide_request cleared every listed request's job before it could
@@ -582,11 +580,10 @@ __global__ void __launch_bounds__(kRaceThreads) race_kernel(Args a) {
     const float* lp = a.target + (size_t)jb.row * a.V;
     const float* lq = a.draft + (size_t)jb.row * a.V;
     const float inv_lp = 1.f / jb.lp, inv_lq = 1.f / jb.lq;
-    const float rT = 1.f / T;
     const float mpb = jb.mp * kLog2e, mqb = jb.mq * kLog2e;
     const int lo = c * a.L.ch_r;
     const int hi = min(a.V, lo + a.L.ch_r);
-    // Running best of this thread as (w, E): v beats it iff w_v E_b > w_b E_v.
+    // Running best of this lane as (w, E): v beats it iff w_v E_b > w_b E_v.
     // E_v >= kEmin for every uniform the generator can produce, so an entry
     // with w_v < w_b / E_b * kEmin can never win: groups of four such entries
     // skip the generator and the logarithm.
@@ -608,7 +605,7 @@ __global__ void __launch_bounds__(kRaceThreads) race_kernel(Args a) {
       return fmaxf(p - ex2(fmaf(div_by(lqv, T, rT), kLog2e, -mqb)) * inv_lq, 0.f);
     };
     if (VEC) {
-      for (int v = lo + 4 * threadIdx.x; v < hi; v += 4 * kRaceThreads) {
+      for (int v = lo + 4 * lane; v < hi; v += 128) {
         const float4 xp = __ldcs(reinterpret_cast<const float4*>(lp) + (v >> 2));
         float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
         if (resid) xq = __ldcs(reinterpret_cast<const float4*>(lq) + (v >> 2));
@@ -622,7 +619,7 @@ __global__ void __launch_bounds__(kRaceThreads) race_kernel(Args a) {
         take(w3, -logf(race_u(bits.d)), v + 3);
       }
     } else {
-      for (int v = lo + threadIdx.x; v < hi; v += kRaceThreads) {
+      for (int v = lo + lane; v < hi; v += 32) {
         const float wv = weight(lp[v], resid ? lq[v] : 0.f);
         if (wv < thr) continue;
         const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
@@ -637,20 +634,19 @@ __global__ void __launch_bounds__(kRaceThreads) race_kernel(Args a) {
       const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
       race_take(best, bi, b2, i2);
     }
-    if (lane == 0) { s_b[wid] = best; s_i[wid] = bi; }
-    __syncthreads();
     RacePart* parts = reinterpret_cast<RacePart*>(a.ws + a.L.race) + (size_t)i * nch;
     int* ticket = reinterpret_cast<int*>(a.ws + a.L.race_tickets) + i;
-    if (threadIdx.x == 0) {
-      for (int k = 1; k < kRaceThreads / 32; ++k) race_take(best, bi, s_b[k], s_i[k]);
+    int last = 0;
+    if (lane == 0) {
       parts[c].key = best;
       parts[c].idx = bi;
       __threadfence();
-      s_last = atomicAdd(ticket, 1) == nch - 1;
+      last = atomicAdd(ticket, 1) == nch - 1;
     }
-    __syncthreads();
-    if (s_last && wid == 0) {
-      // last CTA of request i: reduce the chunk winners
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      // last slice of request i: reduce the slice winners
+      __threadfence();
       float b = -1.f;
       int x = 0x7fffffff;
       for (int k = lane; k < nch; k += 32) race_take(b, x, __ldcg(&parts[k].key), __ldcg(&parts[k].idx));
@@ -665,7 +661,6 @@ __global__ void __launch_bounds__(kRaceThreads) race_kernel(Args a) {
         *ticket = 0;
       }
     }
-    __syncthreads();
   }
 }
 
@@ -739,13 +734,15 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
     SV_LAUNCH_CHECK();
   }
   const long items = (long)bt->n_req * a.L.maxw * (temperature > 0.f ? 2 : 1) * a.L.nch;
-  const unsigned gs = (unsigned)max(1L, min(items, (long)kNumSMs * 8));
+  const long warps = kStatThreads / 32;
+  const unsigned gs = (unsigned)max(1L, min((items + warps - 1) / warps, (long)kNumSMs * 4));
   if (vec) stats_kernel<true><<<gs, kStatThreads, 0, s>>>(a);
   else stats_kernel<false><<<gs, kStatThreads, 0, s>>>(a);
   SV_LAUNCH_CHECK();
   if (temperature > 0.f) {
     const long ritems = (long)bt->n_req * a.L.nch_r;
-    const unsigned gr = (unsigned)max(1L, min(ritems, (long)kNumSMs * 8));
+    const long rwarps = kRaceThreads / 32;
+    const unsigned gr = (unsigned)max(1L, min((ritems + rwarps - 1) / rwarps, (long)kNumSMs * 4));
     if (vec) race_kernel<true><<<gr, kRaceThreads, 0, s>>>(a);
     else race_kernel<false><<<gr, kRaceThreads, 0, s>>>(a);
     SV_LAUNCH_CHECK();

@@ -15,20 +15,27 @@
 //   attend (1 CTA per unit, 4 warps, 2 CTAs per SM)
 //                    the query rows of the whole GQA group (row x head packed
 //                    as "virtual rows") share every KV page.  Pages stream
-//                    through a 3-stage ring of 64-token stages (16-byte
-//                    cp.async copies into XOR-swizzled rows).  A warp owns a
-//                    16-row m-tile and a slice of each stage's tokens: with
-//                    one m-tile the four warps take 16 tokens each, with two
-//                    they take 32, with three or four every warp sees the
-//                    whole stage.  QK^T and PV run on mma.sync m16n8k16 bf16
-//                    -> fp32 with an online softmax in the log2 domain; the
-//                    ancestor mask (built per CTA from the parent links held
-//                    in shared memory) is applied only where staged draft
-//                    slots lie.  Warps that shared an m-tile merge through
-//                    shared memory.  A unit that covers all keys of its rows
-//                    writes bf16 output directly; otherwise it writes (m, l, O)
-//                    partials and the last CTA of the group (atomic ticket)
-//                    merges all splits and writes the output.
+//                    through a 3-stage ring of 64-token stages: thread 0
+//                    issues 2-D tiled TMA loads (cp.async.bulk.tensor, 128-byte
+//                    swizzle, one 64-element x 16-row box per half page) that
+//                    complete on an mbarrier per slot; the warps wait on it
+//                    with a bounded spin.  A warp owns a 16-row m-tile and a
+//                    slice of each stage's tokens: with one m-tile the four
+//                    warps take 16 tokens each, with two they take 32, with
+//                    three or four every warp sees the whole stage.  QK^T and
+//                    PV run on mma.sync m16n8k16 bf16 -> fp32 with an online
+//                    softmax in the log2 domain; the ancestor mask (built per
+//                    CTA from the parent links held in shared memory) is
+//                    applied only where staged draft slots lie.  Warps that
+//                    shared an m-tile merge through shared memory.  A unit
+//                    that covers all keys of its rows writes bf16 output
+//                    directly; otherwise it writes (m, l, O) partials and the
+//                    last CTA of the group (atomic ticket) merges all splits.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "sv_internal.cuh"
 
@@ -36,7 +43,7 @@ namespace sv {
 namespace attn {
 
 constexpr int kTB = 64;          // tokens per pipeline stage (four pages)
-constexpr int kStages = 3;       // cp.async ring depth
+constexpr int kStages = 3;       // TMA ring depth
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileRows = 64;    // virtual rows per unit
@@ -236,23 +243,37 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
 
 // ---------------------------------------------------------------- attend --
 
+// Shared-memory image of one stage: for K then V, 4 pages x (D / 64) boxes of
+// 16 rows x 128 bytes, as TMA writes them with the 128-byte swizzle (16-byte
+// chunk c of row r of a box stored at chunk c ^ (r % 8)).
+template <int D>
+struct StageLayout {
+  static constexpr int kHalves = D / 64;                 // boxes per page
+  static constexpr int kBoxBytes = 16 * 128;
+  static constexpr int kTensorBytes = 4 * kHalves * kBoxBytes;  // 64 tokens
+  static constexpr int kStageBytes = 2 * kTensorBytes;
+  // byte offset of (token t of the stage, 16-byte chunk c of the head dim)
+  __device__ static __forceinline__ uint32_t off(int t, int c) {
+    const int r = t & 15;
+    return (uint32_t)((((t >> 4) * kHalves + (c >> 3)) * kBoxBytes) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  }
+};
+
 template <int D>
 struct Frag {
   float o[D / 8][4];
   float m_a, m_b, l_a, l_b;
 };
 
-// One 64-token stage for a warp: its slice [slice0, slice0 + 64 / TS) of the
-// stage held at shared-memory addresses kbase (K) / vbase (V).
-template <int D, int TS>
-__device__ __forceinline__ void stage_compute(Frag<D>& f, const uint32_t (&qf)[D / 16][4],
-                                              uint32_t kbase, uint32_t vbase, int t0, int slice0,
+// NT * 8 tokens starting at stage row `s0` for this warp's two rows.
+template <int D, int NT>
+__device__ __forceinline__ void slice_compute(Frag<D>& f, const uint32_t (&qf)[D / 16][4],
+                                              uint32_t kbase, uint32_t vbase, int tfirst, int s0,
                                               int ctx, int tok_end, float scale_log2,
                                               unsigned long long mk_a0, unsigned long long mk_a1,
                                               unsigned long long mk_b0, unsigned long long mk_b1,
                                               int lane) {
-  constexpr int NT = kTB / TS / 8;   // 8-token n-tiles of the slice
-  constexpr int KK = kTB / TS / 16;  // 16-token k-steps of PV
+  using SL = StageLayout<D>;
   const int tq = lane & 3;
   float sc[NT][4];
 #pragma unroll
@@ -260,16 +281,16 @@ __device__ __forceinline__ void stage_compute(Frag<D>& f, const uint32_t (&qf)[D
     sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ks += 2) {
-      const int trow = slice0 + nt * 8 + (lane & 7);
+      const int trow = s0 + nt * 8 + (lane & 7);
       const int chunk = 2 * ks + (lane >> 3);
       uint32_t r[4];
-      ldsm_x4(r, kbase + (uint32_t)(trow * D + ((chunk ^ (trow & 7)) << 3)) * 2u);
+      ldsm_x4(r, kbase + SL::off(trow, chunk));
       mma16816(sc[nt], qf[ks], r[0], r[1]);
       mma16816(sc[nt], qf[ks + 1], r[2], r[3]);
     }
   }
-  const int tfirst = t0 + slice0;
-  const bool need_mask = (tfirst + kTB / TS > ctx) || (tfirst + kTB / TS > tok_end);
+  const int tbeg = tfirst + s0;
+  const bool need_mask = (tbeg + NT * 8 > ctx) || (tbeg + NT * 8 > tok_end);
   float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -277,7 +298,7 @@ __device__ __forceinline__ void stage_compute(Frag<D>& f, const uint32_t (&qf)[D
     for (int e = 0; e < 4; ++e) {
       float v = sc[nt][e] * scale_log2;
       if (need_mask) {
-        const int tok = tfirst + nt * 8 + 2 * tq + (e & 1);
+        const int tok = tbeg + nt * 8 + 2 * tq + (e & 1);
         bool ok = tok < tok_end;
         if (ok && tok >= ctx) {
           const int m = tok - ctx;
@@ -321,7 +342,7 @@ __device__ __forceinline__ void stage_compute(Frag<D>& f, const uint32_t (&qf)[D
     f.o[dn][3] *= al_b;
   }
 #pragma unroll
-  for (int kk = 0; kk < KK; ++kk) {
+  for (int kk = 0; kk < NT / 2; ++kk) {
     uint32_t pa[4];
     pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
     pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
@@ -329,10 +350,10 @@ __device__ __forceinline__ void stage_compute(Frag<D>& f, const uint32_t (&qf)[D
     pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
 #pragma unroll
     for (int dn = 0; dn < D / 8; dn += 2) {
-      const int trow = slice0 + 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int trow = s0 + 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
       const int chunk = dn + (lane >> 4);
       uint32_t r[4];
-      ldsm_x4_t(r, vbase + (uint32_t)(trow * D + ((chunk ^ (trow & 7)) << 3)) * 2u);
+      ldsm_x4_t(r, vbase + SL::off(trow, chunk));
       mma16816(f.o[dn], pa, r[0], r[1]);
       mma16816(f.o[dn + 1], pa, r[2], r[3]);
     }
@@ -340,12 +361,15 @@ __device__ __forceinline__ void stage_compute(Frag<D>& f, const uint32_t (&qf)[D
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) attend_kernel(Args a) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  __nv_bfloat16* smem = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+__global__ void __launch_bounds__(kThreads, 2)
+    attend_kernel(Args a, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV) {
+  using SL = StageLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int s_par[kMaxRows];
   __shared__ int s_tbl[kMaxPagesPerSplit];
   __shared__ unsigned long long s_mask[kTileRows][2];
+  __shared__ __align__(8) unsigned long long s_full[kStages];
   __shared__ int s_last;
   const Header* hdr = reinterpret_cast<const Header*>(a.ws + a.L.header);
   const int U = hdr->U;
@@ -382,43 +406,12 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(Args a) {
 
   const int n_stage = (blk1 - blk0 + 3) / 4;
   const int32_t* table = a.tables + (size_t)i * a.max_blocks;
-  constexpr int kChunksPerRow = D / 8;
-  constexpr int kChunksPerTensor = kTB * kChunksPerRow;
-  constexpr int kCopiesPerThread = 2 * kChunksPerTensor / kThreads;
+  // 1024-byte aligned ring for the 128-byte swizzle atoms.
+  const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* ring_ptr = smem_raw + (ring - smem_u32(smem_raw));
 
-  auto issue = [&](int st) {
-    if (st < n_stage) {
-      __nv_bfloat16* buf = smem + (size_t)(st % kStages) * 2 * kTB * D;
-#pragma unroll
-      for (int k = 0; k < kCopiesPerThread; ++k) {
-        const int c = tid + k * kThreads;
-        const int tensor = c / kChunksPerTensor;
-        const int rem = c % kChunksPerTensor;
-        const int row = rem / kChunksPerRow;
-        const int col = rem % kChunksPerRow;
-        const int page = blk0 + 4 * st + (row >> 4);
-        const int tok = page * kBlockSize + (row & 15);
-        const __nv_bfloat16* base = tensor ? a.v : a.k;
-        const void* src = base;
-        int bytes = 0;
-        if (page < blk1 && tok < tok_end) {
-          const int bid = s_tbl[page - blk0];
-          if (bid >= 0 && bid < a.num_blocks) {
-            src = base + (((size_t)bid * a.Hkv + g) * kBlockSize + (row & 15)) * D + col * 8;
-            bytes = 16;
-          } else if (tensor == 0 && (row & 15) == 0 && col == 0) {
-            flag(a.dev_status, SV_DEV_BAD_BLOCK_ID);
-          }
-        }
-        __nv_bfloat16* dst = buf + (size_t)tensor * kTB * D + row * D + ((col ^ (row & 7)) << 3);
-        cp_async16(smem_u32(dst), src, bytes);
-      }
-    }
-    cp_async_commit();
-  };
-
-  // Block ids of this unit's pages (and the request's parent links, if the
-  // unit reaches staged slots) into shared memory with one round trip.
+  // Block ids of this unit's pages (and the parent links, if the unit reaches
+  // staged slots) into shared memory with one round trip.
   const int r_first = vr0 / group;
   const int r_count = (vr0 + Mu - 1) / group - r_first + 1;
   const bool unit_masked = blk1 * kBlockSize > ctx;
@@ -427,7 +420,47 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(Args a) {
     const int rows = a.bt.cu_rows[i + 1] - cu;
     for (int j = tid; j < rows; j += kThreads) s_par[j] = a.bt.parent[cu + j];
   }
+  if (tid == 0) {
+    for (int k = 0; k < kStages; ++k) mbar_init(smem_u32(&s_full[k]), 1);
+    fence_mbar_init();
+  }
   __syncthreads();
+
+  // Thread 0 issues one stage: every valid page of it, K and V, all boxes.
+  auto issue = [&](int st) {
+    if (tid != 0 || st >= n_stage) return;
+    const int slot = st % kStages;
+    const uint32_t bar = smem_u32(&s_full[slot]);
+    const uint32_t kdst = ring + slot * SL::kStageBytes;
+    uint32_t bytes = 0;
+    int bids[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int page = blk0 + 4 * st + p;
+      int bid = -1;
+      if (page < blk1) {
+        bid = s_tbl[page - blk0];
+        if (bid < 0 || bid >= a.num_blocks) {
+          flag(a.dev_status, SV_DEV_BAD_BLOCK_ID);
+          bid = -1;
+        }
+      }
+      bids[p] = bid;
+      if (bid >= 0) bytes += 2 * SL::kHalves * SL::kBoxBytes;
+    }
+    mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      if (bids[p] < 0) continue;
+      const int y = (bids[p] * a.Hkv + g) * kBlockSize;
+#pragma unroll
+      for (int h = 0; h < SL::kHalves; ++h) {
+        const uint32_t o = (uint32_t)((p * SL::kHalves + h) * SL::kBoxBytes);
+        tma_load_2d(kdst + o, &tmK, 64 * h, y, bar);
+        tma_load_2d(kdst + SL::kTensorBytes + o, &tmV, 64 * h, y, bar);
+      }
+    }
+  };
 
 #pragma unroll
   for (int st = 0; st < kStages - 1; ++st) issue(st);
@@ -479,33 +512,61 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(Args a) {
   f.m_a = f.m_b = -INFINITY;
   f.l_a = f.l_b = 0.f;
 
+  int issued_hi = min(kStages - 1, n_stage);  // stages issued so far
+  int abort_at = -1;                           // stage whose wait gave up
   for (int st = 0; st < n_stage; ++st) {
     issue(st + kStages - 1);
-    cp_async_wait<kStages - 1>();
-    __syncthreads();
-    if (active) {
-      const uint32_t kbase = smem_u32(smem + (size_t)(st % kStages) * 2 * kTB * D);
-      const uint32_t vbase = kbase + kTB * D * 2;
-      const int t0 = (blk0 + 4 * st) * kBlockSize;
-      if (TS == 4)
-        stage_compute<D, 4>(f, qf, kbase, vbase, t0, ts * 16, ctx, tok_end, a.scale_log2, mk_a0,
-                            mk_a1, mk_b0, mk_b1, lane);
-      else if (TS == 2)
-        stage_compute<D, 2>(f, qf, kbase, vbase, t0, ts * 32, ctx, tok_end, a.scale_log2, mk_a0,
-                            mk_a1, mk_b0, mk_b1, lane);
-      else
-        stage_compute<D, 1>(f, qf, kbase, vbase, t0, 0, ctx, tok_end, a.scale_log2, mk_a0,
-                            mk_a1, mk_b0, mk_b1, lane);
+    if (st + kStages - 1 < n_stage) issued_hi = st + kStages;
+    const int slot = st % kStages;
+    const bool ok = mbar_wait_bounded(smem_u32(&s_full[slot]), (uint32_t)((st / kStages) & 1));
+    if (__syncthreads_or(!ok)) {
+      abort_at = st;
+      if (tid == 0) flag(a.dev_status, SV_DEV_TIMEOUT);
+      break;
     }
-    __syncthreads();
+    const uint32_t kbase = ring + slot * SL::kStageBytes;
+    const uint32_t vbase = kbase + SL::kTensorBytes;
+    const int t0 = (blk0 + 4 * st) * kBlockSize;
+    if (t0 + kTB > tok_end) {
+      // Slots past the last key may hold anything (unwritten cache slots, or
+      // pages not loaded): zero their V rows so that P = 0 meets V = 0.
+      const int first = max(0, tok_end - t0);
+      for (int x = tid; x < (kTB - first) * (D / 8); x += kThreads) {
+        const int t = first + x / (D / 8), c = x % (D / 8);
+        *reinterpret_cast<int4*>(ring_ptr + (vbase - ring) + SL::off(t, c)) = make_int4(0, 0, 0, 0);
+      }
+      __syncthreads();
+    }
+    if (active) {
+      if (TS == 4) {
+        slice_compute<D, 2>(f, qf, kbase, vbase, t0, ts * 16, ctx, tok_end, a.scale_log2, mk_a0,
+                            mk_a1, mk_b0, mk_b1, lane);
+      } else if (TS == 2) {
+        slice_compute<D, 4>(f, qf, kbase, vbase, t0, ts * 32, ctx, tok_end, a.scale_log2, mk_a0,
+                            mk_a1, mk_b0, mk_b1, lane);
+      } else {
+        slice_compute<D, 4>(f, qf, kbase, vbase, t0, 0, ctx, tok_end, a.scale_log2, mk_a0,
+                            mk_a1, mk_b0, mk_b1, lane);
+        slice_compute<D, 4>(f, qf, kbase, vbase, t0, 32, ctx, tok_end, a.scale_log2, mk_a0,
+                            mk_a1, mk_b0, mk_b1, lane);
+      }
+    }
+    __syncthreads();  // the slot is free: the next issue may overwrite it
   }
-  cp_async_wait<0>();
-  __syncthreads();
+  if (abort_at >= 0) {
+    // Let copies still in flight (stages abort_at .. issued_hi - 1) land
+    // before the CTA leaves; every wait is bounded.
+    if (tid == 0)
+      for (int st = abort_at; st < issued_hi; ++st)
+        mbar_wait_bounded(smem_u32(&s_full[st % kStages]), (uint32_t)((st / kStages) & 1));
+    __syncthreads();
+    return;
+  }
 
   // Warps that split the tokens of one m-tile merge through shared memory
   // (the stage ring is free now): every thread hands its fragment to the
   // same lane of the ts = 0 warp.
-  float* xch = reinterpret_cast<float*>(smem_raw);
+  float* xch = reinterpret_cast<float*>(ring_ptr);
   constexpr int kFragFloats = D / 2 + 4;  // o (D/8 * 4) + m_a, m_b, l_a, l_b
   if (TS > 1) {
     if (active && ts > 0) {
@@ -625,9 +686,39 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(Args a) {
   }
 }
 
+// cuTensorMapEncodeTiled from the driver, fetched through the runtime (no
+// link against the driver library).
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A cache viewed as rows of D bf16 (num_blocks * Hkv * 16 rows), boxes of
+// 64 elements x 16 rows, 128-byte swizzle.
+static bool make_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int D) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_blocks * Hkv * kBlockSize};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 sv_status launch(const Args& a, cudaStream_t stream) {
-  const size_t smem = (size_t)kStages * 2 * kTB * D * sizeof(__nv_bfloat16);
+  const size_t smem = (size_t)kStages * StageLayout<D>::kStageBytes + 1024;
   static int attr_dev_mask = 0;  // devices whose kernel attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
@@ -637,9 +728,12 @@ sv_status launch(const Args& a, cudaStream_t stream) {
       return SV_ERR_CUDA;
     attr_dev_mask |= 1 << (dev & 31);
   }
+  CUtensorMap tmK, tmV;
+  if (!make_map(&tmK, a.k, a.num_blocks, a.Hkv, D) || !make_map(&tmV, a.v, a.num_blocks, a.Hkv, D))
+    return SV_ERR_CUDA;
   plan_kernel<<<1, 1024, 0, stream>>>(a);
   SV_LAUNCH_CHECK();
-  attend_kernel<D><<<a.L.ucap, kThreads, smem, stream>>>(a);
+  attend_kernel<D><<<a.L.ucap, kThreads, smem, stream>>>(a, tmK, tmV);
   SV_LAUNCH_CHECK();
   return SV_OK;
 }
