@@ -71,25 +71,37 @@ inline int race_chunks(int R, int V) {
   const int want = (kNumSMs * 32 + R - 1) / max(1, R);
   return max(1, min(want, maxc));
 }
-inline int chunk_len(int V, int nch) { return ((V + nch - 1) / nch + 3) & ~3; }
+inline __host__ __device__ int chunk_len(int V, int nch) { return ((V + nch - 1) / nch + 3) & ~3; }
 
 Layout layout(int R, int total_rows, int V, int maxw) {
   Layout L;
   L.maxw = max(1, min(maxw, kMaxRows));
   const long bound = min((long)total_rows, (long)R * L.maxw);
   L.nch = stats_chunks((int)max(1L, bound), V);
+  L.nch_cap = max(L.nch, min(min(64, V / 2048), 16384 / max(1, total_rows)));
   L.nch_r = race_chunks(R, V);
-  L.ch = chunk_len(V, L.nch);
-  L.ch_r = chunk_len(V, L.nch_r);
+  L.nch_r_cap = max(L.nch_r, min(min(256, V / 512), 16384 / max(1, R)));
   size_t off = 0;
-  L.parts = off; off += align256(sizeof(StatPart) * (size_t)total_rows * 2 * L.nch);
+  L.parts = off; off += align256(sizeof(StatPart) * (size_t)total_rows * 2 * L.nch_cap);
   L.jobs = off; off += align256(sizeof(Job) * (size_t)R);
-  L.race = off; off += align256(sizeof(RacePart) * (size_t)R * L.nch_r);
+  L.race = off; off += align256(sizeof(RacePart) * (size_t)R * L.nch_r_cap);
   L.race_tickets = off; off += align256(sizeof(int) * (size_t)R);
   L.stat_tickets = off; off += align256(sizeof(int) * (size_t)R);
   L.act = off; off += align256(sizeof(int) * (size_t)(R + 1));  // act[R] = count
   L.total = off;
   return L;
+}
+
+// Slices actually used, from the number of active requests (same value in
+// every kernel of a call): about 32 warps per SM of work.
+__device__ __forceinline__ int stats_slices(const Layout& L, int count, int ntypes) {
+  const long slots = (long)max(1, count) * L.maxw * ntypes;
+  const long want = (kNumSMs * 32 + slots - 1) / slots;
+  return (int)max((long)L.nch, min(want, (long)L.nch_cap));
+}
+__device__ __forceinline__ int race_slices(const Layout& L, int count) {
+  const long want = (kNumSMs * 32 + max(1, count) - 1) / max(1, count);
+  return (int)max((long)L.nch_r, min(want, (long)L.nch_r_cap));
 }
 
 struct Args {
@@ -126,6 +138,7 @@ __device__ __forceinline__ void merge_am(float& v, int& i, float v2, int i2) {
 // into the windows of chunk `chunk` (chunk >= 0) and writes them out.
 __global__ void __launch_bounds__(1024) list_kernel(Args a, int chunk, int cs, const int32_t* done,
                                                     int32_t* rb_out, int32_t* re_out) {
+  griddep_entry();
   const int R = a.bt.n_req;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int* act = reinterpret_cast<int*>(a.ws + a.L.act);
@@ -196,13 +209,13 @@ struct DecideSmem {
   int am[kMaxRows], len[kMaxRows], child[kMaxRows];
 };
 
-__device__ __forceinline__ void row_ml(const Args& a, int r, int type, float& m, float& l) {
+__device__ __forceinline__ void row_ml(const Args& a, int nch, int r, int type, float& m, float& l) {
   const StatPart* parts = reinterpret_cast<const StatPart*>(a.ws + a.L.parts) +
-                          ((size_t)r * 2 + type) * a.L.nch;
+                          ((size_t)r * 2 + type) * nch;
   const int lane = threadIdx.x & 31;
   m = -INFINITY;
   l = 0.f;
-  for (int c = lane; c < a.L.nch; c += 32) merge_ml(m, l, __ldcg(&parts[c].m), __ldcg(&parts[c].l));
+  for (int c = lane; c < nch; c += 32) merge_ml(m, l, __ldcg(&parts[c].m), __ldcg(&parts[c].l));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -211,13 +224,13 @@ __device__ __forceinline__ void row_ml(const Args& a, int r, int type, float& m,
   }
 }
 
-__device__ __forceinline__ void row_argmax(const Args& a, int r, float& v, int& idx) {
+__device__ __forceinline__ void row_argmax(const Args& a, int nch, int r, float& v, int& idx) {
   const StatPart* parts = reinterpret_cast<const StatPart*>(a.ws + a.L.parts) +
-                          ((size_t)r * 2) * a.L.nch;
+                          ((size_t)r * 2) * nch;
   const int lane = threadIdx.x & 31;
   v = -INFINITY;
   idx = 0x7fffffff;
-  for (int c = lane; c < a.L.nch; c += 32) merge_am(v, idx, __ldcg(&parts[c].m), __ldcg(&parts[c].amax));
+  for (int c = lane; c < nch; c += 32) merge_am(v, idx, __ldcg(&parts[c].m), __ldcg(&parts[c].amax));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
@@ -227,7 +240,7 @@ __device__ __forceinline__ void row_argmax(const Args& a, int r, float& v, int& 
 }
 
 // The decision for request i, by one warp, once all its row partials exist.
-__device__ void decide_request(const Args& a, int i, DecideSmem& sm) {
+__device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   const int lane = threadIdx.x & 31;
   Job* job = reinterpret_cast<Job*>(a.ws + a.L.jobs) + i;
   if (a.T > 0.f && lane == 0) {
@@ -279,7 +292,7 @@ __device__ void decide_request(const Args& a, int i, DecideSmem& sm) {
     for (int r = w.b; r < w.e; ++r) {
       float v;
       int idx;
-      row_argmax(a, cu + r, v, idx);
+      row_argmax(a, nch, cu + r, v, idx);
       if (lane == 0) {
         sm.am[r] = idx;
         if (rs) {
@@ -349,14 +362,14 @@ __device__ void decide_request(const Args& a, int i, DecideSmem& sm) {
   const int jmax = min(w.e, w.lim - 1);
   for (int r = w.b; r < w.e; ++r) {
     float m, l;
-    row_ml(a, cu + r, 0, m, l);
+    row_ml(a, nch, cu + r, 0, m, l);
     if (lane == 0) {
       sm.mp[r] = m;
       sm.lp[r] = l;
       if (rs) rs[(size_t)(cu + r) * 4 + 0] = m + logf(l);
     }
     if (r + 1 <= w.lim - 1) {
-      row_ml(a, cu + r, 1, m, l);
+      row_ml(a, nch, cu + r, 1, m, l);
       if (lane == 0) {
         sm.mq[r] = m;
         sm.lq[r] = l;
@@ -445,14 +458,17 @@ __device__ void decide_request(const Args& a, int i, DecideSmem& sm) {
 // decision for it.
 template <bool VEC>
 __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
+  griddep_entry();
   __shared__ DecideSmem s_dec[kStatThreads / 32];
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   int* tickets = reinterpret_cast<int*>(a.ws + a.L.stat_tickets);
   const int R = a.bt.n_req;
   const int count = act[R];
-  const int nch = a.L.nch, maxw = a.L.maxw;
   const float T = a.T;
   const int ntypes = T > 0.f ? 2 : 1;
+  const int maxw = a.L.maxw;
+  const int nch = stats_slices(a.L, count, ntypes);
+  const int chl = chunk_len(a.V, nch);
   const long total = (long)count * maxw * ntypes * nch;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const long stride = (long)gridDim.x * (kStatThreads / 32);
@@ -472,8 +488,8 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
     if (type == 1 && off >= ndraft) continue;
     const int r = a.bt.cu_rows[i] + j;
     const float* row = (type ? a.draft : a.target) + (size_t)r * a.V;
-    const int lo = c * a.L.ch;
-    const int hi = min(a.V, lo + a.L.ch);
+    const int lo = c * chl;
+    const int hi = min(a.V, lo + chl);
     float m = -INFINITY, l = 0.f;
     int am = 0x7fffffff;
     if (T > 0.f) {
@@ -546,7 +562,7 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
       __threadfence();
-      decide_request(a, i, s_dec[wid]);
+      decide_request(a, nch, i, s_dec[wid]);
     }
   }
 }
@@ -560,10 +576,12 @@ __device__ __forceinline__ void race_take(float& best, int& bi, float key, int v
 // row(s) and arrives on the request's ticket; the last one reduces.
 template <bool VEC>
 __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
+  griddep_entry();
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   const int R = a.bt.n_req;
   const int count = act[R];
-  const int nch = a.L.nch_r;
+  const int nch = race_slices(a.L, count);
+  const int chl = chunk_len(a.V, nch);
   const long total = (long)count * nch;
   const float T = a.T;
   const float rT = 1.f / T;
@@ -581,8 +599,8 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
     const float* lq = a.draft + (size_t)jb.row * a.V;
     const float inv_lp = 1.f / jb.lp, inv_lq = 1.f / jb.lq;
     const float mpb = jb.mp * kLog2e, mqb = jb.mq * kLog2e;
-    const int lo = c * a.L.ch_r;
-    const int hi = min(a.V, lo + a.L.ch_r);
+    const int lo = c * chl;
+    const int hi = min(a.V, lo + chl);
     // Running best of this lane as (w, E): v beats it iff w_v E_b > w_b E_v.
     // E_v >= kEmin for every uniform the generator can produce, so an entry
     // with w_v < w_b / E_b * kEmin can never win: groups of four such entries
@@ -695,8 +713,8 @@ sv_status chunk_list(const sv_batch* bt, int chunk, int cs, const int32_t* done,
   a.ws = static_cast<uint8_t*>(ws);
   a.L = layout(bt->n_req, bt->total_rows, vocab, cs);
   a.dev_status = dev_status;
-  list_kernel<<<1, 1024, 0, s>>>(a, chunk, cs, done, rb, re);
-  SV_LAUNCH_CHECK();
+  if (sv::launch(list_kernel, 1, 1024, 0, s, a, chunk, cs, done, rb, re) != cudaSuccess)
+    return SV_ERR_CUDA;
   return SV_OK;
 }
 
@@ -730,22 +748,23 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
   const bool vec = (vocab % 4 == 0) && ((((uintptr_t)target_logits) |
                                          ((uintptr_t)(draft_logits ? draft_logits : target_logits))) & 15) == 0;
   if (!prebuilt_list) {
-    list_kernel<<<1, 1024, 0, s>>>(a, -1, 0, nullptr, nullptr, nullptr);
-    SV_LAUNCH_CHECK();
+    if (sv::launch(list_kernel, 1, 1024, 0, s, a, -1, 0, (const int32_t*)nullptr,
+                   (int32_t*)nullptr, (int32_t*)nullptr) != cudaSuccess)
+      return SV_ERR_CUDA;
   }
-  const long items = (long)bt->n_req * a.L.maxw * (temperature > 0.f ? 2 : 1) * a.L.nch;
+  const long items = (long)bt->n_req * a.L.maxw * (temperature > 0.f ? 2 : 1) * a.L.nch_cap;
   const long warps = kStatThreads / 32;
   const unsigned gs = (unsigned)max(1L, min((items + warps - 1) / warps, (long)kNumSMs * 4));
-  if (vec) stats_kernel<true><<<gs, kStatThreads, 0, s>>>(a);
-  else stats_kernel<false><<<gs, kStatThreads, 0, s>>>(a);
-  SV_LAUNCH_CHECK();
+  if (sv::launch(vec ? stats_kernel<true> : stats_kernel<false>, gs, kStatThreads, 0, s, a) !=
+      cudaSuccess)
+    return SV_ERR_CUDA;
   if (temperature > 0.f) {
-    const long ritems = (long)bt->n_req * a.L.nch_r;
+    const long ritems = (long)bt->n_req * a.L.nch_r_cap;
     const long rwarps = kRaceThreads / 32;
     const unsigned gr = (unsigned)max(1L, min((ritems + rwarps - 1) / rwarps, (long)kNumSMs * 4));
-    if (vec) race_kernel<true><<<gr, kRaceThreads, 0, s>>>(a);
-    else race_kernel<false><<<gr, kRaceThreads, 0, s>>>(a);
-    SV_LAUNCH_CHECK();
+    if (sv::launch(vec ? race_kernel<true> : race_kernel<false>, gr, kRaceThreads, 0, s, a) !=
+        cudaSuccess)
+      return SV_ERR_CUDA;
   }
   return SV_OK;
 }

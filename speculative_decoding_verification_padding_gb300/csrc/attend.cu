@@ -134,6 +134,7 @@ __device__ __forceinline__ void block_excl_scan(int* s_warp, int v, int& excl, i
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
+  griddep_entry();
   const int R = a.bt.n_req;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Header* hdr = reinterpret_cast<Header*>(a.ws + a.L.header);
@@ -364,6 +365,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     attend_kernel(Args a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
+  griddep_entry();
   using SL = StageLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int s_par[kMaxRows];
@@ -731,10 +733,9 @@ sv_status launch(const Args& a, cudaStream_t stream) {
   CUtensorMap tmK, tmV;
   if (!make_map(&tmK, a.k, a.num_blocks, a.Hkv, D) || !make_map(&tmV, a.v, a.num_blocks, a.Hkv, D))
     return SV_ERR_CUDA;
-  plan_kernel<<<1, 1024, 0, stream>>>(a);
-  SV_LAUNCH_CHECK();
-  attend_kernel<D><<<a.L.ucap, kThreads, smem, stream>>>(a, tmK, tmV);
-  SV_LAUNCH_CHECK();
+  if (sv::launch(plan_kernel, 1, 1024, 0, stream, a) != cudaSuccess) return SV_ERR_CUDA;
+  if (sv::launch(attend_kernel<D>, a.L.ucap, kThreads, smem, stream, a, tmK, tmV) != cudaSuccess)
+    return SV_ERR_CUDA;
   return SV_OK;
 }
 

@@ -70,6 +70,7 @@ __device__ __forceinline__ int block_scan_excl(int* s_warp, int v, int& total) {
 }
 
 __global__ void __launch_bounds__(kThreads) budget_kernel(Args a) {
+  griddep_entry();
   extern __shared__ __align__(16) uint32_t sm[];
   uint32_t* kA = sm;
   uint32_t* vA = kA + kMaxCand;
@@ -290,7 +291,8 @@ extern "C" sv_status sv_select_budget(int32_t n_req, int32_t gamma_max, const fl
       return SV_ERR_CUDA;
     attr_dev_mask |= 1 << (dev & 31);
   }
-  bud::budget_kernel<<<1, bud::kThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
-  SV_LAUNCH_CHECK();
+  if (sv::launch(bud::budget_kernel, 1, bud::kThreads, smem, static_cast<cudaStream_t>(stream), a) !=
+      cudaSuccess)
+    return SV_ERR_CUDA;
   return SV_OK;
 }

@@ -20,6 +20,7 @@ namespace chk {
 __global__ void __launch_bounds__(256) windows_kernel(sv_batch bt, int c, int cs,
                                                       const int32_t* done, int32_t* rb,
                                                       int32_t* re, int32_t* dev_status) {
+  griddep_entry();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= bt.n_req) return;
   bt.row_begin = nullptr;
@@ -65,9 +66,10 @@ extern "C" sv_status sv_chunk_windows(const sv_batch* bt, int32_t chunk_index, i
   if (chunk_index > 0 && !done) return SV_ERR_INVALID_ARGUMENT;
   if (bt->n_req == 0) return SV_OK;
   if (!bt->cu_rows) return SV_ERR_INVALID_ARGUMENT;
-  chk::windows_kernel<<<(bt->n_req + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      *bt, chunk_index, chunk_size, done, row_begin, row_end, nullptr);
-  SV_LAUNCH_CHECK();
+  if (sv::launch(chk::windows_kernel, (bt->n_req + 255) / 256, 256, 0,
+                 static_cast<cudaStream_t>(stream), *bt, chunk_index, chunk_size, done, row_begin,
+                 row_end, (int32_t*)nullptr) != cudaSuccess)
+    return SV_ERR_CUDA;
   return SV_OK;
 }
 

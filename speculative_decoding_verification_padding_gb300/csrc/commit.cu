@@ -69,6 +69,7 @@ __device__ bool request_ok(const Args& a, int i, int& rows, int& ctx, int& al, b
 }
 
 __global__ void __launch_bounds__(256) copy_kernel(Args a) {
+  griddep_entry();
   extern __shared__ __align__(16) uint8_t smem_raw[];
   int4* buf = reinterpret_cast<int4*>(smem_raw);
   __shared__ int s_ok, s_moves;
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__(256) copy_kernel(Args a) {
 }
 
 __global__ void __launch_bounds__(1024) release_kernel(Args a) {
+  griddep_entry();
   const int R = a.bt.n_req;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ int s_warp[32];
@@ -236,9 +238,7 @@ extern "C" sv_status sv_commit_kv(const sv_paged_kv* kv, const sv_batch* bt,
       return SV_ERR_CUDA;
     attr_dev_mask |= 1 << (dev & 31);
   }
-  cmt::copy_kernel<<<bt->n_req, 256, smem, s>>>(a);
-  SV_LAUNCH_CHECK();
-  cmt::release_kernel<<<1, 1024, 0, s>>>(a);
-  SV_LAUNCH_CHECK();
+  if (sv::launch(cmt::copy_kernel, bt->n_req, 256, smem, s, a) != cudaSuccess) return SV_ERR_CUDA;
+  if (sv::launch(cmt::release_kernel, 1, 1024, 0, s, a) != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }

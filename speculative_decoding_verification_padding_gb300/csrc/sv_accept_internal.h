@@ -13,9 +13,12 @@ namespace acc {
 
 // Workspace of the accept kernels for a batch whose windows hold at most
 // `maxw` rows per request.
+// nch / nch_r: vocabulary slices per row (statistics) and per request
+// (race) when every listed request is active; the kernels use more slices,
+// up to nch_cap / nch_r_cap, when fewer requests are active.
 struct Layout {
   size_t parts, jobs, race, race_tickets, stat_tickets, act, total;
-  int nch, nch_r, ch, ch_r, maxw;
+  int nch, nch_cap, nch_r, nch_r_cap, maxw;
 };
 Layout layout(int R, int total_rows, int V, int maxw);
 

@@ -212,8 +212,35 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// --------------------------------------------- programmatic dependent launch --
+// Every kernel of the library starts with griddep_entry(): it waits until the
+// previous grid in the stream has completed and its writes are visible
+// (nothing is read or written before that), then lets the next grid begin
+// launching, so that launch latency overlaps the tail of this grid.
+__device__ __forceinline__ void griddep_entry() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // ------------------------------------------------------------ host side --
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Launch with programmatic stream serialization allowed (see griddep_entry).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace sv
 
