@@ -1,18 +1,26 @@
 """Benchmark of one verification step per layer on GB300 (one JSON line).
 
-Workload (default): batch of 64 requests, Llama-3-8B attention shape (32 q /
-8 KV heads, d 128), per-request draft counts U{1..8}, contexts log-normal
-(ln 4096, 1) clipped to [512, 32768], paged bf16 KV (16-token blocks,
-shuffled tables), vocab 128256 fp32 logits, sampling at T = 0.7, chunked
-verification in chunks of 2 with early pruning, then the KV commit.
+Default workload (--workload batch64): 64 requests, Llama-3-8B attention
+shape (32 q / 8 KV heads, d 128), per-request draft counts U{1..8},
+contexts log-normal (ln 4096, 1) clipped to [512, 32768], paged bf16 KV
+(16-token blocks, shuffled tables), vocab 128256 fp32 logits, sampling at
+T = 0.7, chunked verification in chunks of 2 with early pruning, then the KV
+commit.  Other workloads: tiny, chain8b, tree70b (one pass), batch256
+(budget-selected).
 
 One step = restore the block tables / lengths / free list the previous
-step's commit changed, sv_verify_chunked (per chunk: windows, tree-prep +
-split-KV attention + merge, row statistics + accept/reject + resampling),
-sv_commit_kv.  The KV cache (1.7 GB) and the logits (0.36 GB) are larger
-than L2, so no flush is needed between steps.
+step's commit changed, then the workload's calls:
+  chunked  sv_verify_chunked (per chunk: windows + active list, attention
+           plan, split-KV attention, row statistics with the decisions,
+           resampling race) and sv_commit_kv
+  onepass  sv_tree_attend, sv_accept, sv_commit_kv
+  budget   sv_select_budget, sv_tree_attend and sv_accept on the selected
+           prefixes, sv_commit_kv
+Inputs larger than L2 are timed back to back; smaller ones step by step with
+an L2 flush (a 512 MB write) between steps, outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload batch64|tiny|chain8b|tree70b|batch256]
 
 For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of
 the step (the path has no exchange step); the line reports the sum over
@@ -39,13 +47,25 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verify steps/s and verified tokens/s per layer; HBM GB/s vs GB300 8 TB/s"
 UNIT = "verified tokens/s per layer"
+L2_BYTES = 129 * 2 ** 20
 
-
-def workload_description(cfg):
-    return ("batch64: 64 requests, Llama-3-8B attention shape (32 q / 8 kv heads, d 128), "
-            "drafts U{1..8} per request, context lognormal(ln 4096, 1) clipped to [512, 32768], "
-            "paged bf16 KV in 16-token blocks with shuffled tables, vocab 128256 fp32 logits, "
-            "T=0.7 sampling, chunked verification (chunk 2) with early pruning, KV commit")
+WORKLOAD_TEXT = {
+    "batch64": ("batch64: 64 requests, Llama-3-8B attention shape (32 q / 8 kv heads, d 128), "
+                "drafts U{1..8} per request, context lognormal(ln 4096, 1) clipped to [512, 32768], "
+                "paged bf16 KV in 16-token blocks with shuffled tables, vocab 128256 fp32 logits, "
+                "T=0.7 sampling, chunked verification (chunk 2) with early pruning, KV commit"),
+    "tiny": ("tiny: 1 request, 4 drafts, 8 q / 2 kv heads, d 64, context 256, vocab 1024, "
+             "target N(0,2^2), draft = target + N(0,0.5^2), T=1 sampling, one pass, KV commit"),
+    "chain8b": ("chain8b: 1 request, 5 drafts, Llama-3-8B attention shape (32 q / 8 kv, d 128), "
+                "context 4096, vocab 128256 fp32 logits ~N(0,3^2), draft sigma 1, T=1 sampling, "
+                "one pass, KV commit"),
+    "tree70b": ("tree70b: 1 request, 64-node draft tree (depth 6, branching 4,3,2,2,1,1 "
+                "truncated), Llama-3-70B attention shape (64 q / 8 kv, d 128), context 8192, vocab "
+                "128256, greedy longest valid path, KV commit of the path"),
+    "batch256": ("batch256: 256 requests, 40 q / 8 kv heads, d 128, context U{1024..8192}, 4 drafts, "
+                 "vocab 151936, survival c ~ Beta(4,2), budget by argmax tau*SPS(B) with "
+                 "SPS(B)=1000/(1+B/512), then attention + T=1 accept + commit on the selected prefixes"),
+}
 
 
 # ----------------------------------------------------------------- clocks --
@@ -105,53 +125,57 @@ class ClockSampler:
 
 # ---------------------------------------------------------- byte accounting --
 
-def chunk_schedule(w, accepted_len, chunk):
-    """Windows each chunk launch processed, from the step's accepted lengths
-    (a request runs through chunk accepted_len // chunk)."""
+def launch_windows(w, mode, accepted_len, verify_len=None, chunk=2):
+    """The (request, begin, end, lim) windows of every attention / accept
+    launch of one step, from the step's own results."""
     rows = [int(r) for r in np.diff(w.cu_rows)]
-    n_chunks = math.ceil(w.max_rows / chunk)
-    sched = []
-    for c in range(n_chunks):
-        act = []
-        for i in range(w.n_req):
-            b = c * chunk
-            e = min(b + chunk, rows[i])
-            if b < e and c <= int(accepted_len[i]) // chunk:
-                act.append((i, b, e))
-        sched.append(act)
-    return sched
+    R = w.n_req
+    if mode == "chunked":
+        sched = []
+        for c in range(math.ceil(w.max_rows / chunk)):
+            act = []
+            for i in range(R):
+                b, e = c * chunk, min(c * chunk + chunk, rows[i])
+                if b < e and c <= int(accepted_len[i]) // chunk:
+                    act.append((i, b, e, rows[i]))
+            sched.append(act)
+        return sched
+    if mode == "budget":
+        return [[(i, 0, int(verify_len[i]) + 1, int(verify_len[i]) + 1) for i in range(R)]]
+    return [[(i, 0, rows[i], rows[i]) for i in range(R)]]
 
 
 def attend_bytes(w, windows):
+    """KV of context + staged slots up to the window end, Q in, out."""
     cfg = w.cfg
     kvb = cfg.n_kv_heads * cfg.head_dim * 2 * 2
     qo = cfg.n_q_heads * cfg.head_dim * 2 * 2
-    return sum((int(w.cache_lens[i]) + e) * kvb + (e - b) * qo for i, b, e in windows)
+    return sum((int(w.cache_lens[i]) + e) * kvb + (e - b) * qo for i, b, e, _ in windows)
 
 
 def accept_bytes(w, windows, accepted_len, T):
+    """Target rows of the window, draft rows that propose a tested draft
+    (T > 0), and the one or two rows the residual / bonus draw scans."""
     V = int(w.target_logits.shape[1])
-    rows = [int(r) for r in np.diff(w.cu_rows)]
     tot = 0
-    for i, b, e in windows:
-        tot += (e - b) * V * 4                               # target rows
+    for i, b, e, lim in windows:
+        tot += (e - b) * V * 4
         if T > 0:
-            tot += (min(e, rows[i] - 1) - b) * V * 4          # draft rows with a child
+            tot += max(0, min(e, lim - 1) - b) * V * 4
             a = int(accepted_len[i])
-            if b <= a < e:                                    # decided in this window
-                tot += (V * 4 if a == rows[i] - 1 else 2 * V * 4)
+            if b <= a < e:
+                tot += V * 4 if a == lim - 1 else 2 * V * 4
     return tot
 
 
 # ------------------------------------------------------------- CPU baseline --
 
-def oracle_sample(w, n_req, start=0):
-    """The first n_req requests of w (from `start`) as a standalone workload."""
+def oracle_sample(w, idx):
+    """Requests `idx` of w as a standalone workload (same cache arrays)."""
     from speculative_decoding_verification_padding_gb300.workloads import Workload
-    idx = list(range(start, start + n_req))
     cu = w.cu_rows
     rows = [slice(cu[i], cu[i + 1]) for i in idx]
-    new_cu = np.zeros(n_req + 1, dtype=np.int32)
+    new_cu = np.zeros(len(idx) + 1, dtype=np.int32)
     new_cu[1:] = np.cumsum([cu[i + 1] - cu[i] for i in idx])
     cat = lambda a: np.concatenate([a[s] for s in rows])
     return Workload(cfg=w.cfg, cu_rows=new_cu, parent=cat(w.parent), tokens=cat(w.tokens),
@@ -162,31 +186,47 @@ def oracle_sample(w, n_req, start=0):
                     draft_logits=cat(w.draft_logits), seed=w.seed)
 
 
-def time_oracle(w, n_req, threads, start=0):
+def time_oracle(w, mode, idx, threads):
+    """One step of the oracle on requests `idx`: returns (seconds, rows attended)."""
     import oracle
-    s = oracle_sample(w, n_req, start)
     t0 = time.perf_counter()
-    err, st, _, _, attended = oracle.verify_chunked(
-        s.batch(), s.kv(), s.q, s.cfg.n_q_heads, s.softmax_scale, s.target_logits,
-        s.draft_logits, s.cfg.temperature, s.seed, chunk=s.cfg.chunk or 2, n_threads=threads)
-    dt = time.perf_counter() - t0
-    return dt, attended, err
+    vl = None
+    if mode == "budget":
+        _, vl_all, _, _ = oracle.select_budget(w.cond_survival, w.gamma, w.sps)
+        vl = np.ascontiguousarray(vl_all[idx])
+    s = oracle_sample(w, idx)
+    T = s.cfg.temperature
+    draft = s.draft_logits if T > 0 else None
+    if mode == "chunked":
+        _, _, _, _, attended = oracle.verify_chunked(
+            s.batch(), s.kv(), s.q, s.cfg.n_q_heads, s.softmax_scale, s.target_logits, draft, T,
+            s.seed, chunk=s.cfg.chunk or 2, n_threads=threads)
+    else:
+        b = s.batch(verify_len=vl)
+        oracle.tree_attend(b, s.kv(), s.q, s.cfg.n_q_heads, s.softmax_scale, n_threads=threads)
+        oracle.accept(b, s.target_logits, draft, T, s.seed, n_threads=threads)
+        attended = int(s.total_rows if vl is None else (vl + 1).sum())
+    return time.perf_counter() - t0, attended
 
 
-def cpu_baseline(w, budget_s=10.0):
+def cpu_baseline(w, mode, budget_s=10.0):
     import oracle
     oracle.build()
     threads = os.cpu_count() or 1
-    dt1, att1, _ = time_oracle(w, 1, threads)
+    dt1, _ = time_oracle(w, mode, [0], threads)
     n = int(max(1, min(w.n_req, budget_s / max(dt1, 1e-3))))
-    dt, att, err = time_oracle(w, n, threads)
+    dt, att = time_oracle(w, mode, list(range(n)), threads)
     return {"value": att / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"first {n} of {w.n_req} requests of the same step, chunked verification "
-                      f"(attention + accept), {att} rows attended in {dt:.2f} s, fp64 C++ "
-                      f"oracle with {threads} threads", "err": err}
+            "sample": f"first {n} of {w.n_req} requests of the same step ({mode}: attention + "
+                      f"accept), {att} rows attended in {dt:.2f} s, fp64 C++ oracle with "
+                      f"{threads} threads"}
 
 
 # ------------------------------------------------------------------- main --
+
+def mode_of(cfg):
+    return "budget" if cfg.budget else "chunked" if cfg.chunk else "onepass"
+
 
 def run_reference(args, rank):
     """Reference arm: the CPU oracle, timed on this host's cores."""
@@ -196,15 +236,17 @@ def run_reference(args, rank):
     import oracle
     oracle.build()
     w = wl.make_workload(wl.config(args.workload))
+    mode = mode_of(w.cfg)
     threads = os.cpu_count() or 1
-    dt1, _, _ = time_oracle(w, 1, threads)
+    dt1, _ = time_oracle(w, mode, [0], threads)
     per_step_budget = max(0.05, 120.0 / max(1, args.steps + args.warmup))
     n = int(max(1, min(w.n_req, per_step_budget / max(dt1, 1e-3))))
+    span = w.n_req - n + 1
     for k in range(args.warmup):
-        time_oracle(w, n, threads, start=(k * n) % (w.n_req - n + 1))
+        time_oracle(w, mode, [(k * n) % span + j for j in range(n)], threads)
     tot_t, tot_rows = 0.0, 0
     for k in range(args.steps):
-        dt, att, _ = time_oracle(w, n, threads, start=(k * n) % (w.n_req - n + 1))
+        dt, att = time_oracle(w, mode, [(k * n) % span + j for j in range(n)], threads)
         tot_t += dt
         tot_rows += att
     value = tot_rows / tot_t
@@ -212,11 +254,11 @@ def run_reference(args, rank):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_description(w.cfg), "global_batch": w.n_req,
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "global_batch": w.n_req,
                        "parallelism": "host threads"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"{n} of {w.n_req} requests per step (chunked verification: "
-                                       f"attention + accept), fp64 C++ oracle, {threads} threads"},
+                             "sample": f"{n} of {w.n_req} requests per step ({mode}: attention "
+                                       f"+ accept), fp64 C++ oracle, {threads} threads"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -227,7 +269,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="batch64")
+    ap.add_argument("--workload", default="batch64", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="only run this many steps (for a profiler), no timing line")
@@ -260,7 +302,7 @@ def main():
     w = wl.make_workload(wl.config(args.workload),
                          ctx_scale=args.ctx_scale if args.profile_steps else 1.0)
     s = DeviceStep(w, device=dev)
-    chunk = s.chunk
+    mode, chunk, T = s.mode, s.chunk, s.T
     stream = torch.cuda.current_stream()
 
     if args.profile_steps:
@@ -275,9 +317,13 @@ def main():
     if res["dev_status"] != 0:
         raise SystemExit(f"device status {res['dev_status']} during warm-up")
     al = res["accepted_len"]
-    sched = chunk_schedule(w, al, chunk)
-    rows_attended = sum(e - b for ch in sched for _, b, e in ch)
+    vl = s.verify_len.cpu().numpy() if mode == "budget" else None
+    sched = launch_windows(w, mode, al, vl, chunk)
+    rows_attended = sum(e - b for ch in sched for _, b, e, _ in ch)
     accepted_tokens = int((al + 1).sum())
+    step_bytes = sum(attend_bytes(w, ch) + accept_bytes(w, ch, al, T) for ch in sched)
+    flush_l2 = step_bytes < 2 * L2_BYTES
+    flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if flush_l2 else None
 
     def barrier():
         if world > 1:
@@ -290,6 +336,27 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
+    def timed(fn, n):
+        """Mean seconds per call of fn over n calls (flushing L2 between calls
+        for small inputs, outside the events)."""
+        if not flush_l2:
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(n):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            return a0.elapsed_time(a1) / 1e3 / n
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a0, a1 in evs:
+            flush_buf.fill_(1)
+            a0.record(stream)
+            fn()
+            a1.record(stream)
+        torch.cuda.synchronize()
+        return sum(a0.elapsed_time(a1) for a0, a1 in evs) / 1e3 / n
+
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
@@ -297,97 +364,101 @@ def main():
     # ---- headline: K whole steps, device-resident inputs ----
     barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        s.run()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    t_step = max_over_ranks(timed(s.run, args.steps))
     barrier()
-    t_step = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps)
 
-    # ---- per-launch timing of the attention and accept calls, same steps ----
-    n_chunks = math.ceil(w.max_rows / chunk)
-    rb = torch.zeros(w.n_req, dtype=torch.int32, device=dev)
-    re = torch.zeros(w.n_req, dtype=torch.int32, device=dev)
-    bw = api.Batch(s.batch.cu_rows, s.batch.parent, s.batch.tokens, w.max_rows, row_begin=rb, row_end=re)
+    # ---- per-call timing inside the same steps ----
     n_rep = max(5, args.steps // 4)
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(n_chunks)] for _ in range(n_rep)]
+    att_b = [attend_bytes(w, ch) for ch in sched]
+    acc_b = [accept_bytes(w, ch, al, T) for ch in sched]
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    t_att = t_acc = t_sel = 0.0
+    marks = []
     torch.cuda.synchronize()
-    for k in range(n_rep):
-        s.restore_cache_state()
-        for c in range(n_chunks):
-            api.sv_chunk_windows(s.batch, c, chunk, s.done, rb, re)
-            a0, a1, a2 = ev[k][c]
-            a0.record(stream)
-            s.attend(bw)
-            a1.record(stream)
-            s.accept(bw)
-            a2.record(stream)
-        s.commit()
-    torch.cuda.synchronize()
-    t_att = [[ev[k][c][0].elapsed_time(ev[k][c][1]) / 1e3 for c in range(n_chunks)] for k in range(n_rep)]
-    t_acc = [[ev[k][c][1].elapsed_time(ev[k][c][2]) / 1e3 for c in range(n_chunks)] for k in range(n_rep)]
-    att_b = [attend_bytes(w, sched[c]) for c in range(n_chunks)]
-    acc_b = [accept_bytes(w, sched[c], al, s.T) for c in range(n_chunks)]
-    att_time = float(np.mean([sum(t) for t in t_att]))
-    acc_time = float(np.mean([sum(t) for t in t_acc]))
-    att_gbs = sum(att_b) / att_time / 1e9
-    acc_gbs = sum(acc_b) / acc_time / 1e9
+    if mode == "chunked":
+        rb = torch.zeros(w.n_req, dtype=torch.int32, device=dev)
+        re = torch.zeros(w.n_req, dtype=torch.int32, device=dev)
+        bw = api.Batch(s.batch.cu_rows, s.batch.parent, s.batch.tokens, w.max_rows,
+                       row_begin=rb, row_end=re)
+        for _ in range(n_rep):
+            if flush_l2:
+                flush_buf.fill_(1)
+            s.restore_cache_state()
+            for c in range(len(sched)):
+                api.sv_chunk_windows(s.batch, c, chunk, s.done, rb, re)
+                m = (ev(), ev(), ev())
+                m[0].record(stream)
+                s.attend(bw)
+                m[1].record(stream)
+                s.accept(bw)
+                m[2].record(stream)
+                marks.append(m)
+            s.commit()
+        torch.cuda.synchronize()
+        t_att = sum(m[0].elapsed_time(m[1]) for m in marks) / 1e3 / n_rep
+        t_acc = sum(m[1].elapsed_time(m[2]) for m in marks) / 1e3 / n_rep
+    else:
+        b = s.batch_sel if mode == "budget" else s.batch
+        for _ in range(n_rep):
+            if flush_l2:
+                flush_buf.fill_(1)
+            s.restore_cache_state()
+            m = (ev(), ev(), ev(), ev())
+            m[0].record(stream)
+            if mode == "budget":
+                s.select()
+            m[1].record(stream)
+            s.attend(b)
+            m[2].record(stream)
+            s.accept(b)
+            m[3].record(stream)
+            s.commit(b)
+            marks.append(m)
+        torch.cuda.synchronize()
+        t_sel = sum(m[0].elapsed_time(m[1]) for m in marks) / 1e3 / n_rep
+        t_att = sum(m[1].elapsed_time(m[2]) for m in marks) / 1e3 / n_rep
+        t_acc = sum(m[2].elapsed_time(m[3]) for m in marks) / 1e3 / n_rep
+    att_gbs = sum(att_b) / t_att / 1e9
+    acc_gbs = sum(acc_b) / t_acc / 1e9
+    calls = {"attend": {"us_per_step": t_att * 1e6, "GB/s": att_gbs},
+             "accept": {"us_per_step": t_acc * 1e6, "GB/s": acc_gbs}}
+    if mode == "budget":
+        calls["select_budget"] = {"us_per_step": t_sel * 1e6}
 
-    # ---- one-pass attention and accept on the whole batch (no chunking) ----
-    full_sched = [(i, 0, int(w.cu_rows[i + 1] - w.cu_rows[i])) for i in range(w.n_req)]
-    t1 = torch.cuda.Event(enable_timing=True)
-    t2 = torch.cuda.Event(enable_timing=True)
-    t3 = torch.cuda.Event(enable_timing=True)
-    for _ in range(3):
-        s.attend(); s.accept()
-    torch.cuda.synchronize()
-    t1.record(stream)
-    for _ in range(n_rep):
-        s.attend()
-    t2.record(stream)
-    for _ in range(n_rep):
-        s.accept()
-    t3.record(stream)
-    torch.cuda.synchronize()
-    op_att = t1.elapsed_time(t2) / 1e3 / n_rep
-    op_acc = t2.elapsed_time(t3) / 1e3 / n_rep
-    op_att_b = attend_bytes(w, full_sched)
-    op_acc_b = accept_bytes(w, full_sched, al, s.T)
+    # ---- one-pass attention and accept on the whole batch (chunked workload) ----
+    if mode == "chunked":
+        full = launch_windows(w, "onepass", al)[0]
+        op_att = timed(lambda: s.attend(), n_rep)
+        op_acc = timed(lambda: s.accept(), n_rep)
+        calls["attend_onepass"] = {"us": op_att * 1e6, "GB/s": attend_bytes(w, full) / op_att / 1e9}
+        calls["accept_onepass"] = {"us": op_acc * 1e6,
+                                   "GB/s": accept_bytes(w, full, al, T) / op_acc / 1e9}
+        s.run()  # back to the chunked step's state
 
     # ---- end to end through host buffers ----
     pin = lambda t: t.cpu().pin_memory()
-    h_q, h_tgt, h_drf = pin(s.q), pin(s.target), pin(s.draft)
-    h_tok, h_par, h_cu = pin(s.batch.tokens), pin(s.batch.parent), pin(s.batch.cu_rows)
-    h_out = torch.empty_like(s.out, device="cpu").pin_memory()
-    h_al = torch.empty_like(s.accepted_len, device="cpu").pin_memory()
-    h_nodes = torch.empty_like(s.accepted_nodes, device="cpu").pin_memory()
-    h_nt = torch.empty_like(s.next_token, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_tgt, h_drf, h_tok, h_par, h_cu))
-    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_al, h_nodes, h_nt))
-    n_e2e = max(5, args.steps // 4)
-    barrier()
-    torch.cuda.synchronize()
-    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2.record(stream)
-    for _ in range(n_e2e):
-        s.q.copy_(h_q, non_blocking=True)
-        s.target.copy_(h_tgt, non_blocking=True)
-        s.draft.copy_(h_drf, non_blocking=True)
-        s.batch.tokens.copy_(h_tok, non_blocking=True)
-        s.batch.parent.copy_(h_par, non_blocking=True)
-        s.batch.cu_rows.copy_(h_cu, non_blocking=True)
+    ins = [(s.q, pin(s.q)), (s.target, pin(s.target)), (s.batch.tokens, pin(s.batch.tokens)),
+           (s.batch.parent, pin(s.batch.parent)), (s.batch.cu_rows, pin(s.batch.cu_rows))]
+    if s.draft is not None:
+        ins.append((s.draft, pin(s.draft)))
+    if mode == "budget":
+        ins += [(s.cond, pin(s.cond)), (s.gamma, pin(s.gamma)), (s.sps, pin(s.sps))]
+    outs = [(torch.empty_like(t, device="cpu").pin_memory(), t)
+            for t in (s.out, s.accepted_len, s.accepted_nodes, s.next_token)]
+    h2d = sum(h.numel() * h.element_size() for _, h in ins)
+    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+
+    def e2e_step():
+        for d, h in ins:
+            d.copy_(h, non_blocking=True)
         s.run()
-        h_out.copy_(s.out, non_blocking=True)
-        h_al.copy_(s.accepted_len, non_blocking=True)
-        h_nodes.copy_(s.accepted_nodes, non_blocking=True)
-        h_nt.copy_(s.next_token, non_blocking=True)
-    e3.record(stream)
-    torch.cuda.synchronize()
+        for h, d in outs:
+            h.copy_(d, non_blocking=True)
+
     barrier()
-    t_e2e = max_over_ranks(e2.elapsed_time(e3) / 1e3 / n_e2e)
+    torch.cuda.synchronize()
+    t_e2e = max_over_ranks(timed(e2e_step, max(5, args.steps // 4)))
+    barrier()
     clk = clocks.stop()
     res2 = s.results()
     assert np.array_equal(res2["accepted_len"], al), "steps are not reproducible"
@@ -397,61 +468,66 @@ def main():
             dist.destroy_process_group()
         return
 
-    import json as _json
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(peaks_path):
-        peaks = _json.load(open(peaks_path))
-        hbm_peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+        hbm_peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
     else:
         hbm_peak, peak_src = 6800.0, "fallback"
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "attend_traffic.json")
     if os.path.exists(tr_path):
-        tr = _json.load(open(tr_path))
+        tr = json.load(open(tr_path))
         if tr.get("workload") == args.workload and tr.get("kernel_rev") == KERNEL_REV:
             traffic = tr.get("bytes_per_launch")
+    for c in calls.values():
+        if "GB/s" in c:
+            c["frac"] = c["GB/s"] / hbm_peak
 
-    launches_per_step = n_chunks * 5 + 2
+    n_launch = len(sched)
+    per_accept = 3 if T > 0 else 2
+    if mode == "chunked":
+        launches_per_step = n_launch * (2 + 1 + per_accept) + 2
+    else:
+        launches_per_step = 2 + per_accept + 2 + (1 if mode == "budget" else 0)
     value = world * rows_attended / t_step
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 attention (fp32 accumulate), fp32 softmax",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 attention (fp32 accumulate), fp32 softmax",
         "data": "synthetic",
-        "config": {"workload": workload_description(w.cfg), "global_batch": w.n_req * world,
-                   "rows_per_step": int(w.total_rows), "rows_attended_per_step": int(rows_attended),
-                   "chunk": chunk, "vocab": int(w.target_logits.shape[1]),
-                   "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (1.7 GB KV, 0.36 GB logits)"},
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "mode": mode,
+                   "global_batch": w.n_req * world, "rows_per_step": int(w.total_rows),
+                   "rows_attended_per_step": int(rows_attended),
+                   "vocab": int(w.target_logits.shape[1]), "parallelism": f"replicas x{world}",
+                   "l2": ("flushed between steps (512 MB write outside the timed events)"
+                          if flush_l2 else "inputs larger than L2, no flush")},
         "verify_steps_per_s": world / t_step,
         "accepted_tokens_per_s": world * accepted_tokens / t_step,
         "roofline": {"bound": "hbm", "achieved": att_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": att_gbs / hbm_peak, "traffic": traffic,
-                     "kernel": "sv_tree_attend (plan + split-KV attention + merge), chunked launches",
+                     "kernel": "sv_tree_attend (plan + TMA split-KV attention with fused merge)",
                      "peak_source": f"{peak_src} hbm_gbs",
-                     "bytes_per_launch": sum(att_b) / n_chunks,
-                     "us_per_launch": 1e6 * att_time / n_chunks},
-        "calls": {
-            "attend_chunked": {"us_per_step": att_time * 1e6, "GB/s": att_gbs, "frac": att_gbs / hbm_peak},
-            "accept_chunked": {"us_per_step": acc_time * 1e6, "GB/s": acc_gbs, "frac": acc_gbs / hbm_peak},
-            "attend_onepass": {"us": op_att * 1e6, "GB/s": op_att_b / op_att / 1e9,
-                               "frac": op_att_b / op_att / 1e9 / hbm_peak},
-            "accept_onepass": {"us": op_acc * 1e6, "GB/s": op_acc_b / op_acc / 1e9,
-                               "frac": op_acc_b / op_acc / 1e9 / hbm_peak},
-        },
+                     "launches_per_step": n_launch,
+                     "bytes_per_launch": sum(att_b) / n_launch,
+                     "us_per_launch": 1e6 * t_att / n_launch},
+        "calls": calls,
         "e2e": {"value": world * rows_attended / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if mode == "chunked":
+        line["config"]["chunk"] = chunk
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, mode)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
 # Revision tag of the attention kernel the stored ncu traffic belongs to.
-KERNEL_REV = "attend-v2"
+KERNEL_REV = "attend-tma-v1"
 
 if __name__ == "__main__":
     main()
