@@ -484,11 +484,12 @@ def main():
             c["frac"] = c["GB/s"] / hbm_peak
 
     n_launch = len(sched)
-    per_accept = 3 if T > 0 else 2
+    race = 1 if T > 0 else 0
+    # attention: plan + attend; accept: list + stats + decide (+ race); commit: copy + release
     if mode == "chunked":
-        launches_per_step = n_launch * (2 + 1 + per_accept) + 2
+        launches_per_step = n_launch * (1 + 2 + 2 + race) + 2
     else:
-        launches_per_step = 2 + per_accept + 2 + (1 if mode == "budget" else 0)
+        launches_per_step = 2 + 3 + race + 2 + (1 if mode == "budget" else 0)
     value = world * rows_attended / t_step
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -219,7 +219,7 @@ sv_status sv_accept(const sv_batch* batch, const float* target_logits, const flo
  * loads the library and is held until the process exits.
  * Limits and behaviour:
  *   - Problems whose sv_accept_workspace() exceeds
- *     SV_ACCEPT_STATIC_SCRATCH_BYTES (4 MiB; any batch of up to 45,000
+ *     SV_ACCEPT_STATIC_SCRATCH_BYTES (4 MiB; any batch of up to 40,000
  *     packed rows fits) are refused with SV_ERR_WORKSPACE_TOO_SMALL before
  *     anything is enqueued; use sv_accept with a workspace beyond that.
  *   - The first call on a device, with that device current, looks up the

@@ -37,9 +37,7 @@ namespace acc {
 
 struct StatPart {
   float m;      // T > 0: max of x; T == 0: max raw logit
-  float l;      // T > 0: sum exp(x - m)
-  int amax;     // T == 0: lowest index of the max
-  int pad;
+  float lv;     // T > 0: sum exp(x - m); T == 0: bits of the lowest index of the max
 };
 
 struct Job {
@@ -61,8 +59,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Slices per row (stats) and per request (race): about 32 warps per SM in
 // flight, slices of at least 2 KB.
+constexpr int kMaxSlices = 64;  // merge_rows reads slices lane and lane + 32
+
 inline int stats_chunks(int rows_bound, int V) {
-  const int maxc = max(1, min(256, V / 512));
+  const int maxc = max(1, min(kMaxSlices, V / 512));
   const int want = (kNumSMs * 32 + 2 * rows_bound - 1) / max(1, 2 * rows_bound);
   return max(1, min(want, maxc));
 }
@@ -78,7 +78,7 @@ Layout layout(int R, int total_rows, int V, int maxw) {
   L.maxw = max(1, min(maxw, kMaxRows));
   const long bound = min((long)total_rows, (long)R * L.maxw);
   L.nch = stats_chunks((int)max(1L, bound), V);
-  L.nch_cap = max(L.nch, min(min(64, V / 2048), 16384 / max(1, total_rows)));
+  L.nch_cap = max(L.nch, min(min(kMaxSlices, V / 2048), 16384 / max(1, total_rows)));
   L.nch_r = race_chunks(R, V);
   L.nch_r_cap = max(L.nch_r, min(min(256, V / 512), 16384 / max(1, R)));
   size_t off = 0;
@@ -86,7 +86,6 @@ Layout layout(int R, int total_rows, int V, int maxw) {
   L.jobs = off; off += align256(sizeof(Job) * (size_t)R);
   L.race = off; off += align256(sizeof(RacePart) * (size_t)R * L.nch_r_cap);
   L.race_tickets = off; off += align256(sizeof(int) * (size_t)R);
-  L.stat_tickets = off; off += align256(sizeof(int) * (size_t)R);
   L.act = off; off += align256(sizeof(int) * (size_t)(R + 1));  // act[R] = count
   L.total = off;
   return L;
@@ -96,12 +95,13 @@ Layout layout(int R, int total_rows, int V, int maxw) {
 // every kernel of a call): about 32 warps per SM of work.
 __device__ __forceinline__ int stats_slices(const Layout& L, int count, int ntypes) {
   const long slots = (long)max(1, count) * L.maxw * ntypes;
-  const long want = (kNumSMs * 32 + slots - 1) / slots;
+  const long want = (2L * kNumSMs * 32 + slots - 1) / slots;  // about 2 slices per warp
   return (int)max((long)L.nch, min(want, (long)L.nch_cap));
 }
-__device__ __forceinline__ int race_slices(const Layout& L, int count) {
-  const long want = (kNumSMs * 32 + max(1, count) - 1) / max(1, count);
-  return (int)max((long)L.nch_r, min(want, (long)L.nch_r_cap));
+__device__ __forceinline__ int race_slices(const Layout& L, int count, int V) {
+  const long want = (2L * kNumSMs * 32 + max(1, count) - 1) / max(1, count);
+  const long cap = min((long)L.nch_r_cap, max(1L, (long)V / 2048));  // slices of >= 8 KB
+  return (int)max((long)L.nch_r, min(want, cap));
 }
 
 struct Args {
@@ -142,7 +142,6 @@ __global__ void __launch_bounds__(1024) list_kernel(Args a, int chunk, int cs, c
   const int R = a.bt.n_req;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int* act = reinterpret_cast<int*>(a.ws + a.L.act);
-  int* tickets = reinterpret_cast<int*>(a.ws + a.L.stat_tickets);
   __shared__ int s_warp[32];
   __shared__ int s_carry;
   if (tid == 0) s_carry = 0;
@@ -172,7 +171,6 @@ __global__ void __launch_bounds__(1024) list_kernel(Args a, int chunk, int cs, c
         if (!w.ok) flag(a.dev_status, SV_DEV_BAD_WINDOW);
         else if (w.b < w.e && !(w.b > 0 && a.next_token[i] >= 0)) f = 1;
       }
-      if (f) tickets[i] = 0;
     }
     // exclusive scan of the flags
     int x = f;
@@ -206,36 +204,47 @@ __global__ void __launch_bounds__(1024) list_kernel(Args a, int chunk, int cs, c
 // ---------------------------------------------------------------- decide --
 struct DecideSmem {
   float mp[kMaxRows], lp[kMaxRows], mq[kMaxRows], lq[kMaxRows];
-  int am[kMaxRows], len[kMaxRows], child[kMaxRows];
+  int am[kMaxRows], len[kMaxRows], child[kMaxRows], par[kMaxRows], tok[kMaxRows];
 };
 
-__device__ __forceinline__ void row_ml(const Args& a, int nch, int r, int type, float& m, float& l) {
-  const StatPart* parts = reinterpret_cast<const StatPart*>(a.ws + a.L.parts) +
-                          ((size_t)r * 2 + type) * nch;
+// Merge the slice partials of rows [r0, r0 + n) of one type, 4 rows per
+// round of loads (each lane takes slices lane, lane + 32), into the lane-0
+// outputs m_out / lv_out (shared memory).
+__device__ __forceinline__ void merge_rows(const Args& a, int nch, int r0, int n, int type,
+                                           float* m_out, float* lv_out) {
   const int lane = threadIdx.x & 31;
-  m = -INFINITY;
-  l = 0.f;
-  for (int c = lane; c < nch; c += 32) merge_ml(m, l, __ldcg(&parts[c].m), __ldcg(&parts[c].l));
+  const float T = a.T;
+  const StatPart* parts = reinterpret_cast<const StatPart*>(a.ws + a.L.parts);
+  for (int k0 = 0; k0 < n; k0 += 4) {
+    float2 v[4][2];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-    merge_ml(m, l, m2, l2);
-  }
-}
-
-__device__ __forceinline__ void row_argmax(const Args& a, int nch, int r, float& v, int& idx) {
-  const StatPart* parts = reinterpret_cast<const StatPart*>(a.ws + a.L.parts) +
-                          ((size_t)r * 2) * nch;
-  const int lane = threadIdx.x & 31;
-  v = -INFINITY;
-  idx = 0x7fffffff;
-  for (int c = lane; c < nch; c += 32) merge_am(v, idx, __ldcg(&parts[c].m), __ldcg(&parts[c].amax));
+    for (int k = 0; k < 4; ++k)
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-    merge_am(v, idx, v2, i2);
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+        v[k][h] = make_float2(-INFINITY, T > 0.f ? 0.f : __int_as_float(0x7fffffff));
+        if (k0 + k < n && c < nch)
+          v[k][h] = __ldcg(reinterpret_cast<const float2*>(
+              parts + ((size_t)(r0 + k0 + k) * 2 + type) * nch + c));
+      }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float m = v[k][0].x, lv = v[k][0].y;
+      int am = __float_as_int(lv);
+      if (T > 0.f) merge_ml(m, lv, v[k][1].x, v[k][1].y);
+      else merge_am(m, am, v[k][1].x, __float_as_int(v[k][1].y));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, lv, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, am, o);
+        if (T > 0.f) merge_ml(m, lv, m2, l2); else merge_am(m, am, m2, i2);
+      }
+      if (lane == 0 && k0 + k < n) {
+        m_out[k0 + k] = m;
+        lv_out[k0 + k] = T > 0.f ? lv : __int_as_float(am);
+      }
+    }
   }
 }
 
@@ -254,15 +263,18 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   bool chain = true, badp = false, badt = false;
   for (int j = lane; j < w.rows; j += 32) {
     const int p = a.bt.parent[cu + j];
+    const int t = a.bt.tokens[cu + j];
+    sm.par[j] = p;
+    sm.tok[j] = t;
     if (j == 0) {
       if (p != -1) badp = true;
     } else {
       if (p < 0 || p >= j) badp = true;
       if (p != j - 1) chain = false;
-      const int t = a.bt.tokens[cu + j];
       if (t < 0 || t >= V) badt = true;
     }
   }
+  __syncwarp();
   badp = __any_sync(0xffffffffu, badp);
   badt = __any_sync(0xffffffffu, badt);
   chain = __all_sync(0xffffffffu, chain);
@@ -289,16 +301,14 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   float* rs = a.row_stats;
 
   if (a.T == 0.f) {
-    for (int r = w.b; r < w.e; ++r) {
-      float v;
-      int idx;
-      row_argmax(a, nch, cu + r, v, idx);
-      if (lane == 0) {
-        sm.am[r] = idx;
-        if (rs) {
-          rs[(size_t)(cu + r) * 4 + 0] = v;
-          rs[(size_t)(cu + r) * 4 + 1] = (float)idx;
-        }
+    merge_rows(a, nch, cu + w.b, w.e - w.b, 0, sm.mp + w.b, sm.lp + w.b);
+    __syncwarp();
+    for (int r = w.b + lane; r < w.e; r += 32) {
+      const int idx = __float_as_int(sm.lp[r]);
+      sm.am[r] = idx;
+      if (rs) {
+        rs[(size_t)(cu + r) * 4 + 0] = sm.mp[r];
+        rs[(size_t)(cu + r) * 4 + 1] = (float)idx;
       }
     }
     __syncwarp();
@@ -307,7 +317,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
         const int jmax = min(w.e, w.lim - 1);
         for (int j = w.b + 1; j <= jmax; ++j) {
           const int am = sm.am[j - 1];
-          if (a.bt.tokens[cu + j] == am) {
+          if (sm.tok[j] == am) {
             len = j;
             nodes[j] = j;
           } else {
@@ -322,7 +332,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
       for (int n = w.rows - 1; n >= 0; --n) {
         int best = 0, bc = -1;
         for (int c = n + 1 + lane; c < w.rows; c += 32) {
-          if (a.bt.parent[cu + c] == n && a.bt.tokens[cu + c] == sm.am[n]) {
+          if (sm.par[c] == n && sm.tok[c] == sm.am[n]) {
             const int cand = 1 + sm.len[c];
             if (cand > best || (cand == best && bc >= 0 && c < bc)) { best = cand; bc = c; }
           }
@@ -360,24 +370,15 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
 
   // ---- T > 0: speculative sampling on a chain ----
   const int jmax = min(w.e, w.lim - 1);
-  for (int r = w.b; r < w.e; ++r) {
-    float m, l;
-    row_ml(a, nch, cu + r, 0, m, l);
-    if (lane == 0) {
-      sm.mp[r] = m;
-      sm.lp[r] = l;
-      if (rs) rs[(size_t)(cu + r) * 4 + 0] = m + logf(l);
-    }
-    if (r + 1 <= w.lim - 1) {
-      row_ml(a, nch, cu + r, 1, m, l);
-      if (lane == 0) {
-        sm.mq[r] = m;
-        sm.lq[r] = l;
-        if (rs) rs[(size_t)(cu + r) * 4 + 1] = m + logf(l);
-      }
-    }
-  }
+  const int nq = max(0, min(w.e, w.lim - 1) - w.b);  // draft rows with a tested child
+  merge_rows(a, nch, cu + w.b, w.e - w.b, 0, sm.mp + w.b, sm.lp + w.b);
+  merge_rows(a, nch, cu + w.b, nq, 1, sm.mq + w.b, sm.lq + w.b);
   __syncwarp();
+  if (rs)
+    for (int r = w.b + lane; r < w.e; r += 32) {
+      rs[(size_t)(cu + r) * 4 + 0] = sm.mp[r] + logf(sm.lp[r]);
+      if (r - w.b < nq) rs[(size_t)(cu + r) * 4 + 1] = sm.mq[r] + logf(sm.lq[r]);
+    }
   // Lane j - b - 1 evaluates draft j's ratio; lane 0 then scans them.
   const float T = a.T;
   const int nd = jmax - w.b;  // drafts decided by this window
@@ -385,7 +386,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   {
     const int j = w.b + 1 + lane;
     if (lane < nd) {
-      const int x = a.bt.tokens[cu + j];
+      const int x = sm.tok[j];
       const size_t off = (size_t)(cu + j - 1) * V + x;
       const float xp = a.target[off] / T;
       const float xq = a.draft[off] / T;
@@ -406,7 +407,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
     const int j = w.b + 1 + k;
     const double rk = __shfl_sync(0xffffffffu, ratio, k & 31);
     if (k >= 32) {  // windows longer than a warp: evaluate the rest serially
-      const int x = a.bt.tokens[cu + j];
+      const int x = sm.tok[j];
       const size_t off = (size_t)(cu + j - 1) * V + x;
       const double p = exp((double)(a.target[off] / T) - (double)sm.mp[j - 1]) / (double)sm.lp[j - 1];
       const double q = exp((double)(a.draft[off] / T) - (double)sm.mq[j - 1]) / (double)sm.lq[j - 1];
@@ -459,9 +460,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
 template <bool VEC>
 __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
   griddep_entry();
-  __shared__ DecideSmem s_dec[kStatThreads / 32];
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
-  int* tickets = reinterpret_cast<int*>(a.ws + a.L.stat_tickets);
   const int R = a.bt.n_req;
   const int count = act[R];
   const float T = a.T;
@@ -547,24 +546,28 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
       const int i2 = __shfl_xor_sync(0xffffffffu, am, o);
       if (T > 0.f) merge_ml(m, l, m2, l2); else merge_am(m, am, m2, i2);
     }
-    int last = 0;
     if (lane == 0) {
       StatPart sp;
       sp.m = m;
-      sp.l = l;
-      sp.amax = am;
-      sp.pad = 0;
+      sp.lv = T > 0.f ? l : __int_as_float(am);
       reinterpret_cast<StatPart*>(a.ws + a.L.parts)[((size_t)r * 2 + type) * nch + c] = sp;
-      __threadfence();
-      const int expected = nch * ((w.e - w.b) + ndraft);
-      last = atomicAdd(tickets + i, 1) == expected - 1;
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      __threadfence();
-      decide_request(a, nch, i, s_dec[wid]);
     }
   }
+}
+
+// ---------------------------------------------------------------- decide --
+// One warp per active request, once every row partial exists.
+constexpr int kDecideWarps = 4;
+
+__global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
+  griddep_entry();
+  __shared__ DecideSmem s_dec[kDecideWarps];
+  const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
+  const int count = act[a.bt.n_req];
+  const int nch = stats_slices(a.L, count, a.T > 0.f ? 2 : 1);
+  const int wid = threadIdx.x >> 5;
+  for (int ai = blockIdx.x * kDecideWarps + wid; ai < count; ai += gridDim.x * kDecideWarps)
+    decide_request(a, nch, act[ai], s_dec[wid]);
 }
 
 // ------------------------------------------------------------------ race --
@@ -580,7 +583,7 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   const int R = a.bt.n_req;
   const int count = act[R];
-  const int nch = race_slices(a.L, count);
+  const int nch = race_slices(a.L, count, a.V);
   const int chl = chunk_len(a.V, nch);
   const long total = (long)count * nch;
   const float T = a.T;
@@ -623,13 +626,19 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
       return fmaxf(p - ex2(fmaf(div_by(lqv, T, rT), kLog2e, -mqb)) * inv_lq, 0.f);
     };
     if (VEC) {
-      for (int v = lo + 4 * lane; v < hi; v += 128) {
+      // uniform trip count so that the lanes can share their thresholds: the
+      // best key any lane has seen bounds the winner from below
+      float wthr = -1.f;
+      for (int base = lo; base < hi; base += 128) {
+        wthr = fmaxf(wthr, warp_max(thr));
+        const int v = base + 4 * lane;
+        if (v >= hi) continue;
         const float4 xp = __ldcs(reinterpret_cast<const float4*>(lp) + (v >> 2));
         float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
         if (resid) xq = __ldcs(reinterpret_cast<const float4*>(lq) + (v >> 2));
         const float w0 = weight(xp.x, xq.x), w1 = weight(xp.y, xq.y);
         const float w2 = weight(xp.z, xq.z), w3 = weight(xp.w, xq.w);
-        if (fmaxf(fmaxf(w0, w1), fmaxf(w2, w3)) < thr) continue;
+        if (fmaxf(fmaxf(w0, w1), fmaxf(w2, w3)) < fmaxf(thr, wthr)) continue;
         const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
         take(w0, -logf(race_u(bits.a)), v);
         take(w1, -logf(race_u(bits.b)), v + 1);
@@ -758,6 +767,8 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
   if (sv::launch(vec ? stats_kernel<true> : stats_kernel<false>, gs, kStatThreads, 0, s, a) !=
       cudaSuccess)
     return SV_ERR_CUDA;
+  const unsigned gd = (unsigned)max(1, min((bt->n_req + kDecideWarps - 1) / kDecideWarps, kNumSMs * 8));
+  if (sv::launch(decide_kernel, gd, kDecideWarps * 32, 0, s, a) != cudaSuccess) return SV_ERR_CUDA;
   if (temperature > 0.f) {
     const long ritems = (long)bt->n_req * a.L.nch_r_cap;
     const long rwarps = kRaceThreads / 32;

@@ -662,21 +662,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int kQuads = D / 4;
   for (int x = tid; x < Mu * kQuads; x += kThreads) {
     const int vr = x / kQuads, c4 = x % kQuads;
-    float Mx = -INFINITY;
-    for (int sp = 0; sp < ri.nsplit; ++sp)
-      Mx = fmaxf(Mx, __ldcg(ml_all + ((size_t)(gidx + sp) * kTileRows + vr) * 2));
-    const float base = Mx == -INFINITY ? 0.f : Mx;
-    float L = 0.f;
+    // one online pass over the splits (running max, rescaled sums); the
+    // loads of consecutive splits are independent and overlap
+    float Mx = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int sp = 0; sp < ri.nsplit; ++sp) {
       const size_t row = (size_t)(gidx + sp) * kTileRows + vr;
-      const float wgt = exp2f(__ldcg(ml_all + row * 2) - base);
-      L += __ldcg(ml_all + row * 2 + 1) * wgt;
+      const float2 ml2 = __ldcg(reinterpret_cast<const float2*>(ml_all + row * 2));
       const float4 o4 = __ldcg(reinterpret_cast<const float4*>(op_all + row * D) + c4);
-      acc.x += wgt * o4.x;
-      acc.y += wgt * o4.y;
-      acc.z += wgt * o4.z;
-      acc.w += wgt * o4.w;
+      const float nm = fmaxf(Mx, ml2.x);
+      if (nm == -INFINITY) continue;
+      const float s_old = exp2f(Mx - nm), s_new = exp2f(ml2.x - nm);
+      L = L * s_old + ml2.y * s_new;
+      acc.x = acc.x * s_old + o4.x * s_new;
+      acc.y = acc.y * s_old + o4.y * s_new;
+      acc.z = acc.z * s_old + o4.z * s_new;
+      acc.w = acc.w * s_old + o4.w * s_new;
+      Mx = nm;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const int vgl = vr0 + vr;

@@ -17,7 +17,7 @@ namespace acc {
 // (race) when every listed request is active; the kernels use more slices,
 // up to nch_cap / nch_r_cap, when fewer requests are active.
 struct Layout {
-  size_t parts, jobs, race, race_tickets, stat_tickets, act, total;
+  size_t parts, jobs, race, race_tickets, act, total;
   int nch, nch_cap, nch_r, nch_r_cap, maxw;
 };
 Layout layout(int R, int total_rows, int V, int maxw);

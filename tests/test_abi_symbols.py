@@ -66,12 +66,12 @@ def test_host_side_validation_without_gpu(lib):
 
 
 def test_static_scratch_holds_the_documented_batch(lib):
-    # sv_accept_static promises that any batch of up to 45,000 packed rows fits
+    # sv_accept_static promises that any batch of up to 40,000 packed rows fits
     # its fixed scratch array; sv_accept_workspace is a host function.
     import ctypes
     from speculative_decoding_verification_padding_gb300 import _native as N
     worst = 0
-    for rows in (1, 100, 2432, 10000, 30000, 45000):
+    for rows in (1, 100, 2432, 10000, 30000, 40000):
         for per in (1, 2, 5, 9, 128):
             R = max(1, rows // per)
             for maxr in {min(128, per), 128}:
