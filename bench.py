@@ -287,8 +287,8 @@ def main():
         return
 
     import torch
-    import torch.distributed as dist
     from speculative_decoding_verification_padding_gb300 import api
+    from speculative_decoding_verification_padding_gb300.replicas import Replicas
     from speculative_decoding_verification_padding_gb300 import workloads as wl
     from speculative_decoding_verification_padding_gb300.step import DeviceStep
 
@@ -296,8 +296,7 @@ def main():
         raise SystemExit("bench.py needs a CUDA device")
     torch.cuda.set_device(local_rank)
     dev = f"cuda:{local_rank}"
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device(dev))
+    reps = Replicas.from_env("nccl", device=dev)
 
     w = wl.make_workload(wl.config(args.workload),
                          ctx_scale=args.ctx_scale if args.profile_steps else 1.0)
@@ -325,16 +324,7 @@ def main():
     flush_l2 = step_bytes < 2 * L2_BYTES
     flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if flush_l2 else None
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_over_ranks = reps.barrier, reps.max_over_ranks
 
     def timed(fn, n):
         """Mean seconds per call of fn over n calls (flushing L2 between calls
@@ -463,9 +453,9 @@ def main():
     res2 = s.results()
     assert np.array_equal(res2["accepted_len"], al), "steps are not reproducible"
 
-    if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
+    rows_all = reps.sum_over_ranks(rows_attended)  # every rank joins before the leader reports
+    if not reps.leader:
+        reps.close()
         return
 
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -485,12 +475,13 @@ def main():
 
     n_launch = len(sched)
     race = 1 if T > 0 else 0
-    # attention: plan + attend; accept: list + stats + decide (+ race); commit: copy + release
+    # attention: plan + attend; accept: list + stats + decide (+ race); commit: copy + release.
+    # Chunked: list + plan + attend + stats + decide per chunk, one race after the last.
     if mode == "chunked":
-        launches_per_step = n_launch * (1 + 2 + 2 + race) + 2
+        launches_per_step = n_launch * (1 + 2 + 2) + race + 2
     else:
         launches_per_step = 2 + 3 + race + 2 + (1 if mode == "budget" else 0)
-    value = world * rows_attended / t_step
+    value = rows_all / t_step
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
@@ -513,7 +504,7 @@ def main():
                      "bytes_per_launch": sum(att_b) / n_launch,
                      "us_per_launch": 1e6 * t_att / n_launch},
         "calls": calls,
-        "e2e": {"value": world * rows_attended / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": rows_all / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -523,8 +514,7 @@ def main():
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, mode)
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    reps.close()
 
 
 # Revision tag of the attention kernel the stored ncu traffic belongs to.

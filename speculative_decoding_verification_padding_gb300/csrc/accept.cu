@@ -8,24 +8,27 @@
 // the standard lossless speculative-sampling rule (not printed on the pages).
 //
 // Kernels, in stream order:
-//   list   (1 CTA)   the requests whose window is not empty, in request
-//                    order, and a cleared ticket for each (in chunked
-//                    verification the window kernel does this instead).
-//   stats  (grid-stride over active request x window row x {target, draft}
-//                    x vocab chunk)
-//                    one pass over the row slice with 128-bit loads: online
+//   list   (1 CTA)   the requests whose window is not empty and not yet
+//                    decided, in request order (in chunked verification
+//                    the chunk's list pass also writes the windows, and on
+//                    the first chunk clears every request's sampling job).
+//   stats  (warps, grid-stride over active request x window row x
+//                    {target, draft} x vocabulary slice)
+//                    one pass over the slice with 128-bit loads: online
 //                    max / sum of exp(x - max) of x = logit / T (T > 0), or
 //                    max and lowest-index argmax of the raw logits (T = 0);
-//                    one partial per slice.  The CTA that finishes a
-//                    request's last slice (atomic ticket) runs the decision
-//                    for it with one warp: the chain scan (or the tree
-//                    descent) with Philox uniforms; it writes the path and,
-//                    for T > 0, a sampling job for the emitted token.
-//   race   (grid-stride over active request x vocab chunk)
+//                    one 8-byte partial per slice.
+//   decide (one warp per active request)
+//                    merges the slice partials of the window rows, then the
+//                    chain scan (or the tree descent) with Philox uniforms;
+//                    writes the path and, for T > 0, a sampling job for the
+//                    emitted token.
+//   race   (warps, grid-stride over request x vocabulary slice)
 //                    the exponential race argmax_v w_v / E_v over the job's
 //                    row(s), w = max(0, p - q) after a rejection or p for the
-//                    bonus token; the last CTA of a request (atomic ticket)
-//                    reduces the chunk winners.
+//                    bonus token; the warp that brings a request's last
+//                    slice (atomic ticket) reduces the slice winners.  A
+//                    chunked step runs it once, after its last chunk.
 
 #include <math.h>
 
@@ -120,6 +123,7 @@ struct Args {
   uint8_t* ws;
   Layout L;
   int32_t* dev_status;
+  int race_all;   // race kernel: every request 0..R-1 instead of the active list
 };
 
 __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2) {
@@ -166,6 +170,12 @@ __global__ void __launch_bounds__(1024) list_kernel(Args a, int chunk, int cs, c
         rb_out[i] = b;
         re_out[i] = e;
         f = (w.ok && b < e) ? 1 : 0;
+        if (chunk == 0) {
+          // The step's single race pass reads every request's job: none may
+          // be left over from an earlier call.
+          reinterpret_cast<Job*>(a.ws + a.L.jobs)[i].mode = 0;
+          reinterpret_cast<int*>(a.ws + a.L.race_tickets)[i] = 0;
+        }
       } else {
         const Window w = window_of(a.bt, i);
         if (!w.ok) flag(a.dev_status, SV_DEV_BAD_WINDOW);
@@ -453,10 +463,9 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
 }
 
 // ----------------------------------------------------------------- stats --
-// Warp-granular: every warp owns one slice of one row at a time, reduces it
-// with shuffles and arrives on its request's ticket itself, so no warp waits
-// for another; the warp that brings the last slice of a request runs the
-// decision for it.
+// Warp-granular: every warp owns one slice of one row at a time and reduces
+// it with shuffles into one partial (no warp waits for another); the
+// decision kernel merges the partials.
 template <bool VEC>
 __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
   griddep_entry();
@@ -582,7 +591,7 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
   griddep_entry();
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   const int R = a.bt.n_req;
-  const int count = act[R];
+  const int count = a.race_all ? R : act[R];
   const int nch = race_slices(a.L, count, a.V);
   const int chl = chunk_len(a.V, nch);
   const long total = (long)count * nch;
@@ -592,9 +601,11 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
   const long stride = (long)gridDim.x * (kRaceThreads / 32);
   for (long item = (long)blockIdx.x * (kRaceThreads / 32) + wid; item < total; item += stride) {
     const int c = (int)(item % nch);
-    const int i = act[item / nch];
+    const int i = a.race_all ? (int)(item / nch) : act[item / nch];
     // decide_request cleared every listed request's job before it could
-    // return early, so a non-zero mode here was written by this call.
+    // return early (and, for a whole chunked step, the first chunk's list
+    // pass cleared every request's), so a non-zero mode here was written by
+    // this call.
     const Job jb = reinterpret_cast<const Job*>(a.ws + a.L.jobs)[i];
     if (jb.mode == 0) continue;
     const bool resid = jb.mode == 1;
@@ -727,13 +738,31 @@ sv_status chunk_list(const sv_batch* bt, int chunk, int cs, const int32_t* done,
   return SV_OK;
 }
 
-// Enqueue the list pass (unless prebuilt), the statistics with the fused
-// decision, and the race.
+static sv_status launch_race(const Args& a, bool vec, cudaStream_t s) {
+  const long ritems = (long)a.bt.n_req * a.L.nch_r_cap;
+  const long rwarps = kRaceThreads / 32;
+  const unsigned gr = (unsigned)max(1L, min((ritems + rwarps - 1) / rwarps, (long)kNumSMs * 4));
+  if (sv::launch(vec ? race_kernel<true> : race_kernel<false>, gr, kRaceThreads, 0, s, a) !=
+      cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+static bool vec_ok(int32_t vocab, const float* target_logits, const float* draft_logits) {
+  return (vocab % 4 == 0) &&
+         ((((uintptr_t)target_logits) | ((uintptr_t)(draft_logits ? draft_logits : target_logits))) &
+          15) == 0;
+}
+
+// Enqueue the list pass (unless chunk_step), the statistics, the decision
+// and (unless chunk_step) the race.  chunk_step: the active list of `ws` was
+// written by chunk_list for this batch's windows, and the race is left to
+// race_all after the last chunk.
 sv_status run(const sv_batch* bt, const float* target_logits, const float* draft_logits,
               int32_t vocab, float temperature, uint64_t seed, int32_t* accepted_len,
               int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
               float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s,
-              int maxw, bool prebuilt_list) {
+              int maxw, bool chunk_step) {
   sv_status st = check_accept_args(bt, target_logits, draft_logits, vocab, temperature,
                                    accepted_len, accepted_nodes, next_token, ambiguous, ws);
   if (st != SV_OK || bt->n_req == 0 || bt->total_rows == 0) return st;
@@ -753,10 +782,10 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
   a.ws = static_cast<uint8_t*>(ws);
   a.L = layout(bt->n_req, bt->total_rows, vocab, maxw);
   a.dev_status = dev_status;
+  a.race_all = 0;
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
-  const bool vec = (vocab % 4 == 0) && ((((uintptr_t)target_logits) |
-                                         ((uintptr_t)(draft_logits ? draft_logits : target_logits))) & 15) == 0;
-  if (!prebuilt_list) {
+  const bool vec = vec_ok(vocab, target_logits, draft_logits);
+  if (!chunk_step) {
     if (sv::launch(list_kernel, 1, 1024, 0, s, a, -1, 0, (const int32_t*)nullptr,
                    (int32_t*)nullptr, (int32_t*)nullptr) != cudaSuccess)
       return SV_ERR_CUDA;
@@ -769,15 +798,27 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
     return SV_ERR_CUDA;
   const unsigned gd = (unsigned)max(1, min((bt->n_req + kDecideWarps - 1) / kDecideWarps, kNumSMs * 8));
   if (sv::launch(decide_kernel, gd, kDecideWarps * 32, 0, s, a) != cudaSuccess) return SV_ERR_CUDA;
-  if (temperature > 0.f) {
-    const long ritems = (long)bt->n_req * a.L.nch_r_cap;
-    const long rwarps = kRaceThreads / 32;
-    const unsigned gr = (unsigned)max(1L, min((ritems + rwarps - 1) / rwarps, (long)kNumSMs * 4));
-    if (sv::launch(vec ? race_kernel<true> : race_kernel<false>, gr, kRaceThreads, 0, s, a) !=
-        cudaSuccess)
-      return SV_ERR_CUDA;
-  }
+  if (temperature > 0.f && !chunk_step) return launch_race(a, vec, s);
   return SV_OK;
+}
+
+sv_status race_all(const sv_batch* bt, const float* target_logits, const float* draft_logits,
+                   int32_t vocab, float temperature, uint64_t seed, int32_t* next_token, void* ws,
+                   int maxw, int32_t* dev_status, cudaStream_t s) {
+  if (!(temperature > 0.f) || bt->n_req == 0 || bt->total_rows == 0) return SV_OK;
+  Args a{};
+  a.bt = *bt;
+  a.target = target_logits;
+  a.draft = draft_logits;
+  a.V = vocab;
+  a.T = temperature;
+  a.seed = seed;
+  a.next_token = next_token;
+  a.ws = static_cast<uint8_t*>(ws);
+  a.L = layout(bt->n_req, bt->total_rows, vocab, maxw);
+  a.dev_status = dev_status;
+  a.race_all = 1;
+  return launch_race(a, vec_ok(vocab, target_logits, draft_logits), s);
 }
 
 }  // namespace acc
@@ -810,9 +851,10 @@ extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
 // with that device current; make that first call before any stream capture.
 // All calls share the array: two calls whose work overlaps on the GPU (for
 // example on two streams) race on it.  Nothing in it has to start at zero:
-// the accept kernels write every scratch word before they read it (the list
-// pass clears each listed request's ticket, the decision clears its sampling
-// job and race ticket).
+// the accept kernels write every scratch word before they read it (the
+// decision clears each listed request's sampling job and race ticket before
+// anything reads them, and the statistics write every partial the decision
+// merges).
 
 #include <mutex>
 

@@ -122,5 +122,8 @@ extern "C" sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* bt
                   dev_status, s, chunk_size, true);
     if (st != SV_OK) return st;
   }
-  return SV_OK;
+  // Nothing in a later chunk depends on the drawn tokens: one race pass
+  // after the last chunk serves every request at once.
+  return acc::race_all(bt, target_logits, draft_logits, vocab, temperature, seed, next_token,
+                       acc_ws, chunk_size, dev_status, s);
 }

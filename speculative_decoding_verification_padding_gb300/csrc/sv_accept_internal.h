@@ -28,13 +28,20 @@ Layout layout(int R, int total_rows, int V, int maxw);
 sv_status chunk_list(const sv_batch* bt, int chunk, int cs, const int32_t* done, int32_t* rb,
                      int32_t* re, int32_t vocab, void* ws, int32_t* dev_status, cudaStream_t s);
 
-// The accept kernels.  prebuilt_list: the active list of `ws` was written by
-// chunk_list for this batch's windows (otherwise a list pass runs first).
+// The accept kernels.  chunk_step: the active list of `ws` was written by
+// chunk_list for this batch's windows (otherwise a list pass runs first),
+// and the residual / bonus draws are left to race_all.
 sv_status run(const sv_batch* bt, const float* target_logits, const float* draft_logits,
               int32_t vocab, float temperature, uint64_t seed, int32_t* accepted_len,
               int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
               float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s,
-              int maxw, bool prebuilt_list);
+              int maxw, bool chunk_step);
+
+// After the last chunk of a chunked step (T > 0): the residual or bonus draw
+// of every request whose decision set one, in a single pass.
+sv_status race_all(const sv_batch* bt, const float* target_logits, const float* draft_logits,
+                   int32_t vocab, float temperature, uint64_t seed, int32_t* next_token, void* ws,
+                   int maxw, int32_t* dev_status, cudaStream_t s);
 
 }  // namespace acc
 }  // namespace sv
