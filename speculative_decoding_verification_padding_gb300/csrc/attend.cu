@@ -11,7 +11,10 @@
 //                    request) and builds a length-weighted split-KV work list:
 //                    the keys of each (request, KV head, 64-row query tile)
 //                    are cut into splits of P pages so that about kUnitTarget
-//                    units exist; clears the per-group merge tickets.
+//                    units exist (P at least 32 pages, 64 when the work still
+//                    fills every SM); every unit gets a self-contained 48-byte
+//                    work item; clears the per-group merge tickets.  An empty
+//                    call (no keys anywhere) only publishes a zero count.
 //   attend (1 CTA per unit, 4 warps, 2 CTAs per SM)
 //                    the query rows of the whole GQA group (row x head packed
 //                    as "virtual rows") share every KV page.  Pages stream
@@ -47,12 +50,34 @@ constexpr int kStages = 3;       // TMA ring depth
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileRows = 64;    // virtual rows per unit
-constexpr int kUnitTarget = kNumSMs * 8;
-constexpr int kMinPagesPerSplit = 8;
+#ifndef SV_ATTN_UNIT_TARGET
+#define SV_ATTN_UNIT_TARGET (kNumSMs * 8)
+#endif
+#ifndef SV_ATTN_MIN_PAGES
+#define SV_ATTN_MIN_PAGES 32
+#endif
+constexpr int kUnitTarget = SV_ATTN_UNIT_TARGET;
+// Splits never go below kMinPagesPerSplit pages (each unit pays a start-up
+// of a few microseconds and a merge share), nor below twice that when the
+// work still gives every SM such a unit.
+constexpr int kMinPagesPerSplit = SV_ATTN_MIN_PAGES;
 constexpr int kMaxPagesPerSplit = 1024;  // block ids of a unit staged in shared memory
 
 struct ReqInfo {
   int ubase, nsplit, nrt, b, e, ctx, nblk, valid;
+};
+
+// One unit of the work list: everything its CTA needs to start (a single
+// 48-byte load, issued together with the header's unit count).
+struct __align__(16) WorkItem {
+  int i;       // request
+  int local;   // unit within the request: (row tile * Hkv + KV head) * nsplit + split
+  int nsplit, nblk, ctx, b, e;
+  int ubase;   // the request's first unit
+  int cu;      // the request's first packed row
+  int rows;    // the request's packed rows
+  int P;       // pages per split
+  int pad;
 };
 
 struct Header {
@@ -62,7 +87,7 @@ struct Header {
 };
 
 struct Layout {
-  size_t header, info, ubase, ureq, tickets, ml, o, total;
+  size_t header, info, ubase, work, tickets, ml, o, total;
   int ucap;
 };
 
@@ -81,7 +106,7 @@ inline Layout layout(int R, int total_rows, int group, int Hkv, int D, int max_b
   L.header = off; off += align256(sizeof(Header));
   L.info = off; off += align256(sizeof(ReqInfo) * (size_t)R);
   L.ubase = off; off += align256(sizeof(int) * (size_t)(R + 1));
-  L.ureq = off; off += align256(sizeof(int) * (size_t)L.ucap);
+  L.work = off; off += align256(sizeof(WorkItem) * (size_t)L.ucap);
   L.tickets = off; off += align256(sizeof(int) * (size_t)L.ucap);
   L.ml = off; off += align256((size_t)L.ucap * kTileRows * 2 * sizeof(float));
   L.o = off; off += align256((size_t)L.ucap * kTileRows * (size_t)D * sizeof(float));
@@ -201,8 +226,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   if (lane == 0 && myW) atomicAdd(&s_W, myW);
   __syncthreads();
   const unsigned long long W = s_W;
+  if (W == 0) {  // no request has keys to attend in this call (an empty chunk)
+    if (tid == 0) {
+      ubase[R] = 0;
+      hdr->U = 0;
+      hdr->P = kMinPagesPerSplit;
+    }
+    return;
+  }
   int P = (int)min((unsigned long long)kMaxPagesPerSplit, (W + kUnitTarget - 1) / kUnitTarget);
-  if (P < kMinPagesPerSplit) P = kMinPagesPerSplit;
+  const int Pmin = W >= (unsigned long long)kNumSMs * 2 * kMinPagesPerSplit ? 2 * kMinPagesPerSplit
+                                                                            : kMinPagesPerSplit;
+  if (P < Pmin) P = Pmin;
   // Work list offsets (exclusive scan of units per request).
   for (int base = 0; base < R; base += blockDim.x) {
     const int i = base + tid;
@@ -229,11 +264,30 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     if (tid == 0) flag(a.dev_status, SV_DEV_BAD_LENGTH);
   }
   for (int u = tid; u < U; u += blockDim.x) tickets[u] = 0;
-  int* ureq = reinterpret_cast<int*>(a.ws + a.L.ureq);
+  WorkItem* work = reinterpret_cast<WorkItem*>(a.ws + a.L.work);
   if (U > 0)
     for (int i = warp; i < R; i += 32) {
-      const int end = i + 1 < R ? ubase[i + 1] : U;
-      for (int x = ubase[i] + lane; x < end; x += 32) ureq[x] = i;
+      const ReqInfo ri = info[i];
+      const int n = ri.nrt * a.Hkv * ri.nsplit;
+      if (n == 0) continue;
+      const int cu = a.bt.cu_rows[i];
+      const int rows = a.bt.cu_rows[i + 1] - cu;
+      for (int x = lane; x < n; x += 32) {
+        WorkItem it;
+        it.i = i;
+        it.local = x;
+        it.nsplit = ri.nsplit;
+        it.nblk = ri.nblk;
+        it.ctx = ri.ctx;
+        it.b = ri.b;
+        it.e = ri.e;
+        it.ubase = ri.ubase;
+        it.cu = cu;
+        it.rows = rows;
+        it.P = P;
+        it.pad = 0;
+        work[ri.ubase + x] = it;
+      }
     }
   if (tid == 0) {
     ubase[R] = U;
@@ -320,27 +374,31 @@ __device__ __forceinline__ void slice_compute(Frag<D>& f, const uint32_t (&qf)[D
   const float nm_a = fmaxf(f.m_a, mx_a), nm_b = fmaxf(f.m_b, mx_b);
   const float base_a = nm_a == -INFINITY ? 0.f : nm_a;
   const float base_b = nm_b == -INFINITY ? 0.f : nm_b;
-  const float al_a = exp2f(f.m_a - base_a), al_b = exp2f(f.m_b - base_b);
+  const float al_a = ex2(f.m_a - base_a), al_b = ex2(f.m_b - base_b);
   f.m_a = nm_a;
   f.m_b = nm_b;
   float ps_a = 0.f, ps_b = 0.f;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    sc[nt][0] = exp2f(sc[nt][0] - base_a);
-    sc[nt][1] = exp2f(sc[nt][1] - base_a);
-    sc[nt][2] = exp2f(sc[nt][2] - base_b);
-    sc[nt][3] = exp2f(sc[nt][3] - base_b);
+    sc[nt][0] = ex2(sc[nt][0] - base_a);
+    sc[nt][1] = ex2(sc[nt][1] - base_a);
+    sc[nt][2] = ex2(sc[nt][2] - base_b);
+    sc[nt][3] = ex2(sc[nt][3] - base_b);
     ps_a += sc[nt][0] + sc[nt][1];
     ps_b += sc[nt][2] + sc[nt][3];
   }
   f.l_a = f.l_a * al_a + ps_a;
   f.l_b = f.l_b * al_b + ps_b;
+  // Once the running maxima settle, most slices leave every row's max in
+  // the warp unchanged: the factor is then exactly 1 and O is left alone.
+  if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {
 #pragma unroll
-  for (int dn = 0; dn < D / 8; ++dn) {
-    f.o[dn][0] *= al_a;
-    f.o[dn][1] *= al_a;
-    f.o[dn][2] *= al_b;
-    f.o[dn][3] *= al_b;
+    for (int dn = 0; dn < D / 8; ++dn) {
+      f.o[dn][0] *= al_a;
+      f.o[dn][1] *= al_a;
+      f.o[dn][2] *= al_b;
+      f.o[dn][3] *= al_b;
+    }
   }
 #pragma unroll
   for (int kk = 0; kk < NT / 2; ++kk) {
@@ -374,14 +432,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ __align__(8) unsigned long long s_full[kStages];
   __shared__ int s_last;
   const Header* hdr = reinterpret_cast<const Header*>(a.ws + a.L.header);
-  const int U = hdr->U;
   const int u = blockIdx.x;
+  // Both loads at once: the item of a CTA past the unit count is never used
+  // (it lies inside the workspace: the grid is the workspace's unit bound).
+  const int U = hdr->U;
+  const WorkItem ri = reinterpret_cast<const WorkItem*>(a.ws + a.L.work)[u];
   if (u >= U) return;
-  const int P = hdr->P;
-  const ReqInfo* infos = reinterpret_cast<const ReqInfo*>(a.ws + a.L.info);
-  const int i = reinterpret_cast<const int*>(a.ws + a.L.ureq)[u];
-  const ReqInfo ri = infos[i];
-  const int local = u - ri.ubase;
+  const int P = ri.P;
+  const int i = ri.i;
+  const int local = ri.local;
   const int s = local % ri.nsplit;
   const int rest = local / ri.nsplit;
   const int g = rest % a.Hkv;
@@ -394,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int blk1 = min(blk0 + P, ri.nblk);
   const int ctx = ri.ctx;
   const int tok_end = min(ctx + ri.e, blk1 * kBlockSize);
-  const int cu = a.bt.cu_rows[i];
+  const int cu = ri.cu;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
@@ -418,10 +477,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int r_count = (vr0 + Mu - 1) / group - r_first + 1;
   const bool unit_masked = blk1 * kBlockSize > ctx;
   for (int p = tid; p < blk1 - blk0; p += kThreads) s_tbl[p] = __ldg(table + blk0 + p);
-  if (unit_masked) {
-    const int rows = a.bt.cu_rows[i + 1] - cu;
-    for (int j = tid; j < rows; j += kThreads) s_par[j] = a.bt.parent[cu + j];
-  }
+  if (unit_masked)
+    for (int j = tid; j < ri.rows; j += kThreads) s_par[j] = a.bt.parent[cu + j];
   if (tid == 0) {
     for (int k = 0; k < kStages; ++k) mbar_init(smem_u32(&s_full[k]), 1);
     fence_mbar_init();
@@ -537,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int t = first + x / (D / 8), c = x % (D / 8);
         *reinterpret_cast<int4*>(ring_ptr + (vbase - ring) + SL::off(t, c)) = make_int4(0, 0, 0, 0);
       }
+      fence_proxy_async_smem();  // before later TMA writes to the same slot
       __syncthreads();
     }
     if (active) {
