@@ -449,6 +449,41 @@ def main():
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(timed(e2e_step, max(5, args.steps // 4)))
     barrier()
+
+    # ---- step-time distribution: an event pair per step, L2 flushed before each ----
+    flush_any = flush_buf if flush_buf is not None else torch.empty(512 * 2 ** 20, dtype=torch.uint8,
+                                                                    device=dev)
+
+    def per_step_ms(fn, n):
+        evs = [(ev(), ev()) for _ in range(n)]
+        for a0, a1 in evs:
+            flush_any.fill_(1)
+            a0.record(stream)
+            fn()
+            a1.record(stream)
+        torch.cuda.synchronize()
+        return sorted(a0.elapsed_time(a1) for a0, a1 in evs)
+
+    n_dist = max(10, args.steps // 2)
+    st_ms = per_step_ms(s.run, n_dist)
+    step_dist = {"median_ms": st_ms[len(st_ms) // 2], "p90_ms": st_ms[int(0.9 * (len(st_ms) - 1))],
+                 "steps": n_dist, "l2": "flushed (512 MB write outside the events) before each step"}
+
+    # ---- one-request workloads: the same step replayed as one CUDA graph ----
+    graph = None
+    if w.n_req == 1:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                s.run()
+            torch.cuda.synchronize()
+            gr_ms = per_step_ms(g.replay, n_dist)
+            res_g = s.results()
+            assert np.array_equal(res_g["accepted_len"], al), "graph replay changed the results"
+            graph = {"median_ms": gr_ms[len(gr_ms) // 2], "p90_ms": gr_ms[int(0.9 * (len(gr_ms) - 1))],
+                     "steps": n_dist, "l2": step_dist["l2"]}
+        except Exception as e:  # report, do not hide the headline
+            graph = {"error": f"{type(e).__name__}: {e}"[:200]}
     clk = clocks.stop()
     res2 = s.results()
     assert np.array_equal(res2["accepted_len"], al), "steps are not reproducible"
@@ -507,8 +542,11 @@ def main():
         "e2e": {"value": rows_all / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
         "gpu_launches": launches_per_step * args.steps,
+        "step_time_flushed": step_dist,
         "clocks": clk,
     }
+    if graph is not None:
+        line["graph_replay"] = graph
     if mode == "chunked":
         line["config"]["chunk"] = chunk
     if world == 1 and not args.no_cpu_baseline:
