@@ -10,9 +10,9 @@ commit.  Other workloads: tiny, chain8b, tree70b (one pass), batch256
 
 One step = restore the block tables / lengths / free list the previous
 step's commit changed, then the workload's calls:
-  chunked  sv_verify_chunked (per chunk: windows + active list, attention
-           plan, split-KV attention, row statistics with the decisions,
-           resampling race) and sv_commit_kv
+  chunked  sv_verify_chunked (per chunk: attention plan with the chunk's
+           windows and accept list, split-KV attention, row statistics,
+           decisions; one resampling race per step) and sv_commit_kv
   onepass  sv_tree_attend, sv_accept, sv_commit_kv
   budget   sv_select_budget, sv_tree_attend and sv_accept on the selected
            prefixes, sv_commit_kv
@@ -511,9 +511,10 @@ def main():
     n_launch = len(sched)
     race = 1 if T > 0 else 0
     # attention: plan + attend; accept: list + stats + decide (+ race); commit: copy + release.
-    # Chunked: list + plan + attend + stats + decide per chunk, one race after the last.
+    # Chunked: plan (windows + accept list) + attend + stats + decide per chunk, one race
+    # after the last.
     if mode == "chunked":
-        launches_per_step = n_launch * (1 + 2 + 2) + race + 2
+        launches_per_step = n_launch * (2 + 2) + race + 2
     else:
         launches_per_step = 2 + 3 + race + 2 + (1 if mode == "budget" else 0)
     value = rows_all / t_step

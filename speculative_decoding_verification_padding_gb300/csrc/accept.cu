@@ -62,7 +62,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Slices per row (stats) and per request (race): about 32 warps per SM in
 // flight, slices of at least 2 KB.
-constexpr int kMaxSlices = 64;  // merge_rows reads slices lane and lane + 32
+constexpr int kMaxSlices = 64;  // vocabulary slices per row at most
 
 inline int stats_chunks(int rows_bound, int V) {
   const int maxc = max(1, min(kMaxSlices, V / 512));
@@ -124,6 +124,7 @@ struct Args {
   Layout L;
   int32_t* dev_status;
   int race_all;   // race kernel: every request 0..R-1 instead of the active list
+  int clear_jobs; // stats kernel: first clear every request's sampling job and race ticket
 };
 
 __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2) {
@@ -138,10 +139,9 @@ __device__ __forceinline__ void merge_am(float& v, int& i, float v2, int i2) {
 
 // ------------------------------------------------------------------ list --
 // Active requests: window not empty, and (for a continuation window) not
-// already decided.  Also used by the chunk driver, which first turns `done`
-// into the windows of chunk `chunk` (chunk >= 0) and writes them out.
-__global__ void __launch_bounds__(1024) list_kernel(Args a, int chunk, int cs, const int32_t* done,
-                                                    int32_t* rb_out, int32_t* re_out) {
+// already decided, in request order, count at act[R].  (In chunked
+// verification the attention planner writes this list for each chunk.)
+__global__ void __launch_bounds__(1024) list_kernel(Args a) {
   griddep_entry();
   const int R = a.bt.n_req;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -154,33 +154,9 @@ __global__ void __launch_bounds__(1024) list_kernel(Args a, int chunk, int cs, c
     const int i = base + tid;
     int f = 0;
     if (i < R) {
-      if (chunk >= 0) {
-        sv_batch b0 = a.bt;
-        b0.row_begin = nullptr;
-        b0.row_end = nullptr;
-        const Window w = window_of(b0, i);
-        int b = chunk * cs, e = min(b + cs, w.lim);
-        const bool running = chunk == 0 || (done && done[i] == 0);
-        if (!w.ok) {
-          if (chunk == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-          b = e = 0;
-        } else if (!running || b >= e) {
-          b = e = min(b, w.rows);
-        }
-        rb_out[i] = b;
-        re_out[i] = e;
-        f = (w.ok && b < e) ? 1 : 0;
-        if (chunk == 0) {
-          // The step's single race pass reads every request's job: none may
-          // be left over from an earlier call.
-          reinterpret_cast<Job*>(a.ws + a.L.jobs)[i].mode = 0;
-          reinterpret_cast<int*>(a.ws + a.L.race_tickets)[i] = 0;
-        }
-      } else {
-        const Window w = window_of(a.bt, i);
-        if (!w.ok) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-        else if (w.b < w.e && !(w.b > 0 && a.next_token[i] >= 0)) f = 1;
-      }
+      const Window w = window_of(a.bt, i);
+      if (!w.ok) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+      else if (w.b < w.e && !(w.b > 0 && a.next_token[i] >= 0)) f = 1;
     }
     // exclusive scan of the flags
     int x = f;
@@ -217,43 +193,55 @@ struct DecideSmem {
   int am[kMaxRows], len[kMaxRows], child[kMaxRows], par[kMaxRows], tok[kMaxRows];
 };
 
-// Merge the slice partials of rows [r0, r0 + n) of one type, 4 rows per
-// round of loads (each lane takes slices lane, lane + 32), into the lane-0
-// outputs m_out / lv_out (shared memory).
-__device__ __forceinline__ void merge_rows(const Args& a, int nch, int r0, int n, int type,
-                                           float* m_out, float* lv_out) {
+// Merge the slice partials of n0 target rows r0.. (type 0) and n1 draft rows
+// r0.. (type 1) into m*/lv* (shared memory, index from 0).  The pairs are
+// spread over the warp: up to 32 at a time, each on a group of G lanes (the
+// largest power of two that fits), every lane merging slices sub, sub + G, ...
+// of its pair, then log2(G) shuffle rounds inside the group.
+__device__ __forceinline__ void merge_pairs(const Args& a, int nch, int r0, int n0, int n1,
+                                            float* m0, float* lv0, float* m1, float* lv1) {
   const int lane = threadIdx.x & 31;
   const float T = a.T;
   const StatPart* parts = reinterpret_cast<const StatPart*>(a.ws + a.L.parts);
-  for (int k0 = 0; k0 < n; k0 += 4) {
-    float2 v[4][2];
+  const int np = n0 + n1;
+  for (int base = 0; base < np; base += 32) {
+    const int cnt = min(32, np - base);
+    int G = 32;
+    while (G > 1 && G * cnt > 32) G >>= 1;
+    const int p = base + lane / G, sub = lane % G;
+    const bool live = lane / G < cnt;
+    const int type = p < n0 ? 0 : 1;
+    const int row = r0 + (p < n0 ? p : p - n0);
+    float m = -INFINITY, lv = 0.f;
+    int am = 0x7fffffff;
+    if (live) {
+      // 16 loads in flight per lane, then the merges
+      const StatPart* pr = parts + ((size_t)row * 2 + type) * nch;
+      const float2 ident = make_float2(-INFINITY, T > 0.f ? 0.f : __int_as_float(0x7fffffff));
+      for (int c0 = sub; c0 < nch; c0 += 16 * G) {
+        float2 v[16];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 16; ++k) {
+          const int c = c0 + k * G;
+          v[k] = c < nch ? __ldcg(reinterpret_cast<const float2*>(pr + c)) : ident;
+        }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = lane + 32 * h;
-        v[k][h] = make_float2(-INFINITY, T > 0.f ? 0.f : __int_as_float(0x7fffffff));
-        if (k0 + k < n && c < nch)
-          v[k][h] = __ldcg(reinterpret_cast<const float2*>(
-              parts + ((size_t)(r0 + k0 + k) * 2 + type) * nch + c));
+        for (int k = 0; k < 16; ++k) {
+          if (T > 0.f) merge_ml(m, lv, v[k].x, v[k].y);
+          else merge_am(m, am, v[k].x, __float_as_int(v[k].y));
+        }
       }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float m = v[k][0].x, lv = v[k][0].y;
-      int am = __float_as_int(lv);
-      if (T > 0.f) merge_ml(m, lv, v[k][1].x, v[k][1].y);
-      else merge_am(m, am, v[k][1].x, __float_as_int(v[k][1].y));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float l2 = __shfl_xor_sync(0xffffffffu, lv, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, am, o);
-        if (T > 0.f) merge_ml(m, lv, m2, l2); else merge_am(m, am, m2, i2);
-      }
-      if (lane == 0 && k0 + k < n) {
-        m_out[k0 + k] = m;
-        lv_out[k0 + k] = T > 0.f ? lv : __int_as_float(am);
-      }
+    }
+    for (int o = G >> 1; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, lv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, am, o);
+      if (T > 0.f) merge_ml(m, lv, m2, l2); else merge_am(m, am, m2, i2);
+    }
+    if (live && sub == 0) {
+      const float out_lv = T > 0.f ? lv : __int_as_float(am);
+      if (type == 0) { m0[p] = m; lv0[p] = out_lv; }
+      else { m1[p - n0] = m; lv1[p - n0] = out_lv; }
     }
   }
 }
@@ -311,7 +299,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   float* rs = a.row_stats;
 
   if (a.T == 0.f) {
-    merge_rows(a, nch, cu + w.b, w.e - w.b, 0, sm.mp + w.b, sm.lp + w.b);
+    merge_pairs(a, nch, cu + w.b, w.e - w.b, 0, sm.mp + w.b, sm.lp + w.b, nullptr, nullptr);
     __syncwarp();
     for (int r = w.b + lane; r < w.e; r += 32) {
       const int idx = __float_as_int(sm.lp[r]);
@@ -381,21 +369,24 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   // ---- T > 0: speculative sampling on a chain ----
   const int jmax = min(w.e, w.lim - 1);
   const int nq = max(0, min(w.e, w.lim - 1) - w.b);  // draft rows with a tested child
-  merge_rows(a, nch, cu + w.b, w.e - w.b, 0, sm.mp + w.b, sm.lp + w.b);
-  merge_rows(a, nch, cu + w.b, nq, 1, sm.mq + w.b, sm.lq + w.b);
+  merge_pairs(a, nch, cu + w.b, w.e - w.b, nq, sm.mp + w.b, sm.lp + w.b, sm.mq + w.b,
+              sm.lq + w.b);
   __syncwarp();
   if (rs)
     for (int r = w.b + lane; r < w.e; r += 32) {
       rs[(size_t)(cu + r) * 4 + 0] = sm.mp[r] + logf(sm.lp[r]);
       if (r - w.b < nq) rs[(size_t)(cu + r) * 4 + 1] = sm.mq[r] + logf(sm.lq[r]);
     }
-  // Lane j - b - 1 evaluates draft j's ratio; lane 0 then scans them.
+  // Lane j - b - 1 evaluates draft j's ratio and draws its uniform; the scan
+  // then reads them by shuffle.
   const float T = a.T;
   const int nd = jmax - w.b;  // drafts decided by this window
   double ratio = 1.0;
+  float u_lane = 0.f;
   {
     const int j = w.b + 1 + lane;
     if (lane < nd) {
+      u_lane = accept_u(a.seed, i, j);
       const int x = sm.tok[j];
       const size_t off = (size_t)(cu + j - 1) * V + x;
       const float xp = a.target[off] / T;
@@ -416,6 +407,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   for (int k = 0; k < nd; ++k) {
     const int j = w.b + 1 + k;
     const double rk = __shfl_sync(0xffffffffu, ratio, k & 31);
+    const float uk = __shfl_sync(0xffffffffu, u_lane, k & 31);
     if (k >= 32) {  // windows longer than a warp: evaluate the rest serially
       const int x = sm.tok[j];
       const size_t off = (size_t)(cu + j - 1) * V + x;
@@ -428,7 +420,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
       }
     }
     const double r_j = k >= 32 ? ratio : rk;
-    const double u = (double)accept_u(a.seed, i, j);
+    const double u = (double)(k >= 32 ? accept_u(a.seed, i, j) : uk);
     if (fabs(u - r_j) < 1e-6) amb = true;
     if (u < r_j) {
       len = j;
@@ -475,6 +467,15 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
   const float T = a.T;
   const int ntypes = T > 0.f ? 2 : 1;
   const int maxw = a.L.maxw;
+  if (a.clear_jobs) {
+    // First chunk of a chunked step: the step's single race pass reads every
+    // request's job, so none may be left over from an earlier call (the
+    // decision kernel, which runs after this one, writes this step's).
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < R; i += gridDim.x * blockDim.x) {
+      reinterpret_cast<Job*>(a.ws + a.L.jobs)[i].mode = 0;
+      reinterpret_cast<int*>(a.ws + a.L.race_tickets)[i] = 0;
+    }
+  }
   const int nch = stats_slices(a.L, count, ntypes);
   const int chl = chunk_len(a.V, nch);
   const long total = (long)count * maxw * ntypes * nch;
@@ -637,24 +638,35 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
       return fmaxf(p - ex2(fmaf(div_by(lqv, T, rT), kLog2e, -mqb)) * inv_lq, 0.f);
     };
     if (VEC) {
-      // uniform trip count so that the lanes can share their thresholds: the
-      // best key any lane has seen bounds the winner from below
+      // Four 128-entry groups per iteration, their loads issued first.  The
+      // trip count is uniform so that the lanes can share their thresholds:
+      // the best key any lane has seen bounds the winner from below.
+      constexpr int kGroups = 4;
       float wthr = -1.f;
-      for (int base = lo; base < hi; base += 128) {
+      const float4* p4 = reinterpret_cast<const float4*>(lp);
+      const float4* q4 = reinterpret_cast<const float4*>(lq);
+      for (int base = lo; base < hi; base += 128 * kGroups) {
         wthr = fmaxf(wthr, warp_max(thr));
-        const int v = base + 4 * lane;
-        if (v >= hi) continue;
-        const float4 xp = __ldcs(reinterpret_cast<const float4*>(lp) + (v >> 2));
-        float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (resid) xq = __ldcs(reinterpret_cast<const float4*>(lq) + (v >> 2));
-        const float w0 = weight(xp.x, xq.x), w1 = weight(xp.y, xq.y);
-        const float w2 = weight(xp.z, xq.z), w3 = weight(xp.w, xq.w);
-        if (fmaxf(fmaxf(w0, w1), fmaxf(w2, w3)) < fmaxf(thr, wthr)) continue;
-        const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
-        take(w0, -logf(race_u(bits.a)), v);
-        take(w1, -logf(race_u(bits.b)), v + 1);
-        take(w2, -logf(race_u(bits.c)), v + 2);
-        take(w3, -logf(race_u(bits.d)), v + 3);
+        float4 xp[kGroups], xq[kGroups];
+#pragma unroll
+        for (int k = 0; k < kGroups; ++k) {
+          const int v = base + 128 * k + 4 * lane;
+          xp[k] = v < hi ? __ldcs(p4 + (v >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          xq[k] = (resid && v < hi) ? __ldcs(q4 + (v >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < kGroups; ++k) {
+          const int v = base + 128 * k + 4 * lane;
+          if (v >= hi) continue;
+          const float w0 = weight(xp[k].x, xq[k].x), w1 = weight(xp[k].y, xq[k].y);
+          const float w2 = weight(xp[k].z, xq[k].z), w3 = weight(xp[k].w, xq[k].w);
+          if (fmaxf(fmaxf(w0, w1), fmaxf(w2, w3)) < fmaxf(thr, wthr)) continue;
+          const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
+          take(w0, -logf(race_u(bits.a)), v);
+          take(w1, -logf(race_u(bits.b)), v + 1);
+          take(w2, -logf(race_u(bits.c)), v + 2);
+          take(w3, -logf(race_u(bits.d)), v + 3);
+        }
       }
     } else {
       for (int v = lo + lane; v < hi; v += 32) {
@@ -722,22 +734,6 @@ static sv_status check_accept_args(const sv_batch* bt, const float* target_logit
   return SV_OK;
 }
 
-sv_status chunk_list(const sv_batch* bt, int chunk, int cs, const int32_t* done, int32_t* rb,
-                     int32_t* re, int32_t vocab, void* ws, int32_t* dev_status, cudaStream_t s) {
-  if (!bt || chunk < 0 || cs < 1 || !rb || !re || !ws) return SV_ERR_INVALID_ARGUMENT;
-  if (chunk > 0 && !done) return SV_ERR_INVALID_ARGUMENT;
-  if (bt->n_req == 0) return SV_OK;
-  Args a{};
-  a.bt = *bt;
-  a.V = vocab;
-  a.ws = static_cast<uint8_t*>(ws);
-  a.L = layout(bt->n_req, bt->total_rows, vocab, cs);
-  a.dev_status = dev_status;
-  if (sv::launch(list_kernel, 1, 1024, 0, s, a, chunk, cs, done, rb, re) != cudaSuccess)
-    return SV_ERR_CUDA;
-  return SV_OK;
-}
-
 static sv_status launch_race(const Args& a, bool vec, cudaStream_t s) {
   const long ritems = (long)a.bt.n_req * a.L.nch_r_cap;
   const long rwarps = kRaceThreads / 32;
@@ -754,15 +750,15 @@ static bool vec_ok(int32_t vocab, const float* target_logits, const float* draft
           15) == 0;
 }
 
-// Enqueue the list pass (unless chunk_step), the statistics, the decision
-// and (unless chunk_step) the race.  chunk_step: the active list of `ws` was
-// written by chunk_list for this batch's windows, and the race is left to
-// race_all after the last chunk.
+// Enqueue the list pass, the statistics, the decision and the race; in a
+// chunked step (chunk_index >= 0) the attention planner wrote the list and
+// the race is left to race_all after the last chunk.
 sv_status run(const sv_batch* bt, const float* target_logits, const float* draft_logits,
               int32_t vocab, float temperature, uint64_t seed, int32_t* accepted_len,
               int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
               float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s,
-              int maxw, bool chunk_step) {
+              int maxw, int chunk_index) {
+  const bool chunk_step = chunk_index >= 0;
   sv_status st = check_accept_args(bt, target_logits, draft_logits, vocab, temperature,
                                    accepted_len, accepted_nodes, next_token, ambiguous, ws);
   if (st != SV_OK || bt->n_req == 0 || bt->total_rows == 0) return st;
@@ -783,11 +779,11 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
   a.L = layout(bt->n_req, bt->total_rows, vocab, maxw);
   a.dev_status = dev_status;
   a.race_all = 0;
+  a.clear_jobs = chunk_index == 0 ? 1 : 0;
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   const bool vec = vec_ok(vocab, target_logits, draft_logits);
   if (!chunk_step) {
-    if (sv::launch(list_kernel, 1, 1024, 0, s, a, -1, 0, (const int32_t*)nullptr,
-                   (int32_t*)nullptr, (int32_t*)nullptr) != cudaSuccess)
+    if (sv::launch(list_kernel, 1, 1024, 0, s, a) != cudaSuccess)
       return SV_ERR_CUDA;
   }
   const long items = (long)bt->n_req * a.L.maxw * (temperature > 0.f ? 2 : 1) * a.L.nch_cap;
@@ -818,6 +814,7 @@ sv_status race_all(const sv_batch* bt, const float* target_logits, const float* 
   a.L = layout(bt->n_req, bt->total_rows, vocab, maxw);
   a.dev_status = dev_status;
   a.race_all = 1;
+  a.clear_jobs = 0;
   return launch_race(a, vec_ok(vocab, target_logits, draft_logits), s);
 }
 
@@ -840,7 +837,7 @@ extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
   if (!bt) return SV_ERR_INVALID_ARGUMENT;
   return acc::run(bt, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
                   accepted_nodes, next_token, ambiguous, done, row_stats, ws, ws_bytes, dev_status,
-                  static_cast<cudaStream_t>(stream), bt->max_rows_per_req, false);
+                  static_cast<cudaStream_t>(stream), bt->max_rows_per_req, -1);
 }
 
 // ------------------------------------------------ no-allocation variant ----

@@ -40,6 +40,7 @@
 
 #include <mutex>
 
+#include "sv_attend_internal.h"
 #include "sv_internal.cuh"
 
 namespace sv {
@@ -65,6 +66,7 @@ constexpr int kMaxPagesPerSplit = 1024;  // block ids of a unit staged in shared
 
 struct ReqInfo {
   int ubase, nsplit, nrt, b, e, ctx, nblk, valid;
+  int act;     // chunk mode: the window is not empty (the accept list)
 };
 
 // One unit of the work list: everything its CTA needs to start (a single
@@ -128,6 +130,7 @@ struct Args {
   uint8_t* ws;
   Layout L;
   int32_t* dev_status;
+  ChunkPlan chunk;  // chunk.index < 0: windows come from the batch
 };
 
 // ------------------------------------------------------------------ plan --
@@ -169,17 +172,19 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   __shared__ int s_bad;
   __shared__ unsigned long long s_W;
   __shared__ int s_warp[32];
-  __shared__ int s_carry;
+  __shared__ int s_carry, s_acarry;
 
   if (tid == 0) {
     s_bad = (a.bt.cu_rows[0] != 0 || a.bt.cu_rows[R] != a.bt.total_rows) ? 1 : 0;
     s_W = 0ull;
     s_carry = 0;
+    s_acarry = 0;
   }
   __syncthreads();
   if (s_bad) {
     if (tid == 0) {
       flag(a.dev_status, SV_DEV_BAD_WINDOW);
+      if (a.chunk.index >= 0) a.chunk.act[R] = 0;
       hdr->U = 0;
       hdr->P = 1;
     }
@@ -187,8 +192,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   }
   // One warp per request: window, parents, length, work.
   unsigned long long myW = 0;
+  const bool chunked = a.chunk.index >= 0;
   for (int i = warp; i < R; i += 32) {
-    const Window w = window_of(a.bt, i);
+    Window w;
+    bool badw = false;
+    if (chunked) {
+      w = chunk_window(a.bt, i, a.chunk.index, a.chunk.size, a.chunk.done, &badw);
+      if (lane == 0) {
+        a.chunk.row_begin[i] = w.b;
+        a.chunk.row_end[i] = w.e;
+        if (badw && a.chunk.index == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+      }
+    } else {
+      w = window_of(a.bt, i);
+    }
+    if (badw) w.ok = false;  // reported above (once); the window is empty anyway
     const int cu = a.bt.cu_rows[i];
     bool badp = false;
     if (w.ok) {
@@ -200,7 +218,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     badp = __any_sync(0xffffffffu, badp);
     if (lane == 0) {
       bool valid = w.ok && !badp;
-      if (!w.ok) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+      if (!w.ok && !chunked) flag(a.dev_status, SV_DEV_BAD_WINDOW);
       if (badp) flag(a.dev_status, SV_DEV_BAD_PARENT);
       const int ctx = a.cache_lens[i];
       if (valid && (ctx < 0 || (long)ctx + w.rows > (long)a.max_blocks * kBlockSize)) {
@@ -220,32 +238,28 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
       ri.nblk = nblk;
       ri.nsplit = 0;
       ri.ubase = 0;
+      ri.act = (!badw && w.b < w.e) ? 1 : 0;
       info[i] = ri;
     }
   }
   if (lane == 0 && myW) atomicAdd(&s_W, myW);
   __syncthreads();
   const unsigned long long W = s_W;
-  if (W == 0) {  // no request has keys to attend in this call (an empty chunk)
-    if (tid == 0) {
-      ubase[R] = 0;
-      hdr->U = 0;
-      hdr->P = kMinPagesPerSplit;
-    }
-    return;
-  }
   int P = (int)min((unsigned long long)kMaxPagesPerSplit, (W + kUnitTarget - 1) / kUnitTarget);
   const int Pmin = W >= (unsigned long long)kNumSMs * 2 * kMinPagesPerSplit ? 2 * kMinPagesPerSplit
                                                                             : kMinPagesPerSplit;
   if (P < Pmin) P = Pmin;
-  // Work list offsets (exclusive scan of units per request).
+  // Work list offsets (exclusive scan of units per request); in chunk mode
+  // also the accept's list of requests with a non-empty window, in request
+  // order, with its count at act[R].
   for (int base = 0; base < R; base += blockDim.x) {
     const int i = base + tid;
-    int units = 0;
+    int units = 0, act = 0;
     if (i < R) {
       const ReqInfo ri = info[i];
       const int nsplit = ri.valid ? (ri.nblk + P - 1) / P : 0;
       units = ri.nrt * a.Hkv * nsplit;
+      act = ri.act;
       info[i].nsplit = nsplit;
     }
     int excl, total;
@@ -254,10 +268,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
       ubase[i] = s_carry + excl;
       info[i].ubase = s_carry + excl;
     }
+    if (chunked) {
+      int aexcl, atotal;
+      block_excl_scan(s_warp, act, aexcl, atotal);
+      if (act) a.chunk.act[s_acarry + aexcl] = i;
+      __syncthreads();
+      if (tid == 0) s_acarry += atotal;
+    }
     __syncthreads();
     if (tid == 0) s_carry += total;
     __syncthreads();
   }
+  if (chunked && tid == 0) a.chunk.act[R] = s_acarry;
   int U = s_carry;
   if (U > a.L.ucap) {  // cannot happen with the bound used for the workspace
     U = 0;
@@ -829,9 +851,12 @@ extern "C" size_t sv_tree_attend_workspace(const sv_batch* bt, const sv_paged_kv
                       kv->max_blocks_per_req).total;
 }
 
-extern "C" sv_status sv_tree_attend(const sv_paged_kv* kv, const sv_batch* bt, const void* q,
-                                    int32_t n_q_heads, float softmax_scale, void* out, void* ws,
-                                    size_t ws_bytes, int32_t* dev_status, void* stream) {
+namespace sv {
+namespace attn {
+
+sv_status tree_attend(const sv_paged_kv* kv, const sv_batch* bt, const void* q, int32_t n_q_heads,
+                      float softmax_scale, void* out, void* ws, size_t ws_bytes,
+                      int32_t* dev_status, cudaStream_t stream, const ChunkPlan& chunk) {
   sv_status st = check_attend_args(bt, kv, n_q_heads);
   if (st != SV_OK) return st;
   if (bt->n_req == 0 || bt->total_rows == 0) return SV_OK;
@@ -839,8 +864,12 @@ extern "C" sv_status sv_tree_attend(const sv_paged_kv* kv, const sv_batch* bt, c
   if (((uintptr_t)q | (uintptr_t)out) & 3) return SV_ERR_INVALID_ARGUMENT;
   if ((uintptr_t)ws & 255) return SV_ERR_INVALID_ARGUMENT;
   if (!(softmax_scale > 0.f)) return SV_ERR_INVALID_ARGUMENT;
+  if (chunk.index >= 0 &&
+      (chunk.size < 1 || !chunk.row_begin || !chunk.row_end || !chunk.act ||
+       (chunk.index > 0 && !chunk.done)))
+    return SV_ERR_INVALID_ARGUMENT;
   const int group = n_q_heads / kv->n_kv_heads;
-  attn::Args a;
+  Args a;
   a.bt = *bt;
   a.k = static_cast<const __nv_bfloat16*>(kv->k_cache);
   a.v = static_cast<const __nv_bfloat16*>(kv->v_cache);
@@ -855,10 +884,21 @@ extern "C" sv_status sv_tree_attend(const sv_paged_kv* kv, const sv_batch* bt, c
   a.group = group;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.ws = static_cast<uint8_t*>(ws);
-  a.L = attn::layout(bt->n_req, bt->total_rows, group, kv->n_kv_heads, kv->head_dim,
-                      kv->max_blocks_per_req);
+  a.L = layout(bt->n_req, bt->total_rows, group, kv->n_kv_heads, kv->head_dim,
+               kv->max_blocks_per_req);
   a.dev_status = dev_status;
+  a.chunk = chunk;
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return kv->head_dim == 128 ? attn::launch<128>(a, s) : attn::launch<64>(a, s);
+  return kv->head_dim == 128 ? launch<128>(a, stream) : launch<64>(a, stream);
+}
+
+}  // namespace attn
+}  // namespace sv
+
+extern "C" sv_status sv_tree_attend(const sv_paged_kv* kv, const sv_batch* bt, const void* q,
+                                    int32_t n_q_heads, float softmax_scale, void* out, void* ws,
+                                    size_t ws_bytes, int32_t* dev_status, void* stream) {
+  const attn::ChunkPlan none{-1, 0, nullptr, nullptr, nullptr, nullptr};
+  return attn::tree_attend(kv, bt, q, n_q_heads, softmax_scale, out, ws, ws_bytes, dev_status,
+                           static_cast<cudaStream_t>(stream), none);
 }

@@ -6,12 +6,16 @@
 // spent on them) and the operations notes (the verification attention kernel
 // has to run on a part of the rows).
 //
-// The whole step is enqueued on one stream with no host synchronisation: a
-// tiny kernel turns `done` into the next chunk's windows (requests that are
-// done get an empty window, which every later kernel skips), then the
-// attention and accept calls run on those windows.
+// The whole step is enqueued on one stream with no host synchronisation: per
+// chunk, the attention planner turns `done` into the chunk's windows
+// (requests that are done get an empty window, which every later kernel
+// skips) and the accept list, the attention runs on those windows, then the
+// accept statistics and decisions; one race pass after the last chunk draws
+// every request's emitted token.  sv_chunk_windows exposes the window rule
+// on its own.
 
 #include "sv_accept_internal.h"
+#include "sv_attend_internal.h"
 #include "sv_internal.cuh"
 
 namespace sv {
@@ -23,19 +27,11 @@ __global__ void __launch_bounds__(256) windows_kernel(sv_batch bt, int c, int cs
   griddep_entry();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= bt.n_req) return;
-  bt.row_begin = nullptr;
-  bt.row_end = nullptr;
-  const Window w = window_of(bt, i);
-  int b = c * cs, e = min(b + cs, w.lim);
-  const bool running = (c == 0) || (done && done[i] == 0);
-  if (!w.ok) {
-    if (c == 0) flag(dev_status, SV_DEV_BAD_WINDOW);
-    b = e = 0;
-  } else if (!running || b >= e) {
-    b = e = min(b, w.rows);
-  }
-  rb[i] = b;
-  re[i] = e;
+  bool bad = false;
+  const Window w = chunk_window(bt, i, c, cs, done, &bad);
+  if (bad && c == 0) flag(dev_status, SV_DEV_BAD_WINDOW);
+  rb[i] = w.b;
+  re[i] = w.e;
 }
 
 inline size_t windows_bytes(int R) { return align256(sizeof(int32_t) * (size_t)R) * 2; }
@@ -113,13 +109,15 @@ extern "C" sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* bt
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int n_chunks = (bt->max_rows_per_req + chunk_size - 1) / chunk_size;
   for (int c = 0; c < n_chunks; ++c) {
-    sv_status st = acc::chunk_list(bt, c, chunk_size, done, rb, re, vocab, acc_ws, dev_status, s);
-    if (st != SV_OK) return st;
-    st = sv_tree_attend(kv, &b2, q, n_q_heads, softmax_scale, out, att_ws, wa, dev_status, stream);
+    // The planner turns `done` into this chunk's windows and the accept list.
+    const attn::ChunkPlan cp{c, chunk_size, done, rb, re,
+                             reinterpret_cast<int32_t*>(acc_ws + AL.act)};
+    sv_status st = attn::tree_attend(kv, bt, q, n_q_heads, softmax_scale, out, att_ws, wa,
+                                     dev_status, s, cp);
     if (st != SV_OK) return st;
     st = acc::run(&b2, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
                   accepted_nodes, next_token, ambiguous, done, nullptr, acc_ws, AL.total,
-                  dev_status, s, chunk_size, true);
+                  dev_status, s, chunk_size, c);
     if (st != SV_OK) return st;
   }
   // Nothing in a later chunk depends on the drawn tokens: one race pass

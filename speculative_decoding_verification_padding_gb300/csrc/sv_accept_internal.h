@@ -22,20 +22,16 @@ struct Layout {
 };
 Layout layout(int R, int total_rows, int V, int maxw);
 
-// Windows of chunk `chunk` (chunk size cs) from `done`, written to rb / re,
-// plus the list of requests with a non-empty window, into the accept
-// workspace `ws` laid out for (batch, vocab, maxw = cs).
-sv_status chunk_list(const sv_batch* bt, int chunk, int cs, const int32_t* done, int32_t* rb,
-                     int32_t* re, int32_t vocab, void* ws, int32_t* dev_status, cudaStream_t s);
-
-// The accept kernels.  chunk_step: the active list of `ws` was written by
-// chunk_list for this batch's windows (otherwise a list pass runs first),
-// and the residual / bonus draws are left to race_all.
+// The accept kernels.  chunk_index < 0: a list pass, then statistics,
+// decision and race.  chunk_index >= 0 (chunk of a chunked step): the active
+// list in `ws` (at Layout::act) was written by the attention planner for this
+// batch's windows; statistics (the first chunk also clears every sampling
+// job) and decision only, the draws are left to race_all.
 sv_status run(const sv_batch* bt, const float* target_logits, const float* draft_logits,
               int32_t vocab, float temperature, uint64_t seed, int32_t* accepted_len,
               int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
               float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s,
-              int maxw, bool chunk_step);
+              int maxw, int chunk_index);
 
 // After the last chunk of a chunked step (T > 0): the residual or bonus draw
 // of every request whose decision set one, in a single pass.

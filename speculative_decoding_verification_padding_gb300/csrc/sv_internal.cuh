@@ -53,6 +53,30 @@ __device__ __forceinline__ Window window_of(const sv_batch& bt, int i) {
   return w;
 }
 
+// Rows [b, e) of chunk c (chunk size cs) of request i, from a batch given
+// without windows: rows c*cs .. c*cs + cs - 1 of the verified range, empty
+// once the request is done (done[i] != 0, read only for c > 0) or past its
+// rows.  A request whose own window is invalid gets an empty window and
+// *bad = true (the caller reports it once, on chunk 0).
+__device__ __forceinline__ Window chunk_window(sv_batch bt, int i, int c, int cs,
+                                               const int32_t* done, bool* bad) {
+  bt.row_begin = nullptr;
+  bt.row_end = nullptr;
+  Window w = window_of(bt, i);
+  int b = c * cs, e = min(b + cs, w.lim);
+  const bool running = c == 0 || (done && done[i] == 0);
+  *bad = !w.ok;
+  if (!w.ok) {
+    b = e = 0;
+  } else if (!running || b >= e) {
+    b = e = min(b, w.rows);
+  }
+  w.b = b;
+  w.e = e;
+  w.ok = true;
+  return w;
+}
+
 // ------------------------------------------------------------- Philox ----
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of
 // (c0, c1, c2, c3) -> (hi(B*c2) ^ c1 ^ k0, lo(B*c2), hi(A*c0) ^ c3 ^ k1,
