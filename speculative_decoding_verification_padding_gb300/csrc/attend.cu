@@ -18,11 +18,13 @@
 //   attend (1 CTA per unit, 4 warps, 2 CTAs per SM)
 //                    the query rows of the whole GQA group (row x head packed
 //                    as "virtual rows") share every KV page.  Pages stream
-//                    through a 3-stage ring of 64-token stages: thread 0
-//                    issues 2-D tiled TMA loads (cp.async.bulk.tensor, 128-byte
-//                    swizzle, one 64-element x 16-row box per half page) that
-//                    complete on an mbarrier per slot; the warps wait on it
-//                    with a bounded spin.  A warp owns a 16-row m-tile and a
+//                    through a 3-stage ring of 64-token stages: lane 0 of
+//                    warp p issues page p of each stage as 2-D tiled TMA loads
+//                    (cp.async.bulk.tensor, 128-byte swizzle, one 64-element x
+//                    16-row box per half page) that complete on an mbarrier
+//                    per slot (thread 0 arms it with the stage's bytes); the
+//                    warps wait on it with a bounded spin, and one block
+//                    barrier per stage frees the slot.  A warp owns a 16-row m-tile and a
 //                    slice of each stage's tokens: with one m-tile the four
 //                    warps take 16 tokens each, with two they take 32, with
 //                    three or four every warp sees the whole stage.  QK^T and
@@ -453,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ unsigned long long s_mask[kTileRows][2];
   __shared__ __align__(8) unsigned long long s_full[kStages];
   __shared__ int s_last;
+  __shared__ int s_abort;
   const Header* hdr = reinterpret_cast<const Header*>(a.ws + a.L.header);
   const int u = blockIdx.x;
   // Both loads at once: the item of a CTA past the unit count is never used
@@ -502,44 +505,43 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (unit_masked)
     for (int j = tid; j < ri.rows; j += kThreads) s_par[j] = a.bt.parent[cu + j];
   if (tid == 0) {
+    s_abort = 0;
     for (int k = 0; k < kStages; ++k) mbar_init(smem_u32(&s_full[k]), 1);
     fence_mbar_init();
   }
   __syncthreads();
 
-  // Thread 0 issues one stage: every valid page of it, K and V, all boxes.
+  // One stage: lane 0 of warp p issues page p's boxes (K and V); thread 0
+  // also arms the slot's barrier with the stage's total bytes (the barrier's
+  // transaction count may dip below zero until it does).
+  static_assert(kWarps == 4, "one page of a stage per warp");
   auto issue = [&](int st) {
-    if (tid != 0 || st >= n_stage) return;
+    if (lane != 0 || st >= n_stage) return;
     const int slot = st % kStages;
     const uint32_t bar = smem_u32(&s_full[slot]);
     const uint32_t kdst = ring + slot * SL::kStageBytes;
-    uint32_t bytes = 0;
-    int bids[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
+    auto bid_of = [&](int p) {
       const int page = blk0 + 4 * st + p;
-      int bid = -1;
-      if (page < blk1) {
-        bid = s_tbl[page - blk0];
-        if (bid < 0 || bid >= a.num_blocks) {
-          flag(a.dev_status, SV_DEV_BAD_BLOCK_ID);
-          bid = -1;
-        }
-      }
-      bids[p] = bid;
-      if (bid >= 0) bytes += 2 * SL::kHalves * SL::kBoxBytes;
+      if (page >= blk1) return -1;
+      const int bid = s_tbl[page - blk0];
+      return (bid < 0 || bid >= a.num_blocks) ? -2 : bid;
+    };
+    if (warp == 0) {
+      uint32_t bytes = 0;
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        if (bid_of(p) >= 0) bytes += 2 * SL::kHalves * SL::kBoxBytes;
+      mbar_arrive_expect_tx(bar, bytes);
     }
-    mbar_arrive_expect_tx(bar, bytes);
+    const int bid = bid_of(warp);
+    if (bid == -2) flag(a.dev_status, SV_DEV_BAD_BLOCK_ID);
+    if (bid < 0) return;
+    const int y = (bid * a.Hkv + g) * kBlockSize;
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      if (bids[p] < 0) continue;
-      const int y = (bids[p] * a.Hkv + g) * kBlockSize;
-#pragma unroll
-      for (int h = 0; h < SL::kHalves; ++h) {
-        const uint32_t o = (uint32_t)((p * SL::kHalves + h) * SL::kBoxBytes);
-        tma_load_2d(kdst + o, &tmK, 64 * h, y, bar);
-        tma_load_2d(kdst + SL::kTensorBytes + o, &tmV, 64 * h, y, bar);
-      }
+    for (int h = 0; h < SL::kHalves; ++h) {
+      const uint32_t o = (uint32_t)((warp * SL::kHalves + h) * SL::kBoxBytes);
+      tma_load_2d(kdst + o, &tmK, 64 * h, y, bar);
+      tma_load_2d(kdst + SL::kTensorBytes + o, &tmV, 64 * h, y, bar);
     }
   };
 
@@ -599,12 +601,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     issue(st + kStages - 1);
     if (st + kStages - 1 < n_stage) issued_hi = st + kStages;
     const int slot = st % kStages;
-    const bool ok = mbar_wait_bounded(smem_u32(&s_full[slot]), (uint32_t)((st / kStages) & 1));
-    if (__syncthreads_or(!ok)) {
-      abort_at = st;
-      if (tid == 0) flag(a.dev_status, SV_DEV_TIMEOUT);
-      break;
-    }
+    // A wait that gives up marks the CTA; the decision to stop is taken by
+    // all threads together after this stage's barrier.
+    if (!mbar_wait_bounded(smem_u32(&s_full[slot]), (uint32_t)((st / kStages) & 1))) s_abort = 1;
     const uint32_t kbase = ring + slot * SL::kStageBytes;
     const uint32_t vbase = kbase + SL::kTensorBytes;
     const int t0 = (blk0 + 4 * st) * kBlockSize;
@@ -634,6 +633,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     __syncthreads();  // the slot is free: the next issue may overwrite it
+    if (s_abort) {
+      abort_at = st;
+      if (tid == 0) flag(a.dev_status, SV_DEV_TIMEOUT);
+      break;
+    }
   }
   if (abort_at >= 0) {
     // Let copies still in flight (stages abort_at .. issued_hi - 1) land
