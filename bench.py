@@ -510,13 +510,13 @@ def main():
 
     n_launch = len(sched)
     race = 1 if T > 0 else 0
-    # attention: plan + attend; accept: list + stats + decide (+ race); commit: copy + release.
+    # attention: plan + attend; accept: stats + decide (+ race); commit: copy + release.
     # Chunked: plan (windows + accept list) + attend + stats + decide per chunk, one race
     # after the last.
     if mode == "chunked":
         launches_per_step = n_launch * (2 + 2) + race + 2
     else:
-        launches_per_step = 2 + 3 + race + 2 + (1 if mode == "budget" else 0)
+        launches_per_step = 2 + 2 + race + 2 + (1 if mode == "budget" else 0)
     value = rows_all / t_step
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -7,18 +7,18 @@
 // first rejection; chunks of rows).  The accept / reject formula itself is
 // the standard lossless speculative-sampling rule (not printed on the pages).
 //
-// Kernels, in stream order:
-//   list   (1 CTA)   the requests whose window is not empty and not yet
-//                    decided, in request order (in chunked verification
-//                    the chunk's list pass also writes the windows, and on
-//                    the first chunk clears every request's sampling job).
-//   stats  (warps, grid-stride over active request x window row x
-//                    {target, draft} x vocabulary slice)
-//                    one pass over the slice with 128-bit loads: online
-//                    max / sum of exp(x - max) of x = logit / T (T > 0), or
-//                    max and lowest-index argmax of the raw logits (T = 0);
-//                    one 8-byte partial per slice.
-//   decide (one warp per active request)
+// Kernels, in stream order (a call works on every request, skipping those
+// with nothing to decide; in a chunk of a chunked step, on the list of
+// requests with a non-empty window that the attention planner wrote):
+//   stats  (warps, grid-stride over request x window row x {target, draft} x
+//                    vocabulary slice)
+//                    one pass over the slice, eight 128-bit loads in flight
+//                    per lane: online max / sum of exp(x - max) of
+//                    x = logit / T (T > 0), or max and lowest-index argmax of
+//                    the raw logits (T = 0); one 8-byte partial per slice.
+//                    The first chunk of a chunked step also clears every
+//                    request's sampling job.
+//   decide (one warp per request)
 //                    merges the slice partials of the window rows, then the
 //                    chain scan (or the tree descent) with Philox uniforms;
 //                    writes the path and, for T > 0, a sampling job for the
@@ -57,6 +57,7 @@ struct RacePart {
 };
 
 constexpr int kStatThreads = 256;
+constexpr int kDepth = 8;  // 128-bit loads in flight per lane in the statistics pass
 constexpr int kRaceThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -125,6 +126,7 @@ struct Args {
   int32_t* dev_status;
   int race_all;   // race kernel: every request 0..R-1 instead of the active list
   int clear_jobs; // stats kernel: first clear every request's sampling job and race ticket
+  int use_list;   // the requests come from the active list (chunked steps)
 };
 
 __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2) {
@@ -137,54 +139,20 @@ __device__ __forceinline__ void merge_am(float& v, int& i, float v2, int i2) {
   if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
 }
 
-// ------------------------------------------------------------------ list --
-// Active requests: window not empty, and (for a continuation window) not
-// already decided, in request order, count at act[R].  (In chunked
-// verification the attention planner writes this list for each chunk.)
-__global__ void __launch_bounds__(1024) list_kernel(Args a) {
-  griddep_entry();
-  const int R = a.bt.n_req;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int* act = reinterpret_cast<int*>(a.ws + a.L.act);
-  __shared__ int s_warp[32];
-  __shared__ int s_carry;
-  if (tid == 0) s_carry = 0;
-  __syncthreads();
-  for (int base = 0; base < R; base += blockDim.x) {
-    const int i = base + tid;
-    int f = 0;
-    if (i < R) {
-      const Window w = window_of(a.bt, i);
-      if (!w.ok) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-      else if (w.b < w.e && !(w.b > 0 && a.next_token[i] >= 0)) f = 1;
-    }
-    // exclusive scan of the flags
-    int x = f;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) s_warp[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      int wv = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, wv, o);
-        if (lane >= o) wv += y;
-      }
-      s_warp[lane] = wv;
-    }
-    __syncthreads();
-    const int excl = (warp ? s_warp[warp - 1] : 0) + x - f;
-    const int total = s_warp[(blockDim.x >> 5) - 1];
-    if (f) act[s_carry + excl] = i;
-    __syncthreads();
-    if (tid == 0) s_carry += total;
-    __syncthreads();
-  }
-  if (tid == 0) act[R] = s_carry;
+// ------------------------------------------------------------- requests --
+// The requests a call works on: in a chunk of a chunked step, the list the
+// attention planner wrote (requests with a non-empty window, count at
+// act[R]); otherwise every request, each kernel skipping those with nothing
+// to decide (invalid or empty window, or a continuation window already
+// decided).
+__device__ __forceinline__ int n_slots(const Args& a, const int* act) {
+  return a.use_list ? act[a.bt.n_req] : a.bt.n_req;
+}
+__device__ __forceinline__ int req_of(const Args& a, const int* act, int k) {
+  return a.use_list ? act[k] : k;
+}
+__device__ __forceinline__ bool live(const Args& a, const Window& w, int i) {
+  return w.ok && w.b < w.e && !(w.b > 0 && a.next_token[i] >= 0);
 }
 
 // ---------------------------------------------------------------- decide --
@@ -256,6 +224,10 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
     reinterpret_cast<int*>(a.ws + a.L.race_tickets)[i] = 0;
   }
   const Window w = window_of(a.bt, i);
+  if (!a.use_list && !live(a, w, i)) {
+    if (!w.ok && lane == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+    return;
+  }
   const int cu = a.bt.cu_rows[i];
   const int V = a.V;
   bool chain = true, badp = false, badt = false;
@@ -463,7 +435,7 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
   griddep_entry();
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   const int R = a.bt.n_req;
-  const int count = act[R];
+  const int count = n_slots(a, act);
   const float T = a.T;
   const int ntypes = T > 0.f ? 2 : 1;
   const int maxw = a.L.maxw;
@@ -489,8 +461,9 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
     const int type = (int)(rest % ntypes);
     const long ro = rest / ntypes;
     const int off = (int)(ro % maxw);
-    const int i = act[ro / maxw];
+    const int i = req_of(a, act, (int)(ro / maxw));
     const Window w = window_of(a.bt, i);
+    if (!a.use_list && !live(a, w, i)) continue;
     const int j = w.b + off;
     if (j >= w.e) continue;
     const int ndraft = T > 0.f ? max(0, min(w.e, w.lim - 1) - w.b) : 0;
@@ -506,20 +479,38 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
       // the normaliser: the decision recomputes its own x with an exact
       // division and exp in fp64.
       if (VEC) {
+        // kDepth 128-entry groups per round: all loads first (entries past
+        // the slice read as -inf), then one max and at most one rescale.
         const float4* p4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 8
-        for (int v = lo + 4 * lane; v < hi; v += 128) {
-          const float4 x4 = __ldcs(p4 + (v >> 2));
-          const float x0 = unit ? x4.x : div_by(x4.x, T, rT), x1 = unit ? x4.y : div_by(x4.y, T, rT);
-          const float x2 = unit ? x4.z : div_by(x4.z, T, rT), x3 = unit ? x4.w : div_by(x4.w, T, rT);
-          const float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+        for (int v0 = lo + 4 * lane; v0 < hi + 4 * lane; v0 += 128 * kDepth) {
+          float4 x[kDepth];
+#pragma unroll
+          for (int k = 0; k < kDepth; ++k) {
+            const int v = v0 + 128 * k;
+            x[k] = v < hi ? __ldcs(p4 + (v >> 2)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          }
+          float mx = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < kDepth; ++k) {
+            if (!unit && v0 + 128 * k < hi) {  // the -inf padding stays as it is
+              x[k].x = div_by(x[k].x, T, rT);
+              x[k].y = div_by(x[k].y, T, rT);
+              x[k].z = div_by(x[k].z, T, rT);
+              x[k].w = div_by(x[k].w, T, rT);
+            }
+            mx = fmaxf(mx, fmaxf(fmaxf(x[k].x, x[k].y), fmaxf(x[k].z, x[k].w)));
+          }
           if (mx > m) {
             l *= ex2((m - mx) * kLog2e);
             m = mx;
           }
-          const float mb = m * kLog2e;
-          l += (ex2(fmaf(x0, kLog2e, -mb)) + ex2(fmaf(x1, kLog2e, -mb))) +
-               (ex2(fmaf(x2, kLog2e, -mb)) + ex2(fmaf(x3, kLog2e, -mb)));
+          if (m != -INFINITY) {  // nothing but -inf so far adds nothing
+            const float mb = m * kLog2e;
+#pragma unroll
+            for (int k = 0; k < kDepth; ++k)
+              l += (ex2(fmaf(x[k].x, kLog2e, -mb)) + ex2(fmaf(x[k].y, kLog2e, -mb))) +
+                   (ex2(fmaf(x[k].z, kLog2e, -mb)) + ex2(fmaf(x[k].w, kLog2e, -mb)));
+          }
         }
       } else {
         for (int v = lo + lane; v < hi; v += 32) {
@@ -534,13 +525,21 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
     } else {
       if (VEC) {
         const float4* p4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 8
-        for (int v = lo + 4 * lane; v < hi; v += 128) {
-          const float4 x4 = __ldcs(p4 + (v >> 2));
-          if (x4.x > m) { m = x4.x; am = v; }
-          if (x4.y > m) { m = x4.y; am = v + 1; }
-          if (x4.z > m) { m = x4.z; am = v + 2; }
-          if (x4.w > m) { m = x4.w; am = v + 3; }
+        for (int v0 = lo + 4 * lane; v0 < hi + 4 * lane; v0 += 128 * kDepth) {
+          float4 x[kDepth];
+#pragma unroll
+          for (int k = 0; k < kDepth; ++k) {
+            const int v = v0 + 128 * k;
+            x[k] = v < hi ? __ldcs(p4 + (v >> 2)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          }
+#pragma unroll
+          for (int k = 0; k < kDepth; ++k) {
+            const int v = v0 + 128 * k;
+            if (x[k].x > m) { m = x[k].x; am = v; }
+            if (x[k].y > m) { m = x[k].y; am = v + 1; }
+            if (x[k].z > m) { m = x[k].z; am = v + 2; }
+            if (x[k].w > m) { m = x[k].w; am = v + 3; }
+          }
         }
       } else {
         for (int v = lo + lane; v < hi; v += 32) {
@@ -573,11 +572,11 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
   griddep_entry();
   __shared__ DecideSmem s_dec[kDecideWarps];
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
-  const int count = act[a.bt.n_req];
+  const int count = n_slots(a, act);
   const int nch = stats_slices(a.L, count, a.T > 0.f ? 2 : 1);
   const int wid = threadIdx.x >> 5;
   for (int ai = blockIdx.x * kDecideWarps + wid; ai < count; ai += gridDim.x * kDecideWarps)
-    decide_request(a, nch, act[ai], s_dec[wid]);
+    decide_request(a, nch, req_of(a, act, ai), s_dec[wid]);
 }
 
 // ------------------------------------------------------------------ race --
@@ -592,7 +591,7 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
   griddep_entry();
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   const int R = a.bt.n_req;
-  const int count = a.race_all ? R : act[R];
+  const int count = a.race_all ? R : n_slots(a, act);
   const int nch = race_slices(a.L, count, a.V);
   const int chl = chunk_len(a.V, nch);
   const long total = (long)count * nch;
@@ -602,8 +601,8 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
   const long stride = (long)gridDim.x * (kRaceThreads / 32);
   for (long item = (long)blockIdx.x * (kRaceThreads / 32) + wid; item < total; item += stride) {
     const int c = (int)(item % nch);
-    const int i = a.race_all ? (int)(item / nch) : act[item / nch];
-    // decide_request cleared every listed request's job before it could
+    const int i = a.race_all ? (int)(item / nch) : req_of(a, act, (int)(item / nch));
+    // decide_request cleared every request's job before it could
     // return early (and, for a whole chunked step, the first chunk's list
     // pass cleared every request's), so a non-zero mode here was written by
     // this call.
@@ -750,9 +749,9 @@ static bool vec_ok(int32_t vocab, const float* target_logits, const float* draft
           15) == 0;
 }
 
-// Enqueue the list pass, the statistics, the decision and the race; in a
-// chunked step (chunk_index >= 0) the attention planner wrote the list and
-// the race is left to race_all after the last chunk.
+// Enqueue the statistics, the decision and the race; in a chunked step
+// (chunk_index >= 0) the kernels take the attention planner's list and the
+// race is left to race_all after the last chunk.
 sv_status run(const sv_batch* bt, const float* target_logits, const float* draft_logits,
               int32_t vocab, float temperature, uint64_t seed, int32_t* accepted_len,
               int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
@@ -782,10 +781,7 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
   a.clear_jobs = chunk_index == 0 ? 1 : 0;
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   const bool vec = vec_ok(vocab, target_logits, draft_logits);
-  if (!chunk_step) {
-    if (sv::launch(list_kernel, 1, 1024, 0, s, a) != cudaSuccess)
-      return SV_ERR_CUDA;
-  }
+  a.use_list = chunk_step ? 1 : 0;
   const long items = (long)bt->n_req * a.L.maxw * (temperature > 0.f ? 2 : 1) * a.L.nch_cap;
   const long warps = kStatThreads / 32;
   const unsigned gs = (unsigned)max(1L, min((items + warps - 1) / warps, (long)kNumSMs * 4));
@@ -815,6 +811,7 @@ sv_status race_all(const sv_batch* bt, const float* target_logits, const float* 
   a.dev_status = dev_status;
   a.race_all = 1;
   a.clear_jobs = 0;
+  a.use_list = 0;
   return launch_race(a, vec_ok(vocab, target_logits, draft_logits), s);
 }
 
@@ -849,7 +846,7 @@ extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
 // All calls share the array: two calls whose work overlaps on the GPU (for
 // example on two streams) race on it.  Nothing in it has to start at zero:
 // the accept kernels write every scratch word before they read it (the
-// decision clears each listed request's sampling job and race ticket before
+// decision clears every request's sampling job and race ticket before
 // anything reads them, and the statistics write every partial the decision
 // merges).
 

@@ -22,8 +22,8 @@ struct Layout {
 };
 Layout layout(int R, int total_rows, int V, int maxw);
 
-// The accept kernels.  chunk_index < 0: a list pass, then statistics,
-// decision and race.  chunk_index >= 0 (chunk of a chunked step): the active
+// The accept kernels.  chunk_index < 0: statistics, decision and race over
+// every request.  chunk_index >= 0 (chunk of a chunked step): the active
 // list in `ws` (at Layout::act) was written by the attention planner for this
 // batch's windows; statistics (the first chunk also clears every sampling
 // job) and decision only, the draws are left to race_all.
