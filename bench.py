@@ -275,6 +275,9 @@ def main():
                     help="only run this many steps (for a profiler), no timing line")
     ap.add_argument("--ctx-scale", type=float, default=1.0,
                     help="with --profile-steps: shrink every context (smaller profiler captures)")
+    ap.add_argument("--profile-call", default="step", choices=["step", "attend", "accept"],
+                    help="with --profile-steps: run the whole step, or only the one-pass "
+                         "sv_tree_attend / sv_accept call on the whole batch")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -305,8 +308,9 @@ def main():
     stream = torch.cuda.current_stream()
 
     if args.profile_steps:
+        fn = {"step": s.run, "attend": s.attend, "accept": s.accept}[args.profile_call]
         for _ in range(args.profile_steps):
-            s.run()
+            fn()
         torch.cuda.synchronize()
         return
 

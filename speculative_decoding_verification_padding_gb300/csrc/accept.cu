@@ -95,11 +95,16 @@ Layout layout(int R, int total_rows, int V, int maxw) {
   return L;
 }
 
-// Slices actually used, from the number of active requests (same value in
-// every kernel of a call): about 32 warps per SM of work.
-__device__ __forceinline__ int stats_slices(const Layout& L, int count, int ntypes) {
-  const long slots = (long)max(1, count) * L.maxw * ntypes;
-  const long want = (2L * kNumSMs * 32 + slots - 1) / slots;  // about 2 slices per warp
+// Slices actually used (the same value in every kernel of a call).  With an
+// active list the items are (listed request, window row, type, slice): about
+// two per warp of a 32-warps-per-SM grid.  Without a list they are (packed
+// row, type, slice): about four per warp.
+__device__ __forceinline__ int stats_slices(const Layout& L, int count, int ntypes, bool listed,
+                                            int total_rows) {
+  const long slots = listed ? (long)max(1, count) * L.maxw * ntypes
+                            : (long)max(1, total_rows) * ntypes;
+  const long per_warp = listed ? 2 : 4;
+  const long want = (per_warp * kNumSMs * 32 + slots - 1) / slots;
   return (int)max((long)L.nch, min(want, (long)L.nch_cap));
 }
 __device__ __forceinline__ int race_slices(const Layout& L, int count, int V) {
@@ -448,9 +453,11 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
       reinterpret_cast<int*>(a.ws + a.L.race_tickets)[i] = 0;
     }
   }
-  const int nch = stats_slices(a.L, count, ntypes);
+  const bool listed = a.use_list != 0;
+  const int nch = stats_slices(a.L, count, ntypes, listed, a.bt.total_rows);
   const int chl = chunk_len(a.V, nch);
-  const long total = (long)count * maxw * ntypes * nch;
+  const long total = listed ? (long)count * maxw * ntypes * nch
+                            : (long)a.bt.total_rows * ntypes * nch;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const long stride = (long)gridDim.x * (kStatThreads / 32);
   const bool unit = T == 1.f;
@@ -460,12 +467,23 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
     const long rest = item / nch;
     const int type = (int)(rest % ntypes);
     const long ro = rest / ntypes;
-    const int off = (int)(ro % maxw);
-    const int i = req_of(a, act, (int)(ro / maxw));
-    const Window w = window_of(a.bt, i);
-    if (!a.use_list && !live(a, w, i)) continue;
-    const int j = w.b + off;
-    if (j >= w.e) continue;
+    int i, j, off;
+    Window w;
+    if (listed) {
+      off = (int)(ro % maxw);
+      i = act[ro / maxw];
+      w = window_of(a.bt, i);
+      j = w.b + off;
+      if (j >= w.e) continue;
+    } else {
+      // packed row ro of request i
+      i = find_segment(a.bt.cu_rows, R, (int)ro);
+      w = window_of(a.bt, i);
+      if (!live(a, w, i)) continue;
+      j = (int)ro - a.bt.cu_rows[i];
+      if (j < w.b || j >= w.e) continue;
+      off = j - w.b;
+    }
     const int ndraft = T > 0.f ? max(0, min(w.e, w.lim - 1) - w.b) : 0;
     if (type == 1 && off >= ndraft) continue;
     const int r = a.bt.cu_rows[i] + j;
@@ -573,7 +591,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
   __shared__ DecideSmem s_dec[kDecideWarps];
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   const int count = n_slots(a, act);
-  const int nch = stats_slices(a.L, count, a.T > 0.f ? 2 : 1);
+  const int nch = stats_slices(a.L, count, a.T > 0.f ? 2 : 1, a.use_list != 0, a.bt.total_rows);
   const int wid = threadIdx.x >> 5;
   for (int ai = blockIdx.x * kDecideWarps + wid; ai < count; ai += gridDim.x * kDecideWarps)
     decide_request(a, nch, req_of(a, act, ai), s_dec[wid]);
