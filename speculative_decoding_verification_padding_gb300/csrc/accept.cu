@@ -346,6 +346,16 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   // ---- T > 0: speculative sampling on a chain ----
   const int jmax = min(w.e, w.lim - 1);
   const int nq = max(0, min(w.e, w.lim - 1) - w.b);  // draft rows with a tested child
+  const int nd = jmax - w.b;  // drafts decided by this window
+  // The logits at the drafted tokens do not depend on the partials: their
+  // loads go out before the merge.
+  float xp_raw = 0.f, xq_raw = 0.f;
+  if (lane < nd) {
+    const int j = w.b + 1 + lane;
+    const size_t off = (size_t)(cu + j - 1) * V + sm.tok[j];
+    xp_raw = a.target[off];
+    xq_raw = a.draft[off];
+  }
   merge_pairs(a, nch, cu + w.b, w.e - w.b, nq, sm.mp + w.b, sm.lp + w.b, sm.mq + w.b,
               sm.lq + w.b);
   __syncwarp();
@@ -357,17 +367,14 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   // Lane j - b - 1 evaluates draft j's ratio and draws its uniform; the scan
   // then reads them by shuffle.
   const float T = a.T;
-  const int nd = jmax - w.b;  // drafts decided by this window
   double ratio = 1.0;
   float u_lane = 0.f;
   {
     const int j = w.b + 1 + lane;
     if (lane < nd) {
       u_lane = accept_u(a.seed, i, j);
-      const int x = sm.tok[j];
-      const size_t off = (size_t)(cu + j - 1) * V + x;
-      const float xp = a.target[off] / T;
-      const float xq = a.draft[off] / T;
+      const float xp = xp_raw / T;
+      const float xq = xq_raw / T;
       const double p = exp((double)xp - (double)sm.mp[j - 1]) / (double)sm.lp[j - 1];
       const double q = exp((double)xq - (double)sm.mq[j - 1]) / (double)sm.lq[j - 1];
       ratio = q > 0.0 ? fmin(1.0, p / q) : 1.0;
@@ -656,14 +663,26 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
     };
     if (VEC) {
       // Four 128-entry groups per iteration, their loads issued first.  The
-      // trip count is uniform so that the lanes can share their thresholds:
-      // the best key any lane has seen bounds the winner from below.
+      // trip count is uniform so that the lanes can share the best key K any
+      // of them has seen: the winner's key is at least K, so
+      //  - a group whose weights are all below K * kEmin skips the generator;
+      //  - an entry whose uniform is at most exp(-w / K) has E >= w / K, its
+      //    key cannot exceed K, and it skips the logarithm.  The bound is taken
+      //    with ex2.approx minus 2^-20, below exp(-w / K) by more than the
+      //    approximation and rounding errors, so no possible winner is lost.
       constexpr int kGroups = 4;
-      float wthr = -1.f;
+      float K = 0.f;
       const float4* p4 = reinterpret_cast<const float4*>(lp);
       const float4* q4 = reinterpret_cast<const float4*>(lq);
       for (int base = lo; base < hi; base += 128 * kGroups) {
-        wthr = fmaxf(wthr, warp_max(thr));
+        K = fmaxf(K, warp_max(bi == 0x7fffffff ? 0.f : bw / bE));
+        const float nK = K > 0.f ? -kLog2e / K : 0.f;  // exponent scale of exp(-w / K)
+        const float gthr = K > 0.f ? K * kEmin : -1.f;
+        auto entry = [&](float wv, uint32_t bits, int v) {
+          const float u = race_u(bits);
+          if (K > 0.f && u <= ex2(wv * nK) - 0x1p-20f) return;
+          take(wv, -logf(u), v);
+        };
         float4 xp[kGroups], xq[kGroups];
 #pragma unroll
         for (int k = 0; k < kGroups; ++k) {
@@ -677,12 +696,12 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
           if (v >= hi) continue;
           const float w0 = weight(xp[k].x, xq[k].x), w1 = weight(xp[k].y, xq[k].y);
           const float w2 = weight(xp[k].z, xq[k].z), w3 = weight(xp[k].w, xq[k].w);
-          if (fmaxf(fmaxf(w0, w1), fmaxf(w2, w3)) < fmaxf(thr, wthr)) continue;
+          if (fmaxf(fmaxf(w0, w1), fmaxf(w2, w3)) < gthr) continue;
           const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
-          take(w0, -logf(race_u(bits.a)), v);
-          take(w1, -logf(race_u(bits.b)), v + 1);
-          take(w2, -logf(race_u(bits.c)), v + 2);
-          take(w3, -logf(race_u(bits.d)), v + 3);
+          entry(w0, bits.a, v);
+          entry(w1, bits.b, v + 1);
+          entry(w2, bits.c, v + 2);
+          entry(w3, bits.d, v + 3);
         }
       }
     } else {
