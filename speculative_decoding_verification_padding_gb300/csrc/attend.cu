@@ -69,7 +69,11 @@ constexpr int kMaxPagesPerSplit = 1024;  // block ids of a unit staged in shared
 struct ReqInfo {
   int ubase, nsplit, nrt, b, e, ctx, nblk, valid;
   int act;     // chunk mode: the window is not empty (the accept list)
+  int cu, rows;
 };
+// The planner keeps the per-request records in shared memory up to this many
+// requests (about 45 KB), in its workspace beyond.
+constexpr int kPlanSmemRequests = 1024;
 
 // One unit of the work list: everything its CTA needs to start (a single
 // 48-byte load, issued together with the header's unit count).
@@ -91,7 +95,7 @@ struct Header {
 };
 
 struct Layout {
-  size_t header, info, ubase, work, tickets, ml, o, total;
+  size_t header, info, work, tickets, ml, o, total;
   int ucap;
 };
 
@@ -109,7 +113,6 @@ inline Layout layout(int R, int total_rows, int group, int Hkv, int D, int max_b
   L.ucap = unit_cap(R, total_rows, group, Hkv, max_blocks);
   L.header = off; off += align256(sizeof(Header));
   L.info = off; off += align256(sizeof(ReqInfo) * (size_t)R);
-  L.ubase = off; off += align256(sizeof(int) * (size_t)(R + 1));
   L.work = off; off += align256(sizeof(WorkItem) * (size_t)L.ucap);
   L.tickets = off; off += align256(sizeof(int) * (size_t)L.ucap);
   L.ml = off; off += align256((size_t)L.ucap * kTileRows * 2 * sizeof(float));
@@ -168,30 +171,23 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   const int R = a.bt.n_req;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Header* hdr = reinterpret_cast<Header*>(a.ws + a.L.header);
-  ReqInfo* info = reinterpret_cast<ReqInfo*>(a.ws + a.L.info);
-  int* ubase = reinterpret_cast<int*>(a.ws + a.L.ubase);
+  extern __shared__ ReqInfo s_info[];
+  ReqInfo* info = R <= kPlanSmemRequests ? s_info : reinterpret_cast<ReqInfo*>(a.ws + a.L.info);
   int* tickets = reinterpret_cast<int*>(a.ws + a.L.tickets);
-  __shared__ int s_bad;
   __shared__ unsigned long long s_W;
   __shared__ int s_warp[32];
   __shared__ int s_carry, s_acarry;
 
   if (tid == 0) {
-    s_bad = (a.bt.cu_rows[0] != 0 || a.bt.cu_rows[R] != a.bt.total_rows) ? 1 : 0;
+    // Each request's rows are checked against the packed total by its window;
+    // a prefix that does not start at 0 or end at the total is reported too.
+    if (a.bt.cu_rows[0] != 0 || a.bt.cu_rows[R] != a.bt.total_rows)
+      flag(a.dev_status, SV_DEV_BAD_WINDOW);
     s_W = 0ull;
     s_carry = 0;
     s_acarry = 0;
   }
   __syncthreads();
-  if (s_bad) {
-    if (tid == 0) {
-      flag(a.dev_status, SV_DEV_BAD_WINDOW);
-      if (a.chunk.index >= 0) a.chunk.act[R] = 0;
-      hdr->U = 0;
-      hdr->P = 1;
-    }
-    return;
-  }
   // One warp per request: window, parents, length, work.
   unsigned long long myW = 0;
   const bool chunked = a.chunk.index >= 0;
@@ -241,6 +237,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
       ri.nsplit = 0;
       ri.ubase = 0;
       ri.act = (!badw && w.b < w.e) ? 1 : 0;
+      ri.cu = cu;
+      ri.rows = w.rows;
       info[i] = ri;
     }
   }
@@ -266,10 +264,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     }
     int excl, total;
     block_excl_scan(s_warp, units, excl, total);
-    if (i < R) {
-      ubase[i] = s_carry + excl;
-      info[i].ubase = s_carry + excl;
-    }
+    if (i < R) info[i].ubase = s_carry + excl;
     if (chunked) {
       int aexcl, atotal;
       block_excl_scan(s_warp, act, aexcl, atotal);
@@ -294,8 +289,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
       const ReqInfo ri = info[i];
       const int n = ri.nrt * a.Hkv * ri.nsplit;
       if (n == 0) continue;
-      const int cu = a.bt.cu_rows[i];
-      const int rows = a.bt.cu_rows[i + 1] - cu;
+      const int cu = ri.cu;
+      const int rows = ri.rows;
       for (int x = lane; x < n; x += 32) {
         WorkItem it;
         it.i = i;
@@ -314,7 +309,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
       }
     }
   if (tid == 0) {
-    ubase[R] = U;
     hdr->U = U;
     hdr->P = P;
   }
@@ -820,7 +814,9 @@ sv_status launch(const Args& a, cudaStream_t stream) {
   CUtensorMap tmK, tmV;
   if (!make_map(&tmK, a.k, a.num_blocks, a.Hkv, D) || !make_map(&tmV, a.v, a.num_blocks, a.Hkv, D))
     return SV_ERR_CUDA;
-  if (sv::launch(plan_kernel, 1, 1024, 0, stream, a) != cudaSuccess) return SV_ERR_CUDA;
+  const size_t plan_smem =
+      a.bt.n_req <= kPlanSmemRequests ? sizeof(ReqInfo) * (size_t)a.bt.n_req : 0;
+  if (sv::launch(plan_kernel, 1, 1024, plan_smem, stream, a) != cudaSuccess) return SV_ERR_CUDA;
   if (sv::launch(attend_kernel<D>, a.L.ucap, kThreads, smem, stream, a, tmK, tmV) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;

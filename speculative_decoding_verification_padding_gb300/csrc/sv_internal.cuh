@@ -38,8 +38,10 @@ struct Window {
 
 __device__ __forceinline__ Window window_of(const sv_batch& bt, int i) {
   Window w;
-  w.rows = bt.cu_rows[i + 1] - bt.cu_rows[i];
-  w.ok = w.rows >= 1 && w.rows <= bt.max_rows_per_req && w.rows <= kMaxRows;
+  const int c0 = bt.cu_rows[i], c1 = bt.cu_rows[i + 1];
+  w.rows = c1 - c0;
+  w.ok = w.rows >= 1 && w.rows <= bt.max_rows_per_req && w.rows <= kMaxRows && c0 >= 0 &&
+         c1 <= bt.total_rows;
   w.lim = w.rows;
   if (bt.verify_len) {
     int L = bt.verify_len[i];
