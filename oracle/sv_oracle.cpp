@@ -329,8 +329,9 @@ int row_argmax(const float* l, int V) {
 }
 
 // ------------------------------------------------ residual / bonus (a5) --
-// Draw one token from normalize(w) with w_v = max(0, p_v - q_v) (residual,
-// after a rejection) or w_v = p_v (bonus, all drafts accepted), as the
+// Draw one token from normalize(w) with w_v = max(0, p_v - c q_v) (residual:
+// c = 1 after one rejection, larger after several rejections among tree
+// siblings) or w_v = p_v (bonus, all drafts accepted), as the
 // winner of an exponential race: token = argmax_v w_v / E_v with
 // E_v = -log(U_v), U_v ~ U(0,1) independent.  P(v wins) = w_v / sum w, so
 // this is an exact sample of normalize(w) (the race form of the Gumbel-max
@@ -342,12 +343,13 @@ int row_argmax(const float* l, int V) {
 const double RACE_EPS = 2e-6;
 
 int race_sample(const float* lp, const float* lq, int V, float T, const RowSoftmax& sp,
-                const RowSoftmax* sq, uint64_t seed, int i, int pos, bool* ambiguous) {
+                const RowSoftmax* sq, uint64_t seed, int i, int pos, bool* ambiguous,
+                double c = 1.0) {
   std::vector<double> w(V), lo(V), hi(V);
   double W = 0.0;
   for (int v = 0; v < V; ++v) {
     double p = prob(lp, v, T, sp);
-    double q = sq ? prob(lq, v, T, *sq) : 0.0;
+    double q = sq ? c * prob(lq, v, T, *sq) : 0.0;
     double wv = sq ? std::max(0.0, p - q) : p;
     w[v] = wv;
     W += wv;
@@ -394,6 +396,81 @@ struct AcceptArgs {
   double* row_stats;
 };
 
+// ------------------------------------------------ tree sampling (NEXT-1) --
+// T > 0 on a draft tree whose siblings were drawn independently from the
+// parent's draft distribution q_n (with replacement).  From the root, the
+// children of the current node n are tried in index order: child c (token x)
+// is accepted with probability min(1, p'(x) / q_n(x)), where p' is the
+// target distribution left after the siblings rejected before it; on
+// acceptance the walk moves to c, otherwise p' <- normalize(max(0, p' - q_n)).
+// When every child is rejected the emitted token is drawn from p'; at a leaf
+// it is drawn from p_leaf (the bonus).  Tree verification is on the pages
+// ([SwiftSpec] mechanism 2, [SSD]); this rejection rule is the plainest
+// lossless reading for several candidates (each rejection removes exactly
+// the mass the next candidate could have taken).
+//
+// After j rejections p' = max(0, p - c_j q_n) / S(c_j), S(c) = sum_v
+// max(0, p_v - c q_v), with c_0 = 0 (S(0) = 1) and c_{j+1} = c_j + S(c_j):
+// max(0, max(0, p - c q) / S - q) = max(0, p - (c + S) q) / S.  If S reaches
+// 0 (p <= c q everywhere) the residual is undefined: the remaining siblings
+// are not tested and the token is drawn from p_n.  Uniforms: child c uses
+// accept_uniform(seed, i, c); the emitted token uses the race stream at
+// position (accepted nodes + 1), as for a chain.
+double residual_mass(const float* lp, const float* lq, int V, float T, const RowSoftmax& sp,
+                     const RowSoftmax& sq, double c) {
+  double s = 0.0;
+  for (int v = 0; v < V; ++v) s += std::max(0.0, prob(lp, v, T, sp) - c * prob(lq, v, T, sq));
+  return s;
+}
+
+void tree_sample(const AcceptArgs& a, int i, const Window& w, int cu, int32_t* nodes) {
+  const long V = a.V;
+  int n = 0, k = 0, next = -1;
+  bool amb = false;
+  for (;;) {
+    const float* lp = a.target + (cu + n) * V;
+    const float* lq = a.draft + (cu + n) * V;
+    const RowSoftmax sp = row_softmax(lp, a.V, a.T);
+    std::vector<int> kids;
+    for (int c = n + 1; c < w.rows; ++c)
+      if (a.parent[cu + c] == n) kids.push_back(c);
+    if (kids.empty()) {  // leaf: bonus token from p_n
+      next = race_sample(lp, nullptr, a.V, a.T, sp, nullptr, a.seed, i, k + 1, &amb);
+      break;
+    }
+    const RowSoftmax sq = row_softmax(lq, a.V, a.T);
+    double c = 0.0, S = 1.0;
+    bool moved = false, vanished = false;
+    for (int ch : kids) {
+      const int x = a.tokens[cu + ch];
+      const double p = prob(lp, x, a.T, sp), q = prob(lq, x, a.T, sq);
+      const double pres = std::max(0.0, p - c * q) / S;
+      const double ratio = q > 0.0 ? std::min(1.0, pres / q) : 1.0;
+      const double u = accept_uniform(a.seed, i, ch);
+      if (std::fabs(u - ratio) < 1e-6) amb = true;
+      if (u < ratio) {
+        nodes[++k] = ch;
+        n = ch;
+        moved = true;
+        break;
+      }
+      c += S;
+      S = residual_mass(lp, lq, a.V, a.T, sp, sq, c);
+      if (!(S > 0.0)) {
+        vanished = true;
+        break;
+      }
+    }
+    if (moved) continue;
+    next = vanished ? race_sample(lp, nullptr, a.V, a.T, sp, nullptr, a.seed, i, k + 1, &amb)
+                    : race_sample(lp, lq, a.V, a.T, sp, &sq, a.seed, i, k + 1, &amb, c);
+    break;
+  }
+  a.accepted_len[i] = k;
+  a.next_token[i] = next;
+  if (amb) a.ambiguous[i] = 1;
+}
+
 // Accept/reject of one request ([DSpark] glossary: the longest accepted prefix
 // is kept and the target distribution is preserved; [FASER] mechanism 1:
 // every request has its own number of drafts; mechanism 2: a request stops at
@@ -417,7 +494,6 @@ int accept_one(const AcceptArgs& a, int i) {
   if (!chain) {
     // A tree is verified in one call over all its rows.
     if (w.b != 0 || w.e != w.rows) return ORC_BAD_WINDOW;
-    if (a.T > 0.0f) return ORC_UNSUPPORTED;
   }
   if (w.b == 0) {  // first window of this step: reset the request's state
     a.accepted_len[i] = 0;
@@ -480,6 +556,8 @@ int accept_one(const AcceptArgs& a, int i) {
       a.accepted_len[i] = k;
       a.next_token[i] = am[n];
     }
+  } else if (!chain) {
+    tree_sample(a, i, w, cu, nodes);
   } else {
     // ---- speculative sampling (a4 + a5, T > 0, chains) ----
     const float* draft = a.draft;

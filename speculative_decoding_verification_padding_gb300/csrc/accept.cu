@@ -44,10 +44,10 @@ struct StatPart {
 };
 
 struct Job {
-  int mode;     // 0 none, 1 residual, 2 bonus
+  int mode;     // 0 none, 1 residual max(0, p - c q), 2 bonus (p), 3 tree walk pending
   int row;      // packed row of the target (and draft) logits
   int pos;      // position of the emitted token
-  int pad;
+  float c;      // residual coefficient (1 after one rejection)
   float mp, lp, mq, lq;
 };
 
@@ -253,13 +253,9 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   badp = __any_sync(0xffffffffu, badp);
   badt = __any_sync(0xffffffffu, badt);
   chain = __all_sync(0xffffffffu, chain);
-  if (badp || badt || (!chain && (w.b != 0 || w.e != w.rows)) || (!chain && a.T > 0.f)) {
+  if (badp || badt || (!chain && (w.b != 0 || w.e != w.rows))) {
     if (lane == 0)
-      flag(a.dev_status, badp ? SV_DEV_BAD_PARENT
-                              : badt ? SV_DEV_BAD_TOKEN
-                                     : (!chain && a.T > 0.f && w.b == 0 && w.e == w.rows)
-                                           ? SV_DEV_UNSUPPORTED
-                                           : SV_DEV_BAD_WINDOW);
+      flag(a.dev_status, badp ? SV_DEV_BAD_PARENT : badt ? SV_DEV_BAD_TOKEN : SV_DEV_BAD_WINDOW);
     return;
   }
   const int max_rows = a.bt.max_rows_per_req;
@@ -268,6 +264,21 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
     for (int k = lane; k < max_rows; k += 32) nodes[k] = k == 0 ? 0 : -1;
   } else if (a.accepted_len[i] != w.b) {
     if (lane == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+    return;
+  }
+  if (!chain && a.T > 0.f) {
+    // Tree sampling: the walk needs vocabulary passes, one CTA per tree
+    // (tree_kernel) takes it over from here.
+    if (lane == 0) {
+      Job jb{};
+      jb.mode = 3;
+      jb.row = cu;
+      *job = jb;
+      a.accepted_len[i] = 0;
+      a.next_token[i] = -1;
+      a.ambiguous[i] = 0;
+      if (a.done) a.done[i] = 0;
+    }
     return;
   }
   int len = w.b;   // accepted drafts so far
@@ -387,7 +398,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   __syncwarp();
   Job jb;
   jb.mode = 0;
-  jb.pad = 0;
+  jb.c = 1.f;
   for (int k = 0; k < nd; ++k) {
     const int j = w.b + 1 + k;
     const double rk = __shfl_sync(0xffffffffu, ratio, k & 31);
@@ -604,6 +615,143 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
     decide_request(a, nch, req_of(a, act, ai), s_dec[wid]);
 }
 
+// ------------------------------------------------------------- tree walk --
+// Sampling on a draft tree (T > 0; siblings drawn independently from the
+// parent's q), one CTA per tree, after the decision kernel marked it.  From
+// the root, the children of node n are tried in index order: child c (token
+// x) is accepted iff u(i, c) < min(1, p'(x) / q_n(x)) with p' the target
+// distribution left by the siblings rejected before it.  After j rejections
+// p' = max(0, p - c_j q) / S(c_j), S(c) = sum_v max(0, p_v - c q_v),
+// c_0 = 0, S(c_0) = 1, c_{j+1} = c_j + S(c_j): one vocabulary pass per
+// rejection (all threads; per-thread Kahan sums, then fp64).  If S vanishes,
+// the remaining siblings are not tried and the token comes from p_n.  The
+// walk ends at a leaf (bonus from p_leaf) or when every child is rejected
+// (a residual job with coefficient c); the race draws the token.
+constexpr int kTreeThreads = 1024;
+
+__global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
+  griddep_entry();
+  const int i = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  Job* job = reinterpret_cast<Job*>(a.ws + a.L.jobs) + i;
+  __shared__ int s_mode, s_nk, s_dec;
+  __shared__ int s_kids[kMaxRows];
+  __shared__ float s_st[4];  // merged max / normaliser of p and of q at the current node
+  __shared__ double s_red[kTreeThreads / 32];
+  __shared__ double s_S;
+  if (tid == 0) s_mode = job->mode;
+  __syncthreads();
+  if (s_mode != 3) return;
+  const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
+  const int nch = stats_slices(a.L, n_slots(a, act), 2, a.use_list != 0, a.bt.total_rows);
+  const float T = a.T, rT = 1.f / T;
+  const int V = a.V;
+  const int cu = a.bt.cu_rows[i];
+  const int rows = a.bt.cu_rows[i + 1] - cu;  // checked by the decision kernel
+  int32_t* nodes = a.accepted_nodes + (size_t)i * a.bt.max_rows_per_req;
+  int n = 0, k = 0;
+  bool amb = false;
+  Job out{};
+  for (int step = 0; step < kMaxRows; ++step) {  // every move goes to a larger node
+    if (warp == 0) {
+      // children of n in index order, then the merged statistics of row n
+      int cnt = 0;
+      for (int base = n + 1; base < rows; base += 32) {
+        const int c = base + lane;
+        const bool is = c < rows && a.bt.parent[cu + c] == n;
+        const unsigned m = __ballot_sync(0xffffffffu, is);
+        if (is) s_kids[cnt + __popc(m & ((1u << lane) - 1u))] = c;
+        cnt += __popc(m);
+      }
+      if (lane == 0) s_nk = cnt;
+      merge_pairs(a, nch, cu + n, 1, cnt > 0 ? 1 : 0, &s_st[0], &s_st[1], &s_st[2], &s_st[3]);
+    }
+    __syncthreads();
+    const int nk = s_nk;
+    if (nk == 0) {  // leaf: bonus token from p_n
+      out.mode = 2;
+      break;
+    }
+    const float* lp = a.target + (size_t)(cu + n) * V;
+    const float* lq = a.draft + (size_t)(cu + n) * V;
+    double c = 0.0, S = 1.0;
+    bool moved = false, vanished = false;
+    for (int t = 0; t < nk; ++t) {
+      const int ch = s_kids[t];
+      if (tid == 0) {
+        const int x = a.bt.tokens[cu + ch];
+        const double p = exp((double)(lp[x] / T) - (double)s_st[0]) / (double)s_st[1];
+        const double q = exp((double)(lq[x] / T) - (double)s_st[2]) / (double)s_st[3];
+        const double pres = fmax(0.0, p - c * q) / S;
+        const double ratio = q > 0.0 ? fmin(1.0, pres / q) : 1.0;
+        const double u = (double)accept_u(a.seed, i, ch);
+        if (fabs(u - ratio) < 1e-6) amb = true;
+        s_dec = u < ratio ? 1 : 0;
+      }
+      __syncthreads();
+      const int dec = s_dec;
+      __syncthreads();  // s_dec is rewritten by the next test
+      if (dec) {
+        if (tid == 0) nodes[k + 1] = ch;
+        ++k;
+        n = ch;
+        moved = true;
+        break;
+      }
+      c += S;
+      // S(c) over the whole vocabulary
+      const float mpb = s_st[0] * kLog2e, mqb = s_st[2] * kLog2e;
+      const float inv_lp = 1.f / s_st[1], cq = (float)c / s_st[3];
+      float sum = 0.f, comp = 0.f;
+      for (int v = tid; v < V; v += kTreeThreads) {
+        const float pv = ex2(fmaf(div_by(lp[v], T, rT), kLog2e, -mpb)) * inv_lp;
+        const float qv = ex2(fmaf(div_by(lq[v], T, rT), kLog2e, -mqb)) * cq;
+        const float y = fmaxf(pv - qv, 0.f) - comp;
+        const float tsum = sum + y;
+        comp = (tsum - sum) - y;
+        sum = tsum;
+      }
+      double d = (double)sum - (double)comp;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      if (lane == 0) s_red[warp] = d;
+      __syncthreads();
+      if (warp == 0) {
+        double e = lane < kTreeThreads / 32 ? s_red[lane] : 0.0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+        if (lane == 0) s_S = e;
+      }
+      __syncthreads();
+      S = s_S;
+      if (!(S > 0.0)) {
+        vanished = true;
+        break;
+      }
+    }
+    if (moved) continue;
+    out.mode = vanished ? 2 : 1;
+    out.c = (float)c;
+    break;
+  }
+  if (tid != 0) return;
+  out.row = cu + n;
+  out.pos = k + 1;
+  out.mp = s_st[0];
+  out.lp = s_st[1];
+  out.mq = s_st[2];
+  out.lq = s_st[3];
+  if (out.mode == 2) {
+    out.mq = 0.f;
+    out.lq = 1.f;
+  }
+  *job = out;
+  a.accepted_len[i] = k;
+  a.next_token[i] = -1;
+  if (amb) a.ambiguous[i] = 1;
+  if (a.done) a.done[i] = 1;
+}
+
 // ------------------------------------------------------------------ race --
 __device__ __forceinline__ void race_take(float& best, int& bi, float key, int v) {
   if (key > best || (key == best && v < bi)) { best = key; bi = v; }
@@ -632,7 +780,7 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
     // pass cleared every request's), so a non-zero mode here was written by
     // this call.
     const Job jb = reinterpret_cast<const Job*>(a.ws + a.L.jobs)[i];
-    if (jb.mode == 0) continue;
+    if (jb.mode != 1 && jb.mode != 2) continue;
     const bool resid = jb.mode == 1;
     const float* lp = a.target + (size_t)jb.row * a.V;
     const float* lq = a.draft + (size_t)jb.row * a.V;
@@ -656,10 +804,11 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
         thr = wv / E * kEmin;
       }
     };
+    const float cq = jb.c * inv_lq;
     auto weight = [&](float lpv, float lqv) {
       const float p = ex2(fmaf(div_by(lpv, T, rT), kLog2e, -mpb)) * inv_lp;
       if (!resid) return p;
-      return fmaxf(p - ex2(fmaf(div_by(lqv, T, rT), kLog2e, -mqb)) * inv_lq, 0.f);
+      return fmaxf(p - ex2(fmaf(div_by(lqv, T, rT), kLog2e, -mqb)) * cq, 0.f);
     };
     if (VEC) {
       // Four 128-entry groups per iteration, their loads issued first.  The
@@ -827,6 +976,12 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
     return SV_ERR_CUDA;
   const unsigned gd = (unsigned)max(1, min((bt->n_req + kDecideWarps - 1) / kDecideWarps, kNumSMs * 8));
   if (sv::launch(decide_kernel, gd, kDecideWarps * 32, 0, s, a) != cudaSuccess) return SV_ERR_CUDA;
+  if (temperature > 0.f && !chunk_step && bt->max_rows_per_req > 2) {
+    // draft trees at T > 0 (requests the decision marked; a tree is verified
+    // in one window, never in chunks); the other CTAs exit at once
+    if (sv::launch(tree_kernel, (unsigned)bt->n_req, kTreeThreads, 0, s, a) != cudaSuccess)
+      return SV_ERR_CUDA;
+  }
   if (temperature > 0.f && !chunk_step) return launch_race(a, vec, s);
   return SV_OK;
 }

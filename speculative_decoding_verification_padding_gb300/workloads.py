@@ -243,9 +243,16 @@ def make_workload(cfg: Config, *, n_req: int | None = None, ctx_scale: float = 1
     for i in range(R):
         base = int(cu_rows[i])
         tokens[base] = tok_rng.integers(0, V)  # root: last committed token
-        if cfg.gamma[0] == "tree":
-            # siblings are the top-b draft tokens at the parent (distinct,
-            # lower index first on ties)
+        if cfg.gamma[0] == "tree" and T > 0:
+            # sampling: siblings drawn independently from softmax(draft at the
+            # parent / T), with replacement (Gumbel-max)
+            for j in range(1, rows[i]):
+                row = draft[base + int(parents[i][j])]
+                gum = tok_rng.gumbel(size=V)
+                tokens[base + j] = int(np.argmax(row.astype(np.float64) / T + gum))
+        elif cfg.gamma[0] == "tree":
+            # greedy: siblings are the top-b draft tokens at the parent
+            # (distinct, lower index first on ties)
             order_cache = {}
             for j in range(1, rows[i]):
                 p = int(parents[i][j])

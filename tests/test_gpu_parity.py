@@ -376,12 +376,40 @@ def test_bad_block_id_and_bad_parent_are_flagged():
     assert s.dev_status.item() & api.N.SV_DEV_BAD_PARENT
 
 
-def test_tree_with_temperature_is_flagged_unsupported():
-    w = wl.make_workload(wl.config("tree70b"), ctx_scale=0.01, vocab=256, temperature=1.0)
+# Tree sampling (T > 0, siblings drawn i.i.d. from the parent's q): the walk,
+# the sibling-residual passes and the final draw against the oracle, on the
+# 64-node tree at small and full vocabulary, with several draft qualities.
+@pytest.mark.parametrize("vocab,sigma,T", [(256, 1.0, 1.0), (4096, 0.5, 0.7), (4096, 3.0, 1.0),
+                                           (128256, 1.0, 1.0)])
+def test_tree_sampling_matches_oracle(vocab, sigma, T):
+    n_same = 0
+    for seed in range(6):
+        w = wl.make_workload(wl.config("tree70b"), ctx_scale=0.01, vocab=vocab, temperature=T,
+                             draft_sigma=sigma, step_seed=1000 + seed)
+        s = DeviceStep(w, mode="onepass")
+        s.accept()
+        res = s.results()
+        assert res["dev_status"] == 0
+        err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits, T, w.seed)
+        assert err == 0
+        if st.ambiguous[0] or res["ambiguous"][0]:
+            continue
+        _compare_accept(res, st, w, f"tree vocab={vocab} sigma={sigma} seed={seed}")
+        n_same += 1
+    assert n_same >= 4
+
+
+def test_tree_sampling_batch_of_trees_matches_oracle():
+    # several trees in one call (one CTA each), mixed with nothing else
+    w = wl.make_workload(wl.config("tree70b"), n_req=5, ctx_scale=0.01, vocab=2048,
+                         temperature=1.0, draft_sigma=0.7)
     s = DeviceStep(w, mode="onepass")
     s.accept()
-    torch.cuda.synchronize()
-    assert s.dev_status.item() & api.N.SV_DEV_UNSUPPORTED
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits, 1.0, w.seed)
+    assert err == 0
+    _compare_accept(res, st, w, "five trees")
 
 
 def test_small_workspace_is_refused_before_launch():

@@ -12,7 +12,12 @@ p) is the standard lossless rule.  The pins:
     after a rejection as normalize(max(0, p - q)), the bonus token as p;
   * the acceptance rate against sum_v min(p_v, q_v);
   * row statistics against torch.logsumexp / softmax in fp64;
-  * chunked verification equal to one-pass verification.
+  * chunked verification equal to one-pass verification;
+  * tree sampling (T > 0, siblings i.i.d. from q): chi-square of the first
+    emitted token against p_root and of the next token against p_c given the
+    accepted node c, a one-child tree equal to the chain rule, the closed
+    form of the residual after several sibling rejections, and a planted
+    mistake that the statistics see.
 """
 
 import numpy as np
@@ -274,7 +279,118 @@ def test_verify_len_truncates_the_chain():
             assert full.accepted_len[i] >= vl[i]
 
 
-def test_tree_sampling_is_reported_unsupported():
-    w = wl.make_workload(wl.config("tree70b"), ctx_scale=0.01, vocab=64)
-    err, _ = oracle.accept(w.batch(), w.target_logits, w.draft_logits, 1.0, 1)
-    assert err & oracle.ORC_UNSUPPORTED
+# ------------------------------------------------------- tree sampling --
+# Draft trees at T > 0 whose siblings are drawn i.i.d. from the parent's q
+# (with replacement): children tried in index order against the residual
+# left by the siblings rejected before them.  Lossless means the first
+# emitted token is distributed as p_root, and, given that the walk accepted
+# node c, the next emitted token is distributed as p_c.
+
+def _tree_batch(n_req, parent1, tokens):
+    rows = len(parent1)
+    cu = np.arange(n_req + 1, dtype=np.int32) * rows
+    parent = np.tile(np.asarray(parent1, dtype=np.int32), n_req)
+    return {"cu_rows": cu, "parent": parent, "tokens": tokens.astype(np.int32).ravel(),
+            "max_rows": rows}
+
+
+def _tree_run(parent1, T, seed, N=600_000, V=16, bias=1.0):
+    rng = np.random.default_rng(7 + len(parent1) * 13 + int(T * 10))
+    rows = len(parent1)
+    lt = (rng.standard_normal((rows, V)) * 2.0).astype(np.float32)
+    ld = (lt + bias * rng.standard_normal((rows, V))).astype(np.float32)
+    p = [_softmax_T(lt[r], T) for r in range(rows)]
+    q = [_softmax_T(ld[r], T) for r in range(rows)]
+    tokens = np.zeros((N, rows), dtype=np.int32)
+    for c in range(1, rows):
+        tokens[:, c] = rng.choice(V, size=N, p=q[parent1[c]])  # i.i.d. siblings from q_parent
+    b = _tree_batch(N, parent1, tokens)
+    target = np.ascontiguousarray(np.broadcast_to(lt, (N, rows, V)).reshape(N * rows, V))
+    draft = np.ascontiguousarray(np.broadcast_to(ld, (N, rows, V)).reshape(N * rows, V))
+    err, st = oracle.accept(b, target, draft, T, seed)
+    assert err == 0
+    return p, q, tokens, st
+
+
+TREES = {
+    "one child": [-1, 0],
+    "three siblings": [-1, 0, 0, 0],
+    "two levels": [-1, 0, 0, 1, 1, 2, 2],
+}
+
+
+@pytest.mark.parametrize("shape,T", [("one child", 1.0), ("three siblings", 1.0),
+                                     ("three siblings", 0.7), ("two levels", 1.0)])
+def test_tree_sampling_is_lossless_chi2(shape, T):
+    V = 16
+    par = TREES[shape]
+    p, q, tokens, st = _tree_run(par, T, seed=31 + len(par))
+    a = st.accepted_len
+    nodes = st.accepted_nodes
+    assert (st.next_token >= 0).all() and (st.done == 1).all()
+    assert st.ambiguous.mean() < 1e-3
+    # accepted path is a root-to-node path of the tree
+    for r in range(0, len(a), 9973):
+        for k in range(1, a[r] + 1):
+            assert par[nodes[r, k]] == nodes[r, k - 1]
+    # first emitted token ~ p_root
+    n1 = nodes[:, 1]
+    first = np.where(a >= 1, tokens[np.arange(len(a)), np.maximum(n1, 0)], st.next_token)
+    s, crit, dof = _chi2_ok(np.bincount(first, minlength=V), p[0])
+    assert s < crit, (s, crit, dof)
+    # given the walk accepted node c at depth 1, the next token ~ p_c
+    for c in [ch for ch in range(1, len(par)) if par[ch] == 0]:
+        m = (a >= 1) & (n1 == c)
+        if m.sum() < 20_000:
+            continue
+        n2 = nodes[m, 2] if nodes.shape[1] > 2 else np.zeros(m.sum(), dtype=np.int64)
+        second = np.where(a[m] >= 2, tokens[np.where(m)[0], np.maximum(n2, 0)], st.next_token[m])
+        s, crit, _ = _chi2_ok(np.bincount(second, minlength=V), p[c])
+        assert s < crit, (c, s, crit)
+
+
+def test_tree_sampling_with_one_child_equals_the_chain_rule():
+    # A one-child tree is a chain of one draft: same decisions, same tokens.
+    V = 16
+    p, q, tokens, st_tree = _tree_run([-1, 0], 1.0, seed=5, N=20_000)
+    b = _chain_batch(20_000, 1, tokens)
+    rng = np.random.default_rng(7 + 2 * 13 + 10)
+    lt = (rng.standard_normal((2, V)) * 2.0).astype(np.float32)
+    ld = (lt + rng.standard_normal((2, V))).astype(np.float32)
+    target = np.ascontiguousarray(np.broadcast_to(lt, (20_000, 2, V)).reshape(-1, V))
+    draft = np.ascontiguousarray(np.broadcast_to(ld, (20_000, 2, V)).reshape(-1, V))
+    err, st_chain = oracle.accept(b, target, draft, 1.0, 5)
+    assert err == 0
+    assert np.array_equal(st_tree.accepted_len, st_chain.accepted_len)
+    assert np.array_equal(st_tree.next_token, st_chain.next_token)
+
+
+def test_tree_sampling_chi2_detects_a_planted_mistake():
+    # Resampling from p_root instead of the siblings' residual after all of
+    # them were rejected is seen by the same statistics.
+    V = 16
+    p, q, tokens, st = _tree_run(TREES["three siblings"], 1.0, seed=44, N=300_000)
+    rng = np.random.default_rng(9)
+    a = st.accepted_len
+    wrong = np.where(a >= 1, tokens[np.arange(len(a)), np.maximum(st.accepted_nodes[:, 1], 0)],
+                     rng.choice(V, size=len(a), p=p[0]))
+    s, crit, _ = _chi2_ok(np.bincount(wrong, minlength=V), p[0])
+    assert s > crit
+
+
+def test_tree_residual_after_sibling_rejections_matches_the_closed_form():
+    # After j rejections the residual is max(0, p - c_j q) / S(c_j) with
+    # c_{j+1} = c_j + S(c_j): checked against the step-by-step definition
+    # normalize(max(0, p' - q)) in numpy on a random pair of rows.
+    rng = np.random.default_rng(3)
+    p = rng.dirichlet(np.ones(40))
+    q = rng.dirichlet(np.ones(40))
+    pres, c, S = p.copy(), 0.0, 1.0
+    for _ in range(4):
+        nxt = np.maximum(pres - q, 0.0)
+        if nxt.sum() == 0:
+            break
+        pres = nxt / nxt.sum()
+        c += S
+        S = np.maximum(p - c * q, 0.0).sum()
+        assert np.allclose(pres, np.maximum(p - c * q, 0.0) / S, rtol=1e-12, atol=1e-15)
