@@ -275,6 +275,9 @@ def main():
                     help="only run this many steps (for a profiler), no timing line")
     ap.add_argument("--ctx-scale", type=float, default=1.0,
                     help="with --profile-steps: shrink every context (smaller profiler captures)")
+    ap.add_argument("--sps", default="synthetic", choices=["synthetic", "measured"],
+                    help="budget workload: the synthetic SPS(B) table or the one measured "
+                         "from this library's kernels (speculative_decoding_verification_padding_gb300/sps.py)")
     ap.add_argument("--profile-call", default="step", choices=["step", "attend", "accept"],
                     help="with --profile-steps: run the whole step, or only the one-pass "
                          "sv_tree_attend / sv_accept call on the whole batch")
@@ -302,7 +305,7 @@ def main():
     reps = Replicas.from_env("nccl", device=dev)
 
     w = wl.make_workload(wl.config(args.workload),
-                         ctx_scale=args.ctx_scale if args.profile_steps else 1.0)
+                         ctx_scale=args.ctx_scale if args.profile_steps else 1.0, sps=args.sps)
     s = DeviceStep(w, device=dev)
     mode, chunk, T = s.mode, s.chunk, s.T
     stream = torch.cuda.current_stream()
@@ -554,6 +557,8 @@ def main():
         line["graph_replay"] = graph
     if mode == "chunked":
         line["config"]["chunk"] = chunk
+    if mode == "budget":
+        line["config"]["sps"] = args.sps
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, mode)
     print(json.dumps(line), flush=True)

@@ -194,12 +194,14 @@ class Workload:
 def make_workload(cfg: Config, *, n_req: int | None = None, ctx_scale: float = 1.0,
                   vocab: int | None = None, draft_sigma: float | None = None,
                   temperature: float | None = None, step_seed: int | None = None,
-                  slack: float = 0.10) -> Workload:
+                  slack: float = 0.10, sps: str = "synthetic") -> Workload:
     """Draw one verification step of workload ``cfg``.
 
     ``n_req``, ``ctx_scale`` and ``vocab`` shrink the workload for tests that
     the oracle must finish in seconds; ``draft_sigma`` sweeps acceptance;
     ``temperature`` overrides the sampling temperature used to draw drafts.
+    ``sps`` (budget workloads): "synthetic" (1000 / (1 + B / 512)) or
+    "measured" (the table ``sps.py`` measured from this library's kernels).
     """
     rng = np.random.default_rng(cfg.seed)
     R = cfg.n_req if n_req is None else n_req
@@ -300,6 +302,10 @@ def make_workload(cfg: Config, *, n_req: int | None = None, ctx_scale: float = 1
         gmax = int(rows.max()) - 1
         w.cond_survival = b_rng.beta(4.0, 2.0, size=(R, gmax)).astype(np.float32)
         w.gamma = (rows - 1).astype(np.int32)
-        B = np.arange(cfg.sps_b_max + 1, dtype=np.float64)
-        w.sps = (1000.0 / (1.0 + B / 512.0)).astype(np.float32)
+        if sps == "measured":
+            from .sps import load_measured
+            w.sps = load_measured(cfg.sps_b_max)
+        else:
+            B = np.arange(cfg.sps_b_max + 1, dtype=np.float64)
+            w.sps = (1000.0 / (1.0 + B / 512.0)).astype(np.float32)
     return w

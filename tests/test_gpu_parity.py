@@ -9,12 +9,15 @@ absolute and 1e-2 relative of the fp64 oracle (bf16 output, fp32
 accumulation); probabilities within 1e-5 absolute.
 """
 
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from speculative_decoding_verification_padding_gb300 import api, build
+from speculative_decoding_verification_padding_gb300 import sps as sps_mod
 from speculative_decoding_verification_padding_gb300 import workloads as wl
 from speculative_decoding_verification_padding_gb300.step import DeviceStep
 
@@ -240,6 +243,17 @@ def test_budget_full_size_matches_oracle():
     err, vl_o, bB_o, th_o = oracle.select_budget(w.cond_survival, w.gamma, w.sps)
     assert st == 0 and err == 0
     assert np.array_equal(vl, vl_o) and bB == bB_o and th == th_o
+
+
+@pytest.mark.skipif(not os.path.exists(sps_mod.MEASURED), reason="no measured SPS table stored")
+def test_budget_with_measured_sps_matches_oracle():
+    # the SPS(B) table measured from this library's own kernels on GB300
+    w = wl.make_workload(wl.config("batch256"), vocab=64, ctx_scale=0.001, sps="measured")
+    vl, bB, th, st = _budget_gpu(w.cond_survival, w.gamma, w.sps)
+    err, vl_o, bB_o, th_o = oracle.select_budget(w.cond_survival, w.gamma, w.sps)
+    assert st == 0 and err == 0
+    assert np.array_equal(vl, vl_o) and bB == bB_o and th == th_o
+    assert 256 <= bB <= 256 + int(w.gamma.sum())
 
 
 @pytest.mark.parametrize("trial", range(40))
