@@ -15,7 +15,9 @@
  *                     maximising tau * SPS(B);
  *   sv_chunk_windows, sv_verify_chunked
  *                     verification in chunks of rows with early pruning of
- *                     requests whose prefix was rejected.
+ *                     requests whose prefix was rejected;
+ *   sv_adapt_gamma    each request's next draft length from its own
+ *                     acceptance history.
  *
  * Sources (pages by title; section names glossed):
  *   [SwiftSpec] "SwiftSpec: 드래프터와 타깃을 서로 다른 GPU에 분리하고 비동기로
@@ -80,7 +82,7 @@ typedef enum {
                                     invalid accepted path given to commit */
 #define SV_DEV_TIMEOUT 16        /* reserved: a bounded device wait gave up */
 #define SV_DEV_BAD_TOKEN 32      /* draft token outside [0, vocab) */
-#define SV_DEV_UNSUPPORTED 64    /* tree request with temperature > 0 */
+#define SV_DEV_UNSUPPORTED 64    /* reserved (no longer raised: trees at temperature > 0 are sampled) */
 #define SV_DEV_BAD_LENGTH 128    /* ctx + rows does not fit the block table */
 
 /* Paged KV cache ([SSD] PagedAttention; [SwiftSpec] mechanism 2).
@@ -173,6 +175,17 @@ sv_status sv_tree_attend(const sv_paged_kv* kv, const sv_batch* batch, const voi
  *     q_{j-1}(x_j)); at the first rejection emit a token drawn from
  *     normalize(max(0, p_{j-1} - q_{j-1})); if every draft up to lim_i - 1
  *     is accepted emit a token drawn from p_{lim_i - 1}.
+ *   temperature > 0 (trees, one window over all rows; siblings drawn
+ *     independently from the parent's q): from the root, children are tried
+ *     in index order; child c (token x) is accepted iff u(i, c) <
+ *     min(1, p'(x) / q_n(x)), p' the target distribution left by the
+ *     siblings rejected before it: after j rejections p' = max(0, p_n -
+ *     c_j q_n) / S(c_j), S(c) = sum_v max(0, p_n,v - c q_n,v), c_0 = 0,
+ *     c_{j+1} = c_j + S(c_j).  On acceptance the walk moves to c; when every
+ *     child is rejected the emitted token is drawn from p' (from p_n if S
+ *     vanished); at a leaf it is drawn from p_leaf.  (Tree verification is
+ *     on the pages; this multi-candidate rejection rule is the plainest
+ *     lossless reading.)
  *   temperature == 0 (chains and trees): keep the longest root-to-node path
  *     along which each node's token is the target argmax (lowest index on
  *     ties) of its parent row; among equally long paths the one whose first
@@ -182,7 +195,8 @@ sv_status sv_tree_attend(const sv_paged_kv* kv, const sv_batch* batch, const voi
  *   Residual / bonus draws are exponential races: the token is
  *   argmax_v w_v / E_v, E_v = -log U_v, U_v from counter (v/4, i, 1, pos)
  *   word v%4, ((bits >> 9) + 0.5) * 2^-23; pos = position of the emitted
- *   token (j after rejecting draft j, lim_i after the last draft).
+ *   token, accepted drafts + 1 (j after rejecting draft j, lim_i after the
+ *   last draft of a chain).
  * Outputs (state kept across the windows of one step):
  *   accepted_len [n_req]: accepted drafts a_i;
  *   accepted_nodes [n_req][max_rows_per_req]: path, [0] = 0 (root), then the
@@ -294,6 +308,31 @@ sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* batch, const 
                             int32_t* accepted_len, int32_t* accepted_nodes, int32_t* next_token,
                             uint8_t* ambiguous, int32_t* done, void* ws, size_t ws_bytes,
                             int32_t* dev_status, void* stream);
+
+/* ------------------------------------------ per-request draft length --
+ * [FASER] mechanism 1 (per-request speculation length): every request's
+ * previous acceptance feeds back into its own gamma -- raised where drafts
+ * are accepted, lowered where they are rejected.  The pages give no
+ * formula; this controller is one choice, fixed here exactly:
+ *   state [n_req][2] fp64 (S, N): decayed counts of accepted drafts and of
+ *     trials (zero-initialised by the caller for a new request);
+ *   after a step with a_i accepted drafts out of verified_i:
+ *     S <- decay * S + a_i;  N <- decay * N + a_i + (a_i < verified_i);
+ *   alpha = (S + 1) / (N + 2)   (acceptance estimate, Beta(1, 1) prior);
+ *   gamma_next_i = the g in [gamma_min, gamma_max] that maximises
+ *     E(g) / (g + 1 + overhead),  E(g) = sum_{k=0..g} alpha^k
+ *   (expected tokens emitted per step over the rows it verifies plus a
+ *   fixed per-step cost in row units), smallest g on ties.
+ * All of it in IEEE fp64 add / multiply / divide in the order written (no
+ * contraction), so that any implementation gives the same gamma.
+ * verified [n_req]: drafts the step verified for the request (its gamma or
+ * verify_len); a request with verified_i < 0 is left untouched.
+ * Invalid arguments: 0 <= gamma_min <= gamma_max <= 127, 0 < decay <= 1,
+ * overhead >= 0. */
+sv_status sv_adapt_gamma(int32_t n_req, const int32_t* accepted_len, const int32_t* verified,
+                         double* state, int32_t* gamma_next, double decay, double overhead,
+                         int32_t gamma_min, int32_t gamma_max, int32_t* dev_status,
+                         void* stream);
 
 #ifdef __cplusplus
 }

@@ -35,7 +35,8 @@ def build(force: bool = False) -> str:
     """Compile sv_oracle.cpp with g++ -O2 (no fast-math) into liboracle_sv.so."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp]
+        cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+               _SRC, "-o", tmp]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -67,6 +68,9 @@ def _load():
         lib.orc_verify_chunked.argtypes = [I, P, P, P, P, I, I, P, P, I, I, I, I, P, I, P, P, I, F,
                                            P, P, P, P, I, F, U64, P, P, P, P, P, P, I]
         lib.orc_verify_chunked.restype = I
+        D = ctypes.c_double
+        lib.orc_adapt_gamma.argtypes = [I, P, P, P, P, D, D, I, I]
+        lib.orc_adapt_gamma.restype = I
         _lib = lib
     return _lib
 
@@ -222,6 +226,21 @@ def select_budget(cond_survival, gamma, sps):
     err = lib.orc_select_budget(R, gmax, _ptr(c), _ptr(g), _ptr(s), s.shape[0] - 1, _ptr(vl),
                                 _ptr(bb), _ptr(bt))
     return err, vl, int(bb[0]), float(bt[0])
+
+
+def adapt_gamma(accepted_len, verified, state, decay, overhead, gamma_min, gamma_max):
+    """Per-request draft length from the acceptance history (see
+    orc_adapt_gamma).  `state` ([R][2] float64) is updated in place.
+
+    Returns (err, gamma_next)."""
+    lib = _load()
+    a = _i32(accepted_len)
+    v = _i32(verified)
+    assert state.dtype == np.float64 and state.flags["C_CONTIGUOUS"]
+    g = np.full(len(a), -1, dtype=np.int32)
+    err = lib.orc_adapt_gamma(len(a), _ptr(a), _ptr(v), _ptr(state), _ptr(g), float(decay),
+                              float(overhead), int(gamma_min), int(gamma_max))
+    return err, g
 
 
 # ----------------------------------------------------------------- chunked --

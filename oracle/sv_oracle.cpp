@@ -807,4 +807,48 @@ int orc_verify_chunked(int n_req, const int32_t* cu_rows, const int32_t* parent,
   return err;
 }
 
+// -------------------------------------------- draft length (NEXT-4) --
+// Per-request gamma from the request's own acceptance ([FASER] mechanism 1:
+// the previous acceptance rate feeds back, accepting requests get a longer
+// gamma, rejecting ones a shorter).  The pages give no formula; the one
+// written here (and in the library's header) is:
+//   S <- decay * S + a;  N <- decay * N + a + (a < verified);
+//   alpha = (S + 1) / (N + 2);
+//   gamma = argmax_{g in [gmin, gmax]} E(g) / (g + 1 + overhead),
+//   E(g) = sum_{k=0..g} alpha^k, smallest g on ties,
+// in IEEE double, each operation rounded on its own (this file is compiled
+// with -ffp-contract=off).  verified < 0 leaves the request untouched;
+// a < 0 or a > verified is reported.
+int orc_adapt_gamma(int n_req, const int32_t* accepted_len, const int32_t* verified,
+                    double* state, int32_t* gamma_next, double decay, double overhead,
+                    int gmin, int gmax) {
+  if (n_req < 0 || gmin < 0 || gmax < gmin || !(decay > 0.0 && decay <= 1.0) ||
+      !(overhead >= 0.0))
+    return ORC_BAD_ARG;
+  int err = 0;
+  for (int i = 0; i < n_req; ++i) {
+    const int used = verified[i];
+    if (used < 0) continue;
+    const int a = accepted_len[i];
+    if (a < 0 || a > used) { err |= ORC_BAD_LENGTH; continue; }
+    double S = decay * state[2 * i] + (double)a;
+    double N = decay * state[2 * i + 1] + (double)(a + (a < used ? 1 : 0));
+    state[2 * i] = S;
+    state[2 * i + 1] = N;
+    const double alpha = (S + 1.0) / (N + 2.0);
+    double pw = 1.0, E = 0.0;
+    int best = gmin;
+    double best_score = -1.0;
+    for (int g = 0; g <= gmax; ++g) {
+      E = E + pw;
+      pw = pw * alpha;
+      if (g < gmin) continue;
+      const double score = E / ((double)(g + 1) + overhead);
+      if (score > best_score) { best_score = score; best = g; }
+    }
+    gamma_next[i] = best;
+  }
+  return err;
+}
+
 }  // extern "C"

@@ -190,6 +190,20 @@ def sv_select_budget(cond_survival: torch.Tensor, gamma: Optional[torch.Tensor],
                                      _ptr(dev_status), _stream(stream)), "sv_select_budget")
 
 
+def sv_adapt_gamma(accepted_len: torch.Tensor, verified: torch.Tensor, state: torch.Tensor,
+                   gamma_next: torch.Tensor, decay: float = 0.7, overhead: float = 2.0,
+                   gamma_min: int = 1, gamma_max: int = 8,
+                   dev_status: Optional[torch.Tensor] = None, stream=None):
+    _expect(accepted_len, torch.int32, "accepted_len")
+    _expect(verified, torch.int32, "verified")
+    _expect(state, torch.float64, "state")
+    _expect(gamma_next, torch.int32, "gamma_next")
+    N.check(N.lib().sv_adapt_gamma(accepted_len.numel(), _ptr(accepted_len), _ptr(verified),
+                                   _ptr(state), _ptr(gamma_next), float(decay), float(overhead),
+                                   int(gamma_min), int(gamma_max), _ptr(dev_status),
+                                   _stream(stream)), "sv_adapt_gamma")
+
+
 def sv_chunk_windows(batch: Batch, chunk_index: int, chunk_size: int,
                      done: Optional[torch.Tensor], row_begin: torch.Tensor,
                      row_end: torch.Tensor, stream=None):

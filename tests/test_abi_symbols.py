@@ -58,6 +58,12 @@ def test_host_side_validation_without_gpu(lib):
                          None, None) == N.SV_ERR_INVALID_ARGUMENT  # T > 0 needs draft logits
     kv = N.SvPagedKV(256, 256, 10, 16, 2, 96, 1, 4, 1)
     assert lib.sv_tree_attend_workspace(ctypes.byref(b), ctypes.byref(kv), 8) == 0  # head_dim 96
+    # draft-length controller: parameters out of range are refused on the host
+    assert lib.sv_adapt_gamma(4, 1, 1, 1, 1, 0.7, 2.0, 3, 2, None, None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_adapt_gamma(4, 1, 1, 1, 1, 0.0, 2.0, 1, 8, None, None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_adapt_gamma(4, 1, 1, 1, 1, 0.7, -1.0, 1, 8, None, None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_adapt_gamma(4, 1, 1, 1, 1, 0.7, 2.0, 1, 128, None, None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_adapt_gamma(0, None, None, None, None, 0.7, 2.0, 1, 8, None, None) == N.SV_OK
     kv = N.SvPagedKV(256, 256, 10, 16, 2, 64, 1, 4, 1)
     need = lib.sv_tree_attend_workspace(ctypes.byref(b), ctypes.byref(kv), 8)
     assert need > 0

@@ -275,6 +275,33 @@ def test_budget_random_matches_oracle(trial):
     assert np.array_equal(vl, vl_o) and bB == bB_o and th == th_o
 
 
+# ------------------------------------------------------------ draft length --
+
+@pytest.mark.parametrize("trial", range(4))
+def test_adapt_gamma_matches_oracle(trial):
+    rng = np.random.default_rng(500 + trial)
+    R = int(rng.integers(1, 3000))
+    verified = rng.integers(-1, 9, R).astype(np.int32)
+    acc = np.minimum(rng.integers(0, 9, R), np.maximum(verified, 0)).astype(np.int32)
+    if trial == 3:
+        acc[::7] = verified[::7] + 1  # some inconsistent lengths: reported, skipped
+    state = (rng.random((R, 2)) * rng.integers(0, 50, (R, 1))).astype(np.float64)
+    state[:, 0] = np.minimum(state[:, 0], state[:, 1])
+    decay, overhead, gmin, gmax = [(0.7, 2.0, 1, 8), (0.9, 0.5, 0, 16), (1.0, 4.0, 2, 6),
+                                   (0.5, 1.0, 1, 8)][trial]
+    st_o = state.copy()
+    err, g_o = oracle.adapt_gamma(acc, verified, st_o, decay, overhead, gmin, gmax)
+    st_g = torch.from_numpy(state).cuda()
+    g_g = torch.full((R,), -1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.sv_adapt_gamma(torch.from_numpy(acc).cuda(), torch.from_numpy(verified).cuda(), st_g, g_g,
+                       decay, overhead, gmin, gmax, status)
+    torch.cuda.synchronize()
+    assert np.array_equal(g_g.cpu().numpy(), g_o)
+    assert np.array_equal(st_g.cpu().numpy(), st_o)  # every bit of the fp64 state
+    assert bool(status.item() & api.N.SV_DEV_BAD_LENGTH) == bool(err & oracle.ORC_BAD_LENGTH)
+
+
 # ------------------------------------------------------- chunked / budget step --
 
 @pytest.mark.parametrize("T", [0.7, 0.0])
