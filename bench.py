@@ -13,9 +13,9 @@ step's commit changed, then the workload's calls:
   chunked  sv_verify_chunked (per chunk: attention plan with the chunk's
            windows and accept list, split-KV attention, row statistics,
            decisions; one resampling race per step) and sv_commit_kv
-  onepass  sv_tree_attend, sv_accept, sv_commit_kv
-  budget   sv_select_budget, sv_tree_attend and sv_accept on the selected
-           prefixes, sv_commit_kv
+  onepass  sv_tree_attend, sv_accept_commit (accept and KV commit fused)
+  budget   sv_select_budget, sv_tree_attend and sv_accept_commit on the
+           selected prefixes
 Inputs larger than L2 are timed back to back; smaller ones step by step with
 an L2 flush (a 512 MB write) between steps, outside the timed events.
 
@@ -517,13 +517,14 @@ def main():
 
     n_launch = len(sched)
     race = 1 if T > 0 else 0
-    # attention: plan + attend; accept: stats + decide (+ race); commit: copy + release.
     # Chunked: plan (windows + accept list) + attend + stats + decide per chunk, one race
-    # after the last.
+    # after the last, commit (copy + release).  One-pass / budget: [select] + plan + attend +
+    # fused accept-commit (stats + decide [+ tree walk] [+ race]).
+    tree = 1 if (T > 0 and w.max_rows > 2) else 0
     if mode == "chunked":
         launches_per_step = n_launch * (2 + 2) + race + 2
     else:
-        launches_per_step = 2 + 2 + race + 2 + (1 if mode == "budget" else 0)
+        launches_per_step = 2 + 2 + tree + race + (1 if mode == "budget" else 0)
     value = rows_all / t_step
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

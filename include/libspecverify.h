@@ -10,6 +10,7 @@
  *   sv_accept         per-row vocabulary softmax and the lossless accept /
  *                     reject rule (or greedy longest matching prefix);
  *   sv_commit_kv      the accepted path's K/V kept, rejected blocks freed;
+ *   sv_accept_commit  sv_accept and sv_commit_kv fused in the same kernels;
  *   sv_select_budget  how many drafts of each request to verify, by sorting
  *                     every (request, position) by prefix survival and
  *                     maximising tau * SPS(B);
@@ -219,6 +220,24 @@ sv_status sv_accept(const sv_batch* batch, const float* target_logits, const flo
                     int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous,
                     int32_t* done, float* row_stats, void* ws, size_t ws_bytes,
                     int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------- accept + commit fused --
+ * [SwiftSpec] mechanism 3 (the verification result and the KV update fused
+ * into one operation).  sv_accept_commit computes exactly what sv_accept
+ * followed by sv_commit_kv computes (same arguments as each, same results,
+ * same free-list order), but the warp that decides a request's path also
+ * moves its K/V and sets its new length, and the last request to finish
+ * appends every released block to the pool: no separate commit launches,
+ * no second read of accepted_len / accepted_nodes.  One-pass calls only
+ * (windows covering whole requests, as for sv_commit_kv).
+ * ws: at least sv_accept_commit_workspace() bytes, 256-byte aligned. */
+size_t sv_accept_commit_workspace(const sv_batch* batch, int32_t vocab);
+sv_status sv_accept_commit(const sv_batch* batch, const float* target_logits,
+                           const float* draft_logits, int32_t vocab, float temperature,
+                           uint64_t seed, int32_t* accepted_len, int32_t* accepted_nodes,
+                           int32_t* next_token, uint8_t* ambiguous, int32_t* done,
+                           float* row_stats, const sv_paged_kv* kv, const sv_block_pool* pool,
+                           void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------ accept without workspace --
  * No counterpart in the paper: a convenience for callers that cannot

@@ -62,6 +62,9 @@ PROTOTYPES = {
     "sv_accept": (ctypes.c_int, [P, P, P, I32, F32, U64, P, P, P, P, P, P, P, SZ, P, P]),
     "sv_accept_static": (ctypes.c_int, [P, P, P, I32, F32, U64, P, P, P, P, P, P, P, P]),
     "sv_commit_kv": (ctypes.c_int, [P, P, P, P, P, P, P]),
+    "sv_accept_commit_workspace": (SZ, [P, I32]),
+    "sv_accept_commit": (ctypes.c_int, [P, P, P, I32, F32, U64, P, P, P, P, P, P, P, P, P, SZ, P,
+                                        P]),
     "sv_select_budget_workspace": (SZ, [I32, I32]),
     "sv_select_budget": (ctypes.c_int, [I32, I32, P, P, P, I32, P, P, P, P, SZ, P, P]),
     "sv_chunk_windows": (ctypes.c_int, [P, I32, I32, P, P, P, P]),

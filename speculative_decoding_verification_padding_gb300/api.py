@@ -172,6 +172,31 @@ def sv_commit_kv(kv: PagedKV, batch: Batch, accepted_len: torch.Tensor,
                                  _stream(stream)), "sv_commit_kv")
 
 
+def sv_accept_commit_workspace(batch: Batch, vocab: int) -> int:
+    b = batch.c()
+    return N.lib().sv_accept_commit_workspace(ctypes.byref(b), vocab)
+
+
+def sv_accept_commit(batch: Batch, target_logits: torch.Tensor,
+                     draft_logits: Optional[torch.Tensor], vocab: int, temperature: float,
+                     seed: int, accepted_len: torch.Tensor, accepted_nodes: torch.Tensor,
+                     next_token: torch.Tensor, ambiguous: torch.Tensor,
+                     done: Optional[torch.Tensor], row_stats: Optional[torch.Tensor],
+                     kv: PagedKV, pool: BlockPool, ws: torch.Tensor,
+                     dev_status: Optional[torch.Tensor] = None, stream=None):
+    _expect(target_logits, torch.float32, "target_logits")
+    _expect(draft_logits, torch.float32, "draft_logits")
+    _expect(ambiguous, torch.uint8, "ambiguous")
+    _expect(row_stats, torch.float32, "row_stats")
+    b, k, p = batch.c(), kv.c(), pool.c()
+    N.check(N.lib().sv_accept_commit(ctypes.byref(b), _ptr(target_logits), _ptr(draft_logits),
+                                     vocab, temperature, seed & 0xFFFFFFFFFFFFFFFF,
+                                     _ptr(accepted_len), _ptr(accepted_nodes), _ptr(next_token),
+                                     _ptr(ambiguous), _ptr(done), _ptr(row_stats),
+                                     ctypes.byref(k), ctypes.byref(p), _ptr(ws), ws.numel(),
+                                     _ptr(dev_status), _stream(stream)), "sv_accept_commit")
+
+
 def sv_select_budget_workspace(n_req: int, gamma_max: int) -> int:
     return N.lib().sv_select_budget_workspace(n_req, gamma_max)
 

@@ -77,7 +77,7 @@ inline int race_chunks(int R, int V) {
 }
 inline __host__ __device__ int chunk_len(int V, int nch) { return ((V + nch - 1) / nch + 3) & ~3; }
 
-Layout layout(int R, int total_rows, int V, int maxw) {
+Layout layout(int R, int total_rows, int V, int maxw, bool commit) {
   Layout L;
   L.maxw = max(1, min(maxw, kMaxRows));
   const long bound = min((long)total_rows, (long)R * L.maxw);
@@ -91,6 +91,11 @@ Layout layout(int R, int total_rows, int V, int maxw) {
   L.race = off; off += align256(sizeof(RacePart) * (size_t)R * L.nch_r_cap);
   L.race_tickets = off; off += align256(sizeof(int) * (size_t)R);
   L.act = off; off += align256(sizeof(int) * (size_t)(R + 1));  // act[R] = count
+  L.ctick = L.cspan = 0;
+  if (commit) {
+    L.ctick = off; off += align256(sizeof(int));
+    L.cspan = off; off += align256(sizeof(int2) * (size_t)R);
+  }
   L.total = off;
   return L;
 }
@@ -113,6 +118,18 @@ __device__ __forceinline__ int race_slices(const Layout& L, int count, int V) {
   return (int)max((long)L.nch_r, min(want, cap));
 }
 
+// The paged cache and block pool a fused accept + commit updates.
+struct CommitArgs {
+  __nv_bfloat16* k;
+  __nv_bfloat16* v;
+  int num_blocks, Hkv, D, max_blocks;
+  int32_t* tables;
+  int32_t* cache_lens;
+  int32_t* free_list;
+  int32_t* free_count;
+  int capacity;
+};
+
 struct Args {
   sv_batch bt;
   const float* target;
@@ -132,6 +149,8 @@ struct Args {
   int race_all;   // race kernel: every request 0..R-1 instead of the active list
   int clear_jobs; // stats kernel: first clear every request's sampling job and race ticket
   int use_list;   // the requests come from the active list (chunked steps)
+  int commit;     // fused KV commit (sv_accept_commit)
+  CommitArgs kv;
 };
 
 __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2) {
@@ -220,7 +239,11 @@ __device__ __forceinline__ void merge_pairs(const Args& a, int nch, int r0, int 
 }
 
 // The decision for request i, by one warp, once all its row partials exist.
-__device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
+// Returns kFinal when the request's path is decided, kToTree when the tree
+// kernel takes it over, kSkipped when nothing was decided.
+constexpr int kFinal = 0, kToTree = 1, kSkipped = 2;
+
+__device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   const int lane = threadIdx.x & 31;
   Job* job = reinterpret_cast<Job*>(a.ws + a.L.jobs) + i;
   if (a.T > 0.f && lane == 0) {
@@ -231,7 +254,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   const Window w = window_of(a.bt, i);
   if (!a.use_list && !live(a, w, i)) {
     if (!w.ok && lane == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-    return;
+    return kSkipped;
   }
   const int cu = a.bt.cu_rows[i];
   const int V = a.V;
@@ -256,7 +279,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   if (badp || badt || (!chain && (w.b != 0 || w.e != w.rows))) {
     if (lane == 0)
       flag(a.dev_status, badp ? SV_DEV_BAD_PARENT : badt ? SV_DEV_BAD_TOKEN : SV_DEV_BAD_WINDOW);
-    return;
+    return kSkipped;
   }
   const int max_rows = a.bt.max_rows_per_req;
   int32_t* nodes = a.accepted_nodes + (size_t)i * max_rows;
@@ -264,7 +287,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
     for (int k = lane; k < max_rows; k += 32) nodes[k] = k == 0 ? 0 : -1;
   } else if (a.accepted_len[i] != w.b) {
     if (lane == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-    return;
+    return kSkipped;
   }
   if (!chain && a.T > 0.f) {
     // Tree sampling: the walk needs vocabulary passes, one CTA per tree
@@ -279,7 +302,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
       a.ambiguous[i] = 0;
       if (a.done) a.done[i] = 0;
     }
-    return;
+    return kToTree;
   }
   int len = w.b;   // accepted drafts so far
   int next = -1;
@@ -351,7 +374,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
       if (w.b == 0) a.ambiguous[i] = 0;
       if (a.done) a.done[i] = next >= 0 ? 1 : 0;
     }
-    return;
+    return kFinal;
   }
 
   // ---- T > 0: speculative sampling on a chain ----
@@ -431,7 +454,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
       break;
     }
   }
-  if (lane != 0) return;
+  if (lane != 0) return kFinal;
   if (jb.mode == 0 && w.e == w.lim && len == w.lim - 1) {
     jb.mode = 2;
     jb.row = cu + w.lim - 1;
@@ -447,6 +470,7 @@ __device__ void decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   if (w.b == 0) a.ambiguous[i] = 0;
   if (amb) a.ambiguous[i] = 1;
   if (a.done) a.done[i] = jb.mode != 0 ? 1 : 0;
+  return kFinal;
 }
 
 // ----------------------------------------------------------------- stats --
@@ -462,6 +486,8 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
   const float T = a.T;
   const int ntypes = T > 0.f ? 2 : 1;
   const int maxw = a.L.maxw;
+  if (a.commit && blockIdx.x == 0 && threadIdx.x == 0)
+    *reinterpret_cast<int*>(a.ws + a.L.ctick) = 0;  // requests finished so far
   if (a.clear_jobs) {
     // First chunk of a chunked step: the step's single race pass reads every
     // request's job, so none may be left over from an earlier call (the
@@ -600,6 +626,149 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
   }
 }
 
+// ---------------------------------------------------------- fused commit --
+// sv_accept_commit: the warp that finalises a request's path also commits it
+// ([SwiftSpec] mechanism 3: verification result and KV update fused;
+// mechanism 2: the accepted path's KV kept, the rest released), with the
+// same rule and order as sv_commit_kv:
+//   - the K/V of staged slot ctx + path[k] moves to slot ctx + k, for k =
+//     1 .. a in ascending order (a slot written at step k is never the
+//     source of a later step, since path[k'] >= k' > k), every head, by the
+//     warp's lanes;
+//   - the new cache length is ctx + 1 + a; table entries past it are the
+//     blocks to release.
+// Every request of the call counts itself done on a ticket; the warp that
+// brings it to n_req appends all released blocks to the pool in (request,
+// table index) order and clears their table entries.
+
+// Same validity rule as sv_commit_kv; a request failing it is left as it was.
+__device__ bool commit_ok(const Args& a, int i, int& rows, int& ctx, int& al, bool report) {
+  const CommitArgs& c = a.kv;
+  rows = a.bt.cu_rows[i + 1] - a.bt.cu_rows[i];
+  ctx = c.cache_lens[i];
+  al = a.accepted_len[i];
+  const int32_t* path = a.accepted_nodes + (size_t)i * a.bt.max_rows_per_req;
+  if (rows < 1 || rows > a.bt.max_rows_per_req || al < 0 || al > rows - 1 || path[0] != 0) {
+    if (report) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+    return false;
+  }
+  for (int k = 1; k <= al; ++k)
+    if (path[k] <= path[k - 1] || path[k] >= rows) {
+      if (report) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+      return false;
+    }
+  if (ctx < 0 || (long)ctx + rows > (long)c.max_blocks * kBlockSize) {
+    if (report) flag(a.dev_status, SV_DEV_BAD_LENGTH);
+    return false;
+  }
+  const int32_t* table = c.tables + (size_t)i * c.max_blocks;
+  for (int k = 0; k <= al; ++k) {
+    const int b1 = table[(ctx + path[k]) / kBlockSize];
+    const int b2 = table[(ctx + k) / kBlockSize];
+    if (b1 < 0 || b1 >= c.num_blocks || b2 < 0 || b2 >= c.num_blocks) {
+      if (report) flag(a.dev_status, SV_DEV_BAD_BLOCK_ID);
+      return false;
+    }
+  }
+  return true;
+}
+
+// One warp: move the path's K/V, set the new length, record the table span
+// [keep, used) whose blocks the release frees.  final = false: nothing was
+// decided for the request, which is only counted.
+__device__ void commit_request(const Args& a, int i, bool final) {
+  const int lane = threadIdx.x & 31;
+  const CommitArgs& c = a.kv;
+  int2 span = make_int2(0, 0);
+  int rows = 0, ctx = 0, al = 0;
+  bool ok = false;
+  if (final) {
+    if (lane == 0) ok = commit_ok(a, i, rows, ctx, al, true);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    rows = __shfl_sync(0xffffffffu, rows, 0);
+    ctx = __shfl_sync(0xffffffffu, ctx, 0);
+    al = __shfl_sync(0xffffffffu, al, 0);
+  }
+  if (ok) {
+    const int32_t* path = a.accepted_nodes + (size_t)i * a.bt.max_rows_per_req;
+    const int32_t* table = c.tables + (size_t)i * c.max_blocks;
+    const int cpr = c.D / 8;  // int4 per token row of one head
+    for (int k = 1; k <= al; ++k) {
+      const int src = path[k];
+      if (src == k) continue;
+      const int ss = ctx + src, ds = ctx + k;
+      const size_t srow = ((size_t)table[ss / kBlockSize] * c.Hkv) * kBlockSize + ss % kBlockSize;
+      const size_t drow = ((size_t)table[ds / kBlockSize] * c.Hkv) * kBlockSize + ds % kBlockSize;
+      for (int x = lane; x < 2 * c.Hkv * cpr; x += 32) {
+        const int tensor = x / (c.Hkv * cpr), rem = x % (c.Hkv * cpr);
+        const int g = rem / cpr, q = rem % cpr;
+        __nv_bfloat16* base = tensor ? c.v : c.k;
+        const int4 val =
+            reinterpret_cast<const int4*>(base + (srow + (size_t)g * kBlockSize) * c.D)[q];
+        reinterpret_cast<int4*>(base + (drow + (size_t)g * kBlockSize) * c.D)[q] = val;
+      }
+      __syncwarp();
+    }
+    span = make_int2((ctx + 1 + al + kBlockSize - 1) / kBlockSize,
+                     (ctx + rows + kBlockSize - 1) / kBlockSize);
+    if (lane == 0) c.cache_lens[i] = ctx + 1 + al;
+  }
+  int last = 0;
+  if (lane == 0) {
+    reinterpret_cast<int2*>(a.ws + a.L.cspan)[i] = span;
+    __threadfence();
+    last = atomicAdd(reinterpret_cast<int*>(a.ws + a.L.ctick), 1) == a.bt.n_req - 1;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  // Every request is done: release in (request, table index) order.
+  __threadfence();
+  const int R = a.bt.n_req;
+  const int2* spans = reinterpret_cast<const int2*>(a.ws + a.L.cspan);
+  const int fc0 = *c.free_count;
+  int carry = 0, pushed = 0;
+  for (int base = 0; base < R; base += 32) {
+    const int r = base + lane;
+    int nfree = 0;
+    int2 sp = make_int2(0, 0);
+    int32_t* table = nullptr;
+    if (r < R) {
+      sp = __ldcg(spans + r);
+      table = c.tables + (size_t)r * c.max_blocks;
+      for (int t = sp.x; t < sp.y; ++t) nfree += __ldcg(table + t) >= 0;
+    }
+    int x = nfree;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, x, 31);
+    if (nfree) {
+      const long start = (long)fc0 + carry + x - nfree;
+      if (start + nfree <= c.capacity) {
+        int n = 0;
+        for (int t = sp.x; t < sp.y; ++t) {
+          const int blk = table[t];
+          if (blk < 0) continue;
+          c.free_list[start + n++] = blk;
+          table[t] = -1;
+        }
+        pushed = max(pushed, (int)(start + nfree - fc0));
+      } else {
+        flag(a.dev_status, SV_DEV_POOL_OVERFLOW);
+      }
+    }
+    carry += total;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) pushed = max(pushed, __shfl_xor_sync(0xffffffffu, pushed, o));
+  if (lane == 0) {
+    *c.free_count = fc0 + pushed;
+    *reinterpret_cast<int*>(a.ws + a.L.ctick) = 0;
+  }
+}
+
 // ---------------------------------------------------------------- decide --
 // One warp per active request, once every row partial exists.
 constexpr int kDecideWarps = 4;
@@ -611,8 +780,14 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
   const int count = n_slots(a, act);
   const int nch = stats_slices(a.L, count, a.T > 0.f ? 2 : 1, a.use_list != 0, a.bt.total_rows);
   const int wid = threadIdx.x >> 5;
-  for (int ai = blockIdx.x * kDecideWarps + wid; ai < count; ai += gridDim.x * kDecideWarps)
-    decide_request(a, nch, req_of(a, act, ai), s_dec[wid]);
+  for (int ai = blockIdx.x * kDecideWarps + wid; ai < count; ai += gridDim.x * kDecideWarps) {
+    const int i = req_of(a, act, ai);
+    const int outcome = decide_request(a, nch, i, s_dec[wid]);
+    if (a.commit && outcome != kToTree) {
+      __syncwarp();  // the path lane 0 wrote is visible to the warp
+      commit_request(a, i, outcome == kFinal);
+    }
+  }
 }
 
 // ------------------------------------------------------------- tree walk --
@@ -734,22 +909,27 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
     out.c = (float)c;
     break;
   }
-  if (tid != 0) return;
-  out.row = cu + n;
-  out.pos = k + 1;
-  out.mp = s_st[0];
-  out.lp = s_st[1];
-  out.mq = s_st[2];
-  out.lq = s_st[3];
-  if (out.mode == 2) {
-    out.mq = 0.f;
-    out.lq = 1.f;
+  if (tid == 0) {
+    out.row = cu + n;
+    out.pos = k + 1;
+    out.mp = s_st[0];
+    out.lp = s_st[1];
+    out.mq = s_st[2];
+    out.lq = s_st[3];
+    if (out.mode == 2) {
+      out.mq = 0.f;
+      out.lq = 1.f;
+    }
+    *job = out;
+    a.accepted_len[i] = k;
+    a.next_token[i] = -1;
+    if (amb) a.ambiguous[i] = 1;
+    if (a.done) a.done[i] = 1;
   }
-  *job = out;
-  a.accepted_len[i] = k;
-  a.next_token[i] = -1;
-  if (amb) a.ambiguous[i] = 1;
-  if (a.done) a.done[i] = 1;
+  if (a.commit && warp == 0) {
+    __syncwarp();  // the path thread 0 wrote is visible to the warp
+    commit_request(a, i, true);
+  }
 }
 
 // ------------------------------------------------------------------ race --
@@ -942,7 +1122,8 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
               int32_t vocab, float temperature, uint64_t seed, int32_t* accepted_len,
               int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
               float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s,
-              int maxw, int chunk_index) {
+              int maxw, int chunk_index, const sv_paged_kv* commit_kv,
+              const sv_block_pool* commit_pool) {
   const bool chunk_step = chunk_index >= 0;
   sv_status st = check_accept_args(bt, target_logits, draft_logits, vocab, temperature,
                                    accepted_len, accepted_nodes, next_token, ambiguous, ws);
@@ -961,10 +1142,27 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
   a.done = done;
   a.row_stats = row_stats;
   a.ws = static_cast<uint8_t*>(ws);
-  a.L = layout(bt->n_req, bt->total_rows, vocab, maxw);
+  const bool commit = commit_kv != nullptr;
+  if (commit && (chunk_step || !commit_pool)) return SV_ERR_INVALID_ARGUMENT;
+  a.L = layout(bt->n_req, bt->total_rows, vocab, maxw, commit);
   a.dev_status = dev_status;
   a.race_all = 0;
   a.clear_jobs = chunk_index == 0 ? 1 : 0;
+  a.commit = commit ? 1 : 0;
+  a.kv = CommitArgs{};
+  if (commit) {
+    a.kv.k = static_cast<__nv_bfloat16*>(commit_kv->k_cache);
+    a.kv.v = static_cast<__nv_bfloat16*>(commit_kv->v_cache);
+    a.kv.num_blocks = commit_kv->num_blocks;
+    a.kv.Hkv = commit_kv->n_kv_heads;
+    a.kv.D = commit_kv->head_dim;
+    a.kv.max_blocks = commit_kv->max_blocks_per_req;
+    a.kv.tables = commit_kv->block_tables;
+    a.kv.cache_lens = commit_kv->cache_lens;
+    a.kv.free_list = commit_pool->free_list;
+    a.kv.free_count = commit_pool->free_count;
+    a.kv.capacity = commit_pool->capacity;
+  }
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   const bool vec = vec_ok(vocab, target_logits, draft_logits);
   a.use_list = chunk_step ? 1 : 0;
@@ -999,11 +1197,12 @@ sv_status race_all(const sv_batch* bt, const float* target_logits, const float* 
   a.seed = seed;
   a.next_token = next_token;
   a.ws = static_cast<uint8_t*>(ws);
-  a.L = layout(bt->n_req, bt->total_rows, vocab, maxw);
+  a.L = layout(bt->n_req, bt->total_rows, vocab, maxw, false);
   a.dev_status = dev_status;
   a.race_all = 1;
   a.clear_jobs = 0;
   a.use_list = 0;
+  a.commit = 0;
   return launch_race(a, vec_ok(vocab, target_logits, draft_logits), s);
 }
 
@@ -1014,7 +1213,7 @@ using namespace sv;
 
 extern "C" size_t sv_accept_workspace(const sv_batch* bt, int32_t vocab) {
   if (!bt || bt->n_req < 0 || bt->total_rows < 0 || vocab < 1) return 0;
-  return acc::layout(bt->n_req, bt->total_rows, vocab, bt->max_rows_per_req).total;
+  return acc::layout(bt->n_req, bt->total_rows, vocab, bt->max_rows_per_req, false).total;
 }
 
 extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
@@ -1027,6 +1226,34 @@ extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
   return acc::run(bt, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
                   accepted_nodes, next_token, ambiguous, done, row_stats, ws, ws_bytes, dev_status,
                   static_cast<cudaStream_t>(stream), bt->max_rows_per_req, -1);
+}
+
+// ------------------------------------------------- accept + commit fused --
+extern "C" size_t sv_accept_commit_workspace(const sv_batch* bt, int32_t vocab) {
+  if (!bt || bt->n_req < 0 || bt->total_rows < 0 || vocab < 1) return 0;
+  return acc::layout(bt->n_req, bt->total_rows, vocab, bt->max_rows_per_req, true).total;
+}
+
+extern "C" sv_status sv_accept_commit(const sv_batch* bt, const float* target_logits,
+                                      const float* draft_logits, int32_t vocab, float temperature,
+                                      uint64_t seed, int32_t* accepted_len,
+                                      int32_t* accepted_nodes, int32_t* next_token,
+                                      uint8_t* ambiguous, int32_t* done, float* row_stats,
+                                      const sv_paged_kv* kv, const sv_block_pool* pool, void* ws,
+                                      size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (!bt || !kv || !pool) return SV_ERR_INVALID_ARGUMENT;
+  if (kv->block_size != kBlockSize) return SV_ERR_UNSUPPORTED_SHAPE;
+  if (kv->head_dim != 64 && kv->head_dim != 128) return SV_ERR_UNSUPPORTED_SHAPE;
+  if (kv->n_kv_heads < 1 || kv->num_blocks < 0 || kv->max_blocks_per_req < 0 ||
+      pool->capacity < 0)
+    return SV_ERR_INVALID_ARGUMENT;
+  if (bt->n_req > 0 && (!kv->k_cache || !kv->v_cache || !kv->block_tables || !kv->cache_lens ||
+                        !pool->free_list || !pool->free_count))
+    return SV_ERR_INVALID_ARGUMENT;
+  if (((uintptr_t)kv->k_cache | (uintptr_t)kv->v_cache) & 15) return SV_ERR_INVALID_ARGUMENT;
+  return acc::run(bt, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
+                  accepted_nodes, next_token, ambiguous, done, row_stats, ws, ws_bytes, dev_status,
+                  static_cast<cudaStream_t>(stream), bt->max_rows_per_req, -1, kv, pool);
 }
 
 // ------------------------------------------------ no-allocation variant ----

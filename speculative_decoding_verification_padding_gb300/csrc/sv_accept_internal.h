@@ -17,10 +17,10 @@ namespace acc {
 // (race) when every listed request is active; the kernels use more slices,
 // up to nch_cap / nch_r_cap, when fewer requests are active.
 struct Layout {
-  size_t parts, jobs, race, race_tickets, act, total;
+  size_t parts, jobs, race, race_tickets, act, ctick, cspan, total;
   int nch, nch_cap, nch_r, nch_r_cap, maxw;
 };
-Layout layout(int R, int total_rows, int V, int maxw);
+Layout layout(int R, int total_rows, int V, int maxw, bool commit = false);
 
 // The accept kernels.  chunk_index < 0: statistics, decision and race over
 // every request.  chunk_index >= 0 (chunk of a chunked step): the active
@@ -31,7 +31,8 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
               int32_t vocab, float temperature, uint64_t seed, int32_t* accepted_len,
               int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
               float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s,
-              int maxw, int chunk_index);
+              int maxw, int chunk_index, const sv_paged_kv* commit_kv = nullptr,
+              const sv_block_pool* commit_pool = nullptr);
 
 // After the last chunk of a chunked step (T > 0): the residual or bonus draw
 // of every request whose decision set one, in a single pass.

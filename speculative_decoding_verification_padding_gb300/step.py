@@ -3,10 +3,10 @@
 ``DeviceStep`` uploads a workload (``workloads.Workload``) once, allocates the
 outputs and workspaces with torch, and enqueues the library calls of a step:
 
-  onepass   sv_tree_attend -> sv_accept -> sv_commit_kv
+  onepass   sv_tree_attend -> sv_accept_commit (accept and KV commit fused)
   chunked   sv_verify_chunked (windows -> attend -> accept per chunk, early
             pruning) -> sv_commit_kv
-  budget    sv_select_budget -> sv_tree_attend -> sv_accept -> sv_commit_kv,
+  budget    sv_select_budget -> sv_tree_attend -> sv_accept_commit,
             with the selected verify_len feeding the batch
 
 Nothing here computes any part of the step; it only moves memory and calls.
@@ -68,6 +68,7 @@ class DeviceStep:
                                        maxr, verify_len=self.verify_len)
         ws = max(api.sv_tree_attend_workspace(self.batch, self.kv, self.Hq),
                  api.sv_accept_workspace(self.batch, self.V),
+                 api.sv_accept_commit_workspace(self.batch, self.V),
                  api.sv_verify_chunked_workspace(self.batch, self.kv, self.Hq, self.V))
         self.ws = api.workspace(ws, dev)
 
@@ -86,6 +87,12 @@ class DeviceStep:
         api.sv_accept(batch or self.batch, self.target, self.draft, self.V, self.T, self.w.seed,
                       self.accepted_len, self.accepted_nodes, self.next_token, self.ambiguous,
                       self.done, row_stats, self.ws, self.dev_status)
+
+    def accept_commit(self, batch=None, row_stats=None):
+        api.sv_accept_commit(batch or self.batch, self.target, self.draft, self.V, self.T,
+                             self.w.seed, self.accepted_len, self.accepted_nodes,
+                             self.next_token, self.ambiguous, self.done, row_stats, self.kv,
+                             self.pool, self.ws, self.dev_status)
 
     def chunked(self):
         api.sv_verify_chunked(self.kv, self.batch, self.q, self.Hq, self.scale, self.out,
@@ -107,20 +114,23 @@ class DeviceStep:
             self.restore_cache_state()
         if self.mode == "onepass":
             self.attend()
-            self.accept()
-            b = self.batch
+            if commit:
+                self.accept_commit()  # accept and commit fused
+            else:
+                self.accept()
         elif self.mode == "chunked":
             self.chunked()
-            b = self.batch
+            if commit:
+                self.commit(self.batch)
         elif self.mode == "budget":
             self.select()
             self.attend(self.batch_sel)
-            self.accept(self.batch_sel)
-            b = self.batch_sel
+            if commit:
+                self.accept_commit(self.batch_sel)
+            else:
+                self.accept(self.batch_sel)
         else:
             raise ValueError(self.mode)
-        if commit:
-            self.commit(b)
 
     def results(self):
         torch.cuda.synchronize()

@@ -204,6 +204,47 @@ def test_commit_matches_oracle(name, T, kw):
     assert np.array_equal(s.kv.v_cache.view(torch.int16).cpu().numpy().view(np.uint16), kv["v_cache"])
 
 
+@pytest.mark.parametrize("name,T,kw", [
+    ("batch64", 0.7, dict(n_req=48, ctx_scale=0.02, vocab=2048, draft_sigma=0.5)),
+    ("batch64", 0.0, dict(n_req=48, ctx_scale=0.02, vocab=2048, draft_sigma=0.1)),
+    ("tree70b", 0.0, dict(ctx_scale=0.01, vocab=512, draft_sigma=0.05)),
+    ("tree70b", 1.0, dict(n_req=3, ctx_scale=0.01, vocab=2048, draft_sigma=0.3)),
+    ("batch256", 1.0, dict(n_req=200, ctx_scale=0.01, vocab=1024)),
+])
+def test_accept_commit_fused_matches_oracle(name, T, kw):
+    # sv_accept_commit == oracle accept followed by oracle commit: decisions,
+    # tables, lengths, the free list in order, and every K/V byte
+    w = wl.make_workload(wl.config(name), temperature=T, **kw)
+    vl = None
+    if name == "batch256":
+        _, vl, _, _ = oracle.select_budget(w.cond_survival, w.gamma, w.sps)
+    s = DeviceStep(w, mode="onepass")
+    b = s.batch if vl is None else api.Batch(s.batch.cu_rows, s.batch.parent, s.batch.tokens,
+                                             w.max_rows, verify_len=torch.from_numpy(vl).cuda())
+    s.accept_commit(b)
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st = oracle.accept(w.batch(verify_len=vl), w.target_logits,
+                            w.draft_logits if T > 0 else None, T, w.seed)
+    assert err == 0
+    _compare_accept(res, st, w, f"fused {name} T={T}")
+    if (st.ambiguous != 0).any() or (res["ambiguous"] != 0).any():
+        pytest.skip("an ambiguous decision: the commit inputs differ by construction")
+    if name == "tree70b" and T == 0.0:
+        assert st.accepted_len.max() >= 2  # a path that moves slots
+    kv = w.kv_copy()
+    fl = w.free_list.copy()
+    fc = np.array([w.free_count], dtype=np.int32)
+    nodes = np.where(st.accepted_nodes < 0, -1, st.accepted_nodes).astype(np.int32)
+    assert oracle.commit_kv(w.batch(verify_len=vl), kv, st.accepted_len, nodes, fl, fc) == 0
+    assert np.array_equal(s.kv.block_tables.cpu().numpy(), kv["block_tables"])
+    assert np.array_equal(s.kv.cache_lens.cpu().numpy(), kv["cache_lens"])
+    assert s.pool.free_count.item() == fc[0]
+    assert np.array_equal(s.pool.free_list.cpu().numpy()[: fc[0]], fl[: fc[0]])
+    assert np.array_equal(s.kv.k_cache.view(torch.int16).cpu().numpy().view(np.uint16), kv["k_cache"])
+    assert np.array_equal(s.kv.v_cache.view(torch.int16).cpu().numpy().view(np.uint16), kv["v_cache"])
+
+
 def test_commit_pool_overflow_is_flagged_not_faulted():
     w = wl.make_workload(wl.config("batch64"), n_req=16, ctx_scale=0.01, vocab=256,
                          temperature=0.0, draft_sigma=3.0)
