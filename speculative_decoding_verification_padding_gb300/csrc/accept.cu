@@ -937,6 +937,39 @@ __device__ __forceinline__ void race_take(float& best, int& bi, float key, int v
   if (key > best || (key == best && v < bi)) { best = key; bi = v; }
 }
 
+// Constants of one race job for its weights w = p (bonus) or max(0, p - c q).
+struct RaceW {
+  float T, rT, mpb, inv_lp, mqb, cq;
+  bool unit, resid;
+};
+__device__ __forceinline__ float race_p(const RaceW& r, float l) {
+  const float x = r.unit ? l : div_by(l, r.T, r.rT);
+  return ex2(fmaf(x, kLog2e, -r.mpb)) * r.inv_lp;
+}
+__device__ __forceinline__ float race_q(const RaceW& r, float l) {
+  const float x = r.unit ? l : div_by(l, r.T, r.rT);
+  return ex2(fmaf(x, kLog2e, -r.mqb)) * r.cq;
+}
+// Running best (w, E) of a lane: v beats it iff w_v E_b > w_b E_v, lower
+// index on ties.
+__device__ __forceinline__ void race_keep(float wv, float E, int v, float& bw, float& bE, int& bi) {
+  const float lhs = wv * bE, rhs = bw * E;
+  if (lhs > rhs || (lhs == rhs && v < bi)) {
+    bw = wv;
+    bE = E;
+    bi = v;
+  }
+}
+// One entry: its uniform first; p < Km (1 - u) rules it out (see the kernel).
+__device__ __forceinline__ void race_entry(const RaceW& r, float lpv, float lqv, uint32_t bits,
+                                           int v, float Km, float& bw, float& bE, int& bi) {
+  const float u = race_u(bits);
+  const float p = race_p(r, lpv);
+  if (p < Km * (1.f - u)) return;
+  const float wv = r.resid ? fmaxf(p - race_q(r, lqv), 0.f) : p;
+  race_keep(wv, -logf(u), v, bw, bE, bi);
+}
+
 // Warp-granular like the statistics: a warp scans one slice of a request's
 // row(s) and arrives on the request's ticket; the last one reduces.
 template <bool VEC>
@@ -993,25 +1026,20 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
     if (VEC) {
       // Four 128-entry groups per iteration, their loads issued first.  The
       // trip count is uniform so that the lanes can share the best key K any
-      // of them has seen: the winner's key is at least K, so
-      //  - a group whose weights are all below K * kEmin skips the generator;
-      //  - an entry whose uniform is at most exp(-w / K) has E >= w / K, its
-      //    key cannot exceed K, and it skips the logarithm.  The bound is taken
-      //    with ex2.approx minus 2^-20, below exp(-w / K) by more than the
-      //    approximation and rounding errors, so no possible winner is lost.
-      constexpr int kGroups = 4;
+      // of them has seen; the winner's key is at least K.  Every entry draws
+      // its uniform first: since E = -log u >= 1 - u, an entry whose target
+      // probability p is below K (1 - u) (less a 2^-20 margin for rounding)
+      // has w / E <= p / E < K and cannot win -- its draft probability, its
+      // weight and its logarithm are never computed.  Only the rest go to
+      // the exact comparison.
+      constexpr int kGroups = 2;
+      const RaceW rw{T, rT, mpb, inv_lp, mqb, jb.c * inv_lq, T == 1.f, resid};
       float K = 0.f;
       const float4* p4 = reinterpret_cast<const float4*>(lp);
       const float4* q4 = reinterpret_cast<const float4*>(lq);
       for (int base = lo; base < hi; base += 128 * kGroups) {
         K = fmaxf(K, warp_max(bi == 0x7fffffff ? 0.f : bw / bE));
-        const float nK = K > 0.f ? -kLog2e / K : 0.f;  // exponent scale of exp(-w / K)
-        const float gthr = K > 0.f ? K * kEmin : -1.f;
-        auto entry = [&](float wv, uint32_t bits, int v) {
-          const float u = race_u(bits);
-          if (K > 0.f && u <= ex2(wv * nK) - 0x1p-20f) return;
-          take(wv, -logf(u), v);
-        };
+        const float Km = K * (1.f - 0x1p-20f);
         float4 xp[kGroups], xq[kGroups];
 #pragma unroll
         for (int k = 0; k < kGroups; ++k) {
@@ -1023,14 +1051,11 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
         for (int k = 0; k < kGroups; ++k) {
           const int v = base + 128 * k + 4 * lane;
           if (v >= hi) continue;
-          const float w0 = weight(xp[k].x, xq[k].x), w1 = weight(xp[k].y, xq[k].y);
-          const float w2 = weight(xp[k].z, xq[k].z), w3 = weight(xp[k].w, xq[k].w);
-          if (fmaxf(fmaxf(w0, w1), fmaxf(w2, w3)) < gthr) continue;
           const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
-          entry(w0, bits.a, v);
-          entry(w1, bits.b, v + 1);
-          entry(w2, bits.c, v + 2);
-          entry(w3, bits.d, v + 3);
+          race_entry(rw, xp[k].x, xq[k].x, bits.a, v, Km, bw, bE, bi);
+          race_entry(rw, xp[k].y, xq[k].y, bits.b, v + 1, Km, bw, bE, bi);
+          race_entry(rw, xp[k].z, xq[k].z, bits.c, v + 2, Km, bw, bE, bi);
+          race_entry(rw, xp[k].w, xq[k].w, bits.d, v + 3, Km, bw, bE, bi);
         }
       }
     } else {
