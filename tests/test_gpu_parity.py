@@ -494,6 +494,70 @@ def test_tree_sampling_batch_of_trees_matches_oracle():
     _compare_accept(res, st, w, "five trees")
 
 
+# ------------------------------------------------------- the largest windows --
+# 128 rows per request (the 128-bit ancestor masks' upper word, decision
+# windows longer than a warp, merges of more than 32 row/type pairs).
+
+def _max_rows_workload(kind, T=0.0, sigma=0.05, n_req=3):
+    import dataclasses
+    if kind == "chain":
+        cfg = dataclasses.replace(wl.config("chain8b"), gamma=("fixed", 127), n_req=n_req)
+    else:
+        cfg = dataclasses.replace(wl.config("tree70b"), gamma=("tree", (4, 3, 2, 2, 2, 2, 2), 127),
+                                  n_req=n_req)
+    return wl.make_workload(cfg, ctx_scale=0.01, vocab=512, draft_sigma=sigma, temperature=T)
+
+
+@pytest.mark.parametrize("kind", ["chain", "tree"])
+def test_attend_128_rows_matches_oracle(kind):
+    w = _max_rows_workload(kind)
+    assert w.max_rows == 128
+    s = DeviceStep(w, mode="onepass")
+    s.out.fill_(float("nan"))
+    s.attend()
+    torch.cuda.synchronize()
+    assert s.dev_status.item() == 0
+    err, _, ref64 = oracle.tree_attend(w.batch(), w.kv(), w.q, w.cfg.n_q_heads, w.softmax_scale)
+    assert err == 0
+    _check_attention(s.out, ref64, np.arange(w.total_rows))
+
+
+@pytest.mark.parametrize("kind,T,sigma", [("chain", 0.0, 0.05), ("chain", 1.0, 0.02),
+                                          ("tree", 0.0, 0.05), ("tree", 1.0, 0.05)])
+def test_accept_commit_128_rows_matches_oracle(kind, T, sigma):
+    w = _max_rows_workload(kind, T, sigma)
+    s = DeviceStep(w, mode="onepass")
+    s.accept_commit()
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits if T > 0 else None, T, w.seed)
+    assert err == 0
+    _compare_accept(res, st, w, f"128 rows {kind} T={T}")
+    if kind == "chain":
+        assert st.accepted_len.max() > 32  # the decision ran past one warp's lanes
+    if (st.ambiguous != 0).any() or (res["ambiguous"] != 0).any():
+        return
+    kv = w.kv_copy()
+    fl = w.free_list.copy()
+    fc = np.array([w.free_count], dtype=np.int32)
+    nodes = np.where(st.accepted_nodes < 0, -1, st.accepted_nodes).astype(np.int32)
+    assert oracle.commit_kv(w.batch(), kv, st.accepted_len, nodes, fl, fc) == 0
+    assert np.array_equal(s.kv.block_tables.cpu().numpy(), kv["block_tables"])
+    assert np.array_equal(s.pool.free_list.cpu().numpy()[: fc[0]], fl[: fc[0]])
+    assert np.array_equal(s.kv.k_cache.view(torch.int16).cpu().numpy().view(np.uint16), kv["k_cache"])
+
+
+def test_chunked_128_rows_matches_one_pass():
+    w = _max_rows_workload("chain", 0.7, 0.02, n_req=4)
+    s = DeviceStep(w, mode="chunked")
+    s.chunked()
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits, 0.7, w.seed)
+    assert err == 0
+    _compare_accept(res, st, w, "chunked 128 rows")
+
+
 def test_small_workspace_is_refused_before_launch():
     w = _make("tiny", vocab=64)
     s = DeviceStep(w, mode="onepass")
