@@ -353,6 +353,16 @@ sv_status sv_adapt_gamma(int32_t n_req, const int32_t* accepted_len, const int32
                          int32_t gamma_min, int32_t gamma_max, int32_t* dev_status,
                          void* stream);
 
+/* ------------------------------------------------------------ self test --
+ * Every wait inside the library's kernels (on an mbarrier a TMA copy or a
+ * thread completes) gives up after a bounded number of rounds, sets
+ * SV_DEV_TIMEOUT and lets the kernel return, so that a lost copy can never
+ * hang the device.  sv_selftest_bounded_wait runs that wait on a barrier
+ * nothing will complete (limit rounds, 1 .. 2^20), so the timeout path can be
+ * checked on a live GPU: *dev_status gets SV_DEV_TIMEOUT and the context
+ * stays usable.  No other effect. */
+sv_status sv_selftest_bounded_wait(int32_t limit, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -73,6 +73,7 @@ PROTOTYPES = {
                                          P, P, P, SZ, P, P]),
     "sv_adapt_gamma": (ctypes.c_int, [I32, P, P, P, P, ctypes.c_double, ctypes.c_double, I32, I32,
                                       P, P]),
+    "sv_selftest_bounded_wait": (ctypes.c_int, [I32, P, P]),
 }
 
 _lib = None

@@ -229,6 +229,12 @@ def sv_adapt_gamma(accepted_len: torch.Tensor, verified: torch.Tensor, state: to
                                    _stream(stream)), "sv_adapt_gamma")
 
 
+def sv_selftest_bounded_wait(limit: int, dev_status: torch.Tensor, stream=None):
+    _expect(dev_status, torch.int32, "dev_status")
+    N.check(N.lib().sv_selftest_bounded_wait(int(limit), _ptr(dev_status), _stream(stream)),
+            "sv_selftest_bounded_wait")
+
+
 def sv_chunk_windows(batch: Batch, chunk_index: int, chunk_size: int,
                      done: Optional[torch.Tensor], row_begin: torch.Tensor,
                      row_end: torch.Tensor, stream=None):

@@ -54,6 +54,37 @@ extern "C" const char* sv_status_string(sv_status s) {
 
 extern "C" const char* sv_version(void) { return "libspecverify 0.1 (sm_103a)"; }
 
+// ------------------------------------------------- bounded-wait self test --
+// One thread arms an mbarrier for two arrivals, arrives once and waits on
+// the phase with the bounded wait every kernel of the library uses: the wait
+// cannot complete, gives up after `limit` rounds and the kernel reports
+// SV_DEV_TIMEOUT; the second arrival then completes the phase, so nothing is
+// left pending when the CTA exits.
+namespace sv {
+namespace chk {
+__global__ void __launch_bounds__(32) selftest_wait_kernel(int limit, int32_t* dev_status) {
+  griddep_entry();
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 2);
+  fence_mbar_init();
+  mbar_arrive(b);
+  if (!mbar_wait_bounded(b, 0, limit)) flag(dev_status, SV_DEV_TIMEOUT);
+  mbar_arrive(b);
+  if (!mbar_wait_bounded(b, 0, limit)) flag(dev_status, SV_DEV_UNSUPPORTED);  // never expected
+}
+}  // namespace chk
+}  // namespace sv
+
+extern "C" sv_status sv_selftest_bounded_wait(int32_t limit, int32_t* dev_status, void* stream) {
+  if (limit < 1 || limit > kWaitLimit || !dev_status) return SV_ERR_INVALID_ARGUMENT;
+  if (sv::launch(chk::selftest_wait_kernel, 1, 32, 0, static_cast<cudaStream_t>(stream),
+                 (int)limit, dev_status) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
 extern "C" sv_status sv_chunk_windows(const sv_batch* bt, int32_t chunk_index, int32_t chunk_size,
                                       const int32_t* done, int32_t* row_begin, int32_t* row_end,
                                       void* stream) {

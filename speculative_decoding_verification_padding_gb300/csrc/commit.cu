@@ -16,6 +16,8 @@
 //           table index) order, clears their table entries and sets the new
 //           cache length.
 
+#include <mutex>
+
 #include "sv_internal.cuh"
 
 namespace sv {
@@ -229,14 +231,19 @@ extern "C" sv_status sv_commit_kv(const sv_paged_kv* kv, const sv_batch* bt,
   // one head of every moved slot, K and V: 2 * 127 * 128 * 2 B = 65 KB at most
   const size_t smem = (size_t)2 * (bt->max_rows_per_req - 1 > 0 ? bt->max_rows_per_req - 1 : 1) *
                       kv->head_dim * 2;
-  static int attr_dev_mask = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (smem > 48 * 1024 && !(attr_dev_mask & (1 << (dev & 31)))) {
-    if (cudaFuncSetAttribute(cmt::copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             96 * 1024) != cudaSuccess)
-      return SV_ERR_CUDA;
-    attr_dev_mask |= 1 << (dev & 31);
+  if (smem > 48 * 1024) {
+    // once per device (calls may come from several host threads)
+    static std::mutex mu;
+    static bool set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!set[dev]) {
+      if (cudaFuncSetAttribute(cmt::copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               96 * 1024) != cudaSuccess)
+        return SV_ERR_CUDA;
+      set[dev] = true;
+    }
   }
   if (sv::launch(cmt::copy_kernel, bt->n_req, 256, smem, s, a) != cudaSuccess) return SV_ERR_CUDA;
   if (sv::launch(cmt::release_kernel, 1, 1024, 0, s, a) != cudaSuccess) return SV_ERR_CUDA;

@@ -64,6 +64,9 @@ def test_host_side_validation_without_gpu(lib):
     assert lib.sv_adapt_gamma(4, 1, 1, 1, 1, 0.7, -1.0, 1, 8, None, None) == N.SV_ERR_INVALID_ARGUMENT
     assert lib.sv_adapt_gamma(4, 1, 1, 1, 1, 0.7, 2.0, 1, 128, None, None) == N.SV_ERR_INVALID_ARGUMENT
     assert lib.sv_adapt_gamma(0, None, None, None, None, 0.7, 2.0, 1, 8, None, None) == N.SV_OK
+    assert lib.sv_selftest_bounded_wait(0, 1, None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_selftest_bounded_wait(1 << 21, 1, None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_selftest_bounded_wait(100, None, None) == N.SV_ERR_INVALID_ARGUMENT
     kv = N.SvPagedKV(256, 256, 10, 16, 2, 64, 1, 4, 1)
     need = lib.sv_tree_attend_workspace(ctypes.byref(b), ctypes.byref(kv), 8)
     assert need > 0

@@ -558,6 +558,19 @@ def test_chunked_128_rows_matches_one_pass():
     _compare_accept(res, st, w, "chunked 128 rows")
 
 
+def test_bounded_wait_times_out_and_the_context_survives():
+    # the wait every kernel uses, on a barrier nothing completes: it gives up,
+    # reports SV_DEV_TIMEOUT, and the next calls run normally
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.sv_selftest_bounded_wait(4096, st)
+    torch.cuda.synchronize()
+    assert st.item() == api.N.SV_DEV_TIMEOUT
+    w = wl.make_workload(wl.config("tiny"))
+    s = DeviceStep(w, mode="onepass")
+    s.run()
+    assert s.results()["dev_status"] == 0
+
+
 def test_small_workspace_is_refused_before_launch():
     w = _make("tiny", vocab=64)
     s = DeviceStep(w, mode="onepass")
