@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   __shared__ int s_warp[32];
   __shared__ int s_carry, s_acarry;
 
+  __shared__ int s_none;
   if (tid == 0) {
     // Each request's rows are checked against the packed total by its window;
     // a prefix that does not start at 0 or end at the total is reported too.
@@ -186,8 +187,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     s_W = 0ull;
     s_carry = 0;
     s_acarry = 0;
+    // A chunk after one that listed no request is empty too (requests only
+    // ever stop): nothing to plan.
+    s_none = (a.chunk.index > 0 && a.chunk.act[R] == 0) ? 1 : 0;
+    if (s_none) hdr->U = 0;
   }
   __syncthreads();
+  if (s_none) return;
   // One warp per request: window, parents, length, work.
   unsigned long long myW = 0;
   const bool chunked = a.chunk.index >= 0;
