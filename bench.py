@@ -4,15 +4,16 @@ Default workload (--workload batch64): 64 requests, Llama-3-8B attention
 shape (32 q / 8 KV heads, d 128), per-request draft counts U{1..8},
 contexts log-normal (ln 4096, 1) clipped to [512, 32768], paged bf16 KV
 (16-token blocks, shuffled tables), vocab 128256 fp32 logits, sampling at
-T = 0.7, chunked verification in chunks of 2 with early pruning, then the KV
-commit.  Other workloads: tiny, chain8b, tree70b (one pass), batch256
-(budget-selected).
+T = 0.7, chunked verification in chunks of 2 with early pruning, each
+request's KV committed in the chunk that stops it.  Other workloads: tiny,
+chain8b, tree70b (one pass), batch256 (budget-selected).
 
 One step = restore the block tables / lengths / free list the previous
 step's commit changed, then the workload's calls:
-  chunked  sv_verify_chunked (per chunk: attention plan with the chunk's
-           windows and accept list, split-KV attention, row statistics,
-           decisions; one resampling race per step) and sv_commit_kv
+  chunked  sv_verify_chunked_commit (per chunk: attention plan with the
+           chunk's windows and accept list, split-KV attention, row
+           statistics, decisions with the KV commit of every request they
+           stop; one resampling race per step)
   onepass  sv_tree_attend, sv_accept_commit (accept and KV commit fused)
   budget   sv_select_budget, sv_tree_attend and sv_accept_commit on the
            selected prefixes
@@ -517,12 +518,13 @@ def main():
 
     n_launch = len(sched)
     race = 1 if T > 0 else 0
-    # Chunked: plan (windows + accept list) + attend + stats + decide per chunk, one race
-    # after the last, commit (copy + release).  One-pass / budget: [select] + plan + attend +
-    # fused accept-commit (stats + decide [+ tree walk] [+ race]).
+    # Chunked: plan (windows + accept list) + attend + stats + decide (with the commit) per
+    # chunk [+ tree walk after the first when a chunk holds a tree], one race after the
+    # last.  One-pass / budget: [select] + plan + attend + fused accept-commit (stats +
+    # decide [+ tree walk] [+ race]).
     tree = 1 if (T > 0 and w.max_rows > 2) else 0
     if mode == "chunked":
-        launches_per_step = n_launch * (2 + 2) + race + 2
+        launches_per_step = n_launch * (2 + 2) + race + (tree if chunk > 2 else 0)
     else:
         launches_per_step = 2 + 2 + tree + race + (1 if mode == "budget" else 0)
     value = rows_all / t_step

@@ -14,7 +14,7 @@
  *   sv_select_budget  how many drafts of each request to verify, by sorting
  *                     every (request, position) by prefix survival and
  *                     maximising tau * SPS(B);
- *   sv_chunk_windows, sv_verify_chunked
+ *   sv_chunk_windows, sv_verify_chunked, sv_verify_chunked_commit
  *                     verification in chunks of rows with early pruning of
  *                     requests whose prefix was rejected;
  *   sv_adapt_gamma    each request's next draft length from its own
@@ -314,7 +314,21 @@ sv_status sv_select_budget(int32_t n_req, int32_t gamma_max, const float* cond_s
  * met a rejection or emitted their bonus token stop being attended and
  * tested.  batch->row_begin / row_end are ignored (the call uses its own);
  * done [n_req] is required.  Results equal one-pass verification: the
- * uniforms are keyed by position.  ws: sv_verify_chunked_workspace(). */
+ * uniforms are keyed by position.  A draft tree is verified whole in the
+ * first chunk, so it needs chunk_size >= its rows (a tree cut by a chunk
+ * boundary sets SV_DEV_BAD_WINDOW and gets no result).
+ * ws: sv_verify_chunked_workspace() (the same size serves
+ * sv_verify_chunked_commit).
+ * sv_verify_chunked_commit: the same step with [SwiftSpec] mechanisms 2-3
+ * fused in -- it computes exactly what sv_verify_chunked followed by
+ * sv_commit_kv(kv, batch, accepted_len, accepted_nodes, pool) computes
+ * (same K/V moves, cache lengths, free list and its order), but each request
+ * is committed by the decision that stops it, in that chunk's kernels, and
+ * the last request to stop appends every released block to the pool.  A
+ * stopped request is never attended again, so moving its K/V mid-step
+ * changes nothing the later chunks read.  Requests whose window is invalid
+ * are left as they were; one whose parents or tokens are invalid is flagged,
+ * stops (done = 1) and is left as it was. */
 sv_status sv_chunk_windows(const sv_batch* batch, int32_t chunk_index, int32_t chunk_size,
                            const int32_t* done, int32_t* row_begin, int32_t* row_end,
                            void* stream);
@@ -327,6 +341,14 @@ sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* batch, const 
                             int32_t* accepted_len, int32_t* accepted_nodes, int32_t* next_token,
                             uint8_t* ambiguous, int32_t* done, void* ws, size_t ws_bytes,
                             int32_t* dev_status, void* stream);
+sv_status sv_verify_chunked_commit(const sv_paged_kv* kv, const sv_batch* batch, const void* q,
+                                   int32_t n_q_heads, float softmax_scale, void* out,
+                                   const float* target_logits, const float* draft_logits,
+                                   int32_t vocab, float temperature, uint64_t seed,
+                                   int32_t chunk_size, int32_t* accepted_len,
+                                   int32_t* accepted_nodes, int32_t* next_token,
+                                   uint8_t* ambiguous, int32_t* done, const sv_block_pool* pool,
+                                   void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------ per-request draft length --
  * [FASER] mechanism 1 (per-request speculation length): every request's

@@ -71,6 +71,8 @@ PROTOTYPES = {
     "sv_verify_chunked_workspace": (SZ, [P, P, I32, I32]),
     "sv_verify_chunked": (ctypes.c_int, [P, P, P, I32, F32, P, P, P, I32, F32, U64, I32, P, P, P,
                                          P, P, P, SZ, P, P]),
+    "sv_verify_chunked_commit": (ctypes.c_int, [P, P, P, I32, F32, P, P, P, I32, F32, U64, I32, P,
+                                                P, P, P, P, P, P, SZ, P, P]),
     "sv_adapt_gamma": (ctypes.c_int, [I32, P, P, P, P, ctypes.c_double, ctypes.c_double, I32, I32,
                                       P, P]),
     "sv_selftest_bounded_wait": (ctypes.c_int, [I32, P, P]),

@@ -264,3 +264,23 @@ def sv_verify_chunked(kv: PagedKV, batch: Batch, q: torch.Tensor, n_q_heads: int
                                       _ptr(accepted_nodes), _ptr(next_token), _ptr(ambiguous),
                                       _ptr(done), _ptr(ws), ws.numel(), _ptr(dev_status),
                                       _stream(stream)), "sv_verify_chunked")
+
+
+def sv_verify_chunked_commit(kv: PagedKV, batch: Batch, q: torch.Tensor, n_q_heads: int,
+                             softmax_scale: float, out: torch.Tensor,
+                             target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor],
+                             vocab: int, temperature: float, seed: int, chunk_size: int,
+                             accepted_len: torch.Tensor, accepted_nodes: torch.Tensor,
+                             next_token: torch.Tensor, ambiguous: torch.Tensor,
+                             done: torch.Tensor, pool: BlockPool, ws: torch.Tensor,
+                             dev_status: Optional[torch.Tensor] = None, stream=None):
+    b, k, p = batch.c(), kv.c(), pool.c()
+    N.check(N.lib().sv_verify_chunked_commit(ctypes.byref(k), ctypes.byref(b), _ptr(q), n_q_heads,
+                                             softmax_scale, _ptr(out), _ptr(target_logits),
+                                             _ptr(draft_logits), vocab, temperature,
+                                             seed & 0xFFFFFFFFFFFFFFFF, chunk_size,
+                                             _ptr(accepted_len), _ptr(accepted_nodes),
+                                             _ptr(next_token), _ptr(ambiguous), _ptr(done),
+                                             ctypes.byref(p), _ptr(ws), ws.numel(),
+                                             _ptr(dev_status), _stream(stream)),
+            "sv_verify_chunked_commit")

@@ -486,8 +486,12 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
   const float T = a.T;
   const int ntypes = T > 0.f ? 2 : 1;
   const int maxw = a.L.maxw;
-  if (a.commit && blockIdx.x == 0 && threadIdx.x == 0)
-    *reinterpret_cast<int*>(a.ws + a.L.ctick) = 0;  // requests finished so far
+  // Requests finished so far (fused commit): none in a one-pass call; in the
+  // first chunk of a chunked step, the ones the planner did not list (their
+  // window is invalid: no chunk ever runs them).
+  const bool commit_start = a.use_list ? a.clear_jobs != 0 : true;
+  if (a.commit && commit_start && blockIdx.x == 0 && threadIdx.x == 0)
+    *reinterpret_cast<int*>(a.ws + a.L.ctick) = a.use_list ? R - count : 0;
   if (a.clear_jobs) {
     // First chunk of a chunked step: the step's single race pass reads every
     // request's job, so none may be left over from an earlier call (the
@@ -641,77 +645,92 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
 // brings it to n_req appends all released blocks to the pool in (request,
 // table index) order and clears their table entries.
 
-// Same validity rule as sv_commit_kv; a request failing it is left as it was.
-__device__ bool commit_ok(const Args& a, int i, int& rows, int& ctx, int& al, bool report) {
+// Same validity rule as sv_commit_kv, checked by the whole warp (every
+// lane holds the same rows, ctx, al): 0 when the commit is valid, else the
+// SV_DEV_* bit of the first rule broken, in the order path / window, cache
+// length, block ids.  A request failing it is left as it was.
+__device__ __forceinline__ int commit_check(const Args& a, int rows, int ctx, int al, const int32_t* path,
+                            const int32_t* table) {
+  const int lane = threadIdx.x & 31;
   const CommitArgs& c = a.kv;
-  rows = a.bt.cu_rows[i + 1] - a.bt.cu_rows[i];
-  ctx = c.cache_lens[i];
-  al = a.accepted_len[i];
-  const int32_t* path = a.accepted_nodes + (size_t)i * a.bt.max_rows_per_req;
-  if (rows < 1 || rows > a.bt.max_rows_per_req || al < 0 || al > rows - 1 || path[0] != 0) {
-    if (report) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-    return false;
+  if (rows < 1 || rows > a.bt.max_rows_per_req || al < 0 || al > rows - 1)
+    return SV_DEV_BAD_WINDOW;
+  bool bad = false;
+  for (int k = lane; k <= al; k += 32) {
+    const int pk = path[k];
+    bad |= k == 0 ? pk != 0 : (pk <= path[k - 1] || pk >= rows);
   }
-  for (int k = 1; k <= al; ++k)
-    if (path[k] <= path[k - 1] || path[k] >= rows) {
-      if (report) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-      return false;
-    }
-  if (ctx < 0 || (long)ctx + rows > (long)c.max_blocks * kBlockSize) {
-    if (report) flag(a.dev_status, SV_DEV_BAD_LENGTH);
-    return false;
-  }
-  const int32_t* table = c.tables + (size_t)i * c.max_blocks;
-  for (int k = 0; k <= al; ++k) {
+  if (__any_sync(0xffffffffu, bad)) return SV_DEV_BAD_WINDOW;
+  if (ctx < 0 || (long)ctx + rows > (long)c.max_blocks * kBlockSize) return SV_DEV_BAD_LENGTH;
+  // path[k] in [0, rows) now, so both table indexes are below max_blocks
+  for (int k = lane; k <= al; k += 32) {
     const int b1 = table[(ctx + path[k]) / kBlockSize];
     const int b2 = table[(ctx + k) / kBlockSize];
-    if (b1 < 0 || b1 >= c.num_blocks || b2 < 0 || b2 >= c.num_blocks) {
-      if (report) flag(a.dev_status, SV_DEV_BAD_BLOCK_ID);
-      return false;
-    }
+    bad |= b1 < 0 || b1 >= c.num_blocks || b2 < 0 || b2 >= c.num_blocks;
   }
-  return true;
+  if (__any_sync(0xffffffffu, bad)) return SV_DEV_BAD_BLOCK_ID;
+  return 0;
 }
 
 // One warp: move the path's K/V, set the new length, record the table span
 // [keep, used) whose blocks the release frees.  final = false: nothing was
-// decided for the request, which is only counted.
-__device__ void commit_request(const Args& a, int i, bool final) {
+// decided for the request, which is only counted.  The lanes look up the
+// moves of 32 path positions at once (chains move nothing); the moves
+// themselves run in ascending k, every lane copying part of the slot.
+__device__ __forceinline__ void commit_request(const Args& a, int i, bool final) {
   const int lane = threadIdx.x & 31;
   const CommitArgs& c = a.kv;
   int2 span = make_int2(0, 0);
-  int rows = 0, ctx = 0, al = 0;
-  bool ok = false;
   if (final) {
-    if (lane == 0) ok = commit_ok(a, i, rows, ctx, al, true);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    rows = __shfl_sync(0xffffffffu, rows, 0);
-    ctx = __shfl_sync(0xffffffffu, ctx, 0);
-    al = __shfl_sync(0xffffffffu, al, 0);
-  }
-  if (ok) {
+    const int rows = a.bt.cu_rows[i + 1] - a.bt.cu_rows[i];
+    const int ctx = c.cache_lens[i];
+    const int al = a.accepted_len[i];
     const int32_t* path = a.accepted_nodes + (size_t)i * a.bt.max_rows_per_req;
     const int32_t* table = c.tables + (size_t)i * c.max_blocks;
-    const int cpr = c.D / 8;  // int4 per token row of one head
-    for (int k = 1; k <= al; ++k) {
-      const int src = path[k];
-      if (src == k) continue;
-      const int ss = ctx + src, ds = ctx + k;
-      const size_t srow = ((size_t)table[ss / kBlockSize] * c.Hkv) * kBlockSize + ss % kBlockSize;
-      const size_t drow = ((size_t)table[ds / kBlockSize] * c.Hkv) * kBlockSize + ds % kBlockSize;
-      for (int x = lane; x < 2 * c.Hkv * cpr; x += 32) {
-        const int tensor = x / (c.Hkv * cpr), rem = x % (c.Hkv * cpr);
-        const int g = rem / cpr, q = rem % cpr;
-        __nv_bfloat16* base = tensor ? c.v : c.k;
-        const int4 val =
-            reinterpret_cast<const int4*>(base + (srow + (size_t)g * kBlockSize) * c.D)[q];
-        reinterpret_cast<int4*>(base + (drow + (size_t)g * kBlockSize) * c.D)[q] = val;
+    const int bad = commit_check(a, rows, ctx, al, path, table);
+    if (bad) {
+      if (lane == 0) flag(a.dev_status, bad);
+    } else {
+      const int cpr = c.D / 8;  // int4 per token row of one head
+      const int per_slot = 2 * c.Hkv * cpr;
+      for (int k0 = 1; k0 <= al; k0 += 32) {
+        const int k = k0 + lane;
+        unsigned long long srow = 0, drow = 0;
+        bool mv = false;
+        if (k <= al) {
+          const int src = path[k];
+          mv = src != k;
+          if (mv) {
+            const int ss = ctx + src, ds = ctx + k;
+            srow = ((unsigned long long)table[ss / kBlockSize] * c.Hkv) * kBlockSize +
+                   ss % kBlockSize;
+            drow = ((unsigned long long)table[ds / kBlockSize] * c.Hkv) * kBlockSize +
+                   ds % kBlockSize;
+          }
+        }
+        // A slot written at step k is never the source of a later step
+        // (path[k'] >= k' > k), so ascending k reads every source first.
+        unsigned m = __ballot_sync(0xffffffffu, mv);
+        while (m) {
+          const int j = __ffs(m) - 1;
+          m &= m - 1;
+          const unsigned long long sr = __shfl_sync(0xffffffffu, srow, j);
+          const unsigned long long dr = __shfl_sync(0xffffffffu, drow, j);
+          for (int x = lane; x < per_slot; x += 32) {
+            const int tensor = x / (c.Hkv * cpr), rem = x % (c.Hkv * cpr);
+            const int g = rem / cpr, q = rem % cpr;
+            __nv_bfloat16* base = tensor ? c.v : c.k;
+            const int4 val =
+                reinterpret_cast<const int4*>(base + (sr + (size_t)g * kBlockSize) * c.D)[q];
+            reinterpret_cast<int4*>(base + (dr + (size_t)g * kBlockSize) * c.D)[q] = val;
+          }
+          __syncwarp();
+        }
       }
-      __syncwarp();
+      span = make_int2((ctx + 1 + al + kBlockSize - 1) / kBlockSize,
+                       (ctx + rows + kBlockSize - 1) / kBlockSize);
+      if (lane == 0) c.cache_lens[i] = ctx + 1 + al;
     }
-    span = make_int2((ctx + 1 + al + kBlockSize - 1) / kBlockSize,
-                     (ctx + rows + kBlockSize - 1) / kBlockSize);
-    if (lane == 0) c.cache_lens[i] = ctx + 1 + al;
   }
   int last = 0;
   if (lane == 0) {
@@ -773,7 +792,7 @@ __device__ void commit_request(const Args& a, int i, bool final) {
 // One warp per active request, once every row partial exists.
 constexpr int kDecideWarps = 4;
 
-__global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
+__global__ void __launch_bounds__(kDecideWarps * 32, 1) decide_kernel(Args a) {
   griddep_entry();
   __shared__ DecideSmem s_dec[kDecideWarps];
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
@@ -784,8 +803,18 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(Args a) {
     const int i = req_of(a, act, ai);
     const int outcome = decide_request(a, nch, i, s_dec[wid]);
     if (a.commit && outcome != kToTree) {
-      __syncwarp();  // the path lane 0 wrote is visible to the warp
-      commit_request(a, i, outcome == kFinal);
+      __syncwarp();  // the path and state lane 0 wrote are visible to the warp
+      bool now = true;
+      if (a.use_list) {
+        // Chunked step: a request is committed in the chunk that stops it; one
+        // whose input is invalid stops here and is only counted.
+        if (outcome == kSkipped) {
+          if ((threadIdx.x & 31) == 0) a.done[i] = 1;
+        } else {
+          now = a.done[i] != 0;
+        }
+      }
+      if (now) commit_request(a, i, outcome == kFinal);
     }
   }
 }
@@ -1168,7 +1197,7 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
   a.row_stats = row_stats;
   a.ws = static_cast<uint8_t*>(ws);
   const bool commit = commit_kv != nullptr;
-  if (commit && (chunk_step || !commit_pool)) return SV_ERR_INVALID_ARGUMENT;
+  if (commit && (!commit_pool || (chunk_step && !done))) return SV_ERR_INVALID_ARGUMENT;
   a.L = layout(bt->n_req, bt->total_rows, vocab, maxw, commit);
   a.dev_status = dev_status;
   a.race_all = 0;
@@ -1199,9 +1228,12 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
     return SV_ERR_CUDA;
   const unsigned gd = (unsigned)max(1, min((bt->n_req + kDecideWarps - 1) / kDecideWarps, kNumSMs * 8));
   if (sv::launch(decide_kernel, gd, kDecideWarps * 32, 0, s, a) != cudaSuccess) return SV_ERR_CUDA;
-  if (temperature > 0.f && !chunk_step && bt->max_rows_per_req > 2) {
-    // draft trees at T > 0 (requests the decision marked; a tree is verified
-    // in one window, never in chunks); the other CTAs exit at once
+  if (temperature > 0.f && bt->max_rows_per_req > 2 &&
+      (!chunk_step || (chunk_index == 0 && a.L.maxw > 2))) {
+    // draft trees at T > 0 (requests the decision marked); the other CTAs
+    // exit at once.  A tree is verified in one window: in a chunked step only
+    // the first chunk, and only when a chunk holds more than a chain's two
+    // rows, can take one whole.
     if (sv::launch(tree_kernel, (unsigned)bt->n_req, kTreeThreads, 0, s, a) != cudaSuccess)
       return SV_ERR_CUDA;
   }

@@ -225,7 +225,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
       if (!w.ok && !chunked) flag(a.dev_status, SV_DEV_BAD_WINDOW);
       if (badp) flag(a.dev_status, SV_DEV_BAD_PARENT);
       const int ctx = a.cache_lens[i];
-      if (valid && (ctx < 0 || (long)ctx + w.rows > (long)a.max_blocks * kBlockSize)) {
+      // A request that stopped in an earlier chunk may have been committed
+      // already (its cache length moved on): nothing of it is read now.
+      const bool stopped = chunked && a.chunk.index > 0 && w.b >= w.e;
+      if (valid && !stopped && (ctx < 0 || (long)ctx + w.rows > (long)a.max_blocks * kBlockSize)) {
         valid = false;
         flag(a.dev_status, SV_DEV_BAD_LENGTH);
       }

@@ -107,25 +107,32 @@ extern "C" size_t sv_verify_chunked_workspace(const sv_batch* bt, const sv_paged
   if (!wa) return 0;
   // The chunk size is not an argument here: the accept part is sized for
   // one-row windows, the largest of its layouts (fewer rows per window give
-  // more vocabulary slices per row), so it fits every chunk size.
-  const size_t wb = acc::layout(bt->n_req, bt->total_rows, vocab, 1).total;
+  // more vocabulary slices per row), so it fits every chunk size; it also
+  // holds the fused commit's ticket and spans.
+  const size_t wb = acc::layout(bt->n_req, bt->total_rows, vocab, 1, true).total;
   return chk::windows_bytes(bt->n_req) + align256(wb) + wa;
 }
 
-extern "C" sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* bt, const void* q,
-                                       int32_t n_q_heads, float softmax_scale, void* out,
-                                       const float* target_logits, const float* draft_logits,
-                                       int32_t vocab, float temperature, uint64_t seed,
-                                       int32_t chunk_size, int32_t* accepted_len,
-                                       int32_t* accepted_nodes, int32_t* next_token,
-                                       uint8_t* ambiguous, int32_t* done, void* ws,
-                                       size_t ws_bytes, int32_t* dev_status, void* stream) {
+namespace {
+
+// The chunked step; with `pool` the accept kernels also commit every request
+// in the chunk where it stops (the same cache `kv` the attention reads: a
+// stopped request is never attended again, and its released blocks go back
+// to the pool only after the last request has stopped).
+sv_status verify_chunked(const sv_paged_kv* kv, const sv_batch* bt, const void* q,
+                         int32_t n_q_heads, float softmax_scale, void* out,
+                         const float* target_logits, const float* draft_logits, int32_t vocab,
+                         float temperature, uint64_t seed, int32_t chunk_size,
+                         int32_t* accepted_len, int32_t* accepted_nodes, int32_t* next_token,
+                         uint8_t* ambiguous, int32_t* done, const sv_block_pool* pool, void* ws,
+                         size_t ws_bytes, int32_t* dev_status, void* stream) {
   if (!kv || !bt || chunk_size < 1 || !done) return SV_ERR_INVALID_ARGUMENT;
   if (bt->n_req < 0 || bt->max_rows_per_req < 1) return SV_ERR_INVALID_ARGUMENT;
   if (bt->n_req == 0 || bt->total_rows == 0) return SV_OK;
   const size_t wa = sv_tree_attend_workspace(bt, kv, n_q_heads);
   if (!wa || vocab < 1) return SV_ERR_INVALID_ARGUMENT;
-  const acc::Layout AL = acc::layout(bt->n_req, bt->total_rows, vocab, chunk_size);
+  const bool commit = pool != nullptr;
+  const acc::Layout AL = acc::layout(bt->n_req, bt->total_rows, vocab, chunk_size, commit);
   const size_t need = chk::windows_bytes(bt->n_req) + align256(AL.total) + wa;
   if (!ws || ((uintptr_t)ws & 255)) return SV_ERR_INVALID_ARGUMENT;
   if (ws_bytes < need) return SV_ERR_WORKSPACE_TOO_SMALL;
@@ -148,11 +155,47 @@ extern "C" sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* bt
     if (st != SV_OK) return st;
     st = acc::run(&b2, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
                   accepted_nodes, next_token, ambiguous, done, nullptr, acc_ws, AL.total,
-                  dev_status, s, chunk_size, c);
+                  dev_status, s, chunk_size, c, commit ? kv : nullptr, pool);
     if (st != SV_OK) return st;
   }
   // Nothing in a later chunk depends on the drawn tokens: one race pass
   // after the last chunk serves every request at once.
   return acc::race_all(bt, target_logits, draft_logits, vocab, temperature, seed, next_token,
                        acc_ws, chunk_size, dev_status, s);
+}
+
+}  // namespace
+
+extern "C" sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* bt, const void* q,
+                                       int32_t n_q_heads, float softmax_scale, void* out,
+                                       const float* target_logits, const float* draft_logits,
+                                       int32_t vocab, float temperature, uint64_t seed,
+                                       int32_t chunk_size, int32_t* accepted_len,
+                                       int32_t* accepted_nodes, int32_t* next_token,
+                                       uint8_t* ambiguous, int32_t* done, void* ws,
+                                       size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return verify_chunked(kv, bt, q, n_q_heads, softmax_scale, out, target_logits, draft_logits,
+                        vocab, temperature, seed, chunk_size, accepted_len, accepted_nodes,
+                        next_token, ambiguous, done, nullptr, ws, ws_bytes, dev_status, stream);
+}
+
+extern "C" sv_status sv_verify_chunked_commit(
+    const sv_paged_kv* kv, const sv_batch* bt, const void* q, int32_t n_q_heads,
+    float softmax_scale, void* out, const float* target_logits, const float* draft_logits,
+    int32_t vocab, float temperature, uint64_t seed, int32_t chunk_size, int32_t* accepted_len,
+    int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
+    const sv_block_pool* pool, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (!kv || !bt || !pool) return SV_ERR_INVALID_ARGUMENT;
+  if (kv->block_size != kBlockSize) return SV_ERR_UNSUPPORTED_SHAPE;
+  if (kv->head_dim != 64 && kv->head_dim != 128) return SV_ERR_UNSUPPORTED_SHAPE;
+  if (kv->n_kv_heads < 1 || kv->num_blocks < 0 || kv->max_blocks_per_req < 0 ||
+      pool->capacity < 0)
+    return SV_ERR_INVALID_ARGUMENT;
+  if (bt->n_req > 0 && (!kv->k_cache || !kv->v_cache || !kv->block_tables || !kv->cache_lens ||
+                        !pool->free_list || !pool->free_count))
+    return SV_ERR_INVALID_ARGUMENT;
+  if (((uintptr_t)kv->k_cache | (uintptr_t)kv->v_cache) & 15) return SV_ERR_INVALID_ARGUMENT;
+  return verify_chunked(kv, bt, q, n_q_heads, softmax_scale, out, target_logits, draft_logits,
+                        vocab, temperature, seed, chunk_size, accepted_len, accepted_nodes,
+                        next_token, ambiguous, done, pool, ws, ws_bytes, dev_status, stream);
 }

@@ -4,8 +4,9 @@
 outputs and workspaces with torch, and enqueues the library calls of a step:
 
   onepass   sv_tree_attend -> sv_accept_commit (accept and KV commit fused)
-  chunked   sv_verify_chunked (windows -> attend -> accept per chunk, early
-            pruning) -> sv_commit_kv
+  chunked   sv_verify_chunked_commit (windows -> attend -> accept per chunk,
+            early pruning; each request's KV committed in the chunk that
+            stops it)
   budget    sv_select_budget -> sv_tree_attend -> sv_accept_commit,
             with the selected verify_len feeding the batch
 
@@ -100,6 +101,13 @@ class DeviceStep:
                               self.accepted_len, self.accepted_nodes, self.next_token,
                               self.ambiguous, self.done, self.ws, self.dev_status)
 
+    def chunked_commit(self):
+        api.sv_verify_chunked_commit(self.kv, self.batch, self.q, self.Hq, self.scale, self.out,
+                                     self.target, self.draft, self.V, self.T, self.w.seed,
+                                     self.chunk, self.accepted_len, self.accepted_nodes,
+                                     self.next_token, self.ambiguous, self.done, self.pool,
+                                     self.ws, self.dev_status)
+
     def select(self):
         api.sv_select_budget(self.cond, self.gamma, self.sps, self.verify_len, self.best_B,
                              self.best_theta, None, self.dev_status)
@@ -119,9 +127,10 @@ class DeviceStep:
             else:
                 self.accept()
         elif self.mode == "chunked":
-            self.chunked()
             if commit:
-                self.commit(self.batch)
+                self.chunked_commit()  # accept and commit fused into the chunks
+            else:
+                self.chunked()
         elif self.mode == "budget":
             self.select()
             self.attend(self.batch_sel)

@@ -72,6 +72,22 @@ def test_host_side_validation_without_gpu(lib):
     assert need > 0
     assert lib.sv_tree_attend(ctypes.byref(kv), ctypes.byref(b), 256, 8, 0.125, 256, 256, need - 1,
                               None, None) == N.SV_ERR_WORKSPACE_TOO_SMALL
+    # chunked step with the fused commit: the pool is required, and the
+    # commit's cache rules (16-token blocks, head_dim 64 / 128) hold
+    pool = N.SvBlockPool(256, 256, 4)
+    args = (256, 8, 0.125, 256, 256, None, 16, 0.0, 0, 2, 256, 256, 256, 256, 256)
+    assert lib.sv_verify_chunked_commit(ctypes.byref(kv), ctypes.byref(b), *args, None, 256, 1 << 20,
+                                        None, None) == N.SV_ERR_INVALID_ARGUMENT
+    kv96 = N.SvPagedKV(256, 256, 10, 16, 2, 96, 1, 4, 1)
+    assert lib.sv_verify_chunked_commit(ctypes.byref(kv96), ctypes.byref(b), *args,
+                                        ctypes.byref(pool), 256, 1 << 20, None,
+                                        None) == N.SV_ERR_UNSUPPORTED_SHAPE
+    # its workspace is the chunked step's, which also holds the commit's ticket
+    wsz = lib.sv_verify_chunked_workspace(ctypes.byref(b), ctypes.byref(kv), 8, 16)
+    assert wsz > 0
+    assert lib.sv_verify_chunked_commit(ctypes.byref(kv), ctypes.byref(b), *args,
+                                        ctypes.byref(pool), 256, wsz - 1, None,
+                                        None) == N.SV_ERR_WORKSPACE_TOO_SMALL
 
 
 def test_static_scratch_holds_the_documented_batch(lib):

@@ -365,6 +365,90 @@ def test_chunked_step_matches_oracle(T):
     assert torch.isnan(s.out[torch.from_numpy(~att).cuda()].float()).all()
 
 
+def _check_commit_against_oracle(s, w, st, vl=None, skip=()):
+    """The cache state after a fused commit == oracle commit of the oracle's
+    decisions (requests in `skip` are left as they were: the oracle is
+    given an invalid length for them)."""
+    kv = w.kv_copy()
+    fl = w.free_list.copy()
+    fc = np.array([w.free_count], dtype=np.int32)
+    nodes = np.where(st.accepted_nodes < 0, -1, st.accepted_nodes).astype(np.int32)
+    al = st.accepted_len.astype(np.int32).copy()
+    al[list(skip)] = -1
+    err = oracle.commit_kv(w.batch(verify_len=vl), kv, al, nodes, fl, fc)
+    assert err == (oracle.ORC_BAD_WINDOW if len(skip) else 0)
+    assert np.array_equal(s.kv.block_tables.cpu().numpy(), kv["block_tables"])
+    assert np.array_equal(s.kv.cache_lens.cpu().numpy(), kv["cache_lens"])
+    assert s.pool.free_count.item() == fc[0]
+    assert np.array_equal(s.pool.free_list.cpu().numpy()[: fc[0]], fl[: fc[0]])
+    assert np.array_equal(s.kv.k_cache.view(torch.int16).cpu().numpy().view(np.uint16), kv["k_cache"])
+    assert np.array_equal(s.kv.v_cache.view(torch.int16).cpu().numpy().view(np.uint16), kv["v_cache"])
+
+
+@pytest.mark.parametrize("name,T,chunk,kw", [
+    ("batch64", 0.7, 2, dict(n_req=48, ctx_scale=0.02, vocab=2048, draft_sigma=0.5)),
+    ("batch64", 0.0, 2, dict(n_req=48, ctx_scale=0.02, vocab=2048, draft_sigma=0.1)),
+    ("batch64", 0.7, 3, dict(n_req=40, ctx_scale=0.05, vocab=2048, draft_sigma=0.3)),
+    ("tree70b", 0.0, None, dict(ctx_scale=0.01, vocab=512, draft_sigma=0.05)),
+    ("tree70b", 1.0, None, dict(n_req=3, ctx_scale=0.01, vocab=2048, draft_sigma=0.3)),
+])
+def test_chunked_commit_fused_matches_oracle(name, T, chunk, kw):
+    # sv_verify_chunked_commit == oracle chunked verification followed by the
+    # oracle commit: decisions, attention of the attended rows, tables,
+    # lengths, the free list in order and every K/V byte.  Trees are taken
+    # whole by the first chunk (chunk = max rows), at T > 0 by the tree walk.
+    w = wl.make_workload(wl.config(name), temperature=T, **kw)
+    chunk = chunk or w.max_rows
+    s = DeviceStep(w, mode="chunked", chunk=chunk)
+    s.out.fill_(float("nan"))
+    s.run()
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st, _, ref64, attended = oracle.verify_chunked(
+        w.batch(), w.kv(), w.q, w.cfg.n_q_heads, w.softmax_scale, w.target_logits,
+        w.draft_logits if T > 0 else None, T, w.seed, chunk=chunk)
+    assert err == 0
+    _compare_accept(res, st, w, f"chunked commit {name} T={T} chunk={chunk}")
+    att = ~np.isnan(ref64[:, 0, 0])
+    assert int(att.sum()) == attended
+    _check_attention(s.out, ref64, np.nonzero(att)[0])
+    if name == "tree70b":
+        assert st.accepted_len.max() >= 2  # a path that moves slots
+    if (st.ambiguous != 0).any() or (res["ambiguous"] != 0).any():
+        pytest.skip("an ambiguous decision: the commit inputs differ by construction")
+    _check_commit_against_oracle(s, w, st)
+
+
+def test_chunked_commit_invalid_window_is_left_alone():
+    # one request with verify_len < 0: reported, never listed, never
+    # committed; every other request is committed and the release still runs
+    w = wl.make_workload(wl.config("batch64"), n_req=24, ctx_scale=0.02, vocab=1024,
+                         temperature=0.7, draft_sigma=0.5)
+    vl = np.diff(w.cu_rows).astype(np.int32) - 1
+    bad = 5
+    vl[bad] = -1
+    s = DeviceStep(w, mode="chunked")
+    b = api.Batch(s.batch.cu_rows, s.batch.parent, s.batch.tokens, w.max_rows,
+                  verify_len=torch.from_numpy(vl).cuda())
+    api.sv_verify_chunked_commit(s.kv, b, s.q, s.Hq, s.scale, s.out, s.target, s.draft, s.V, s.T,
+                                 w.seed, 2, s.accepted_len, s.accepted_nodes, s.next_token,
+                                 s.ambiguous, s.done, s.pool, s.ws, s.dev_status)
+    res = s.results()
+    assert res["dev_status"] & api.N.SV_DEV_BAD_WINDOW
+    err, st, _, _, _ = oracle.verify_chunked(
+        w.batch(verify_len=vl), w.kv(), w.q, w.cfg.n_q_heads, w.softmax_scale, w.target_logits,
+        w.draft_logits, 0.7, w.seed, chunk=2)
+    assert err & oracle.ORC_BAD_WINDOW
+    keep = np.arange(w.n_req) != bad
+    amb = (st.ambiguous != 0) | (res["ambiguous"] != 0)
+    ok = keep & ~amb
+    assert np.array_equal(res["accepted_len"][ok], st.accepted_len[ok])
+    assert np.array_equal(res["next_token"][ok], st.next_token[ok])
+    if amb.any():
+        pytest.skip("an ambiguous decision: the commit inputs differ by construction")
+    _check_commit_against_oracle(s, w, st, vl=vl, skip=(bad,))
+
+
 def test_budget_step_matches_oracle():
     w = wl.make_workload(wl.config("batch256"), ctx_scale=0.02, vocab=2048)
     s = DeviceStep(w, mode="budget")
@@ -589,13 +673,13 @@ def batch64_full():
 
 def test_batch64_full_size_chunked_step(batch64_full):
     """The bench workload at full size, run as the bench runs it (chunked,
-    with commit): every accept output against the oracle, attention on a
-    sample of requests."""
+    with the commit fused into the chunks): every accept output against the
+    oracle, attention on a sample of requests, the new cache lengths."""
     w = batch64_full
     s = DeviceStep(w)
     assert s.mode == "chunked"
     s.out.fill_(float("nan"))
-    s.run(commit=False)
+    s.run()
     res = s.results()
     assert res["dev_status"] == 0
     err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits, w.cfg.temperature, w.seed)
@@ -611,9 +695,6 @@ def test_batch64_full_size_chunked_step(batch64_full):
                                        row_begin=rb, row_end=re)
     att = ~np.isnan(ref64[:, 0, 0])
     _check_attention(s.out, ref64, np.nonzero(att)[0])
-    # and the commit that follows
-    s.commit()
-    torch.cuda.synchronize()
-    assert s.dev_status.item() == 0
+    # and the commit fused into the step
     new_lens = s.kv.cache_lens.cpu().numpy()
     assert np.array_equal(new_lens, w.cache_lens + 1 + res["accepted_len"])
