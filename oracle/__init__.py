@@ -57,6 +57,8 @@ def _load():
         lib.orc_accept_uniform.restype = ctypes.c_double
         lib.orc_race_uniform.argtypes = [U64, I, I, I]
         lib.orc_race_uniform.restype = ctypes.c_double
+        lib.orc_pick_uniform.argtypes = [U64, I, I, I]
+        lib.orc_pick_uniform.restype = ctypes.c_double
         lib.orc_tree_attend.argtypes = [I, P, P, P, P, P, P, P, I, I, I, I, P, I, P, P, I, F, P, P, I]
         lib.orc_tree_attend.restype = I
         lib.orc_accept.argtypes = [I, P, P, P, P, P, P, P, P, I, F, U64, P, P, I, P, P, P, P, I]
@@ -105,8 +107,14 @@ def accept_uniform(seed: int, i: int, j: int) -> float:
     return _load().orc_accept_uniform(seed, i, j)
 
 
-def race_uniform(seed: int, i: int, pos: int, v: int) -> float:
-    return _load().orc_race_uniform(seed, i, pos, v)
+def race_uniform(seed: int, i: int, pos: int, g: int) -> float:
+    """The race uniform of group g (entries 4g .. 4g+3)."""
+    return _load().orc_race_uniform(seed, i, pos, g)
+
+
+def pick_uniform(seed: int, i: int, pos: int, g: int) -> float:
+    """The uniform that picks the entry inside the winning group g."""
+    return _load().orc_pick_uniform(seed, i, pos, g)
 
 
 # --------------------------------------------------------------- attention --

@@ -119,15 +119,28 @@ double accept_uniform(uint64_t seed, int i, int j) {
   return (double)(out[0] >> 8) * (1.0 / 16777216.0);
 }
 
-// Uniform in (0, 1) for vocabulary entry v of the sampling race that emits the
-// token at position pos of request i: counter (v/4, i, 1, pos), word v%4, top
-// 23 bits plus one half -> (0, 1), exact in fp32 as well as fp64.
-double race_uniform(uint64_t seed, int i, int pos, int v) {
-  uint32_t ctr[4] = {(uint32_t)(v >> 2), (uint32_t)i, 1u, (uint32_t)pos};
+// Uniform in (0, 1) for group g (vocabulary entries 4g .. 4g+3) of the
+// sampling race that emits the token at position pos of request i.  Groups
+// are numbered in blocks of 128: group g = 128 b + 32 k + l takes word k of
+// counter (32 b + l, i, 1, pos).  Top 23 bits plus one half -> (0, 1), exact
+// in fp32 as well as fp64.
+double race_uniform(uint64_t seed, int i, int pos, int g) {
+  const uint32_t b = (uint32_t)g >> 7, k = ((uint32_t)g >> 5) & 3u, l = (uint32_t)g & 31u;
+  uint32_t ctr[4] = {32u * b + l, (uint32_t)i, 1u, (uint32_t)pos};
   uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
   uint32_t out[4];
   philox4x32_10(ctr, key, out);
-  return ((double)(out[v & 3] >> 9) + 0.5) * (1.0 / 8388608.0);
+  return ((double)(out[k] >> 9) + 0.5) * (1.0 / 8388608.0);
+}
+
+// Uniform in (0, 1) that picks the entry inside the race's winning group g:
+// word 0 of counter (g, i, 2, pos), same conversion.
+double pick_uniform(uint64_t seed, int i, int pos, int g) {
+  uint32_t ctr[4] = {(uint32_t)g, (uint32_t)i, 2u, (uint32_t)pos};
+  uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  philox4x32_10(ctr, key, out);
+  return ((double)(out[0] >> 9) + 0.5) * (1.0 / 8388608.0);
 }
 
 // ------------------------------------------------------------ windows ----
@@ -187,7 +200,8 @@ void orc_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* out) 
   philox4x32_10(ctr, key, out);
 }
 double orc_accept_uniform(uint64_t seed, int i, int j) { return accept_uniform(seed, i, j); }
-double orc_race_uniform(uint64_t seed, int i, int pos, int v) { return race_uniform(seed, i, pos, v); }
+double orc_race_uniform(uint64_t seed, int i, int pos, int g) { return race_uniform(seed, i, pos, g); }
+double orc_pick_uniform(uint64_t seed, int i, int pos, int g) { return pick_uniform(seed, i, pos, g); }
 
 // -------------------------------------------------------- attention (a2) --
 // For every row r of every request inside its window and every query head h:
@@ -331,55 +345,82 @@ int row_argmax(const float* l, int V) {
 // ------------------------------------------------ residual / bonus (a5) --
 // Draw one token from normalize(w) with w_v = max(0, p_v - c q_v) (residual:
 // c = 1 after one rejection, larger after several rejections among tree
-// siblings) or w_v = p_v (bonus, all drafts accepted), as the
-// winner of an exponential race: token = argmax_v w_v / E_v with
-// E_v = -log(U_v), U_v ~ U(0,1) independent.  P(v wins) = w_v / sum w, so
-// this is an exact sample of normalize(w) (the race form of the Gumbel-max
-// trick); ties go to the lowest index.
+// siblings) or w_v = p_v (bonus, all drafts accepted), in two steps:
+//   1. a race among groups of four entries: group g (entries 4g .. 4g+3, the
+//      last one possibly shorter) has weight W_g = sum of its w_v and key
+//      W_g / E_g with E_g = -log(U_g), U_g ~ U(0,1) independent; the group
+//      with the largest key wins (lowest g on ties).  P(g wins) = W_g / sum W
+//      (the race form of the Gumbel-max trick, over groups);
+//   2. inside the winning group, with u ~ U(0,1): the first entry whose
+//      running sum of w (in index order) exceeds u W_g.
+// P(v) = W_g / sum W * w_v / W_g = w_v / sum w: an exact sample of
+// normalize(w).
 //
-// The race is also checked for closeness: if a device computing p and q in
-// fp32 (relative error at most RACE_EPS per term) could pick another winner,
-// the decision is flagged ambiguous.
+// Both steps are also checked for closeness: if a device computing p and q in
+// fp32 (relative error at most RACE_EPS per term) could pick another group,
+// or land on the other side of a running-sum boundary, the decision is
+// flagged ambiguous.
 const double RACE_EPS = 2e-6;
 
 int race_sample(const float* lp, const float* lq, int V, float T, const RowSoftmax& sp,
                 const RowSoftmax* sq, uint64_t seed, int i, int pos, bool* ambiguous,
                 double c = 1.0) {
-  std::vector<double> w(V), lo(V), hi(V);
+  std::vector<double> w(V), err(V);
   double W = 0.0;
   for (int v = 0; v < V; ++v) {
     double p = prob(lp, v, T, sp);
     double q = sq ? c * prob(lq, v, T, *sq) : 0.0;
-    double wv = sq ? std::max(0.0, p - q) : p;
-    w[v] = wv;
-    W += wv;
-    lo[v] = std::max(0.0, wv - RACE_EPS * (p + q));
-    hi[v] = wv + RACE_EPS * (p + q);
+    w[v] = sq ? std::max(0.0, p - q) : p;
+    err[v] = RACE_EPS * (p + q);
+    W += w[v];
   }
   if (W <= 0.0) {  // p == q everywhere: normalize(max(0, p-q)) is undefined; use p
     for (int v = 0; v < V; ++v) {
       double p = prob(lp, v, T, sp);
       w[v] = p;
-      lo[v] = p * (1.0 - RACE_EPS);
-      hi[v] = p * (1.0 + RACE_EPS);
+      err[v] = RACE_EPS * p;
     }
+  }
+  // 1. the race among groups
+  const int G = (V + 3) / 4;
+  std::vector<double> Wg(G, 0.0), Eg(G), eg(G, 0.0);
+  for (int g = 0; g < G; ++g) {
+    for (int v = 4 * g; v < std::min(V, 4 * g + 4); ++v) {
+      Wg[g] += w[v];
+      eg[g] += err[v];
+    }
+    Eg[g] = -std::log(race_uniform(seed, i, pos, g));
   }
   int best = -1;
   double best_key = -1.0;
-  std::vector<double> E(V);
-  for (int v = 0; v < V; ++v) {
-    E[v] = -std::log(race_uniform(seed, i, pos, v));
-    double key = w[v] / E[v];
-    if (key > best_key) { best_key = key; best = v; }
+  for (int g = 0; g < G; ++g) {
+    double key = Wg[g] / Eg[g];
+    if (key > best_key) { best_key = key; best = g; }
   }
-  // Closeness: smallest plausible winner key against the largest plausible
-  // key of every other entry.
-  double win_lo = lo[best] / E[best] * (1.0 - RACE_EPS);
-  for (int v = 0; v < V; ++v) {
-    if (v == best) continue;
-    if (hi[v] / E[v] * (1.0 + RACE_EPS) >= win_lo) { *ambiguous = true; break; }
+  const double win_lo = std::max(0.0, Wg[best] - eg[best]) / Eg[best] * (1.0 - RACE_EPS);
+  for (int g = 0; g < G; ++g) {
+    if (g == best) continue;
+    if ((Wg[g] + eg[g]) / Eg[g] * (1.0 + RACE_EPS) >= win_lo) { *ambiguous = true; break; }
   }
-  return best;
+  // 2. the entry inside the winning group
+  const int v0 = 4 * best, v1 = std::min(V, v0 + 4);
+  const double t = pick_uniform(seed, i, pos, best) * Wg[best];
+  int pick = -1;
+  double S = 0.0;
+  for (int v = v0; v < v1; ++v) {
+    S += w[v];
+    if (t < S) { pick = v; break; }
+  }
+  if (pick < 0)  // t at the very top of the group's range: its last positive entry
+    for (int v = v0; v < v1; ++v)
+      if (w[v] > 0.0) pick = v;
+  const double tol = 2.0 * (eg[best] + RACE_EPS * Wg[best]);
+  S = 0.0;
+  for (int v = v0; v + 1 < v1; ++v) {
+    S += w[v];
+    if (std::fabs(t - S) <= tol) *ambiguous = true;
+  }
+  return pick;
 }
 
 struct AcceptArgs {

@@ -24,13 +24,19 @@
 //                    writes the path and, for T > 0, a sampling job for the
 //                    emitted token.
 //   race   (warps, grid-stride over request x vocabulary slice)
-//                    the exponential race argmax_v w_v / E_v over the job's
-//                    row(s), w = max(0, p - q) after a rejection or p for the
-//                    bonus token; the warp that brings a request's last
-//                    slice (atomic ticket) reduces the slice winners.  A
-//                    chunked step runs it once, after its last chunk.
+//                    the residual / bonus token, w = max(0, p - q) after a
+//                    rejection or p for the bonus token: an exponential race
+//                    among groups of four entries, then the entry inside the
+//                    winning group; each warp streams its slice of target
+//                    logits through a shared-memory ring (bulk copies) and
+//                    prunes groups that cannot win; the warp that brings a
+//                    request's last slice (atomic ticket) reduces the slice
+//                    winners and picks the entry.  A chunked step runs it
+//                    once, after its last chunk.
 
 #include <math.h>
+
+#include <mutex>
 
 #include "sv_accept_internal.h"
 #include "sv_internal.cuh"
@@ -89,7 +95,8 @@ Layout layout(int R, int total_rows, int V, int maxw, bool commit) {
   L.parts = off; off += align256(sizeof(StatPart) * (size_t)total_rows * 2 * L.nch_cap);
   L.jobs = off; off += align256(sizeof(Job) * (size_t)R);
   L.race = off; off += align256(sizeof(RacePart) * (size_t)R * L.nch_r_cap);
-  L.race_tickets = off; off += align256(sizeof(int) * (size_t)R);
+  // per request: the race ticket, then the best key any warp has found (bits)
+  L.race_tickets = off; off += align256(sizeof(int) * 2 * (size_t)R);
   L.act = off; off += align256(sizeof(int) * (size_t)(R + 1));  // act[R] = count
   L.ctick = L.cspan = 0;
   if (commit) {
@@ -112,10 +119,13 @@ __device__ __forceinline__ int stats_slices(const Layout& L, int count, int ntyp
   const long want = (per_warp * kNumSMs * 32 + slots - 1) / slots;
   return (int)max((long)L.nch, min(want, (long)L.nch_cap));
 }
+// Race slices: at most one per warp of the race grid (24 warps per SM), so
+// that no warp takes two slices one after the other; slices of >= 2 KB.
+constexpr int kRaceWarpsPerSM = 24;
 __device__ __forceinline__ int race_slices(const Layout& L, int count, int V) {
-  const long want = (2L * kNumSMs * 32 + max(1, count) - 1) / max(1, count);
-  const long cap = min((long)L.nch_r_cap, max(1L, (long)V / 2048));  // slices of >= 8 KB
-  return (int)max((long)L.nch_r, min(want, cap));
+  const long want = (long)kNumSMs * kRaceWarpsPerSM / max(1, count);
+  const long cap = min((long)L.nch_r_cap, max(1L, (long)V / 512));
+  return (int)max(1L, min(want, cap));
 }
 
 // The paged cache and block pool a fused accept + commit updates.
@@ -250,6 +260,7 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
     // Only jobs created by this call may reach the race kernel.
     job->mode = 0;
     reinterpret_cast<int*>(a.ws + a.L.race_tickets)[i] = 0;
+    reinterpret_cast<int*>(a.ws + a.L.race_tickets)[a.bt.n_req + i] = 0;
   }
   const Window w = window_of(a.bt, i);
   if (!a.use_list && !live(a, w, i)) {
@@ -499,6 +510,7 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < R; i += gridDim.x * blockDim.x) {
       reinterpret_cast<Job*>(a.ws + a.L.jobs)[i].mode = 0;
       reinterpret_cast<int*>(a.ws + a.L.race_tickets)[i] = 0;
+      reinterpret_cast<int*>(a.ws + a.L.race_tickets)[R + i] = 0;
     }
   }
   const bool listed = a.use_list != 0;
@@ -962,9 +974,21 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
 }
 
 // ------------------------------------------------------------------ race --
+// The residual / bonus token in two steps, both exact ([DSpark] glossary: the
+// target distribution is preserved):
+//   1. a race among groups of four entries: group g has weight W_g, the sum
+//      of its entries' w = max(0, p - c q) (residual) or p (bonus), and key
+//      W_g / E_g with E_g = -log(U_g); the largest key wins, lowest g on
+//      ties, so P(g) = W_g / sum W;
+//   2. inside the winning group, with u from pick_u: the first entry whose
+//      running sum of w (index order) exceeds u W_g, so P(v | g) = w_v / W_g.
+// One uniform per group (one generator call per lane per 16 entries) instead
+// of one per entry.
 __device__ __forceinline__ void race_take(float& best, int& bi, float key, int v) {
   if (key > best || (key == best && v < bi)) { best = key; bi = v; }
 }
+
+constexpr int kRaceBlock = 512;  // entries of 128 groups: one counter per lane
 
 // Constants of one race job for its weights w = p (bonus) or max(0, p - c q).
 struct RaceW {
@@ -979,42 +1003,76 @@ __device__ __forceinline__ float race_q(const RaceW& r, float l) {
   const float x = r.unit ? l : div_by(l, r.T, r.rT);
   return ex2(fmaf(x, kLog2e, -r.mqb)) * r.cq;
 }
-// Running best (w, E) of a lane: v beats it iff w_v E_b > w_b E_v, lower
-// index on ties.
-__device__ __forceinline__ void race_keep(float wv, float E, int v, float& bw, float& bE, int& bi) {
-  const float lhs = wv * bE, rhs = bw * E;
-  if (lhs > rhs || (lhs == rhs && v < bi)) {
-    bw = wv;
+// p of the n valid entries of a group (the rest 0), and the weights w.
+__device__ __forceinline__ float4 group_p(const RaceW& r, float4 x, int n) {
+  return make_float4(n > 0 ? race_p(r, x.x) : 0.f, n > 1 ? race_p(r, x.y) : 0.f,
+                     n > 2 ? race_p(r, x.z) : 0.f, n > 3 ? race_p(r, x.w) : 0.f);
+}
+__device__ __forceinline__ float4 group_w(const RaceW& r, float4 p, float4 xq, int n) {
+  if (!r.resid) return p;
+  return make_float4(n > 0 ? fmaxf(p.x - race_q(r, xq.x), 0.f) : 0.f,
+                     n > 1 ? fmaxf(p.y - race_q(r, xq.y), 0.f) : 0.f,
+                     n > 2 ? fmaxf(p.z - race_q(r, xq.z), 0.f) : 0.f,
+                     n > 3 ? fmaxf(p.w - race_q(r, xq.w), 0.f) : 0.f);
+}
+__device__ __forceinline__ float sum4(float4 w) { return ((w.x + w.y) + w.z) + w.w; }
+
+// Running best (W, E) of a lane: group g beats it iff W_g E_b > W_b E_g,
+// lower index on ties.
+__device__ __forceinline__ void race_keep(float wg, float E, int g, float& bw, float& bE, int& bi) {
+  const float lhs = wg * bE, rhs = bw * E;
+  if (lhs > rhs || (lhs == rhs && g < bi)) {
+    bw = wg;
     bE = E;
-    bi = v;
+    bi = g;
   }
 }
-// One entry: its uniform first; p < Km (1 - u) rules it out (see the kernel).
-__device__ __forceinline__ void race_entry(const RaceW& r, float lpv, float lqv, uint32_t bits,
-                                           int v, float Km, float& bw, float& bE, int& bi) {
-  const float u = race_u(bits);
-  const float p = race_p(r, lpv);
-  if (p < Km * (1.f - u)) return;
-  const float wv = r.resid ? fmaxf(p - race_q(r, lqv), 0.f) : p;
-  race_keep(wv, -logf(u), v, bw, bE, bi);
-}
 
-// Warp-granular like the statistics: a warp scans one slice of a request's
-// row(s) and arrives on the request's ticket; the last one reduces.
+// Shared-memory ring of the vectorised race: per warp kRaceStages blocks in
+// flight, each the block's target logits then (residual jobs) its draft
+// logits, 2 KB apiece, filled by bulk copies.
+constexpr int kRaceStages = 2;
+constexpr int kRaceWarps = kRaceThreads / 32;
+constexpr int kRaceStageFloats = 2 * kRaceBlock;
+constexpr size_t kRaceSmem =
+    (size_t)kRaceWarps * kRaceStages * (kRaceStageFloats * sizeof(float) + sizeof(uint64_t));
+
+// Warp-granular like the statistics: a warp scans one slice (whole blocks of
+// 128 groups) of a request's row(s) and arrives on the request's ticket; the
+// last one reduces and picks the entry.  With VEC the warp's logits stream
+// through its ring, kRaceStages - 1 blocks ahead of their use, so that no
+// step waits on a global load; else they are plain loads.
 template <bool VEC>
-__global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
+__global__ void __launch_bounds__(kRaceThreads, 3) race_kernel(Args a) {
   griddep_entry();
+  extern __shared__ __align__(128) uint8_t s_race[];
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   const int R = a.bt.n_req;
   const int count = a.race_all ? R : n_slots(a, act);
-  const int nch = race_slices(a.L, count, a.V);
-  const int chl = chunk_len(a.V, nch);
+  const int V = a.V;
+  int nch = race_slices(a.L, count, V);
+  const int chl = (V + nch - 1) / nch + kRaceBlock - 1 - ((V + nch - 1) / nch + kRaceBlock - 1) % kRaceBlock;
+  nch = (V + chl - 1) / chl;
   const long total = (long)count * nch;
   const float T = a.T;
   const float rT = 1.f / T;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const long stride = (long)gridDim.x * (kRaceThreads / 32);
-  for (long item = (long)blockIdx.x * (kRaceThreads / 32) + wid; item < total; item += stride) {
+  // this warp's ring: stage buffers, then their barriers
+  float* ring = reinterpret_cast<float*>(s_race) + (size_t)wid * kRaceStages * kRaceStageFloats;
+  const uint32_t bar0 =
+      smem_u32(s_race + (size_t)kRaceWarps * kRaceStages * kRaceStageFloats * 4) +
+      (uint32_t)(wid * kRaceStages * 8);
+  if (VEC) {
+    if (lane == 0)
+      for (int st = 0; st < kRaceStages; ++st) mbar_init(bar0 + 8 * st, 1);
+    fence_mbar_init();
+    __syncwarp();
+  }
+  uint32_t issued = 0, used = 0;  // blocks this warp has requested / consumed
+  bool timed_out = false;
+  const long stride = (long)gridDim.x * kRaceWarps;
+  for (long item = (long)blockIdx.x * kRaceWarps + wid; item < total && !timed_out;
+       item += stride) {
     const int c = (int)(item % nch);
     const int i = a.race_all ? (int)(item / nch) : req_of(a, act, (int)(item / nch));
     // decide_request cleared every request's job before it could
@@ -1024,78 +1082,159 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
     const Job jb = reinterpret_cast<const Job*>(a.ws + a.L.jobs)[i];
     if (jb.mode != 1 && jb.mode != 2) continue;
     const bool resid = jb.mode == 1;
-    const float* lp = a.target + (size_t)jb.row * a.V;
-    const float* lq = a.draft + (size_t)jb.row * a.V;
-    const float inv_lp = 1.f / jb.lp, inv_lq = 1.f / jb.lq;
-    const float mpb = jb.mp * kLog2e, mqb = jb.mq * kLog2e;
+    const float* lp = a.target + (size_t)jb.row * V;
+    const float* lq = a.draft + (size_t)jb.row * V;
+    const float inv_lq = 1.f / jb.lq;
+    const RaceW rw{T, rT, jb.mp * kLog2e, 1.f / jb.lp, jb.mq * kLog2e, jb.c * inv_lq, T == 1.f,
+                   resid};
     const int lo = c * chl;
-    const int hi = min(a.V, lo + chl);
-    // Running best of this lane as (w, E): v beats it iff w_v E_b > w_b E_v.
-    // E_v >= kEmin for every uniform the generator can produce, so an entry
-    // with w_v < w_b / E_b * kEmin can never win: groups of four such entries
-    // skip the generator and the logarithm.
-    const float kEmin = 5.9e-8f;  // -log(1 - 2^-24) = 5.96e-8, rounded down
-    float bw = -1.f, bE = 1.f, thr = -1.f;
-    int bi = 0x7fffffff;
-    auto take = [&](float wv, float E, int v) {
-      const float lhs = wv * bE, rhs = bw * E;
-      if (lhs > rhs || (lhs == rhs && v < bi)) {
-        bw = wv;
-        bE = E;
-        bi = v;
-        thr = wv / E * kEmin;
-      }
-    };
-    const float cq = jb.c * inv_lq;
-    auto weight = [&](float lpv, float lqv) {
-      const float p = ex2(fmaf(div_by(lpv, T, rT), kLog2e, -mpb)) * inv_lp;
-      if (!resid) return p;
-      return fmaxf(p - ex2(fmaf(div_by(lqv, T, rT), kLog2e, -mqb)) * cq, 0.f);
+    const int hi = min(V, lo + chl);
+    const int nb = (hi - lo + kRaceBlock - 1) / kRaceBlock;
+    // Request block b of the slice into the ring (lane 0).
+    auto request = [&](int b) {
+      const int st = (int)(issued % kRaceStages);
+      const int base = lo + b * kRaceBlock;
+      const uint32_t bytes = (uint32_t)(min(hi, base + kRaceBlock) - base) * 4u;
+      float* dst = ring + st * kRaceStageFloats;
+      mbar_arrive_expect_tx(bar0 + 8 * st, resid ? 2u * bytes : bytes);
+      bulk_load(smem_u32(dst), lp + base, bytes, bar0 + 8 * st);
+      if (resid) bulk_load(smem_u32(dst + kRaceBlock), lq + base, bytes, bar0 + 8 * st);
     };
     if (VEC) {
-      // Four 128-entry groups per iteration, their loads issued first.  The
-      // trip count is uniform so that the lanes can share the best key K any
-      // of them has seen; the winner's key is at least K.  Every entry draws
-      // its uniform first: since E = -log u >= 1 - u, an entry whose target
-      // probability p is below K (1 - u) (less a 2^-20 margin for rounding)
-      // has w / E <= p / E < K and cannot win -- its draft probability, its
-      // weight and its logarithm are never computed.  Only the rest go to
-      // the exact comparison.
-      constexpr int kGroups = 2;
-      const RaceW rw{T, rT, mpb, inv_lp, mqb, jb.c * inv_lq, T == 1.f, resid};
-      float K = 0.f;
-      const float4* p4 = reinterpret_cast<const float4*>(lp);
-      const float4* q4 = reinterpret_cast<const float4*>(lq);
-      for (int base = lo; base < hi; base += 128 * kGroups) {
-        K = fmaxf(K, warp_max(bi == 0x7fffffff ? 0.f : bw / bE));
-        const float Km = K * (1.f - 0x1p-20f);
-        float4 xp[kGroups], xq[kGroups];
+      if (lane == 0)
+        for (int b = 0; b < min(nb, kRaceStages); ++b, ++issued) request(b);
+      __syncwarp();
+      issued = __shfl_sync(0xffffffffu, issued, 0);
+    }
+    // valid entries of group k of the block at `base` (with VEC the vocabulary
+    // is a multiple of 4: a group is whole or absent)
+    auto nof = [&](int base, int k) {
+      const int v = base + 128 * k + 4 * lane;
+      return VEC ? (v < hi ? 4 : 0) : max(0, min(4, hi - v));
+    };
+    // Running best of this lane as (W, E).  K bounds the winner's key from
+    // below: the best key this warp has seen, or any other warp of the
+    // request (published in kbest, an atomic max on the bits of a
+    // non-negative float, read one block ahead of its use), taken with a fast
+    // division whose error the 2^-20 margin below covers.  W_g <= P_g (the
+    // group's target mass) <= B_g = 4 p(max logit of the group) (p is
+    // monotone in the logit; the factor 1 + 2^-16 covers the rounding of p
+    // and of the sum), and E_g >= 1 - u_g, so a group with B_g < K (1 - u_g)
+    // (less a 2^-20 margin) cannot win: its exact mass, draft probabilities
+    // and logarithm are never computed.  While K is 0 (the first block) every
+    // group is keyed exactly.  The trip count is uniform across the warp so
+    // that the lanes can share K.
+    int* kbest = reinterpret_cast<int*>(a.ws + a.L.race_tickets) + R + i;
+    float bw = -1.f, bE = 1.f, K = 0.f;
+    int bi = 0x7fffffff;
+    int kg_bits = 0;
+    for (int b = 0; b < nb; ++b) {
+      const int base = lo + b * kRaceBlock;
+      const int st = (int)(used % kRaceStages);
+      const float4* r4 = reinterpret_cast<const float4*>(ring + st * kRaceStageFloats);
+      float4 xp[4];
+      if (VEC) {
+        if (!mbar_wait_sleep_bounded(bar0 + 8 * st, (used / kRaceStages) & 1u)) timed_out = true;
+        timed_out = __any_sync(0xffffffffu, timed_out);
+        if (timed_out) break;  // the block stays counted as in flight
 #pragma unroll
-        for (int k = 0; k < kGroups; ++k) {
-          const int v = base + 128 * k + 4 * lane;
-          xp[k] = v < hi ? __ldcs(p4 + (v >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          xq[k] = (resid && v < hi) ? __ldcs(q4 + (v >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int k = 0; k < 4; ++k) xp[k] = r4[32 * k + lane];
+      } else {
 #pragma unroll
-        for (int k = 0; k < kGroups; ++k) {
+        for (int k = 0; k < 4; ++k) {
           const int v = base + 128 * k + 4 * lane;
-          if (v >= hi) continue;
-          const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
-          race_entry(rw, xp[k].x, xq[k].x, bits.a, v, Km, bw, bE, bi);
-          race_entry(rw, xp[k].y, xq[k].y, bits.b, v + 1, Km, bw, bE, bi);
-          race_entry(rw, xp[k].z, xq[k].z, bits.c, v + 2, Km, bw, bE, bi);
-          race_entry(rw, xp[k].w, xq[k].w, bits.d, v + 3, Km, bw, bE, bi);
+          const int nk = nof(base, k);
+          xp[k] = make_float4(nk > 0 ? lp[v] : -INFINITY, nk > 1 ? lp[v + 1] : -INFINITY,
+                              nk > 2 ? lp[v + 2] : -INFINITY, nk > 3 ? lp[v + 3] : -INFINITY);
         }
       }
-    } else {
-      for (int v = lo + lane; v < hi; v += 32) {
-        const float wv = weight(lp[v], resid ? lq[v] : 0.f);
-        if (wv < thr) continue;
-        const U4 bits = race_bits(a.seed, i, jb.pos, v >> 2);
-        const uint32_t bw4 = (v & 3) == 0 ? bits.a : (v & 3) == 1 ? bits.b : (v & 3) == 2 ? bits.c : bits.d;
-        take(wv, -logf(race_u(bw4)), v);
+      if (b > 0) {
+        // (one value for the whole warp: K decides warp-wide branches below)
+        const float kg = __shfl_sync(0xffffffffu, __int_as_float(kg_bits), 0);
+        const float mine = warp_max(bi == 0x7fffffff ? 0.f : __fdividef(bw, bE));
+        if (lane == 0 && mine > kg) atomicMax(kbest, __float_as_int(mine));
+        K = fmaxf(K, fmaxf(kg, mine));
+        if (lane == 0) kg_bits = __ldcg(kbest);
+      }
+      const U4 bits = race_bits(a.seed, i, jb.pos, (base / kRaceBlock) * 32 + lane);
+      const uint32_t wd[4] = {bits.a, bits.b, bits.c, bits.d};
+      float Bk[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float mx = fmaxf(fmaxf(xp[k].x, xp[k].y), fmaxf(xp[k].z, xp[k].w));
+        Bk[k] = nof(base, k) > 0 ? race_p(rw, mx) * (4.f * (1.f + 0x1p-16f)) : 0.f;
+      }
+      // Exact key of group k of this lane (all lanes at once).
+      auto key_exact = [&](int k) {
+        const int nk = nof(base, k);
+        float4 xk, xq = make_float4(0.f, 0.f, 0.f, 0.f);
+        uint32_t wk = wd[0];
+#pragma unroll
+        for (int t = 1; t < 4; ++t)
+          if (k == t) wk = wd[t];
+        if (VEC) {
+          xk = r4[32 * k + lane];
+          if (resid) xq = r4[kRaceBlock / 4 + 32 * k + lane];
+        } else {
+          const int v = base + 128 * k + 4 * lane;
+          xk = make_float4(lp[v], nk > 1 ? lp[v + 1] : 0.f, nk > 2 ? lp[v + 2] : 0.f,
+                           nk > 3 ? lp[v + 3] : 0.f);
+          if (resid)
+            xq = make_float4(lq[v], nk > 1 ? lq[v + 1] : 0.f, nk > 2 ? lq[v + 2] : 0.f,
+                             nk > 3 ? lq[v + 3] : 0.f);
+        }
+        const float4 pk = group_p(rw, xk, nk);
+        const float Wg = resid ? sum4(group_w(rw, pk, xq, nk)) : sum4(pk);
+        race_keep(Wg, -logf(race_u(wk)), base / 4 + 32 * k + lane, bw, bE, bi);
+      };
+      unsigned todo = 0;  // groups of this lane still to key exactly
+      if (K == 0.f) {
+        // Start (the first block): each lane keys its group with the largest
+        // bound B_g / (1 - u_g); the best of those keys bounds the rest.
+        float ub = -1.f;
+        int kk = -1;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float c = nof(base, k) > 0 ? __fdividef(Bk[k], 1.f - race_u(wd[k])) : -1.f;
+          if (c > ub) { ub = c; kk = k; }
+        }
+        if (kk >= 0) key_exact(kk);
+        K = warp_max(bi == 0x7fffffff ? 0.f : __fdividef(bw, bE));
+        const float Km = K * (1.f - 0x1p-20f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (k != kk && nof(base, k) > 0 && !(Bk[k] < Km * (1.f - race_u(wd[k]))))
+            todo |= 1u << k;
+      } else {
+        const float Km = K * (1.f - 0x1p-20f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (nof(base, k) > 0 && !(Bk[k] < Km * (1.f - race_u(wd[k])))) todo |= 1u << k;
+      }
+      // Usually no group of the warp is left: a warp-wide test, so that the
+      // exact path is not issued at all then; else the lanes key their
+      // remaining groups side by side.
+      while (__any_sync(0xffffffffu, todo != 0)) {
+        if (todo) {
+          const int k = __ffs(todo) - 1;
+          todo &= todo - 1;
+          key_exact(k);
+        }
+      }
+      if (VEC) {
+        // the stage is read: refill it with block b + kRaceStages
+        ++used;
+        __syncwarp();
+        if (b + kRaceStages < nb) {
+          if (lane == 0) {
+            fence_proxy_async_smem();
+            request(b + kRaceStages);
+          }
+          ++issued;
+        }
       }
     }
+    if (timed_out) break;
     float best = bi == 0x7fffffff ? -1.f : bw / bE;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -1114,22 +1253,47 @@ __global__ void __launch_bounds__(kRaceThreads, 4) race_kernel(Args a) {
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
-      // last slice of request i: reduce the slice winners
+      // last slice of request i: the winning group, then its entry
       __threadfence();
-      float b = -1.f;
-      int x = 0x7fffffff;
-      for (int k = lane; k < nch; k += 32) race_take(b, x, __ldcg(&parts[k].key), __ldcg(&parts[k].idx));
+      float bk = -1.f;
+      int g = 0x7fffffff;
+      for (int k = lane; k < nch; k += 32) race_take(bk, g, __ldcg(&parts[k].key), __ldcg(&parts[k].idx));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        const float b2 = __shfl_xor_sync(0xffffffffu, b, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, x, o);
-        race_take(b, x, b2, i2);
+        const float b2 = __shfl_xor_sync(0xffffffffu, bk, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, g, o);
+        race_take(bk, g, b2, i2);
       }
-      if (lane == 0) {
-        a.next_token[i] = x;
+      const bool found = g >= 0 && g < (V + 3) / 4;  // every non-empty slice finds one
+      const int v0 = found ? 4 * g : 0;
+      const int n = found ? min(4, V - v0) : 0;
+      if (lane == 0 && n > 0) {
+        const float4 xp = make_float4(lp[v0], n > 1 ? lp[v0 + 1] : 0.f, n > 2 ? lp[v0 + 2] : 0.f,
+                                      n > 3 ? lp[v0 + 3] : 0.f);
+        float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (resid)
+          xq = make_float4(lq[v0], n > 1 ? lq[v0 + 1] : 0.f, n > 2 ? lq[v0 + 2] : 0.f,
+                           n > 3 ? lq[v0 + 3] : 0.f);
+        const float4 w = group_w(rw, group_p(rw, xp, n), xq, n);
+        const float s1 = w.x, s2 = s1 + w.y, s3 = s2 + w.z, W = s3 + w.w;
+        const float t = pick_u(a.seed, i, jb.pos, g) * W;
+        int k = t < s1 ? 0 : t < s2 ? 1 : t < s3 ? 2 : t < W ? 3 : -1;
+        if (k < 0)  // t at the very top of the range: the last positive entry
+          k = w.w > 0.f ? 3 : w.z > 0.f ? 2 : w.y > 0.f ? 1 : 0;
+        a.next_token[i] = v0 + k;
+        *ticket = 0;
+      } else if (lane == 0) {
+        a.next_token[i] = -1;  // no group (empty vocabulary slice set)
         *ticket = 0;
       }
     }
+  }
+  if (timed_out && lane == 0) {
+    // a copy that never completed: report, and wait (bounded) for every copy
+    // still in flight so that none lands after the warp has gone
+    flag(a.dev_status, SV_DEV_TIMEOUT);
+    for (; used < issued; ++used)
+      mbar_wait_sleep_bounded(bar0 + 8 * (int)(used % kRaceStages), (used / kRaceStages) & 1u);
   }
 }
 
@@ -1156,9 +1320,25 @@ static sv_status check_accept_args(const sv_batch* bt, const float* target_logit
 static sv_status launch_race(const Args& a, bool vec, cudaStream_t s) {
   const long ritems = (long)a.bt.n_req * a.L.nch_r_cap;
   const long rwarps = kRaceThreads / 32;
-  const unsigned gr = (unsigned)max(1L, min((ritems + rwarps - 1) / rwarps, (long)kNumSMs * 4));
-  if (sv::launch(vec ? race_kernel<true> : race_kernel<false>, gr, kRaceThreads, 0, s, a) !=
-      cudaSuccess)
+  const unsigned gr = (unsigned)max(
+      1L, min((ritems + rwarps - 1) / rwarps, (long)kNumSMs * kRaceWarpsPerSM / rwarps));
+  if (vec) {
+    // the ring is above the 48 KB default: allowed once per device (calls may
+    // come from several host threads)
+    static std::mutex mu;
+    static bool set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!set[dev]) {
+      if (cudaFuncSetAttribute(race_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kRaceSmem) != cudaSuccess)
+        return SV_ERR_CUDA;
+      set[dev] = true;
+    }
+  }
+  if (sv::launch(vec ? race_kernel<true> : race_kernel<false>, gr, kRaceThreads,
+                 vec ? kRaceSmem : 0, s, a) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;
 }
@@ -1326,7 +1506,6 @@ extern "C" sv_status sv_accept_commit(const sv_batch* bt, const float* target_lo
 // anything reads them, and the statistics write every partial the decision
 // merges).
 
-#include <mutex>
 
 namespace {
 

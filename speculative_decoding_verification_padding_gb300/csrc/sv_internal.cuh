@@ -114,14 +114,23 @@ __device__ __forceinline__ float accept_u(uint64_t seed, int i, int j) {
   return (float)(o.a >> 8) * 5.9604644775390625e-08f;  // 2^-24
 }
 
-// Race uniforms for vocabulary entries 4k .. 4k+3 of the draw at position
-// pos: counter (k, i, 1, pos), ((bits >> 9) + 0.5) * 2^-23 in (0, 1).
-__device__ __forceinline__ U4 race_bits(uint64_t seed, int i, int pos, int k) {
-  U4 c{(uint32_t)k, (uint32_t)i, 1u, (uint32_t)pos};
+// Race uniforms of the draw at position pos.  The race is among groups of
+// four vocabulary entries (group g = entries 4g .. 4g+3); groups are numbered
+// in blocks of 128, and group 128 b + 32 k + l takes word k of counter
+// (32 b + l, i, 1, pos): race_bits(..., 32 b + l) serves the four groups
+// 128 b + l, + 32, + 64, + 96.  ((bits >> 9) + 0.5) * 2^-23 is in (0, 1).
+__device__ __forceinline__ U4 race_bits(uint64_t seed, int i, int pos, int ctr) {
+  U4 c{(uint32_t)ctr, (uint32_t)i, 1u, (uint32_t)pos};
   return philox10(c, (uint32_t)seed, (uint32_t)(seed >> 32));
 }
 __device__ __forceinline__ float race_u(uint32_t bits) {
   return ((float)(bits >> 9) + 0.5f) * 1.1920928955078125e-07f;  // 2^-23
+}
+// The uniform that picks the entry inside the winning group g: word 0 of
+// counter (g, i, 2, pos), same conversion.
+__device__ __forceinline__ float pick_u(uint64_t seed, int i, int pos, int g) {
+  U4 c{(uint32_t)g, (uint32_t)i, 2u, (uint32_t)pos};
+  return race_u(philox10(c, (uint32_t)seed, (uint32_t)(seed >> 32)).a);
 }
 
 // ------------------------------------------------------ fast arithmetic ----
@@ -244,6 +253,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+// The same wait for a thread with nothing else to do: each try may suspend it
+// for up to 50 us while the phase is incomplete, instead of spinning; at
+// most 40000 tries (2 s) before it gives up.
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint32_t bar, uint32_t parity) {
+  for (int it = 0; it < 40000; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(50000u)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
 // 2-D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
                                             uint32_t bar) {
@@ -251,6 +276,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
       "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// 1-D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 

@@ -159,6 +159,22 @@ def test_accept_matches_oracle(name, T, sigma):
         assert np.array_equal(g[:, 0], o[:, 0])  # max logit
 
 
+@pytest.mark.parametrize("vocab,T", [(1021, 0.7), (13, 1.0), (130, 1.0)])
+def test_accept_odd_vocab_matches_oracle(vocab, T):
+    # vocabularies that are not a multiple of four: scalar loads, and the
+    # residual / bonus race has a short last group
+    w = wl.make_workload(wl.config("batch64"), n_req=48, ctx_scale=0.01, vocab=vocab,
+                         temperature=T, draft_sigma=0.5)
+    s = DeviceStep(w, mode="onepass")
+    s.accept()
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits, T, w.seed)
+    assert err == 0
+    _compare_accept(res, st, w, f"vocab {vocab} T={T}")
+    assert (st.accepted_len < np.diff(w.cu_rows) - 1).any()  # some residual draws
+
+
 def test_accept_verify_len_truncation():
     w = wl.make_workload(wl.config("batch256"), n_req=64, ctx_scale=0.01, vocab=4096, draft_sigma=0.3)
     vl = np.random.default_rng(2).integers(0, 5, w.n_req).astype(np.int32)

@@ -11,6 +11,9 @@ p) is the standard lossless rule.  The pins:
     distributed as p (T = 1 and 0.7, 1 and 3 drafts), the resampled token
     after a rejection as normalize(max(0, p - q)), the bonus token as p;
   * the acceptance rate against sum_v min(p_v, q_v);
+  * the two-step draw (a race among groups of four entries, then the entry
+    inside the winning group) at a vocabulary whose last group is short,
+    and a planted mistake in the second step that the statistics see;
   * row statistics against torch.logsumexp / softmax in fp64;
   * chunked verification equal to one-pass verification;
   * tree sampling (T > 0, siblings i.i.d. from q): chi-square of the first
@@ -190,6 +193,39 @@ def test_bonus_token_after_all_accepted_is_p_of_last_row():
     bonus = st.next_token[st.accepted_len == 1]
     s, crit, _ = _chi2_ok(np.bincount(bonus, minlength=V), p[1])
     assert s < crit
+
+
+@pytest.mark.parametrize("V,T", [(18, 1.0), (13, 0.7)])
+def test_grouped_race_with_a_short_last_group_chi2(V, T):
+    # Vocabularies that are not a multiple of four: the last group of the
+    # race is short.  First emitted token ~ p0, residual after a rejection ~
+    # normalize(max(0, p0 - q0)), bonus ~ p1.
+    p, q, tokens, st = _sampling_run(1, T, seed=31 + V, N=600_000, V=V)
+    a = st.accepted_len
+    assert st.ambiguous.mean() < 1e-3
+    first = np.where(a >= 1, tokens[:, 1], st.next_token)
+    s, crit, _ = _chi2_ok(np.bincount(first, minlength=V), p[0])
+    assert s < crit
+    res = np.maximum(p[0] - q[0], 0)
+    res /= res.sum()
+    s, crit, _ = _chi2_ok(np.bincount(st.next_token[a == 0], minlength=V), res)
+    assert s < crit
+    s, crit, _ = _chi2_ok(np.bincount(st.next_token[a == 1], minlength=V), p[1])
+    assert s < crit
+
+
+def test_chi2_detects_a_planted_mistake_inside_the_group():
+    # A second step that always took the group's first entry (the group race
+    # alone) gives the right group but the wrong entry: the statistics reject
+    # it.
+    V = 16
+    p, q, tokens, st = _sampling_run(1, 1.0, seed=41, N=300_000)
+    bonus = st.next_token[st.accepted_len == 1]
+    s, crit, _ = _chi2_ok(np.bincount(bonus, minlength=V), p[1])
+    assert s < crit
+    wrong = bonus - bonus % 4
+    s, crit, _ = _chi2_ok(np.bincount(wrong, minlength=V), p[1])
+    assert s > crit
 
 
 def test_chi2_detects_a_planted_mistake():

@@ -206,12 +206,21 @@ def test_philox_accept_uniforms_are_uniform():
 
 
 def test_philox_race_uniforms_open_interval_and_fp32_exact():
-    u = np.array([oracle.race_uniform(7, 3, 5, v) for v in range(20000)])
-    assert u.min() > 0.0 and u.max() < 1.0
-    assert np.array_equal(u.astype(np.float32).astype(np.float64), u)
-    assert stats.kstest(u, "uniform").pvalue > 1e-3
-    # adjacent vocabulary entries are uncorrelated
-    assert abs(np.corrcoef(u[:-1], u[1:])[0, 1]) < 0.03
+    for draw in (oracle.race_uniform, oracle.pick_uniform):
+        u = np.array([draw(7, 3, 5, g) for g in range(20000)])
+        assert u.min() > 0.0 and u.max() < 1.0
+        assert np.array_equal(u.astype(np.float32).astype(np.float64), u)
+        assert stats.kstest(u, "uniform").pvalue > 1e-3
+        # adjacent groups are uncorrelated
+        assert abs(np.corrcoef(u[:-1], u[1:])[0, 1]) < 0.03
+    # every group has its own uniform: the 128 groups of a block take the
+    # four words of 32 counters, no word twice
+    u = [oracle.race_uniform(7, 3, 5, g) for g in range(512)]
+    assert len(set(u)) == 512
+    # the pick and race streams are distinct
+    a = np.array([oracle.race_uniform(7, 3, 5, g) for g in range(4000)])
+    b = np.array([oracle.pick_uniform(7, 3, 5, g) for g in range(4000)])
+    assert abs(np.corrcoef(a, b)[0, 1]) < 0.05
 
 
 def test_philox_counter_and_key_sensitivity():
