@@ -73,6 +73,8 @@ def _load():
         D = ctypes.c_double
         lib.orc_adapt_gamma.argtypes = [I, P, P, P, P, D, D, I, I]
         lib.orc_adapt_gamma.restype = I
+        lib.orc_select_chunk.argtypes = [I, P, P, P, D, D, U64, P, P, P]
+        lib.orc_select_chunk.restype = I
         _lib = lib
     return _lib
 
@@ -249,6 +251,23 @@ def adapt_gamma(accepted_len, verified, state, decay, overhead, gamma_min, gamma
     err = lib.orc_adapt_gamma(len(a), _ptr(a), _ptr(v), _ptr(state), _ptr(g), float(decay),
                               float(overhead), int(gamma_min), int(gamma_max))
     return err, g
+
+
+def select_chunk(rows, ctx, state, kv_bytes, row_bytes, chunk_bytes):
+    """Chunk size of least expected cost (see orc_select_chunk).
+
+    Returns (err, chunk, cost, costs[128])."""
+    lib = _load()
+    r = _i32(rows)
+    c = _i32(ctx)
+    st = np.ascontiguousarray(state, dtype=np.float64)
+    ch = np.zeros(1, dtype=np.int32)
+    co = np.zeros(1, dtype=np.uint64)
+    costs = np.zeros(128, dtype=np.uint64)
+    err = lib.orc_select_chunk(len(r), _ptr(r), _ptr(c), _ptr(st), float(kv_bytes),
+                               float(row_bytes), int(chunk_bytes), _ptr(ch), _ptr(co),
+                               _ptr(costs))
+    return err, int(ch[0]), int(co[0]), costs
 
 
 # ----------------------------------------------------------------- chunked --

@@ -892,4 +892,71 @@ int orc_adapt_gamma(int n_req, const int32_t* accepted_len, const int32_t* verif
   return err;
 }
 
+// -------------------------------------------- chunk size (NEXT-4) --
+// [FASER] "FASER의 세 가지 메커니즘", mechanism 2 (verification in chunks,
+// requests leave at their first rejection) with the remark that the chunk
+// size follows the load.  The pages give no rule; the one written here (and
+// in the library's header) is the expected cost of a chunked step:
+//   a_i = min(1, (S_i + 1) / (N_i + 2))   (acceptance estimate from the
+//         draft-length controller's state);
+//   for a chunk size c in 1..max_rows (max_rows = max_i rows_i), chunk k
+//   covers rows [b, e) = [k c, min((k+1) c, rows_i)) of request i, which
+//   reaches it when drafts 1..k c were all accepted: P_ik = a_i^(k c)
+//   (P_i0 = 1, P_i,k+1 = P_ik * a_i^c, a_i^c by c multiplications);
+//   then it reads bytes_ik = (ctx_i + e) kv_bytes + (e - b) row_bytes;
+//   cost(c) = K(c) chunk_bytes + sum over i, k of trunc(P_ik bytes_ik)
+//   (u64), K(c) = ceil(max_rows / c);
+//   chunk = the c of least cost, the largest c on ties.
+// fp64, each operation rounded on its own (this file is compiled with
+// -ffp-contract=off).  Requests with rows outside [1, 128], a negative
+// context or a state that is not finite and non-negative are reported and
+// left out.  costs[c - 1] for c > max_rows is UINT64_MAX.
+int orc_select_chunk(int n_req, const int32_t* rows, const int32_t* ctx, const double* state,
+                     double kv_bytes, double row_bytes, uint64_t chunk_bytes, int32_t* chunk,
+                     uint64_t* cost, uint64_t* costs) {
+  if (n_req < 0 || !(kv_bytes >= 0.0) || !(row_bytes >= 0.0)) return ORC_BAD_ARG;
+  int err = 0;
+  int max_rows = 0;
+  std::vector<char> ok(n_req, 0);
+  std::vector<double> alpha(n_req, 0.0);
+  for (int i = 0; i < n_req; ++i) {
+    const double S = state[2 * i], N = state[2 * i + 1];
+    if (rows[i] < 1 || rows[i] > 128 || ctx[i] < 0 || !std::isfinite(S) || !std::isfinite(N) ||
+        S < 0.0 || N < 0.0) {
+      err |= ORC_BAD_LENGTH;
+      continue;
+    }
+    ok[i] = 1;
+    alpha[i] = std::min(1.0, (S + 1.0) / (N + 2.0));
+    max_rows = std::max(max_rows, (int)rows[i]);
+  }
+  for (int c = 1; c <= 128; ++c) costs[c - 1] = UINT64_MAX;
+  int best = 1;
+  uint64_t best_cost = 0;
+  for (int c = 1; c <= max_rows; ++c) {
+    const uint64_t K = (uint64_t)((max_rows + c - 1) / c);
+    uint64_t total = K * chunk_bytes;
+    for (int i = 0; i < n_req; ++i) {
+      if (!ok[i]) continue;
+      double ac = 1.0;
+      for (int t = 0; t < c; ++t) ac = ac * alpha[i];
+      double P = 1.0;
+      for (int b = 0; b < rows[i]; b += c) {
+        const int e = std::min(b + c, (int)rows[i]);
+        const double bytes = (double)(ctx[i] + e) * kv_bytes + (double)(e - b) * row_bytes;
+        total += (uint64_t)(P * bytes);
+        P = P * ac;
+      }
+    }
+    costs[c - 1] = total;
+    if (c == 1 || total <= best_cost) {
+      best = c;
+      best_cost = total;
+    }
+  }
+  *chunk = best;
+  *cost = best_cost;
+  return err;
+}
+
 }  // extern "C"
