@@ -124,6 +124,15 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def hbm_peak_gbs():
+    """The HBM denominator: the machine's measured copy bandwidth, else the
+    fallback figure."""
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        return float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
 # ---------------------------------------------------------- byte accounting --
 
 def launch_windows(w, mode, accepted_len, verify_len=None, chunk=2):
@@ -433,6 +442,33 @@ def main():
                                    "GB/s": accept_bytes(w, full, al, T) / op_acc / 1e9}
         s.run()  # back to the chunked step's state
 
+    # ---- the chunk-size rule on this step's own acceptance (outside the timing) ----
+    chunk_policy = None
+    if mode == "chunked":
+        rows_np = np.diff(w.cu_rows).astype(np.int32)
+        a_np = np.asarray(al, dtype=np.int64)
+        state = np.stack([a_np, a_np + (a_np < rows_np - 1)], axis=1).astype(np.float64)
+        fixed_us = 25.0  # plan + statistics + decision latency of one chunk, launch list
+        chunk_b = int(fixed_us * 1e-6 * hbm_peak_gbs()[0] * 1e9)
+        kvb = 2.0 * 2 * w.cfg.n_kv_heads * w.cfg.head_dim
+        rowb = 4.0 * w.target_logits.shape[1] * (2 if T > 0 else 1)
+        g_ch = torch.zeros(1, dtype=torch.int32, device=dev)
+        g_cost = torch.zeros(1, dtype=torch.int64, device=dev)
+        g_costs = torch.zeros(128, dtype=torch.int64, device=dev)
+        api.sv_select_chunk(torch.from_numpy(rows_np).to(dev),
+                            torch.from_numpy(w.cache_lens.astype(np.int32)).to(dev),
+                            torch.from_numpy(state).to(dev), kvb, rowb, chunk_b, g_ch, g_cost,
+                            g_costs)
+        torch.cuda.synchronize()
+        cs = g_costs.cpu().numpy().view(np.uint64)
+        sel = int(g_ch.item())
+        chunk_policy = {
+            "selected_chunk": sel, "per_chunk_fixed_MB": chunk_b / 1e6,
+            "modelled_MB": {str(chunk): float(cs[chunk - 1]) / 1e6, str(sel): float(cs[sel - 1]) / 1e6},
+            "measured_us": {f"chunk {chunk} step": t_step * 1e6,
+                            "one pass (attend + accept)": calls["attend_onepass"]["us"]
+                            + calls["accept_onepass"]["us"]}}
+
     # ---- end to end through host buffers ----
     pin = lambda t: t.cpu().pin_memory()
     ins = [(s.q, pin(s.q)), (s.target, pin(s.target)), (s.batch.tokens, pin(s.batch.tokens)),
@@ -501,11 +537,7 @@ def main():
         reps.close()
         return
 
-    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(peaks_path):
-        hbm_peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
-    else:
-        hbm_peak, peak_src = 6800.0, "fallback"
+    hbm_peak, peak_src = hbm_peak_gbs()
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "attend_traffic.json")
     if os.path.exists(tr_path):
@@ -550,6 +582,7 @@ def main():
                      "bytes_per_launch": sum(att_b) / n_launch,
                      "us_per_launch": 1e6 * t_att / n_launch},
         "calls": calls,
+        **({"chunk_policy": chunk_policy} if chunk_policy else {}),
         "e2e": {"value": rows_all / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
         "gpu_launches": launches_per_step * args.steps,

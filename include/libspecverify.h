@@ -18,7 +18,9 @@
  *                     verification in chunks of rows with early pruning of
  *                     requests whose prefix was rejected;
  *   sv_adapt_gamma    each request's next draft length from its own
- *                     acceptance history.
+ *                     acceptance history;
+ *   sv_select_chunk   the chunk size of least expected cost for the next
+ *                     chunked step.
  *
  * Sources (pages by title; section names glossed):
  *   [SwiftSpec] "SwiftSpec: 드래프터와 타깃을 서로 다른 GPU에 분리하고 비동기로
@@ -349,6 +351,34 @@ sv_status sv_verify_chunked_commit(const sv_paged_kv* kv, const sv_batch* batch,
                                    int32_t* accepted_nodes, int32_t* next_token,
                                    uint8_t* ambiguous, int32_t* done, const sv_block_pool* pool,
                                    void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------ chunk size --
+ * [FASER] mechanism 2 (verification in chunks; requests leave at their
+ * first rejection) and its remark that the chunk size follows the load.  The
+ * pages give no rule; this one is fixed here exactly.  For request i with
+ * rows_i verified rows (1 + drafts, at most 128), ctx_i cached tokens and the
+ * draft-length controller's state (S_i, N_i) (sv_adapt_gamma):
+ *   a_i = min(1, (S_i + 1) / (N_i + 2))  (acceptance estimate);
+ *   for a chunk size c = 1 .. max_rows (max_rows = max_i rows_i), chunk k
+ *   covers rows [b, e) = [k c, min((k+1) c, rows_i)), which request i reaches
+ *   when drafts 1 .. k c were all accepted: P_ik = a_i^(k c), computed as
+ *   P_i0 = 1, P_i,k+1 = P_ik * a_i^c with a_i^c by c multiplications;
+ *   bytes_ik = (ctx_i + e) * kv_bytes + (e - b) * row_bytes (context KV is
+ *   read again by every chunk, logits once per row);
+ *   cost(c) = ceil(max_rows / c) * chunk_bytes
+ *             + sum over i and k of trunc(P_ik * bytes_ik)   (u64),
+ *   chunk_bytes being one chunk's fixed cost (its launches and latency
+ *   chains) in bytes of HBM time.  Every fp64 operation is rounded on its
+ *   own (no fused multiply-add).
+ * Outputs: *chunk = the size of least cost (the larger on ties), *cost its
+ * cost, costs [128]: cost(c) at c - 1 (UINT64_MAX past max_rows).  A chunk of
+ * max_rows is one-pass verification.  Requests with rows outside [1, 128],
+ * ctx < 0 or a state that is not finite and non-negative set
+ * SV_DEV_BAD_LENGTH and are left out.  All pointers are device memory. */
+sv_status sv_select_chunk(int32_t n_req, const int32_t* rows, const int32_t* ctx,
+                          const double* state, double kv_bytes, double row_bytes,
+                          uint64_t chunk_bytes, int32_t* chunk, uint64_t* cost, uint64_t* costs,
+                          int32_t* dev_status, void* stream);
 
 /* ------------------------------------------ per-request draft length --
  * [FASER] mechanism 1 (per-request speculation length): every request's

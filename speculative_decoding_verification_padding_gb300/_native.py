@@ -75,6 +75,8 @@ PROTOTYPES = {
                                                 P, P, P, P, P, P, SZ, P, P]),
     "sv_adapt_gamma": (ctypes.c_int, [I32, P, P, P, P, ctypes.c_double, ctypes.c_double, I32, I32,
                                       P, P]),
+    "sv_select_chunk": (ctypes.c_int, [I32, P, P, P, ctypes.c_double, ctypes.c_double, U64, P, P,
+                                       P, P, P]),
     "sv_selftest_bounded_wait": (ctypes.c_int, [I32, P, P]),
 }
 

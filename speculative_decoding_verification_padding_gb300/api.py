@@ -229,6 +229,25 @@ def sv_adapt_gamma(accepted_len: torch.Tensor, verified: torch.Tensor, state: to
                                    _stream(stream)), "sv_adapt_gamma")
 
 
+def sv_select_chunk(rows: torch.Tensor, ctx: torch.Tensor, state: torch.Tensor,
+                    kv_bytes: float, row_bytes: float, chunk_bytes: int, chunk: torch.Tensor,
+                    cost: torch.Tensor, costs: torch.Tensor,
+                    dev_status: Optional[torch.Tensor] = None, stream=None):
+    _expect(rows, torch.int32, "rows")
+    _expect(ctx, torch.int32, "ctx")
+    _expect(state, torch.float64, "state")
+    _expect(chunk, torch.int32, "chunk")
+    # cost and costs hold u64 values: any 8-byte integer tensor will do
+    if cost.numel() < 1 or cost.element_size() != 8 or cost.is_floating_point():
+        raise N.SpecVerifyError("cost: one 8-byte integer")
+    if costs.numel() < 128 or costs.element_size() != 8 or costs.is_floating_point():
+        raise N.SpecVerifyError("costs: 128 8-byte integers")
+    N.check(N.lib().sv_select_chunk(rows.numel(), _ptr(rows), _ptr(ctx), _ptr(state),
+                                    float(kv_bytes), float(row_bytes), int(chunk_bytes),
+                                    _ptr(chunk), _ptr(cost), _ptr(costs), _ptr(dev_status),
+                                    _stream(stream)), "sv_select_chunk")
+
+
 def sv_selftest_bounded_wait(limit: int, dev_status: torch.Tensor, stream=None):
     _expect(dev_status, torch.int32, "dev_status")
     N.check(N.lib().sv_selftest_bounded_wait(int(limit), _ptr(dev_status), _stream(stream)),

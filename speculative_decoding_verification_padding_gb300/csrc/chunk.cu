@@ -77,6 +77,114 @@ __global__ void __launch_bounds__(32) selftest_wait_kernel(int limit, int32_t* d
 }  // namespace chk
 }  // namespace sv
 
+// Chunk size of least expected cost ([FASER] mechanism 2, the chunk size
+// following the load; the rule is the one in the header).  One CTA per
+// candidate size c: its threads take the requests, each term in fp64 with
+// every operation rounded on its own (__dmul_rn / __dadd_rn), truncated to
+// whole bytes and summed as u64 (any order gives the same integer); then one
+// warp picks the least cost, the larger size on ties.
+namespace sv {
+namespace chk {
+constexpr int kChunkThreads = 256;
+
+__global__ void __launch_bounds__(kChunkThreads) chunk_cost_kernel(
+    int n_req, const int32_t* rows, const int32_t* ctx, const double* state, double kv_bytes,
+    double row_bytes, unsigned long long chunk_bytes, unsigned long long* costs,
+    int32_t* dev_status) {
+  griddep_entry();
+  const int c = blockIdx.x + 1;
+  __shared__ int s_max[kChunkThreads / 32];
+  __shared__ unsigned long long s_total;
+  // the largest valid rows_i (every CTA computes it)
+  int mr = 0;
+  for (int i = threadIdx.x; i < n_req; i += kChunkThreads) {
+    const int r = rows[i], x = ctx[i];
+    const double S = state[2 * i], N = state[2 * i + 1];
+    const bool ok = r >= 1 && r <= kMaxRows && x >= 0 && isfinite(S) && isfinite(N) &&
+                    S >= 0.0 && N >= 0.0;
+    if (ok) mr = max(mr, r);
+    else if (c == 1) flag(dev_status, SV_DEV_BAD_LENGTH);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mr = max(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mr;
+  if (threadIdx.x == 0) s_total = 0ull;
+  __syncthreads();
+  int max_rows = 0;
+  for (int w = 0; w < kChunkThreads / 32; ++w) max_rows = max(max_rows, s_max[w]);
+  if (c > max_rows) {
+    if (threadIdx.x == 0) costs[c - 1] = ~0ull;
+    return;
+  }
+  unsigned long long part = 0ull;
+  for (int i = threadIdx.x; i < n_req; i += kChunkThreads) {
+    const int r = rows[i], x = ctx[i];
+    const double S = state[2 * i], N = state[2 * i + 1];
+    if (!(r >= 1 && r <= kMaxRows && x >= 0 && isfinite(S) && isfinite(N) && S >= 0.0 &&
+          N >= 0.0))
+      continue;
+    const double alpha = fmin(1.0, __ddiv_rn(__dadd_rn(S, 1.0), __dadd_rn(N, 2.0)));
+    double ac = 1.0;
+    for (int t = 0; t < c; ++t) ac = __dmul_rn(ac, alpha);
+    double P = 1.0;
+    for (int b = 0; b < r; b += c) {
+      const int e = min(b + c, r);
+      const double bytes = __dadd_rn(__dmul_rn((double)(x + e), kv_bytes),
+                                     __dmul_rn((double)(e - b), row_bytes));
+      part += __double2ull_rz(__dmul_rn(P, bytes));
+      P = __dmul_rn(P, ac);
+    }
+  }
+  atomicAdd(&s_total, part);
+  __syncthreads();
+  if (threadIdx.x == 0)
+    costs[c - 1] = (unsigned long long)((max_rows + c - 1) / c) * chunk_bytes + s_total;
+}
+
+__global__ void __launch_bounds__(32) chunk_pick_kernel(const unsigned long long* costs,
+                                                        int32_t* chunk,
+                                                        unsigned long long* cost) {
+  griddep_entry();
+  if (threadIdx.x != 0) return;
+  int best = 1;
+  unsigned long long bc = 0ull;
+  bool any = false;
+  for (int c = 1; c <= kMaxRows; ++c) {
+    const unsigned long long v = costs[c - 1];
+    if (v == ~0ull) continue;
+    if (!any || v <= bc) {
+      best = c;
+      bc = v;
+      any = true;
+    }
+  }
+  *chunk = best;
+  *cost = any ? bc : 0ull;
+}
+}  // namespace chk
+}  // namespace sv
+
+extern "C" sv_status sv_select_chunk(int32_t n_req, const int32_t* rows, const int32_t* ctx,
+                                     const double* state, double kv_bytes, double row_bytes,
+                                     uint64_t chunk_bytes, int32_t* chunk, uint64_t* cost,
+                                     uint64_t* costs, int32_t* dev_status, void* stream) {
+  if (n_req < 0 || !(kv_bytes >= 0.0) || !(row_bytes >= 0.0) || isinf(kv_bytes) ||
+      isinf(row_bytes))
+    return SV_ERR_INVALID_ARGUMENT;
+  if (!chunk || !cost || !costs || (n_req > 0 && (!rows || !ctx || !state)))
+    return SV_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long* c64 = reinterpret_cast<unsigned long long*>(costs);
+  if (sv::launch(chk::chunk_cost_kernel, kMaxRows, chk::kChunkThreads, 0, s, (int)n_req, rows,
+                 ctx, state, kv_bytes, row_bytes, (unsigned long long)chunk_bytes, c64,
+                 dev_status) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (sv::launch(chk::chunk_pick_kernel, 1, 32, 0, s, (const unsigned long long*)c64, chunk,
+                 reinterpret_cast<unsigned long long*>(cost)) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
 extern "C" sv_status sv_selftest_bounded_wait(int32_t limit, int32_t* dev_status, void* stream) {
   if (limit < 1 || limit > kWaitLimit || !dev_status) return SV_ERR_INVALID_ARGUMENT;
   if (sv::launch(chk::selftest_wait_kernel, 1, 32, 0, static_cast<cudaStream_t>(stream),

@@ -82,6 +82,15 @@ def test_host_side_validation_without_gpu(lib):
     assert lib.sv_verify_chunked_commit(ctypes.byref(kv96), ctypes.byref(b), *args,
                                         ctypes.byref(pool), 256, 1 << 20, None,
                                         None) == N.SV_ERR_UNSUPPORTED_SHAPE
+    # chunk-size rule: sizes and pointers checked on the host
+    assert lib.sv_select_chunk(-1, None, None, None, 4096.0, 1.0, 0, 256, 256, 256, None,
+                               None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_select_chunk(4, None, 256, 256, 4096.0, 1.0, 0, 256, 256, 256, None,
+                               None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_select_chunk(4, 256, 256, 256, -1.0, 1.0, 0, 256, 256, 256, None,
+                               None) == N.SV_ERR_INVALID_ARGUMENT
+    assert lib.sv_select_chunk(4, 256, 256, 256, 4096.0, 1.0, 0, 256, 256, None, None,
+                               None) == N.SV_ERR_INVALID_ARGUMENT
     # its workspace is the chunked step's, which also holds the commit's ticket
     wsz = lib.sv_verify_chunked_workspace(ctypes.byref(b), ctypes.byref(kv), 8, 16)
     assert wsz > 0

@@ -359,6 +359,64 @@ def test_adapt_gamma_matches_oracle(trial):
     assert bool(status.item() & api.N.SV_DEV_BAD_LENGTH) == bool(err & oracle.ORC_BAD_LENGTH)
 
 
+# -------------------------------------------------------------- chunk size --
+
+def _chunk_inputs(R, seed, bad=()):
+    rng = np.random.default_rng(seed)
+    rows = rng.integers(1, 10, R).astype(np.int32)
+    ctx = np.clip(np.rint(rng.lognormal(np.log(4096), 1.0, R)), 512, 32768).astype(np.int32)
+    N = rng.uniform(0, 40, R)
+    S = N * rng.uniform(0, 1, R)
+    st = np.ascontiguousarray(np.stack([S, N], axis=1))
+    for i in bad:
+        rows[i] = 0 if i % 2 else 200
+    return rows, ctx, st
+
+
+@pytest.mark.parametrize("R,seed,bad,chunk_mb", [(64, 0, (), 170), (1, 1, (), 0), (1000, 2, (), 50),
+                                                  (64, 3, (5, 17), 170), (300, 4, (), 0)])
+def test_select_chunk_matches_oracle(R, seed, bad, chunk_mb):
+    rows, ctx, st = _chunk_inputs(R, seed, bad)
+    kv, row, cb = 4096.0, 2 * 4 * 128256.0, chunk_mb * 10 ** 6
+    err, ch, cost, costs = oracle.select_chunk(rows, ctx, st, kv, row, cb)
+    dev = "cuda"
+    t_rows, t_ctx, t_st = (torch.from_numpy(rows).to(dev), torch.from_numpy(ctx).to(dev),
+                           torch.from_numpy(st).to(dev))
+    g_ch = torch.zeros(1, dtype=torch.int32, device=dev)
+    g_cost = torch.zeros(1, dtype=torch.int64, device=dev)
+    g_costs = torch.zeros(128, dtype=torch.int64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    api.sv_select_chunk(t_rows, t_ctx, t_st, kv, row, cb, g_ch, g_cost, g_costs, status)
+    torch.cuda.synchronize()
+    assert g_ch.item() == ch
+    assert g_cost.cpu().numpy().view(np.uint64)[0] == np.uint64(cost)
+    assert np.array_equal(g_costs.cpu().numpy().view(np.uint64), costs)
+    assert bool(status.item() & api.N.SV_DEV_BAD_LENGTH) == bool(err & oracle.ORC_BAD_LENGTH)
+
+
+def test_select_chunk_prefers_one_pass_at_batch64_on_this_gpu():
+    # the bench workload's first-step acceptance, this GPU's per-chunk fixed
+    # cost (about 25 us of plan, statistics and decision at 6.8 TB/s): the
+    # chunked step re-reads context for little pruning, one pass is cheapest
+    w = wl.make_workload(wl.config("batch64"))
+    err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits, w.cfg.temperature, w.seed)
+    rows = np.diff(w.cu_rows).astype(np.int32)
+    a = st.accepted_len
+    state = np.ascontiguousarray(np.stack([a, a + (a < rows - 1)], axis=1).astype(np.float64))
+    dev = "cuda"
+    g_ch = torch.zeros(1, dtype=torch.int32, device=dev)
+    g_cost = torch.zeros(1, dtype=torch.int64, device=dev)
+    g_costs = torch.zeros(128, dtype=torch.int64, device=dev)
+    api.sv_select_chunk(torch.from_numpy(rows).to(dev),
+                        torch.from_numpy(w.cache_lens.astype(np.int32)).to(dev),
+                        torch.from_numpy(state).to(dev), 4096.0, 2 * 4 * 128256.0,
+                        170 * 10 ** 6, g_ch, g_cost, g_costs)
+    torch.cuda.synchronize()
+    assert g_ch.item() == rows.max()
+    c = g_costs.cpu().numpy().view(np.uint64)
+    assert c[1] > c[rows.max() - 1]  # chunks of 2 cost more than one pass
+
+
 # ------------------------------------------------------- chunked / budget step --
 
 @pytest.mark.parametrize("T", [0.7, 0.0])
