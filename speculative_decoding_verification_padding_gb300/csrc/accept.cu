@@ -253,7 +253,16 @@ __device__ __forceinline__ void merge_pairs(const Args& a, int nch, int r0, int 
 // kernel takes it over, kSkipped when nothing was decided.
 constexpr int kFinal = 0, kToTree = 1, kSkipped = 2;
 
-__device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
+// What a fused commit of a decided chain of at most 32 rows takes from the
+// decision instead of reading it again: the rows, the accepted drafts, the
+// cache length and, per lane k < rows, the block id of slot ctx + k (loaded
+// with the parents and tokens).
+struct CommitHint {
+  int rows, al, ctx, blk;
+  bool chain;
+};
+
+__device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm, CommitHint& h) {
   const int lane = threadIdx.x & 31;
   Job* job = reinterpret_cast<Job*>(a.ws + a.L.jobs) + i;
   if (a.T > 0.f && lane == 0) {
@@ -263,6 +272,11 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
     reinterpret_cast<int*>(a.ws + a.L.race_tickets)[a.bt.n_req + i] = 0;
   }
   const Window w = window_of(a.bt, i);
+  // loaded with the window: the accepted drafts of the earlier windows, and
+  // for a fused commit the cache length
+  const int prev_len = a.accepted_len[i];
+  const int ctx_c = a.commit ? a.kv.cache_lens[i] : 0;
+  h.chain = false;
   if (!a.use_list && !live(a, w, i)) {
     if (!w.ok && lane == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
     return kSkipped;
@@ -270,6 +284,10 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
   const int cu = a.bt.cu_rows[i];
   const int V = a.V;
   bool chain = true, badp = false, badt = false;
+  h.blk = -1;
+  if (a.commit && w.rows <= 32 && lane < w.rows && ctx_c >= 0 &&
+      (long)ctx_c + lane < (long)a.kv.max_blocks * kBlockSize)
+    h.blk = a.kv.tables[(size_t)i * a.kv.max_blocks + (ctx_c + lane) / kBlockSize];
   for (int j = lane; j < w.rows; j += 32) {
     const int p = a.bt.parent[cu + j];
     const int t = a.bt.tokens[cu + j];
@@ -292,11 +310,14 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
       flag(a.dev_status, badp ? SV_DEV_BAD_PARENT : badt ? SV_DEV_BAD_TOKEN : SV_DEV_BAD_WINDOW);
     return kSkipped;
   }
+  h.rows = w.rows;
+  h.ctx = ctx_c;
+  h.chain = chain && w.rows <= 32;
   const int max_rows = a.bt.max_rows_per_req;
   int32_t* nodes = a.accepted_nodes + (size_t)i * max_rows;
   if (w.b == 0) {
     for (int k = lane; k < max_rows; k += 32) nodes[k] = k == 0 ? 0 : -1;
-  } else if (a.accepted_len[i] != w.b) {
+  } else if (prev_len != w.b) {
     if (lane == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
     return kSkipped;
   }
@@ -385,6 +406,7 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
       if (w.b == 0) a.ambiguous[i] = 0;
       if (a.done) a.done[i] = next >= 0 ? 1 : 0;
     }
+    h.al = __shfl_sync(0xffffffffu, len, 0);
     return kFinal;
   }
 
@@ -465,6 +487,7 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm) {
       break;
     }
   }
+  h.al = len;
   if (lane != 0) return kFinal;
   if (jb.mode == 0 && w.e == w.lim && len == w.lim - 1) {
     jb.mode = 2;
@@ -689,11 +712,32 @@ __device__ __forceinline__ int commit_check(const Args& a, int rows, int ctx, in
 // decided for the request, which is only counted.  The lanes look up the
 // moves of 32 path positions at once (chains move nothing); the moves
 // themselves run in ascending k, every lane copying part of the slot.
-__device__ __forceinline__ void commit_request(const Args& a, int i, bool final) {
+__device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
+                                               const CommitHint* hint) {
   const int lane = threadIdx.x & 31;
   const CommitArgs& c = a.kv;
   int2 span = make_int2(0, 0);
-  if (final) {
+  if (final && hint && hint->chain) {
+    // A chain the decision just decided: its path is 0..al (nothing moves);
+    // the same rules as commit_check, on the values the decision holds.
+    const int rows = hint->rows, ctx = hint->ctx, al = hint->al;
+    int bad = 0;
+    if (rows < 1 || rows > a.bt.max_rows_per_req || al < 0 || al > rows - 1) {
+      bad = SV_DEV_BAD_WINDOW;
+    } else if (ctx < 0 || (long)ctx + rows > (long)c.max_blocks * kBlockSize) {
+      bad = SV_DEV_BAD_LENGTH;
+    } else if (__any_sync(0xffffffffu,
+                          lane <= al && (hint->blk < 0 || hint->blk >= c.num_blocks))) {
+      bad = SV_DEV_BAD_BLOCK_ID;
+    }
+    if (bad) {
+      if (lane == 0) flag(a.dev_status, bad);
+    } else {
+      span = make_int2((ctx + 1 + al + kBlockSize - 1) / kBlockSize,
+                       (ctx + rows + kBlockSize - 1) / kBlockSize);
+      if (lane == 0) c.cache_lens[i] = ctx + 1 + al;
+    }
+  } else if (final) {
     const int rows = a.bt.cu_rows[i + 1] - a.bt.cu_rows[i];
     const int ctx = c.cache_lens[i];
     const int al = a.accepted_len[i];
@@ -813,7 +857,8 @@ __global__ void __launch_bounds__(kDecideWarps * 32, 1) decide_kernel(Args a) {
   const int wid = threadIdx.x >> 5;
   for (int ai = blockIdx.x * kDecideWarps + wid; ai < count; ai += gridDim.x * kDecideWarps) {
     const int i = req_of(a, act, ai);
-    const int outcome = decide_request(a, nch, i, s_dec[wid]);
+    CommitHint hint;
+    const int outcome = decide_request(a, nch, i, s_dec[wid], hint);
     if (a.commit && outcome != kToTree) {
       __syncwarp();  // the path and state lane 0 wrote are visible to the warp
       bool now = true;
@@ -826,7 +871,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32, 1) decide_kernel(Args a) {
           now = a.done[i] != 0;
         }
       }
-      if (now) commit_request(a, i, outcome == kFinal);
+      if (now) commit_request(a, i, outcome == kFinal, outcome == kFinal ? &hint : nullptr);
     }
   }
 }
@@ -969,7 +1014,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
   }
   if (a.commit && warp == 0) {
     __syncwarp();  // the path thread 0 wrote is visible to the warp
-    commit_request(a, i, true);
+    commit_request(a, i, true, nullptr);
   }
 }
 
