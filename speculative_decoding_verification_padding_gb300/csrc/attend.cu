@@ -179,6 +179,22 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   __shared__ int s_carry, s_acarry;
 
   __shared__ int s_none;
+  const bool chunked = a.chunk.index >= 0;
+  // One thread per request: its window (and in a chunked step its done flag)
+  // and its cache length are loaded before the header check below, so both
+  // round trips overlap.
+  auto window_at = [&](int i, bool& badw) {
+    badw = false;
+    return chunked ? chunk_window(a.bt, i, a.chunk.index, a.chunk.size, a.chunk.done, &badw)
+                   : window_of(a.bt, i);
+  };
+  bool badw0 = false;
+  Window w0{};
+  int ctx0 = 0;
+  if (tid < R) {
+    w0 = window_at(tid, badw0);
+    ctx0 = a.cache_lens[tid];
+  }
   if (tid == 0) {
     // Each request's rows are checked against the packed total by its window;
     // a prefix that does not start at 0 or end at the total is reported too.
@@ -194,63 +210,61 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   }
   __syncthreads();
   if (s_none) return;
-  // One warp per request: window, parents, length, work.
+  // Per request: window, parents (all loads of a thread issued together),
+  // length, work.
   unsigned long long myW = 0;
-  const bool chunked = a.chunk.index >= 0;
-  for (int i = warp; i < R; i += 32) {
-    Window w;
-    bool badw = false;
+  for (int i = tid; i < R; i += blockDim.x) {
+    bool badw = badw0;
+    Window w = w0;
+    int ctx = ctx0;
+    if (i != tid) {
+      w = window_at(i, badw);
+      ctx = a.cache_lens[i];
+    }
     if (chunked) {
-      w = chunk_window(a.bt, i, a.chunk.index, a.chunk.size, a.chunk.done, &badw);
-      if (lane == 0) {
-        a.chunk.row_begin[i] = w.b;
-        a.chunk.row_end[i] = w.e;
-        if (badw && a.chunk.index == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-      }
-    } else {
-      w = window_of(a.bt, i);
+      a.chunk.row_begin[i] = w.b;
+      a.chunk.row_end[i] = w.e;
+      if (badw && a.chunk.index == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
     }
     if (badw) w.ok = false;  // reported above (once); the window is empty anyway
     const int cu = a.bt.cu_rows[i];
     bool badp = false;
     if (w.ok) {
-      for (int j = lane; j < w.rows; j += 32) {
+      for (int j = 0; j < w.rows; ++j) {
         const int p = a.bt.parent[cu + j];
         badp |= (j == 0) ? (p != -1) : (p < 0 || p >= j);
       }
     }
-    badp = __any_sync(0xffffffffu, badp);
-    if (lane == 0) {
-      bool valid = w.ok && !badp;
-      if (!w.ok && !chunked) flag(a.dev_status, SV_DEV_BAD_WINDOW);
-      if (badp) flag(a.dev_status, SV_DEV_BAD_PARENT);
-      const int ctx = a.cache_lens[i];
-      // A request that stopped in an earlier chunk may have been committed
-      // already (its cache length moved on): nothing of it is read now.
-      const bool stopped = chunked && a.chunk.index > 0 && w.b >= w.e;
-      if (valid && !stopped && (ctx < 0 || (long)ctx + w.rows > (long)a.max_blocks * kBlockSize)) {
-        valid = false;
-        flag(a.dev_status, SV_DEV_BAD_LENGTH);
-      }
-      const int nw = valid ? max(0, w.e - w.b) : 0;
-      const int nrt = (a.group * nw + kTileRows - 1) / kTileRows;
-      const int nblk = nw ? (ctx + w.e + kBlockSize - 1) / kBlockSize : 0;
-      myW += (unsigned long long)nrt * a.Hkv * nblk;
-      ReqInfo ri;
-      ri.valid = valid && nw > 0;
-      ri.b = w.b;
-      ri.e = w.e;
-      ri.ctx = ctx;
-      ri.nrt = nrt;
-      ri.nblk = nblk;
-      ri.nsplit = 0;
-      ri.ubase = 0;
-      ri.act = (!badw && w.b < w.e) ? 1 : 0;
-      ri.cu = cu;
-      ri.rows = w.rows;
-      info[i] = ri;
+    bool valid = w.ok && !badp;
+    if (!w.ok && !chunked) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+    if (badp) flag(a.dev_status, SV_DEV_BAD_PARENT);
+    // A request that stopped in an earlier chunk may have been committed
+    // already (its cache length moved on): nothing of it is read now.
+    const bool stopped = chunked && a.chunk.index > 0 && w.b >= w.e;
+    if (valid && !stopped && (ctx < 0 || (long)ctx + w.rows > (long)a.max_blocks * kBlockSize)) {
+      valid = false;
+      flag(a.dev_status, SV_DEV_BAD_LENGTH);
     }
+    const int nw = valid ? max(0, w.e - w.b) : 0;
+    const int nrt = (a.group * nw + kTileRows - 1) / kTileRows;
+    const int nblk = nw ? (ctx + w.e + kBlockSize - 1) / kBlockSize : 0;
+    myW += (unsigned long long)nrt * a.Hkv * nblk;
+    ReqInfo ri;
+    ri.valid = valid && nw > 0;
+    ri.b = w.b;
+    ri.e = w.e;
+    ri.ctx = ctx;
+    ri.nrt = nrt;
+    ri.nblk = nblk;
+    ri.nsplit = 0;
+    ri.ubase = 0;
+    ri.act = (!badw && w.b < w.e) ? 1 : 0;
+    ri.cu = cu;
+    ri.rows = w.rows;
+    info[i] = ri;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) myW += __shfl_xor_sync(0xffffffffu, myW, o);
   if (lane == 0 && myW) atomicAdd(&s_W, myW);
   __syncthreads();
   const unsigned long long W = s_W;
