@@ -493,6 +493,57 @@ def test_chunked_commit_fused_matches_oracle(name, T, chunk, kw):
     _check_commit_against_oracle(s, w, st)
 
 
+def test_chunked_commit_in_one_chunk_equals_the_one_pass_fused_commit():
+    # a chunk that holds every row: the chunked step with its fused commit
+    # leaves exactly the state of sv_accept_commit after sv_tree_attend
+    kw = dict(n_req=24, ctx_scale=0.02, vocab=1024, temperature=0.7, draft_sigma=0.5)
+    w = wl.make_workload(wl.config("batch64"), **kw)
+    a = DeviceStep(w, mode="chunked", chunk=w.max_rows)
+    a.run()
+    ra = a.results()
+    b = DeviceStep(w, mode="onepass")
+    b.run()
+    rb = b.results()
+    assert ra["dev_status"] == 0 and rb["dev_status"] == 0
+    for k in ("accepted_len", "accepted_nodes", "next_token", "ambiguous", "done"):
+        assert np.array_equal(ra[k], rb[k]), k
+    for x, y in ((a.kv.block_tables, b.kv.block_tables), (a.kv.cache_lens, b.kv.cache_lens),
+                 (a.pool.free_count, b.pool.free_count)):
+        assert torch.equal(x, y)
+    n = b.pool.free_count.item()
+    assert torch.equal(a.pool.free_list[:n], b.pool.free_list[:n])
+    assert torch.equal(a.kv.k_cache, b.kv.k_cache) and torch.equal(a.kv.v_cache, b.kv.v_cache)
+
+
+@pytest.mark.parametrize("vocab", [2, 3, 5])
+def test_accept_tiny_vocab_matches_oracle(vocab):
+    # one short race group (or one and a bit): the second step picks inside it
+    w = wl.make_workload(wl.config("batch64"), n_req=40, ctx_scale=0.01, vocab=vocab,
+                         temperature=1.0, draft_sigma=1.0)
+    s = DeviceStep(w, mode="onepass")
+    s.accept()
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits, 1.0, w.seed)
+    assert err == 0
+    _compare_accept(res, st, w, f"vocab {vocab}")
+
+
+def test_select_chunk_without_requests():
+    dev = "cuda"
+    e = torch.zeros(0, dtype=torch.int32, device=dev)
+    ch = torch.full((1,), -5, dtype=torch.int32, device=dev)
+    cost = torch.full((1,), 7, dtype=torch.int64, device=dev)
+    costs = torch.zeros(128, dtype=torch.int64, device=dev)
+    api.sv_select_chunk(e, e, torch.zeros((0, 2), dtype=torch.float64, device=dev), 4096.0, 1.0,
+                        1000, ch, cost, costs)
+    torch.cuda.synchronize()
+    err, och, ocost, ocosts = oracle.select_chunk([], [], np.zeros((0, 2)), 4096.0, 1.0, 1000)
+    assert err == 0
+    assert ch.item() == och and cost.item() == ocost
+    assert np.array_equal(costs.cpu().numpy().view(np.uint64), ocosts)
+
+
 def test_chunked_commit_invalid_window_is_left_alone():
     # one request with verify_len < 0: reported, never listed, never
     # committed; every other request is committed and the release still runs
