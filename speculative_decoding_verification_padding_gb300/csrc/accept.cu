@@ -159,6 +159,7 @@ struct Args {
   int race_all;   // race kernel: every request 0..R-1 instead of the active list
   int clear_jobs; // stats kernel: first clear every request's sampling job and race ticket
   int use_list;   // the requests come from the active list (chunked steps)
+  const int4* act4;  // with the list: (request, first row, rows, draft rows) per entry
   int commit;     // fused KV commit (sv_accept_commit)
   CommitArgs kv;
 };
@@ -550,14 +551,24 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
     const long rest = item / nch;
     const int type = (int)(rest % ntypes);
     const long ro = rest / ntypes;
-    int i, j, off;
+    int i, j, off, r, ndraft;
     Window w;
-    if (listed) {
+    if (listed && a.act4) {
+      // the planner's row range of the listed request: one load
+      off = (int)(ro % maxw);
+      const int4 e4 = a.act4[ro / maxw];
+      if (off >= e4.z) continue;
+      i = e4.x;
+      r = e4.y + off;
+      ndraft = T > 0.f ? e4.w : 0;
+    } else if (listed) {
       off = (int)(ro % maxw);
       i = act[ro / maxw];
       w = window_of(a.bt, i);
       j = w.b + off;
       if (j >= w.e) continue;
+      ndraft = T > 0.f ? max(0, min(w.e, w.lim - 1) - w.b) : 0;
+      r = a.bt.cu_rows[i] + j;
     } else {
       // packed row ro of request i
       i = find_segment(a.bt.cu_rows, R, (int)ro);
@@ -566,10 +577,10 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
       j = (int)ro - a.bt.cu_rows[i];
       if (j < w.b || j >= w.e) continue;
       off = j - w.b;
+      ndraft = T > 0.f ? max(0, min(w.e, w.lim - 1) - w.b) : 0;
+      r = (int)ro;
     }
-    const int ndraft = T > 0.f ? max(0, min(w.e, w.lim - 1) - w.b) : 0;
     if (type == 1 && off >= ndraft) continue;
-    const int r = a.bt.cu_rows[i] + j;
     const float* row = (type ? a.draft : a.target) + (size_t)r * a.V;
     const int lo = c * chl;
     const int hi = min(a.V, lo + chl);
@@ -1402,7 +1413,7 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
               int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
               float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s,
               int maxw, int chunk_index, const sv_paged_kv* commit_kv,
-              const sv_block_pool* commit_pool) {
+              const sv_block_pool* commit_pool, const int4* act4) {
   const bool chunk_step = chunk_index >= 0;
   sv_status st = check_accept_args(bt, target_logits, draft_logits, vocab, temperature,
                                    accepted_len, accepted_nodes, next_token, ambiguous, ws);
@@ -1445,6 +1456,7 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   const bool vec = vec_ok(vocab, target_logits, draft_logits);
   a.use_list = chunk_step ? 1 : 0;
+  a.act4 = chunk_step ? act4 : nullptr;
   const long items = (long)bt->n_req * a.L.maxw * (temperature > 0.f ? 2 : 1) * a.L.nch_cap;
   const long warps = kStatThreads / 32;
   const unsigned gs = (unsigned)max(1L, min((items + warps - 1) / warps, (long)kNumSMs * 4));

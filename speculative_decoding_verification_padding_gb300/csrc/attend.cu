@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     ri.nblk = nblk;
     ri.nsplit = 0;
     ri.ubase = 0;
-    ri.act = (!badw && w.b < w.e) ? 1 : 0;
+    // listed: 1 + the window's rows with a tested child (draft rows)
+    ri.act = (!badw && w.b < w.e) ? 1 + max(0, min(w.e, w.lim - 1) - w.b) : 0;
     ri.cu = cu;
     ri.rows = w.rows;
     info[i] = ri;
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
       const ReqInfo ri = info[i];
       const int nsplit = ri.valid ? (ri.nblk + P - 1) / P : 0;
       units = ri.nrt * a.Hkv * nsplit;
-      act = ri.act;
+      act = ri.act != 0;
       info[i].nsplit = nsplit;
     }
     int excl, total;
@@ -291,7 +292,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     if (chunked) {
       int aexcl, atotal;
       block_excl_scan(s_warp, act, aexcl, atotal);
-      if (act) a.chunk.act[s_acarry + aexcl] = i;
+      if (act) {
+        const ReqInfo ri = info[i];
+        a.chunk.act[s_acarry + aexcl] = i;
+        a.chunk.act4[s_acarry + aexcl] = make_int4(i, ri.cu + ri.b, ri.e - ri.b, ri.act - 1);
+      }
       __syncthreads();
       if (tid == 0) s_acarry += atotal;
     }

@@ -34,7 +34,11 @@ __global__ void __launch_bounds__(256) windows_kernel(sv_batch bt, int c, int cs
   re[i] = w.e;
 }
 
-inline size_t windows_bytes(int R) { return align256(sizeof(int32_t) * (size_t)R) * 2; }
+// The chunk driver's own part of the workspace: row_begin and row_end [R],
+// then the accept list's row ranges [R] (int4 per listed request).
+inline size_t windows_bytes(int R) {
+  return align256(sizeof(int32_t) * (size_t)R) * 2 + align256(sizeof(int4) * (size_t)R);
+}
 
 }  // namespace chk
 }  // namespace sv
@@ -247,6 +251,7 @@ sv_status verify_chunked(const sv_paged_kv* kv, const sv_batch* bt, const void* 
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* rb = reinterpret_cast<int32_t*>(w);
   int32_t* re = reinterpret_cast<int32_t*>(w + align256(sizeof(int32_t) * (size_t)bt->n_req));
+  int4* act4 = reinterpret_cast<int4*>(w + 2 * align256(sizeof(int32_t) * (size_t)bt->n_req));
   uint8_t* acc_ws = w + chk::windows_bytes(bt->n_req);
   uint8_t* att_ws = acc_ws + align256(AL.total);
   sv_batch b2 = *bt;
@@ -257,13 +262,13 @@ sv_status verify_chunked(const sv_paged_kv* kv, const sv_batch* bt, const void* 
   for (int c = 0; c < n_chunks; ++c) {
     // The planner turns `done` into this chunk's windows and the accept list.
     const attn::ChunkPlan cp{c, chunk_size, done, rb, re,
-                             reinterpret_cast<int32_t*>(acc_ws + AL.act)};
+                             reinterpret_cast<int32_t*>(acc_ws + AL.act), act4};
     sv_status st = attn::tree_attend(kv, bt, q, n_q_heads, softmax_scale, out, att_ws, wa,
                                      dev_status, s, cp);
     if (st != SV_OK) return st;
     st = acc::run(&b2, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
                   accepted_nodes, next_token, ambiguous, done, nullptr, acc_ws, AL.total,
-                  dev_status, s, chunk_size, c, commit ? kv : nullptr, pool);
+                  dev_status, s, chunk_size, c, commit ? kv : nullptr, pool, act4);
     if (st != SV_OK) return st;
   }
   // Nothing in a later chunk depends on the drawn tokens: one race pass

@@ -32,7 +32,7 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
               int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
               float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s,
               int maxw, int chunk_index, const sv_paged_kv* commit_kv = nullptr,
-              const sv_block_pool* commit_pool = nullptr);
+              const sv_block_pool* commit_pool = nullptr, const int4* act4 = nullptr);
 
 // After the last chunk of a chunked step (T > 0): the residual or bonus draw
 // of every request whose decision set one, in a single pass.
