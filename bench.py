@@ -431,6 +431,13 @@ def main():
              "accept": {"us_per_step": t_acc * 1e6, "GB/s": acc_gbs}}
     if mode == "budget":
         calls["select_budget"] = {"us_per_step": t_sel * 1e6}
+    if mode == "chunked":
+        # The per-call accept above runs a public sv_accept per chunk, each with
+        # its own resampling race; inside the step the chunks share one race.
+        # Derived: the step's time less its attention calls, over the same bytes.
+        t_in = max(t_step - t_att, 1e-9)
+        calls["accept_in_step"] = {"us_per_step": t_in * 1e6, "GB/s": sum(acc_b) / t_in / 1e9,
+                                   "derived": "step time - attention calls"}
 
     # ---- one-pass attention and accept on the whole batch (chunked workload) ----
     if mode == "chunked":
