@@ -1,4 +1,6 @@
-// chunk.cu — chunked verification with early pruning, and the status strings.
+// chunk.cu — chunked verification with early pruning (with the KV commit
+// fused in), the chunk-size rule, the bounded-wait self test and the status
+// strings.
 //
 // Source: [FASER] "FASER의 세 가지 메커니즘", mechanism 2 (early token
 // pruning: verification is cut into chunks and, at every chunk boundary, the
@@ -11,8 +13,11 @@
 // (requests that are done get an empty window, which every later kernel
 // skips) and the accept list, the attention runs on those windows, then the
 // accept statistics and decisions; one race pass after the last chunk draws
-// every request's emitted token.  sv_chunk_windows exposes the window rule
-// on its own.
+// every request's emitted token.  With the fused commit, the decision that
+// stops a request also commits it, and the last request to stop releases the
+// freed blocks.  sv_chunk_windows exposes the window rule on its own;
+// sv_select_chunk prices each chunk size for the next step (the FASER remark
+// that the chunk size follows the load).
 
 #include "sv_accept_internal.h"
 #include "sv_attend_internal.h"
