@@ -33,9 +33,8 @@
 // target distribution preserved).
 //
 // Parity status of each function (what pins it) is listed in the tests; the
-// Philox generator's identity with the published Random123 streams is
-// parity unpinned (no known-answer vectors are available here); it is pinned
-// statistically and by bitwise agreement of two independent implementations.
+// Philox generator reproduces the published Random123 known-answer vectors
+// (tests/golden/philox4x32_10_kat.txt) and is pinned statistically as well.
 
 #include <algorithm>
 #include <cmath>

@@ -14,6 +14,8 @@ uniformity, counter and key sensitivity.
 
 import itertools
 
+import os
+
 import numpy as np
 import pytest
 from scipy import stats
@@ -221,6 +223,21 @@ def test_philox_race_uniforms_open_interval_and_fp32_exact():
     a = np.array([oracle.race_uniform(7, 3, 5, g) for g in range(4000)])
     b = np.array([oracle.pick_uniform(7, 3, 5, g) for g in range(4000)])
     assert abs(np.corrcoef(a, b)[0, 1]) < 0.05
+
+
+def test_philox_reproduces_the_published_known_answer_vectors():
+    # Random123's known-answer vectors for philox4x32 with 10 rounds (Salmon
+    # et al., SC'11), read from tests/golden
+    path = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
+    n = 0
+    for line in open(path):
+        if not line.strip() or line.startswith("#"):
+            continue
+        w = [int(x, 16) for x in line.split()]
+        ctr, key, want = w[:4], w[4:6], w[6:10]
+        assert [int(x) for x in oracle.philox4x32_10(ctr, key)] == want, line
+        n += 1
+    assert n == 3
 
 
 def test_philox_counter_and_key_sensitivity():
