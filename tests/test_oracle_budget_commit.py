@@ -13,7 +13,6 @@ uniformity, counter and key sensitivity.
 """
 
 import itertools
-
 import os
 
 import numpy as np
