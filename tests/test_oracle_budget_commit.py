@@ -7,9 +7,9 @@ Theta = tau * SPS(B).
 Commit ([SwiftSpec] mechanism 2): conservation of blocks, no duplicates,
 committed slot k == staged row path[k], the released blocks are exactly
 those past the new length.
-Philox4x32-10: its identity with the published generator is parity
-unpinned (no known-answer vectors available); here it is checked for
-uniformity, counter and key sensitivity.
+Philox4x32-10: the published Random123 known-answer vectors
+(tests/golden/philox4x32_10_kat.txt), uniformity, counter and key
+sensitivity.
 """
 
 import itertools
