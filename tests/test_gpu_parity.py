@@ -493,6 +493,33 @@ def test_chunked_commit_fused_matches_oracle(name, T, chunk, kw):
     _check_commit_against_oracle(s, w, st)
 
 
+def test_more_requests_than_the_planner_keeps_in_shared_memory():
+    # 1300 requests: the planner's per-request records live in the workspace,
+    # its threads take several requests each; one-pass attention and a chunked
+    # step with the fused commit, both against the oracle
+    w = wl.make_workload(wl.config("batch64"), n_req=1300, ctx_scale=0.002, vocab=64,
+                         temperature=0.7, draft_sigma=0.7)
+    s = DeviceStep(w, mode="onepass")
+    s.out.fill_(float("nan"))
+    s.attend()
+    torch.cuda.synchronize()
+    assert s.dev_status.item() == 0
+    err, _, ref64 = oracle.tree_attend(w.batch(), w.kv(), w.q, w.cfg.n_q_heads, w.softmax_scale)
+    assert err == 0
+    _check_attention(s.out, ref64, np.arange(w.total_rows))
+    c = DeviceStep(w, mode="chunked")
+    c.run()
+    res = c.results()
+    assert res["dev_status"] == 0
+    err, st, _, _, _ = oracle.verify_chunked(
+        w.batch(), w.kv(), w.q, w.cfg.n_q_heads, w.softmax_scale, w.target_logits,
+        w.draft_logits, 0.7, w.seed, chunk=2)
+    assert err == 0
+    _compare_accept(res, st, w, "1300 requests chunked")
+    lens = c.kv.cache_lens.cpu().numpy()
+    assert np.array_equal(lens, w.cache_lens + 1 + res["accepted_len"])
+
+
 def test_chunked_commit_in_one_chunk_equals_the_one_pass_fused_commit():
     # a chunk that holds every row: the chunked step with its fused commit
     # leaves exactly the state of sv_accept_commit after sv_tree_attend
