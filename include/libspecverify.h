@@ -330,7 +330,10 @@ sv_status sv_select_budget(int32_t n_req, int32_t gamma_max, const float* cond_s
  * stopped request is never attended again, so moving its K/V mid-step
  * changes nothing the later chunks read.  Requests whose window is invalid
  * are left as they were; one whose parents or tokens are invalid is flagged,
- * stops (done = 1) and is left as it was. */
+ * stops (done = 1) and is left as it was.  pool is required and kv must meet
+ * the commit's rules (16-token blocks, head_dim 64 or 128, K and V caches
+ * 16-byte aligned): else SV_ERR_INVALID_ARGUMENT / SV_ERR_UNSUPPORTED_SHAPE
+ * before anything is enqueued. */
 sv_status sv_chunk_windows(const sv_batch* batch, int32_t chunk_index, int32_t chunk_size,
                            const int32_t* done, int32_t* row_begin, int32_t* row_end,
                            void* stream);
@@ -374,7 +377,10 @@ sv_status sv_verify_chunked_commit(const sv_paged_kv* kv, const sv_batch* batch,
  * cost, costs [128]: cost(c) at c - 1 (UINT64_MAX past max_rows).  A chunk of
  * max_rows is one-pass verification.  Requests with rows outside [1, 128],
  * ctx < 0 or a state that is not finite and non-negative set
- * SV_DEV_BAD_LENGTH and are left out.  All pointers are device memory. */
+ * SV_DEV_BAD_LENGTH and are left out; with no valid request *chunk = 1 and
+ * *cost = 0.  All pointers are device memory.  n_req < 0, negative or
+ * infinite byte sizes, or a missing output: SV_ERR_INVALID_ARGUMENT before
+ * anything is enqueued. */
 sv_status sv_select_chunk(int32_t n_req, const int32_t* rows, const int32_t* ctx,
                           const double* state, double kv_bytes, double row_bytes,
                           uint64_t chunk_bytes, int32_t* chunk, uint64_t* cost, uint64_t* costs,
