@@ -535,6 +535,9 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
       reinterpret_cast<Job*>(a.ws + a.L.jobs)[i].mode = 0;
       reinterpret_cast<int*>(a.ws + a.L.race_tickets)[i] = 0;
       reinterpret_cast<int*>(a.ws + a.L.race_tickets)[R + i] = 0;
+      // fused commit: a request no chunk lists (invalid window) never writes
+      // its released span, which the release still reads
+      if (a.commit) reinterpret_cast<int2*>(a.ws + a.L.cspan)[i] = make_int2(0, 0);
     }
   }
   const bool listed = a.use_list != 0;

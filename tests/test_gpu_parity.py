@@ -571,6 +571,75 @@ def test_select_chunk_without_requests():
     assert np.array_equal(costs.cpu().numpy().view(np.uint64), ocosts)
 
 
+@pytest.mark.parametrize("T", [0.7, 0.0])
+def test_chunked_commit_with_truncated_requests_matches_oracle(T):
+    # verify_len cuts some chains short (budget-selected prefixes verified in
+    # chunks): windows stop at verify_len + 1 rows, the commit still releases
+    # every staged row past the accepted path
+    w = wl.make_workload(wl.config("batch64"), n_req=40, ctx_scale=0.02, vocab=1024,
+                         temperature=T, draft_sigma=0.3)
+    rows = np.diff(w.cu_rows).astype(np.int32)
+    vl = np.minimum(rows - 1, np.random.default_rng(9).integers(0, 9, w.n_req)).astype(np.int32)
+    s = DeviceStep(w, mode="chunked")
+    b = api.Batch(s.batch.cu_rows, s.batch.parent, s.batch.tokens, w.max_rows,
+                  verify_len=torch.from_numpy(vl).cuda())
+    api.sv_verify_chunked_commit(s.kv, b, s.q, s.Hq, s.scale, s.out, s.target, s.draft, s.V, s.T,
+                                 w.seed, 2, s.accepted_len, s.accepted_nodes, s.next_token,
+                                 s.ambiguous, s.done, s.pool, s.ws, s.dev_status)
+    res = s.results()
+    assert res["dev_status"] == 0
+    err, st, _, _, _ = oracle.verify_chunked(
+        w.batch(verify_len=vl), w.kv(), w.q, w.cfg.n_q_heads, w.softmax_scale, w.target_logits,
+        w.draft_logits if T > 0 else None, T, w.seed, chunk=2)
+    assert err == 0
+    _compare_accept(res, st, w, f"chunked commit verify_len T={T}")
+    assert (st.accepted_len <= vl).all()
+    if (st.ambiguous != 0).any() or (res["ambiguous"] != 0).any():
+        pytest.skip("an ambiguous decision: the commit inputs differ by construction")
+    _check_commit_against_oracle(s, w, st, vl=vl)
+
+
+@pytest.mark.parametrize("mode,name,kw", [
+    ("onepass", "batch64", dict(n_req=24, ctx_scale=0.02, vocab=1024, temperature=0.7)),
+    ("chunked", "batch64", dict(n_req=24, ctx_scale=0.02, vocab=1024, temperature=0.7)),
+    ("budget", "batch256", dict(n_req=48, ctx_scale=0.01, vocab=512)),
+    ("onepass", "tree70b", dict(ctx_scale=0.01, vocab=512, temperature=1.0, draft_sigma=0.3)),
+])
+def test_results_do_not_depend_on_workspace_contents(mode, name, kw):
+    # every workspace word a call reads is written by that call first: the
+    # same step on a zeroed and on a garbage-filled workspace (one request
+    # with an invalid window in the chunked case) leaves the same state
+    w = wl.make_workload(wl.config(name), **kw)
+    vl = None
+    if mode == "chunked":
+        vl = np.diff(w.cu_rows).astype(np.int32) - 1
+        vl[3] = -1
+
+    def run(fill):
+        s = DeviceStep(w, mode=mode)
+        s.ws.fill_(fill)
+        if mode == "chunked":
+            b = api.Batch(s.batch.cu_rows, s.batch.parent, s.batch.tokens, w.max_rows,
+                          verify_len=torch.from_numpy(vl).cuda())
+            api.sv_verify_chunked_commit(s.kv, b, s.q, s.Hq, s.scale, s.out, s.target, s.draft,
+                                         s.V, s.T, w.seed, 2, s.accepted_len, s.accepted_nodes,
+                                         s.next_token, s.ambiguous, s.done, s.pool, s.ws,
+                                         s.dev_status)
+        else:
+            s.run()
+        res = s.results()
+        n = s.pool.free_count.item()
+        return res, (s.kv.block_tables.cpu(), s.kv.cache_lens.cpu(), s.pool.free_list[:n].cpu(),
+                     s.kv.k_cache.cpu(), s.out.cpu())
+
+    r0, c0 = run(0)
+    r1, c1 = run(0xA5)
+    for k in ("accepted_len", "accepted_nodes", "next_token", "ambiguous", "dev_status"):
+        assert np.array_equal(r0[k], r1[k]), k
+    for x, y in zip(c0, c1):
+        assert torch.equal(x, y)
+
+
 def test_chunked_commit_invalid_window_is_left_alone():
     # one request with verify_len < 0: reported, never listed, never
     # committed; every other request is committed and the release still runs
