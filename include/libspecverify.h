@@ -49,6 +49,10 @@
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  Errors that the host can see (null pointers, bad
  *     sizes, small workspace) are returned before anything is enqueued.
+ *   - A workspace (`ws`) is scratch owned by the caller: its contents need no
+ *     initialisation and are not kept between calls (every word a call reads
+ *     it has written first).  Two calls whose work overlaps on the GPU need
+ *     separate workspaces.
  *   - Errors that depend on device data (a block id out of range, a parent
  *     that is not an earlier row, an invalid window, a full free list) are
  *     OR-ed as SV_DEV_* bits into *dev_status (a caller-owned device int32
