@@ -226,10 +226,29 @@ def cpu_baseline(w, mode, budget_s=10.0):
     dt1, _ = time_oracle(w, mode, [0], threads)
     n = int(max(1, min(w.n_req, budget_s / max(dt1, 1e-3))))
     dt, att = time_oracle(w, mode, list(range(n)), threads)
+    # the same oracle on one thread, on a smaller sample of the same step
+    d1, _ = time_oracle(w, mode, [0], 1)
+    n1 = int(max(1, min(n, 0.5 * budget_s / max(d1, 1e-3))))
+    dts, atts = time_oracle(w, mode, list(range(n1)), 1)
     return {"value": att / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"first {n} of {w.n_req} requests of the same step ({mode}: attention + "
                       f"accept), {att} rows attended in {dt:.2f} s, fp64 C++ oracle with "
-                      f"{threads} threads"}
+                      f"{threads} threads",
+            "single_thread": {"value": atts / dts, "unit": UNIT,
+                              "sample": f"first {n1} requests, {atts} rows in {dts:.2f} s"},
+            "cpu_model": cpu_model()}
+
+
+def cpu_model():
+    """The host CPU as lscpu names it (model name and count of online CPUs)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        info = dict(l.split(":", 1) for l in out.splitlines() if ":" in l)
+        name = (info.get("Model name") or info.get("Vendor ID") or "").strip()
+        cpus = (info.get("CPU(s)") or "").strip()
+        return f"{name}, {cpus} CPUs" if name else None
+    except Exception:
+        return None
 
 
 # ------------------------------------------------------------------- main --
