@@ -1180,9 +1180,10 @@ __global__ void __launch_bounds__(kRaceThreads, 3) race_kernel(Args a) {
     // monotone in the logit; the factor 1 + 2^-16 covers the rounding of p
     // and of the sum), and E_g >= 1 - u_g, so a group with B_g < K (1 - u_g)
     // (less a 2^-20 margin) cannot win: its exact mass, draft probabilities
-    // and logarithm are never computed.  While K is 0 (the first block) every
-    // group is keyed exactly.  The trip count is uniform across the warp so
-    // that the lanes can share K.
+    // and logarithm are never computed.  While K is 0 (the first block) each
+    // lane first keys its group with the largest B_g / (1 - u_g) exactly, and
+    // the best of those keys bounds the rest.  The trip count is uniform
+    // across the warp so that the lanes can share K.
     int* kbest = reinterpret_cast<int*>(a.ws + a.L.race_tickets) + R + i;
     float bw = -1.f, bE = 1.f, K = 0.f;
     int bi = 0x7fffffff;
