@@ -332,6 +332,21 @@ def test_budget_random_matches_oracle(trial):
     assert np.array_equal(vl, vl_o) and bB == bB_o and th == th_o
 
 
+@pytest.mark.parametrize("R,gmax", [(1024, 8), (8192, 1), (2048, 4)])
+def test_budget_at_the_largest_candidate_count_matches_oracle(R, gmax):
+    # n_req * gamma_max = 8192 candidates, the documented limit, with many
+    # equal survivals (tie order) and an SPS table long enough for every B
+    rng = np.random.default_rng(R + gmax)
+    c = (np.round(rng.beta(4, 2, size=(R, gmax)) * 16) / 16).astype(np.float32)
+    gamma = rng.integers(0, gmax + 1, R).astype(np.int32)
+    B = np.arange(R + R * gmax + 1, dtype=np.float64)
+    sps = (1000.0 / (1.0 + B / 2048.0)).astype(np.float32)
+    vl, bB, th, st = _budget_gpu(c, gamma, sps)
+    err, vl_o, bB_o, th_o = oracle.select_budget(c, gamma, sps)
+    assert st == 0 and err == 0
+    assert np.array_equal(vl, vl_o) and bB == bB_o and th == th_o
+
+
 # ------------------------------------------------------------ draft length --
 
 @pytest.mark.parametrize("trial", range(4))
