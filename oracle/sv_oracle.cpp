@@ -777,8 +777,11 @@ int orc_select_budget(int n_req, int gamma_max, const float* cond_survival, cons
       if (!(c >= 0.0f && c <= 1.0f)) return ORC_BAD_ARG;
       s = s * c;
       S[(long)i * gamma_max + k - 1] = s;
+      // The sort is by the value of S: -0 (from a factor c = -0) is the same
+      // survival as +0 and takes +0's key.
+      const float key_s = (s == 0.0f) ? 0.0f : s;
       uint32_t bits;
-      std::memcpy(&bits, &s, 4);
+      std::memcpy(&bits, &key_s, 4);
       keys.push_back(((uint64_t)(~bits) << 32) | (uint64_t)(i * gamma_max + k - 1));
     }
   }

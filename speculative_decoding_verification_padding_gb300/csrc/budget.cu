@@ -10,7 +10,8 @@
 //
 // One CTA of 1024 threads:
 //   1. S_{i,k} = c_{i,1} * ... * c_{i,k} (fp32, left to right); sort key
-//      ~bits(S) (S is non-negative, so the bits order like the values).
+//      ~bits(S) (S is non-negative, so the bits order like the values; -0 is
+//      keyed as +0).
 //   2. Stable LSD radix sort of the 32-bit keys, 8-bit digits, 4 passes,
 //      in shared memory; candidates enter in (request, position) order, so
 //      equal S keep the lower request, then the lower position.  Ranking
@@ -112,7 +113,9 @@ __global__ void __launch_bounds__(kThreads) budget_kernel(Args a) {
         s = s * ck;
         const int idx = s_carry + excl + k - 1;
         if (idx < kMaxCand) {
-          kA[idx] = ~__float_as_uint(s);
+          // a survival of -0 (a factor c = -0) is the value 0: its key is +0's
+          const uint32_t sb = __float_as_uint(s);
+          kA[idx] = ~(sb == 0x80000000u ? 0u : sb);
           vA[idx] = (uint32_t)(i * gmax + k - 1);
         }
       }
@@ -273,6 +276,7 @@ extern "C" sv_status sv_select_budget(int32_t n_req, int32_t gamma_max, const fl
                                       int32_t* verify_len, int32_t* best_B, double* best_theta,
                                       void* ws, size_t ws_bytes, int32_t* dev_status,
                                       void* stream) {
+  SV_TRACE("sv_select_budget");
   (void)ws;
   (void)ws_bytes;
   if (n_req < 1 || gamma_max < 0 || b_max < n_req) return SV_ERR_INVALID_ARGUMENT;
@@ -282,15 +286,8 @@ extern "C" sv_status sv_select_budget(int32_t n_req, int32_t gamma_max, const fl
   bud::Args a{n_req, gamma_max, b_max, cond_survival, gamma, sps, verify_len, best_B, best_theta,
               dev_status};
   const size_t smem = bud::smem_bytes();
-  static int attr_dev_mask = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!(attr_dev_mask & (1 << (dev & 31)))) {
-    if (cudaFuncSetAttribute(bud::budget_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return SV_ERR_CUDA;
-    attr_dev_mask |= 1 << (dev & 31);
-  }
+  static PerDevice smem_set;  // the keys live in 160 KB of shared memory
+  if (smem_limit_once(smem_set, bud::budget_kernel, smem) != cudaSuccess) return SV_ERR_CUDA;
   if (sv::launch(bud::budget_kernel, 1, bud::kThreads, smem, static_cast<cudaStream_t>(stream), a) !=
       cudaSuccess)
     return SV_ERR_CUDA;

@@ -349,6 +349,30 @@ def test_budget_at_the_largest_candidate_count_matches_oracle(R, gmax):
 
 # ------------------------------------------------------------ draft length --
 
+def test_budget_negative_zero_survival_matches_oracle():
+    """Survival factors of -0.0 mixed in: the kernel keys them as +0, like the
+    oracle."""
+    rng = np.random.default_rng(5)
+    R, gmax = 200, 4
+    c = rng.beta(4, 2, size=(R, gmax)).astype(np.float32)
+    c[rng.random(c.shape) < 0.2] = np.float32(-0.0)
+    gamma = rng.integers(0, gmax + 1, R).astype(np.int32)
+    sps = (1000.0 / (1.0 + np.arange(R * (gmax + 1) + 1) / 256.0)).astype(np.float32)
+    err, vl, bB, th = oracle.select_budget(c, gamma, sps)
+    assert err == 0
+    dev = "cuda"
+    out_vl = torch.zeros(R, dtype=torch.int32, device=dev)
+    out_B = torch.zeros(1, dtype=torch.int32, device=dev)
+    out_th = torch.zeros(1, dtype=torch.float64, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    api.sv_select_budget(torch.from_numpy(c).to(dev), torch.from_numpy(gamma).to(dev),
+                         torch.from_numpy(sps).to(dev), out_vl, out_B, out_th, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(out_vl.cpu().numpy(), vl)
+    assert out_B.item() == bB and out_th.item() == th
+
+
 @pytest.mark.parametrize("trial", range(4))
 def test_adapt_gamma_matches_oracle(trial):
     rng = np.random.default_rng(500 + trial)

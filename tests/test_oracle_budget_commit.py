@@ -98,6 +98,33 @@ def test_budget_constant_sps_admits_everything_that_fits():
     assert vl.sum() == 7 and best_B == 17
 
 
+def test_budget_negative_zero_survival_is_zero():
+    """A conditional survival of -0.0 is the value 0: its candidates sort with
+    the other zero survivals, after every positive one.  (Keyed by its raw
+    bits, ~bits(-0.0) would put them first.)"""
+    c = np.array([[0.9, 0.8], [-0.0, 0.7]], dtype=np.float32)
+    gamma = np.array([2, 2], dtype=np.int32)
+    sps = np.array([1.0, 1.0, 1.0, 1.0, 0.0, 0.0, 0.0], dtype=np.float32)  # at most one admitted
+    err, vl, best_B, theta = oracle.select_budget(c, gamma, sps)
+    assert err == 0
+    assert list(vl) == [1, 0] and best_B == 3
+    assert theta == pytest.approx(2.9, rel=1e-6)
+    ref_theta, ref_L, _ = _brute_force(c, gamma, sps)
+    assert tuple(vl) == tuple(ref_L) and theta == pytest.approx(ref_theta, rel=1e-9)
+    # the same selection as with +0.0 in its place, on random inputs too
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        c = rng.beta(4, 2, size=(6, 3)).astype(np.float32)
+        zero = rng.random(c.shape) < 0.3
+        c_pos = np.where(zero, np.float32(0.0), c).astype(np.float32)
+        c_neg = np.where(zero, np.float32(-0.0), c).astype(np.float32)
+        gamma = rng.integers(0, 4, 6).astype(np.int32)
+        sps = (1000.0 / (1.0 + np.arange(6 + 18 + 1) / 4.0)).astype(np.float32)
+        a = oracle.select_budget(c_pos, gamma, sps)
+        b = oracle.select_budget(c_neg, gamma, sps)
+        assert np.array_equal(a[1], b[1]) and a[2] == b[2] and a[3] == b[3]
+
+
 def test_budget_full_size_has_interior_optimum():
     w = wl.make_workload(wl.config("batch256"), vocab=64, ctx_scale=0.001)
     err, vl, best_B, theta = oracle.select_budget(w.cond_survival, w.gamma, w.sps)
