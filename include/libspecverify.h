@@ -263,7 +263,9 @@ sv_status sv_accept_commit(const sv_batch* batch, const float* target_logits,
  *     anything is enqueued; use sv_accept with a workspace beyond that.
  *   - The first call on a device, with that device current, looks up the
  *     array's device address once; make that first call before any stream
- *     capture begins.
+ *     capture begins.  The address is kept for the life of the process: a
+ *     device reset (cudaDeviceReset) ends the context it belongs to, so do
+ *     not call sv_accept_static on a device after resetting it.
  *   - Every call shares the one array: calls whose work overlaps on the GPU
  *     (for instance on two streams) race on it and must be ordered by the
  *     caller. */

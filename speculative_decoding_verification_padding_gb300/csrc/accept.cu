@@ -71,25 +71,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 // flight, slices of at least 2 KB.
 constexpr int kMaxSlices = 64;  // vocabulary slices per row at most
 
-inline int stats_chunks(int rows_bound, int V) {
+inline int stats_chunks(int rows_bound, int V, int nsm) {
   const int maxc = max(1, min(kMaxSlices, V / 512));
-  const int want = (kNumSMs * 32 + 2 * rows_bound - 1) / max(1, 2 * rows_bound);
+  const int want = (nsm * 32 + 2 * rows_bound - 1) / max(1, 2 * rows_bound);
   return max(1, min(want, maxc));
 }
-inline int race_chunks(int R, int V) {
+inline int race_chunks(int R, int V, int nsm) {
   const int maxc = max(1, min(1024, V / 512));
-  const int want = (kNumSMs * 32 + R - 1) / max(1, R);
+  const int want = (nsm * 32 + R - 1) / max(1, R);
   return max(1, min(want, maxc));
 }
 inline __host__ __device__ int chunk_len(int V, int nch) { return ((V + nch - 1) / nch + 3) & ~3; }
 
 Layout layout(int R, int total_rows, int V, int maxw, bool commit) {
   Layout L;
+  L.nsm = sizing_sms();
   L.maxw = max(1, min(maxw, kMaxRows));
   const long bound = min((long)total_rows, (long)R * L.maxw);
-  L.nch = stats_chunks((int)max(1L, bound), V);
+  L.nch = stats_chunks((int)max(1L, bound), V, L.nsm);
   L.nch_cap = max(L.nch, min(min(kMaxSlices, V / 2048), 16384 / max(1, total_rows)));
-  L.nch_r = race_chunks(R, V);
+  L.nch_r = race_chunks(R, V, L.nsm);
   L.nch_r_cap = max(L.nch_r, min(min(256, V / 512), 16384 / max(1, R)));
   size_t off = 0;
   L.parts = off; off += align256(sizeof(StatPart) * (size_t)total_rows * 2 * L.nch_cap);
@@ -116,14 +117,14 @@ __device__ __forceinline__ int stats_slices(const Layout& L, int count, int ntyp
   const long slots = listed ? (long)max(1, count) * L.maxw * ntypes
                             : (long)max(1, total_rows) * ntypes;
   const long per_warp = listed ? 2 : 4;
-  const long want = (per_warp * kNumSMs * 32 + slots - 1) / slots;
+  const long want = (per_warp * L.nsm * 32 + slots - 1) / slots;
   return (int)max((long)L.nch, min(want, (long)L.nch_cap));
 }
 // Race slices: at most one per warp of the race grid (24 warps per SM), so
 // that no warp takes two slices one after the other; slices of >= 2 KB.
 constexpr int kRaceWarpsPerSM = 24;
 __device__ __forceinline__ int race_slices(const Layout& L, int count, int V) {
-  const long want = (long)kNumSMs * kRaceWarpsPerSM / max(1, count);
+  const long want = (long)L.nsm * kRaceWarpsPerSM / max(1, count);
   const long cap = min((long)L.nch_r_cap, max(1L, (long)V / 512));
   return (int)max(1L, min(want, cap));
 }
@@ -1381,21 +1382,10 @@ static sv_status launch_race(const Args& a, bool vec, cudaStream_t s) {
   const long ritems = (long)a.bt.n_req * a.L.nch_r_cap;
   const long rwarps = kRaceThreads / 32;
   const unsigned gr = (unsigned)max(
-      1L, min((ritems + rwarps - 1) / rwarps, (long)kNumSMs * kRaceWarpsPerSM / rwarps));
+      1L, min((ritems + rwarps - 1) / rwarps, (long)a.L.nsm * kRaceWarpsPerSM / rwarps));
   if (vec) {
-    // the ring is above the 48 KB default: allowed once per device (calls may
-    // come from several host threads)
-    static std::mutex mu;
-    static bool set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!set[dev]) {
-      if (cudaFuncSetAttribute(race_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kRaceSmem) != cudaSuccess)
-        return SV_ERR_CUDA;
-      set[dev] = true;
-    }
+    static PerDevice smem_set;  // the ring is above the 48 KB default
+    if (smem_limit_once(smem_set, race_kernel<true>, kRaceSmem) != cudaSuccess) return SV_ERR_CUDA;
   }
   if (sv::launch(vec ? race_kernel<true> : race_kernel<false>, gr, kRaceThreads,
                  vec ? kRaceSmem : 0, s, a) != cudaSuccess)
@@ -1463,11 +1453,11 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
   a.act4 = chunk_step ? act4 : nullptr;
   const long items = (long)bt->n_req * a.L.maxw * (temperature > 0.f ? 2 : 1) * a.L.nch_cap;
   const long warps = kStatThreads / 32;
-  const unsigned gs = (unsigned)max(1L, min((items + warps - 1) / warps, (long)kNumSMs * 4));
+  const unsigned gs = (unsigned)max(1L, min((items + warps - 1) / warps, (long)a.L.nsm * 4));
   if (sv::launch(vec ? stats_kernel<true> : stats_kernel<false>, gs, kStatThreads, 0, s, a) !=
       cudaSuccess)
     return SV_ERR_CUDA;
-  const unsigned gd = (unsigned)max(1, min((bt->n_req + kDecideWarps - 1) / kDecideWarps, kNumSMs * 8));
+  const unsigned gd = (unsigned)max(1, min((bt->n_req + kDecideWarps - 1) / kDecideWarps, a.L.nsm * 8));
   if (sv::launch(decide_kernel, gd, kDecideWarps * 32, 0, s, a) != cudaSuccess) return SV_ERR_CUDA;
   if (temperature > 0.f && bt->max_rows_per_req > 2 &&
       (!chunk_step || (chunk_index == 0 && a.L.maxw > 2))) {
@@ -1520,6 +1510,7 @@ extern "C" sv_status sv_accept(const sv_batch* bt, const float* target_logits,
                                int32_t* next_token, uint8_t* ambiguous, int32_t* done,
                                float* row_stats, void* ws, size_t ws_bytes, int32_t* dev_status,
                                void* stream) {
+  SV_TRACE("sv_accept");
   if (!bt) return SV_ERR_INVALID_ARGUMENT;
   return acc::run(bt, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
                   accepted_nodes, next_token, ambiguous, done, row_stats, ws, ws_bytes, dev_status,
@@ -1539,6 +1530,7 @@ extern "C" sv_status sv_accept_commit(const sv_batch* bt, const float* target_lo
                                       uint8_t* ambiguous, int32_t* done, float* row_stats,
                                       const sv_paged_kv* kv, const sv_block_pool* pool, void* ws,
                                       size_t ws_bytes, int32_t* dev_status, void* stream) {
+  SV_TRACE("sv_accept_commit");
   if (!bt || !kv || !pool) return SV_ERR_INVALID_ARGUMENT;
   if (kv->block_size != kBlockSize) return SV_ERR_UNSUPPORTED_SHAPE;
   if (kv->head_dim != 64 && kv->head_dim != 128) return SV_ERR_UNSUPPORTED_SHAPE;
@@ -1560,7 +1552,9 @@ extern "C" sv_status sv_accept_commit(const sv_batch* bt, const float* target_lo
 // until the process exits.  The address of that array on the current device
 // is looked up once per device (cudaGetSymbolAddress) on the first call made
 // with that device current; make that first call before any stream capture.
-// All calls share the array: two calls whose work overlaps on the GPU (for
+// The cached address belongs to the device's context as it was then: after a
+// device reset it is stale, so the header tells callers not to use this entry
+// point on a device they have reset.  All calls share the array: two calls whose work overlaps on the GPU (for
 // example on two streams) race on it.  Nothing in it has to start at zero:
 // the accept kernels write every scratch word before they read it (the
 // decision clears every request's sampling job and race ticket before
@@ -1597,6 +1591,7 @@ extern "C" sv_status sv_accept_static(const sv_batch* bt, const float* target_lo
                                       int32_t* accepted_nodes, int32_t* next_token,
                                       uint8_t* ambiguous, int32_t* done, float* row_stats,
                                       int32_t* dev_status, void* stream) {
+  SV_TRACE("sv_accept_static");
   if (!bt || bt->n_req < 0 || bt->total_rows < 0 || vocab < 1) return SV_ERR_INVALID_ARGUMENT;
   const size_t need = sv_accept_workspace(bt, vocab);
   if (need > (size_t)SV_ACCEPT_STATIC_SCRATCH_BYTES) return SV_ERR_WORKSPACE_TOO_SMALL;

@@ -65,6 +65,7 @@ extern "C" sv_status sv_adapt_gamma(int32_t n_req, const int32_t* accepted_len,
                                     const int32_t* verified, double* state, int32_t* gamma_next,
                                     double decay, double overhead, int32_t gamma_min,
                                     int32_t gamma_max, int32_t* dev_status, void* stream) {
+  SV_TRACE("sv_adapt_gamma");
   if (n_req < 0 || gamma_min < 0 || gamma_max < gamma_min || gamma_max > kMaxRows - 1)
     return SV_ERR_INVALID_ARGUMENT;
   if (!(decay > 0.0 && decay <= 1.0) || !(overhead >= 0.0)) return SV_ERR_INVALID_ARGUMENT;

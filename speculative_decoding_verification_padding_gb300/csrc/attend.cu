@@ -53,17 +53,12 @@ constexpr int kStages = 3;       // TMA ring depth
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileRows = 64;    // virtual rows per unit
-#ifndef SV_ATTN_UNIT_TARGET
-#define SV_ATTN_UNIT_TARGET (kNumSMs * 8)
-#endif
-#ifndef SV_ATTN_MIN_PAGES
-#define SV_ATTN_MIN_PAGES 32
-#endif
-constexpr int kUnitTarget = SV_ATTN_UNIT_TARGET;
+// About this many units per SM are aimed for (two resident CTAs, four waves).
+constexpr int kUnitsPerSM = 8;
 // Splits never go below kMinPagesPerSplit pages (each unit pays a start-up
 // of a few microseconds and a merge share), nor below twice that when the
 // work still gives every SM such a unit.
-constexpr int kMinPagesPerSplit = SV_ATTN_MIN_PAGES;
+constexpr int kMinPagesPerSplit = 32;
 constexpr int kMaxPagesPerSplit = 1024;  // block ids of a unit staged in shared memory
 
 struct ReqInfo {
@@ -97,20 +92,24 @@ struct Header {
 struct Layout {
   size_t header, info, work, tickets, ml, o, total;
   int ucap;
+  int nsm;          // SMs of the device the call runs on
+  int unit_target;  // units the planner aims for: kUnitsPerSM per SM
 };
 
-// Units are at most W / P + Hkv * (row tiles): P >= W / kUnitTarget unless it
+// Units are at most W / P + Hkv * (row tiles): P >= W / unit_target unless it
 // is capped at kMaxPagesPerSplit, and W <= Hkv * (row tiles) * max_blocks.
-inline int unit_cap(int R, int total_rows, int group, int Hkv, int max_blocks) {
+inline int unit_cap(int R, int total_rows, int group, int Hkv, int max_blocks, int unit_target) {
   long nrt = (long)group * total_rows / kTileRows + R + 1;
   long rt_units = (long)Hkv * nrt;
-  return (int)(rt_units + kUnitTarget + (rt_units * max_blocks + kMaxPagesPerSplit - 1) / kMaxPagesPerSplit);
+  return (int)(rt_units + unit_target + (rt_units * max_blocks + kMaxPagesPerSplit - 1) / kMaxPagesPerSplit);
 }
 
 inline Layout layout(int R, int total_rows, int group, int Hkv, int D, int max_blocks) {
   Layout L;
   size_t off = 0;
-  L.ucap = unit_cap(R, total_rows, group, Hkv, max_blocks);
+  L.nsm = sizing_sms();
+  L.unit_target = L.nsm * kUnitsPerSM;
+  L.ucap = unit_cap(R, total_rows, group, Hkv, max_blocks, L.unit_target);
   L.header = off; off += align256(sizeof(Header));
   L.info = off; off += align256(sizeof(ReqInfo) * (size_t)R);
   L.work = off; off += align256(sizeof(WorkItem) * (size_t)L.ucap);
@@ -269,8 +268,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   if (lane == 0 && myW) atomicAdd(&s_W, myW);
   __syncthreads();
   const unsigned long long W = s_W;
-  int P = (int)min((unsigned long long)kMaxPagesPerSplit, (W + kUnitTarget - 1) / kUnitTarget);
-  const int Pmin = W >= (unsigned long long)kNumSMs * 2 * kMinPagesPerSplit ? 2 * kMinPagesPerSplit
+  const unsigned long long target = (unsigned long long)a.L.unit_target;
+  int P = (int)min((unsigned long long)kMaxPagesPerSplit, (W + target - 1) / target);
+  const int Pmin = W >= (unsigned long long)a.L.nsm * 2 * kMinPagesPerSplit ? 2 * kMinPagesPerSplit
                                                                             : kMinPagesPerSplit;
   if (P < Pmin) P = Pmin;
   // Work list offsets (exclusive scan of units per request); in chunk mode
@@ -830,15 +830,8 @@ static bool make_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv
 template <int D>
 sv_status launch(const Args& a, cudaStream_t stream) {
   const size_t smem = (size_t)kStages * StageLayout<D>::kStageBytes + 1024;
-  static int attr_dev_mask = 0;  // devices whose kernel attribute is set
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!(attr_dev_mask & (1 << (dev & 31)))) {
-    if (cudaFuncSetAttribute(attend_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return SV_ERR_CUDA;
-    attr_dev_mask |= 1 << (dev & 31);
-  }
+  static PerDevice smem_set;  // the ring is above the 48 KB default
+  if (smem_limit_once(smem_set, attend_kernel<D>, smem) != cudaSuccess) return SV_ERR_CUDA;
   CUtensorMap tmK, tmV;
   if (!make_map(&tmK, a.k, a.num_blocks, a.Hkv, D) || !make_map(&tmV, a.v, a.num_blocks, a.Hkv, D))
     return SV_ERR_CUDA;
@@ -926,6 +919,7 @@ sv_status tree_attend(const sv_paged_kv* kv, const sv_batch* bt, const void* q, 
 extern "C" sv_status sv_tree_attend(const sv_paged_kv* kv, const sv_batch* bt, const void* q,
                                     int32_t n_q_heads, float softmax_scale, void* out, void* ws,
                                     size_t ws_bytes, int32_t* dev_status, void* stream) {
+  SV_TRACE("sv_tree_attend");
   const attn::ChunkPlan none{-1, 0, nullptr, nullptr, nullptr, nullptr};
   return attn::tree_attend(kv, bt, q, n_q_heads, softmax_scale, out, ws, ws_bytes, dev_status,
                            static_cast<cudaStream_t>(stream), none);

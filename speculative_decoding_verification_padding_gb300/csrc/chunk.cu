@@ -19,6 +19,8 @@
 // sv_select_chunk prices each chunk size for the next step (the FASER remark
 // that the chunk size follows the load).
 
+#include <stdio.h>
+
 #include "sv_accept_internal.h"
 #include "sv_attend_internal.h"
 #include "sv_internal.cuh"
@@ -177,6 +179,7 @@ extern "C" sv_status sv_select_chunk(int32_t n_req, const int32_t* rows, const i
                                      const double* state, double kv_bytes, double row_bytes,
                                      uint64_t chunk_bytes, int32_t* chunk, uint64_t* cost,
                                      uint64_t* costs, int32_t* dev_status, void* stream) {
+  SV_TRACE("sv_select_chunk");
   if (n_req < 0 || !(kv_bytes >= 0.0) || !(row_bytes >= 0.0) || isinf(kv_bytes) ||
       isinf(row_bytes))
     return SV_ERR_INVALID_ARGUMENT;
@@ -195,6 +198,7 @@ extern "C" sv_status sv_select_chunk(int32_t n_req, const int32_t* rows, const i
 }
 
 extern "C" sv_status sv_selftest_bounded_wait(int32_t limit, int32_t* dev_status, void* stream) {
+  SV_TRACE("sv_selftest_bounded_wait");
   if (limit < 1 || limit > kWaitLimit || !dev_status) return SV_ERR_INVALID_ARGUMENT;
   if (sv::launch(chk::selftest_wait_kernel, 1, 32, 0, static_cast<cudaStream_t>(stream),
                  (int)limit, dev_status) != cudaSuccess)
@@ -205,6 +209,7 @@ extern "C" sv_status sv_selftest_bounded_wait(int32_t limit, int32_t* dev_status
 extern "C" sv_status sv_chunk_windows(const sv_batch* bt, int32_t chunk_index, int32_t chunk_size,
                                       const int32_t* done, int32_t* row_begin, int32_t* row_end,
                                       void* stream) {
+  SV_TRACE("sv_chunk_windows");
   if (!bt || chunk_index < 0 || chunk_size < 1 || !row_begin || !row_end || bt->n_req < 0)
     return SV_ERR_INVALID_ARGUMENT;
   if (chunk_index > 0 && !done) return SV_ERR_INVALID_ARGUMENT;
@@ -265,6 +270,9 @@ sv_status verify_chunked(const sv_paged_kv* kv, const sv_batch* bt, const void* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int n_chunks = (bt->max_rows_per_req + chunk_size - 1) / chunk_size;
   for (int c = 0; c < n_chunks; ++c) {
+    char name[32];
+    snprintf(name, sizeof(name), "chunk %d", c);
+    TraceRange chunk_range(name);
     // The planner turns `done` into this chunk's windows and the accept list.
     const attn::ChunkPlan cp{c, chunk_size, done, rb, re,
                              reinterpret_cast<int32_t*>(acc_ws + AL.act), act4};
@@ -292,6 +300,7 @@ extern "C" sv_status sv_verify_chunked(const sv_paged_kv* kv, const sv_batch* bt
                                        int32_t* accepted_nodes, int32_t* next_token,
                                        uint8_t* ambiguous, int32_t* done, void* ws,
                                        size_t ws_bytes, int32_t* dev_status, void* stream) {
+  SV_TRACE("sv_verify_chunked");
   return verify_chunked(kv, bt, q, n_q_heads, softmax_scale, out, target_logits, draft_logits,
                         vocab, temperature, seed, chunk_size, accepted_len, accepted_nodes,
                         next_token, ambiguous, done, nullptr, ws, ws_bytes, dev_status, stream);
@@ -303,6 +312,7 @@ extern "C" sv_status sv_verify_chunked_commit(
     int32_t vocab, float temperature, uint64_t seed, int32_t chunk_size, int32_t* accepted_len,
     int32_t* accepted_nodes, int32_t* next_token, uint8_t* ambiguous, int32_t* done,
     const sv_block_pool* pool, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  SV_TRACE("sv_verify_chunked_commit");
   if (!kv || !bt || !pool) return SV_ERR_INVALID_ARGUMENT;
   if (kv->block_size != kBlockSize) return SV_ERR_UNSUPPORTED_SHAPE;
   if (kv->head_dim != 64 && kv->head_dim != 128) return SV_ERR_UNSUPPORTED_SHAPE;

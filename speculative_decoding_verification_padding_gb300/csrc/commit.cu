@@ -198,6 +198,7 @@ using namespace sv;
 extern "C" sv_status sv_commit_kv(const sv_paged_kv* kv, const sv_batch* bt,
                                   const int32_t* accepted_len, const int32_t* accepted_nodes,
                                   const sv_block_pool* pool, int32_t* dev_status, void* stream) {
+  SV_TRACE("sv_commit_kv");
   if (!kv || !bt || !pool) return SV_ERR_INVALID_ARGUMENT;
   if (bt->n_req < 0 || bt->max_rows_per_req < 1) return SV_ERR_INVALID_ARGUMENT;
   if (bt->max_rows_per_req > kMaxRows) return SV_ERR_UNSUPPORTED_SHAPE;
@@ -232,18 +233,8 @@ extern "C" sv_status sv_commit_kv(const sv_paged_kv* kv, const sv_batch* bt,
   const size_t smem = (size_t)2 * (bt->max_rows_per_req - 1 > 0 ? bt->max_rows_per_req - 1 : 1) *
                       kv->head_dim * 2;
   if (smem > 48 * 1024) {
-    // once per device (calls may come from several host threads)
-    static std::mutex mu;
-    static bool set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!set[dev]) {
-      if (cudaFuncSetAttribute(cmt::copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               96 * 1024) != cudaSuccess)
-        return SV_ERR_CUDA;
-      set[dev] = true;
-    }
+    static PerDevice smem_set;
+    if (smem_limit_once(smem_set, cmt::copy_kernel, 96 * 1024) != cudaSuccess) return SV_ERR_CUDA;
   }
   if (sv::launch(cmt::copy_kernel, bt->n_req, 256, smem, s, a) != cudaSuccess) return SV_ERR_CUDA;
   if (sv::launch(cmt::release_kernel, 1, 1024, 0, s, a) != cudaSuccess) return SV_ERR_CUDA;

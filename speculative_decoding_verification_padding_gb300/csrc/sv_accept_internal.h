@@ -19,6 +19,7 @@ namespace acc {
 struct Layout {
   size_t parts, jobs, race, race_tickets, act, ctick, cspan, total;
   int nch, nch_cap, nch_r, nch_r_cap, maxw;
+  int nsm;  // SMs of the device the call runs on
 };
 Layout layout(int R, int total_rows, int V, int maxw, bool commit = false);
 

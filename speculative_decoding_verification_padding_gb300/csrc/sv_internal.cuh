@@ -5,13 +5,17 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <vector>
+
+#include <nvtx3/nvToolsExt.h>
+
 #include "libspecverify.h"
 
 namespace sv {
 
 constexpr int kBlockSize = 16;   // tokens per KV page
 constexpr int kMaxRows = 128;    // rows per request (ancestor masks are 128 bits)
-constexpr int kNumSMs = 152;     // GB300
 
 // Device findings are OR-ed into the caller's status word; a null word drops
 // them (the affected request is still skipped).
@@ -302,6 +306,66 @@ __device__ __forceinline__ void griddep_entry() {
 // ------------------------------------------------------------ host side --
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Per-device state set up once per device and kept for the process (calls may
+// come from several host threads): run(fn) calls fn() for the current device
+// the first time it is asked to, under a lock, and remembers success.
+class PerDevice {
+ public:
+  template <class F>
+  cudaError_t run(F&& fn) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu_);
+    if ((size_t)dev >= done_.size()) done_.resize((size_t)dev + 1, 0);
+    if (done_[(size_t)dev]) return cudaSuccess;
+    e = fn(dev);
+    if (e == cudaSuccess) done_[(size_t)dev] = 1;
+    return e;
+  }
+
+ private:
+  std::mutex mu_;
+  std::vector<char> done_;
+};
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once
+// per device (`once` is the kernel's own record).
+template <typename K>
+inline cudaError_t smem_limit_once(PerDevice& once, K kernel, size_t bytes) {
+  return once.run([&](int) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  });
+}
+
+// Streaming multiprocessors of the current device, queried once per device;
+// grids and work splits are sized from it.  0 if the query fails.
+inline int num_sms() {
+  static std::mutex mu;
+  static std::vector<int> sms;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if ((size_t)dev >= sms.size()) sms.resize((size_t)dev + 1, 0);
+  if (!sms[(size_t)dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      return 0;
+    sms[(size_t)dev] = n;
+  }
+  return sms[(size_t)dev];
+}
+
+// The SM count that sizes workspaces and work splits: the current device's,
+// or, for a size query made where no device is visible (nothing can be
+// launched then), the count of the GB300 this library is built for.
+constexpr int kSmsWithoutDevice = 152;
+inline int sizing_sms() {
+  const int n = num_sms();
+  return n > 0 ? n : kSmsWithoutDevice;
+}
+
 // Launch with programmatic stream serialization allowed (see griddep_entry).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -319,7 +383,19 @@ inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// A named NVTX range around the host part of a call (what it enqueues), so
+// that profilers group the call's kernels under the call's name.
+class TraceRange {
+ public:
+  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
+};
+
 }  // namespace sv
+
+#define SV_TRACE(name) ::sv::TraceRange sv_trace_range_(name)
 
 #define SV_LAUNCH_CHECK()                                  \
   do {                                                     \
