@@ -72,3 +72,28 @@ def test_accept_bytes_follow_the_definition():
     assert got == want
     # greedy: target rows only
     assert bench.accept_bytes(w, win, acc, 0.0) == sum(rows) * V * 4
+
+
+def test_attend_flops_follow_the_definition():
+    # chain: row j sees the context and rows 0..j (j + 1 staged slots)
+    w = wl.make_workload(wl.config("tiny"))
+    win = bench.launch_windows(w, "onepass", np.zeros(1, np.int32))
+    per_key = 4 * 64 * 8        # QK^T and PV, d 64, 8 query heads
+    assert bench.attend_flops(w, win[0]) == per_key * sum(256 + j + 1 for j in range(5))
+    # tree: a node sees its ancestors and itself, counted by brute force over
+    # the ancestor sets; the 65-row tree at context 8192 is about 17.5 GFLOP
+    w = wl.make_workload(wl.config("tree70b"), vocab=64)
+    par = w.parent
+    depth_sum = 0
+    for r in range(w.total_rows):
+        anc = {r}
+        m = r
+        while par[m] >= 0:
+            m = int(par[m])
+            anc.add(m)
+        depth_sum += len(anc)
+    per_key = 4 * 128 * 64
+    want = per_key * (65 * 8192 + depth_sum)
+    win = bench.launch_windows(w, "onepass", np.zeros(1, np.int32))
+    assert bench.attend_flops(w, win[0]) == want
+    assert abs(want / 1e9 - 17.46) < 0.01
