@@ -631,15 +631,17 @@ def main():
     roofline.update({"launches_per_step": n_launch, "bytes_per_launch": sum(att_b) / n_launch,
                      "us_per_launch": 1e6 * t_att / n_launch})
     race = 1 if T > 0 else 0
-    # Chunked: plan (windows + accept list) + attend + stats + decide (with the commit) per
-    # chunk [+ tree walk after the first when a chunk holds a tree], one race after the
-    # last.  One-pass / budget: [select] + plan + attend + fused accept-commit (stats +
-    # decide [+ tree walk] [+ race]).
+    # Chunked: plan (windows + accept list) + attend [+ tcgen05 attend] + stats + decide
+    # (with the commit) per chunk [+ tree walk after the first when a chunk holds a
+    # tree], one race after the last.  One-pass / budget: [select] + plan + attend
+    # [+ tcgen05 attend] + fused accept-commit (stats + decide [+ tree walk] [+ race]).
     tree = 1 if (T > 0 and w.max_rows > 2) else 0
+    tc = 1 if (w.cfg.head_dim == 128 and
+               w.cfg.n_q_heads // w.cfg.n_kv_heads * w.max_rows >= 128) else 0
     if mode == "chunked":
-        launches_per_step = n_launch * (2 + 2) + race + (tree if chunk > 2 else 0)
+        launches_per_step = n_launch * (2 + tc + 2) + race + (tree if chunk > 2 else 0)
     else:
-        launches_per_step = 2 + 2 + tree + race + (1 if mode == "budget" else 0)
+        launches_per_step = 2 + tc + 2 + tree + race + (1 if mode == "budget" else 0)
     value = rows_all / t_step
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

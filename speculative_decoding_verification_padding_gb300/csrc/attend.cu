@@ -44,6 +44,7 @@
 
 #include "sv_attend_internal.h"
 #include "sv_internal.cuh"
+#include "sv_tcgen05.cuh"
 
 namespace sv {
 namespace attn {
@@ -65,7 +66,16 @@ struct ReqInfo {
   int ubase, nsplit, nrt, b, e, ctx, nblk, valid;
   int act;     // chunk mode: the window is not empty (the accept list)
   int cu, rows;
+  int tc;      // units of 128 virtual rows on the tcgen05 kernel
 };
+
+// Requests whose window holds at least this many virtual rows (query rows x
+// GQA group) per KV head form dense 128-row tiles: they run on the tcgen05
+// kernel (tensor memory accumulators), the others on the mma.sync kernel.
+constexpr int kTcRows = 128;       // virtual rows per tcgen05 unit (one M = 128 tile)
+constexpr int kTcMinRows = 128;
+constexpr int kTcMinPages = 16;    // pages per split at least (four stages)
+constexpr int kTcMaxPages = 256;   // pages per split at most (block ids in shared memory)
 // The planner keeps the per-request records in shared memory up to this many
 // requests (about 45 KB), in its workspace beyond.
 constexpr int kPlanSmemRequests = 1024;
@@ -84,14 +94,17 @@ struct __align__(16) WorkItem {
 };
 
 struct Header {
-  int U;     // units in the work list
+  int U;     // units in the work list (mma.sync kernel)
   int P;     // pages per split
-  int pad[62];
+  int Utc;   // units in the tcgen05 work list
+  int Ptc;   // pages per split there
+  int pad[60];
 };
 
 struct Layout {
-  size_t header, info, work, tickets, ml, o, total;
-  int ucap;
+  size_t header, info, work, tickets, ml, o;
+  size_t work_tc, ml_tc, o_tc, total;
+  int ucap, ucap_tc;
   int nsm;          // SMs of the device the call runs on
   int unit_target;  // units the planner aims for: kUnitsPerSM per SM
 };
@@ -104,18 +117,32 @@ inline int unit_cap(int R, int total_rows, int group, int Hkv, int max_blocks, i
   return (int)(rt_units + unit_target + (rt_units * max_blocks + kMaxPagesPerSplit - 1) / kMaxPagesPerSplit);
 }
 
-inline Layout layout(int R, int total_rows, int group, int Hkv, int D, int max_blocks) {
+// tcgen05 units: the planner picks Ptc >= W_tc / (2 SMs - row-tile units),
+// so they number at most two per SM unless Ptc is capped at kTcMaxPages.
+inline int unit_cap_tc(int R, int total_rows, int group, int Hkv, int D, int max_rows,
+                       int max_blocks, int nsm) {
+  if (D != 128 || group * max_rows < kTcMinRows) return 0;
+  const long rt = (long)Hkv * ((long)group * total_rows / kTcRows + R + 1);
+  return (int)(2L * nsm + rt + (rt * max_blocks + kTcMaxPages - 1) / kTcMaxPages);
+}
+
+inline Layout layout(int R, int total_rows, int group, int Hkv, int D, int max_blocks,
+                     int max_rows) {
   Layout L;
   size_t off = 0;
   L.nsm = sizing_sms();
   L.unit_target = L.nsm * kUnitsPerSM;
   L.ucap = unit_cap(R, total_rows, group, Hkv, max_blocks, L.unit_target);
+  L.ucap_tc = unit_cap_tc(R, total_rows, group, Hkv, D, max_rows, max_blocks, L.nsm);
   L.header = off; off += align256(sizeof(Header));
   L.info = off; off += align256(sizeof(ReqInfo) * (size_t)R);
   L.work = off; off += align256(sizeof(WorkItem) * (size_t)L.ucap);
   L.tickets = off; off += align256(sizeof(int) * (size_t)L.ucap);
   L.ml = off; off += align256((size_t)L.ucap * kTileRows * 2 * sizeof(float));
   L.o = off; off += align256((size_t)L.ucap * kTileRows * (size_t)D * sizeof(float));
+  L.work_tc = off; off += align256(sizeof(WorkItem) * (size_t)L.ucap_tc);
+  L.ml_tc = off; off += align256((size_t)L.ucap_tc * kTcRows * 2 * sizeof(float));
+  L.o_tc = off; off += align256((size_t)L.ucap_tc * kTcRows * (size_t)D * sizeof(float));
   L.total = off;
   return L;
 }
@@ -173,9 +200,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   extern __shared__ ReqInfo s_info[];
   ReqInfo* info = R <= kPlanSmemRequests ? s_info : reinterpret_cast<ReqInfo*>(a.ws + a.L.info);
   int* tickets = reinterpret_cast<int*>(a.ws + a.L.tickets);
-  __shared__ unsigned long long s_W;
+  __shared__ unsigned long long s_W, s_Wtc;
   __shared__ int s_warp[32];
-  __shared__ int s_carry, s_acarry;
+  __shared__ int s_carry, s_acarry, s_carry_tc, s_Rtc;
 
   __shared__ int s_none;
   const bool chunked = a.chunk.index >= 0;
@@ -200,18 +227,25 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     if (a.bt.cu_rows[0] != 0 || a.bt.cu_rows[R] != a.bt.total_rows)
       flag(a.dev_status, SV_DEV_BAD_WINDOW);
     s_W = 0ull;
+    s_Wtc = 0ull;
     s_carry = 0;
     s_acarry = 0;
+    s_carry_tc = 0;
+    s_Rtc = 0;
     // A chunk after one that listed no request is empty too (requests only
     // ever stop): nothing to plan.
     s_none = (a.chunk.index > 0 && a.chunk.act[R] == 0) ? 1 : 0;
-    if (s_none) hdr->U = 0;
+    if (s_none) {
+      hdr->U = 0;
+      hdr->Utc = 0;
+    }
   }
   __syncthreads();
   if (s_none) return;
   // Per request: window, parents (all loads of a thread issued together),
   // length, work.
-  unsigned long long myW = 0;
+  unsigned long long myW = 0, myWtc = 0;
+  int myRtc = 0;
   for (int i = tid; i < R; i += blockDim.x) {
     bool badw = badw0;
     Window w = w0;
@@ -228,7 +262,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     if (badw) w.ok = false;  // reported above (once); the window is empty anyway
     const int cu = a.bt.cu_rows[i];
     bool badp = false;
-    if (w.ok) {
+    // parents are checked once per call: a later chunk of a chunked step runs
+    // only requests the first chunk found valid (one with bad parents stops
+    // there)
+    if (w.ok && !(chunked && a.chunk.index > 0)) {
       for (int j = 0; j < w.rows; ++j) {
         const int p = a.bt.parent[cu + j];
         badp |= (j == 0) ? (p != -1) : (p < 0 || p >= j);
@@ -245,9 +282,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
       flag(a.dev_status, SV_DEV_BAD_LENGTH);
     }
     const int nw = valid ? max(0, w.e - w.b) : 0;
-    const int nrt = (a.group * nw + kTileRows - 1) / kTileRows;
+    const bool tc = a.L.ucap_tc > 0 && a.group * nw >= kTcMinRows;
+    const int nrt = tc ? (a.group * nw + kTcRows - 1) / kTcRows
+                       : (a.group * nw + kTileRows - 1) / kTileRows;
     const int nblk = nw ? (ctx + w.e + kBlockSize - 1) / kBlockSize : 0;
-    myW += (unsigned long long)nrt * a.Hkv * nblk;
+    if (tc) {
+      myWtc += (unsigned long long)nrt * a.Hkv * nblk;
+      myRtc += nrt * a.Hkv;
+    } else {
+      myW += (unsigned long long)nrt * a.Hkv * nblk;
+    }
     ReqInfo ri;
     ri.valid = valid && nw > 0;
     ri.b = w.b;
@@ -261,13 +305,30 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     ri.act = (!badw && w.b < w.e) ? 1 + max(0, min(w.e, w.lim - 1) - w.b) : 0;
     ri.cu = cu;
     ri.rows = w.rows;
+    ri.tc = tc ? 1 : 0;
     info[i] = ri;
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) myW += __shfl_xor_sync(0xffffffffu, myW, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    myW += __shfl_xor_sync(0xffffffffu, myW, o);
+    myWtc += __shfl_xor_sync(0xffffffffu, myWtc, o);
+    myRtc += __shfl_xor_sync(0xffffffffu, myRtc, o);
+  }
   if (lane == 0 && myW) atomicAdd(&s_W, myW);
+  if (lane == 0 && myWtc) {
+    atomicAdd(&s_Wtc, myWtc);
+    atomicAdd(&s_Rtc, myRtc);
+  }
   __syncthreads();
   const unsigned long long W = s_W;
+  // tcgen05 units: about two per SM (two resident CTAs): splits of
+  // W_tc / (2 SMs - row-tile units) pages, within [kTcMinPages, kTcMaxPages].
+  int Ptc = 0;
+  if (s_Wtc) {
+    const long avail = max(1L, 2L * a.L.nsm - s_Rtc);
+    Ptc = (int)min((unsigned long long)kTcMaxPages, (s_Wtc + avail - 1) / avail);
+    Ptc = max(Ptc, kTcMinPages);
+  }
   const unsigned long long target = (unsigned long long)a.L.unit_target;
   int P = (int)min((unsigned long long)kMaxPagesPerSplit, (W + target - 1) / target);
   const int Pmin = W >= (unsigned long long)a.L.nsm * 2 * kMinPagesPerSplit ? 2 * kMinPagesPerSplit
@@ -278,17 +339,19 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   // order, with its count at act[R].
   for (int base = 0; base < R; base += blockDim.x) {
     const int i = base + tid;
-    int units = 0, act = 0;
+    int units = 0, units_tc = 0, act = 0;
     if (i < R) {
       const ReqInfo ri = info[i];
-      const int nsplit = ri.valid ? (ri.nblk + P - 1) / P : 0;
-      units = ri.nrt * a.Hkv * nsplit;
+      const int Pi = ri.tc ? Ptc : P;
+      const int nsplit = ri.valid ? (ri.nblk + Pi - 1) / Pi : 0;
+      (ri.tc ? units_tc : units) = ri.nrt * a.Hkv * nsplit;
       act = ri.act != 0;
       info[i].nsplit = nsplit;
     }
-    int excl, total;
+    int excl, total, excl_tc = 0, total_tc = 0;
     block_excl_scan(s_warp, units, excl, total);
-    if (i < R) info[i].ubase = s_carry + excl;
+    if (a.L.ucap_tc > 0) block_excl_scan(s_warp, units_tc, excl_tc, total_tc);
+    if (i < R) info[i].ubase = info[i].tc ? s_carry_tc + excl_tc : s_carry + excl;
     if (chunked) {
       int aexcl, atotal;
       block_excl_scan(s_warp, act, aexcl, atotal);
@@ -301,22 +364,28 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
       if (tid == 0) s_acarry += atotal;
     }
     __syncthreads();
-    if (tid == 0) s_carry += total;
+    if (tid == 0) {
+      s_carry += total;
+      s_carry_tc += total_tc;
+    }
     __syncthreads();
   }
   if (chunked && tid == 0) a.chunk.act[R] = s_acarry;
-  int U = s_carry;
-  if (U > a.L.ucap) {  // cannot happen with the bound used for the workspace
-    U = 0;
+  int U = s_carry, Utc = s_carry_tc;
+  if (U > a.L.ucap || Utc > a.L.ucap_tc) {  // cannot happen with the workspace's bounds
+    U = Utc = 0;
     if (tid == 0) flag(a.dev_status, SV_DEV_BAD_LENGTH);
   }
   for (int u = tid; u < U; u += blockDim.x) tickets[u] = 0;
   WorkItem* work = reinterpret_cast<WorkItem*>(a.ws + a.L.work);
-  if (U > 0)
+  WorkItem* work_tc = reinterpret_cast<WorkItem*>(a.ws + a.L.work_tc);
+  if (U > 0 || Utc > 0)
     for (int i = warp; i < R; i += 32) {
       const ReqInfo ri = info[i];
       const int n = ri.nrt * a.Hkv * ri.nsplit;
-      if (n == 0) continue;
+      if (n == 0 || (ri.tc ? Utc : U) == 0) continue;
+      WorkItem* list = ri.tc ? work_tc : work;
+      const int Pi = ri.tc ? Ptc : P;
       const int cu = ri.cu;
       const int rows = ri.rows;
       for (int x = lane; x < n; x += 32) {
@@ -331,18 +400,63 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
         it.ubase = ri.ubase;
         it.cu = cu;
         it.rows = rows;
-        it.P = P;
+        it.P = Pi;
         it.pad = 0;
-        work[ri.ubase + x] = it;
+        list[ri.ubase + x] = it;
       }
     }
   if (tid == 0) {
     hdr->U = U;
     hdr->P = P;
+    hdr->Utc = Utc;
+    hdr->Ptc = Ptc;
   }
 }
 
 // ---------------------------------------------------------------- attend --
+
+// The last CTA of a (request, row tile, KV head) group merges the (m, l, O)
+// partials of all the group's splits -- m in the log2 domain, O unnormalised
+// -- in one online pass per (virtual row, 4 columns) and writes bf16 rows.
+// ml_all / op_all: partials of TILE rows per unit; gidx: the group's split-0
+// unit; row0: packed row of the window's first row.
+template <int D, int TILE>
+__device__ __forceinline__ void merge_splits(const Args& a, const float* ml_all,
+                                             const float* op_all, int gidx, int nsplit, int r0,
+                                             int r1, int vr0, int row0, int g, int tid,
+                                             int nthreads) {
+  constexpr int kQuads = D / 4;
+  const int group = a.group;
+  for (int x = tid; x < (r1 - r0) * kQuads; x += nthreads) {
+    const int vr = r0 + x / kQuads, c4 = x % kQuads;
+    // one online pass over the splits (running max, rescaled sums); the
+    // loads of consecutive splits are independent and overlap
+    float Mx = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const size_t row = (size_t)(gidx + sp) * TILE + vr;
+      const float2 ml2 = __ldcg(reinterpret_cast<const float2*>(ml_all + row * 2));
+      const float4 o4 = __ldcg(reinterpret_cast<const float4*>(op_all + row * D) + c4);
+      const float nm = fmaxf(Mx, ml2.x);
+      if (nm == -INFINITY) continue;
+      const float s_old = exp2f(Mx - nm), s_new = exp2f(ml2.x - nm);
+      L = L * s_old + ml2.y * s_new;
+      acc.x = acc.x * s_old + o4.x * s_new;
+      acc.y = acc.y * s_old + o4.y * s_new;
+      acc.z = acc.z * s_old + o4.z * s_new;
+      acc.w = acc.w * s_old + o4.w * s_new;
+      Mx = nm;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int vgl = vr0 + vr;
+    const int prow = row0 + vgl / group;
+    const int head = g * group + vgl % group;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + ((size_t)prow * a.Hq + head) * D + c4 * 4);
+    dst[0] = pack_bf16(acc.x * inv, acc.y * inv);
+    dst[1] = pack_bf16(acc.z * inv, acc.w * inv);
+  }
+}
 
 // Shared-memory image of one stage: for K then V, 4 pages x (D / 64) boxes of
 // 16 rows x 128 bytes, as TMA writes them with the 128-byte swizzle (16-byte
@@ -764,37 +878,420 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // Merge: thread -> (virtual row, 4 consecutive columns).
-  constexpr int kQuads = D / 4;
-  for (int x = tid; x < Mu * kQuads; x += kThreads) {
-    const int vr = x / kQuads, c4 = x % kQuads;
-    // one online pass over the splits (running max, rescaled sums); the
-    // loads of consecutive splits are independent and overlap
-    float Mx = -INFINITY, L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int sp = 0; sp < ri.nsplit; ++sp) {
-      const size_t row = (size_t)(gidx + sp) * kTileRows + vr;
-      const float2 ml2 = __ldcg(reinterpret_cast<const float2*>(ml_all + row * 2));
-      const float4 o4 = __ldcg(reinterpret_cast<const float4*>(op_all + row * D) + c4);
-      const float nm = fmaxf(Mx, ml2.x);
-      if (nm == -INFINITY) continue;
-      const float s_old = exp2f(Mx - nm), s_new = exp2f(ml2.x - nm);
-      L = L * s_old + ml2.y * s_new;
-      acc.x = acc.x * s_old + o4.x * s_new;
-      acc.y = acc.y * s_old + o4.y * s_new;
-      acc.z = acc.z * s_old + o4.z * s_new;
-      acc.w = acc.w * s_old + o4.w * s_new;
-      Mx = nm;
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int vgl = vr0 + vr;
-    const int prow = cu + ri.b + vgl / group;
-    const int head = g * group + vgl % group;
-    uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + ((size_t)prow * a.Hq + head) * D + c4 * 4);
-    dst[0] = pack_bf16(acc.x * inv, acc.y * inv);
-    dst[1] = pack_bf16(acc.z * inv, acc.w * inv);
+  merge_splits<D, kTileRows>(a, ml_all, op_all, gidx, ri.nsplit, 0, Mu, vr0, cu + ri.b, g, tid,
+                             kThreads);
+}
+
+// ------------------------------------------------------------ tcgen05 --
+// Units of 128 virtual rows (the dense tiles of draft trees and long chains:
+// query rows x GQA group >= 128 per KV head) run on the fifth-generation
+// tensor cores with the accumulators in tensor memory:
+//   S = Q K^T (M 128 x N 64 tokens x K 128) and O += P V (M 128 x N 128 x
+//   K 64 tokens) per 64-token stage, both tcgen05.mma from shared-memory
+//   descriptors, issued by one thread;
+//   warps 0-3: thread t owns virtual row t (TMEM lane t): it loads S from
+//     tensor memory, masks, keeps the running max and sum, writes P (bf16)
+//     over the stage's K tile (128-byte swizzled, K-major), and rescales the
+//     O accumulator in tensor memory only when its max grows by more than
+//     2^8 (P stays below 256: exact in fp32, within bf16's range);
+//   warp 4: tensor-memory allocation and the TMA loads of K and V pages into
+//     a 2-slot ring (each slot K 16 KB then V 16 KB, 64-element halves of d
+//     as 8-row swizzle atoms, the layout both MMAs read);
+//   warp 5: the MMA thread (QK^T of stage s + 1 is issued before PV of stage
+//     s, so the tensor cores work while the softmax warps do).
+// Two CTAs per SM (97 KB of shared memory and 256 TMEM columns each).
+// Every wait is bounded; a CTA that gives up flags SV_DEV_TIMEOUT, lets its
+// copies and MMAs land and frees its tensor memory before it returns.
+namespace tcu {
+constexpr int kTok = 64;                      // tokens per stage
+constexpr int kThreads = 192;
+constexpr int kQBytes = kTcRows * 256;        // Q: two halves of d, 128 rows x 128 B each
+constexpr int kHalf = kTok * 128;             // one 64-element half of d for 64 tokens
+constexpr int kSlotBytes = 4 * kHalf;         // K (two halves), then V (two halves)
+constexpr int kSmem = kQBytes + 2 * kSlotBytes + 1024;  // + 1024-byte alignment
+constexpr uint32_t kTmemCols = 256;           // S of two stages (64 columns each), O (128)
+constexpr uint32_t kColO = 128;
+}  // namespace tcu
+
+// Keys t0 .. t0 + 63 that a row sees, bit j for key t0 + j: every key below
+// ctx, key ctx + m for m an ancestor-or-self of the row (bit m of the 128-bit
+// mask mk1:mk0), none at or past tok_end.
+__device__ __forceinline__ unsigned long long stage_visible(int t0, int ctx, int tok_end,
+                                                            unsigned long long mk0,
+                                                            unsigned long long mk1) {
+  auto low_bits = [](int n) {  // bits 0 .. n - 1, n clamped to [0, 64]
+    return n <= 0 ? 0ull : n >= 64 ? ~0ull : (1ull << n) - 1ull;
+  };
+  unsigned long long staged;  // bit j = ancestor bit (t0 + j - ctx)
+  const int sh = t0 - ctx;
+  if (sh >= 128 || sh <= -64) {
+    staged = 0ull;
+  } else if (sh >= 64) {
+    staged = mk1 >> (sh - 64);
+  } else if (sh > 0) {
+    staged = (mk0 >> sh) | (mk1 << (64 - sh));
+  } else if (sh == 0) {
+    staged = mk0;
+  } else {
+    staged = mk0 << (-sh);
   }
+  return (low_bits(ctx - t0) | (staged & ~low_bits(ctx - t0))) & low_bits(tok_end - t0);
+}
+
+template <int D>
+__global__ void __launch_bounds__(tcu::kThreads, 2)
+    attend_tc_kernel(const __grid_constant__ Args a, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV) {
+  static_assert(D == 128, "tcgen05 units: head_dim 128");
+  griddep_entry();
+  using tcu::kTok;
+  using tcu::kQBytes;
+  using tcu::kHalf;
+  using tcu::kSlotBytes;
+  using tcu::kTmemCols;
+  using tcu::kColO;
+  constexpr int kThreads = tcu::kThreads;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ int s_tbl[kTcMaxPages];
+  __shared__ int s_par[kMaxRows];
+  __shared__ __align__(8) unsigned long long s_full[2], s_empty[2], s_sfull[2], s_pfull[2], s_odone,
+      s_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_issued[2];  // last stage the producer issued into each slot (-1: none)
+  const Header* hdr = reinterpret_cast<const Header*>(a.ws + a.L.header);
+  const int u = blockIdx.x;
+  const int U = hdr->Utc;
+  const WorkItem ri = reinterpret_cast<const WorkItem*>(a.ws + a.L.work_tc)[u];
+  if (u >= U) return;
+  const int P = ri.P;
+  const int s = ri.local % ri.nsplit;
+  const int rest = ri.local / ri.nsplit;
+  const int g = rest % a.Hkv;
+  const int rt = rest / a.Hkv;
+  const int group = a.group;
+  const int M = group * (ri.e - ri.b);
+  const int vr0 = rt * kTcRows;
+  const int Mu = min(kTcRows, M - vr0);
+  const int blk0 = s * P;
+  const int blk1 = min(blk0 + P, ri.nblk);
+  const int ctx = ri.ctx;
+  const int tok_end = min(ctx + ri.e, blk1 * kBlockSize);
+  const int cu = ri.cu;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_stage = (blk1 - blk0 + 3) / 4;
+  const int32_t* table = a.tables + (size_t)ri.i * a.max_blocks;
+  const bool unit_masked = blk1 * kBlockSize > ctx;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - smem_u32(smem_raw));
+  const uint32_t qs = base, ring = base + kQBytes;
+
+  for (int p = tid; p < blk1 - blk0; p += kThreads) s_tbl[p] = __ldg(table + blk0 + p);
+  if (unit_masked)
+    for (int j = tid; j < ri.rows; j += kThreads) s_par[j] = a.bt.parent[cu + j];
+  if (tid == 0) {
+    s_abort = 0;
+    s_issued[0] = s_issued[1] = -1;
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&s_full[k]), 1);
+      mbar_init(smem_u32(&s_empty[k]), 1);
+      mbar_init(smem_u32(&s_sfull[k]), 1);
+      mbar_init(smem_u32(&s_pfull[k]), 128);
+    }
+    mbar_init(smem_u32(&s_odone), 1);
+    mbar_init(smem_u32(&s_drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tc5::tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+    tc5::tmem_relinquish();
+  }
+  // Q tile: thread t < 128 copies virtual row vr0 + t (zeros past the tile's
+  // rows) into the K-major swizzled layout (half h of d at h * 16 KB).
+  const bool real = tid < 128 && tid < Mu;
+  const int va = vr0 + tid;
+  const int lrow = real ? va / group : 0;  // row within the window
+  if (tid < 128) {
+    const int4* src = reinterpret_cast<const int4*>(
+        a.q + ((size_t)(cu + ri.b + lrow) * a.Hq + g * group + (real ? va % group : 0)) * D);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int4 v = real ? __ldg(src + c) : make_int4(0, 0, 0, 0);
+      const uint32_t off = (uint32_t)((c >> 3) * (kTcRows * 128) + tid * 128 + (((c & 7) ^ (tid & 7)) << 4));
+      *reinterpret_cast<int4*>(base_ptr + off) = v;
+    }
+    fence_proxy_async_smem();
+  }
+  tc5::fence_before_sync();
+  __syncthreads();
+  tc5::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------- producer --
+    if (lane == 0) {
+      for (int st = 0; st < n_stage; ++st) {
+        const int slot = st & 1;
+        if (st >= 2 &&
+            !mbar_wait_bounded(smem_u32(&s_empty[slot]), (uint32_t)(((st - 2) >> 1) & 1))) {
+          s_abort = 1;
+          break;
+        }
+        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+        const uint32_t bar = smem_u32(&s_full[slot]);
+        int bids[4];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const int page = blk0 + 4 * st + p;
+          int bid = page < blk1 ? s_tbl[page - blk0] : -1;
+          if (page < blk1 && (bid < 0 || bid >= a.num_blocks)) {
+            flag(a.dev_status, SV_DEV_BAD_BLOCK_ID);
+            bid = -1;
+          }
+          bids[p] = bid;
+          if (bid >= 0) bytes += 4u * 2048u;
+        }
+        mbar_arrive_expect_tx(bar, bytes);
+        const uint32_t kdst = ring + slot * kSlotBytes;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          if (bids[p] < 0) continue;
+          const int y = (bids[p] * a.Hkv + g) * kBlockSize;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_load_2d(kdst + h * kHalf + p * 2048, &tmK, 64 * h, y, bar);
+            tma_load_2d(kdst + 2 * kHalf + h * kHalf + p * 2048, &tmV, 64 * h, y, bar);
+          }
+        }
+        s_issued[slot] = st;
+      }
+    }
+  } else if (warp == 5) {
+    // --------------------------------------------------------- MMA issue --
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = tc5::idesc_bf16_f32(kTcRows, kTok, false);
+      constexpr uint32_t idesc_pv = tc5::idesc_bf16_f32(kTcRows, D, true);
+      // O += P V of stage j (P over the stage's K tile, V MN-major)
+      auto pv = [&](int j) -> bool {
+        const int slot = j & 1;
+        if (!mbar_wait_bounded(smem_u32(&s_pfull[slot]), (uint32_t)((j >> 1) & 1))) return false;
+        tc5::fence_after_sync();
+        const uint32_t sb = ring + slot * kSlotBytes;
+#pragma unroll
+        for (int ks = 0; ks < kTok / 16; ++ks) {
+          const uint64_t ad = tc5::sw128_desc(sb + ks * 32, 16, 1024);
+          const uint64_t bd = tc5::sw128_desc(sb + 2 * kHalf + ks * 2048, kHalf, 1024);
+          tc5::mma_bf16(tmem + kColO, ad, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc5::commit(smem_u32(&s_empty[slot]));
+        tc5::commit(smem_u32(&s_odone));
+        return true;
+      };
+      bool ok = true;
+      for (int st = 0; st < n_stage && ok; ++st) {
+        const int slot = st & 1;
+        if (!mbar_wait_bounded(smem_u32(&s_full[slot]), (uint32_t)((st >> 1) & 1)) ||
+            *reinterpret_cast<volatile int*>(&s_abort)) {
+          ok = false;
+          break;
+        }
+        tc5::fence_after_sync();
+        const uint32_t sb = ring + slot * kSlotBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t ad = tc5::sw128_desc(qs + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd = tc5::sw128_desc(sb + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
+          tc5::mma_bf16(tmem + (uint32_t)(slot * kTok), ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+        }
+        tc5::commit(smem_u32(&s_sfull[slot]));
+        if (st >= 1) ok = pv(st - 1);
+      }
+      if (ok && n_stage > 0) ok = pv(n_stage - 1);
+      if (!ok) s_abort = 1;
+      // every MMA this thread issued has completed before the CTA moves on
+      tc5::commit(smem_u32(&s_drain));
+      mbar_wait_bounded(smem_u32(&s_drain), 0);
+    }
+  } else {
+    // ----------------------------------------------------- softmax, rows --
+    // ancestor-or-self mask of this thread's row (only where staged slots lie)
+    unsigned long long mk0 = 0ull, mk1 = 0ull;
+    if (unit_masked && real) {
+      int m = ri.b + lrow;
+      for (int steps = 0; m >= 0 && steps <= kMaxRows; ++steps) {  // parents validated by plan
+        if (m < 64) mk0 |= 1ull << m; else mk1 |= 1ull << (m - 64);
+        m = s_par[m];
+      }
+    }
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int st = 0; st < n_stage; ++st) {
+      const int slot = st & 1;
+      const bool got = mbar_wait_bounded(smem_u32(&s_sfull[slot]), (uint32_t)((st >> 1) & 1));
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc5::fence_after_sync();
+      uint32_t sv[kTok];
+      tc5::tmem_ld_x64(tmem + lane_base + (uint32_t)(slot * kTok), sv);
+      const int t0 = (blk0 + 4 * st) * kBlockSize;
+      float x[kTok];
+#pragma unroll
+      for (int j = 0; j < kTok; ++j) x[j] = __uint_as_float(sv[j]) * a.scale_log2;
+      if (t0 + kTok > ctx || t0 + kTok > tok_end) {
+        // Keys of this stage the row sees, as one 64-bit word: the context,
+        // then the staged slots of its ancestors-or-self, none past tok_end.
+        const unsigned long long vis = stage_visible(t0, ctx, tok_end, mk0, mk1);
+#pragma unroll
+        for (int j = 0; j < kTok; ++j)
+          if (!((vis >> j) & 1ull)) x[j] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kTok; ++j) mx = fmaxf(mx, x[j]);
+      // a new reference max only when the row max passes it by 2^8
+      const bool grow = mx > m_ref + 8.f;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float m_new = grow ? mx : m_ref;
+        const float alpha = grow ? ex2(m_ref - m_new) : 1.f;  // 0 while m_ref is -inf
+        if (st > 0) {
+          // O holds PV of the earlier stages: wait for the last one to land
+          const bool g2 = mbar_wait_bounded(smem_u32(&s_odone), (uint32_t)((st - 1) & 1));
+          if (!__all_sync(0xffffffffu, g2)) {
+            ok = false;
+            break;
+          }
+          tc5::fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t ov[32];
+            tc5::tmem_ld_x32(tmem + lane_base + kColO + c, ov);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+            tc5::tmem_st_x32(tmem + lane_base + kColO + c, ov);
+          }
+        }
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float mb = m_ref == -INFINITY ? 0.f : m_ref;
+      float rs = 0.f;
+      uint32_t pk[kTok / 2];
+#pragma unroll
+      for (int j = 0; j < kTok; j += 2) {
+        const float p0 = ex2(x[j] - mb), p1 = ex2(x[j + 1] - mb);
+        rs += p0 + p1;
+        pk[j / 2] = pack_bf16(p0, p1);
+      }
+      l += rs;
+      // Slots past the last key may hold anything (unwritten cache slots, or
+      // pages not loaded): zero their V rows so that P = 0 meets V = 0.
+      const uint32_t sb = ring + slot * kSlotBytes;
+      if (t0 + kTok > tok_end) {
+        const int first = max(0, tok_end - t0);
+        for (int xx = tid; xx < (kTok - first) * 16; xx += 128) {
+          const int t = first + (xx >> 4), c = xx & 15;
+          const uint32_t off = 2 * kHalf + (c >> 3) * kHalf + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+          *reinterpret_cast<int4*>(base_ptr + (sb - base) + off) = make_int4(0, 0, 0, 0);
+        }
+      }
+      // P row t over the stage's K tile: 64 tokens = one 128-byte swizzled row
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t off = (uint32_t)(tid * 128 + ((c ^ (tid & 7)) << 4));
+        *reinterpret_cast<int4*>(base_ptr + (sb - base) + off) =
+            make_int4((int)pk[4 * c], (int)pk[4 * c + 1], (int)pk[4 * c + 2], (int)pk[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      tc5::fence_before_sync();
+      mbar_arrive(smem_u32(&s_pfull[slot]));
+    }
+    // The last PV has landed: O row t, normalised, to the output or to the
+    // split partials.
+    if (ok && n_stage > 0) {
+      const bool g3 = mbar_wait_bounded(smem_u32(&s_odone), (uint32_t)((n_stage - 1) & 1));
+      if (!__all_sync(0xffffffffu, g3)) ok = false;
+    }
+    if (!ok) {
+      s_abort = 1;
+    } else {
+      tc5::fence_after_sync();
+      const int prow = cu + ri.b + lrow;
+      const int head = g * group + (real ? va % group : 0);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t ov[32];
+        tc5::tmem_ld_x32(tmem + lane_base + kColO + c, ov);
+        if (!real) continue;
+        if (ri.nsplit == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t)prow * a.Hq + head) * D + c);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            dst[k] = make_uint4(pack_bf16(__uint_as_float(ov[8 * k]) * inv, __uint_as_float(ov[8 * k + 1]) * inv),
+                                pack_bf16(__uint_as_float(ov[8 * k + 2]) * inv, __uint_as_float(ov[8 * k + 3]) * inv),
+                                pack_bf16(__uint_as_float(ov[8 * k + 4]) * inv, __uint_as_float(ov[8 * k + 5]) * inv),
+                                pack_bf16(__uint_as_float(ov[8 * k + 6]) * inv, __uint_as_float(ov[8 * k + 7]) * inv));
+        } else {
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.ws + a.L.o_tc) +
+                                                  ((size_t)u * kTcRows + tid) * D + c);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1]),
+                                 __uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3]));
+        }
+      }
+      if (real && ri.nsplit > 1)
+        reinterpret_cast<float2*>(a.ws + a.L.ml_tc)[(size_t)u * kTcRows + tid] = make_float2(m_ref, l);
+    }
+  }
+
+  // Every role is done with tensor memory and the ring.
+  tc5::fence_before_sync();
+  __syncthreads();
+  tc5::fence_after_sync();
+  if (s_abort) {
+    // copies still in flight land before the CTA leaves (bounded waits)
+    if (tid == 0) {
+      flag(a.dev_status, SV_DEV_TIMEOUT);
+      for (int k = 0; k < 2; ++k)
+        if (s_issued[k] >= 0)
+          mbar_wait_bounded(smem_u32(&s_full[k]), (uint32_t)((s_issued[k] >> 1) & 1));
+    }
+    __syncthreads();
+  }
+  if (warp == 4) tc5::tmem_dealloc(tmem, kTmemCols);
+}
+
+// After the tcgen05 kernel: the units of a split group merge the group's
+// partials together, unit s of the group taking rows [s, s + 1) x
+// ceil(rows / nsplit) -- all splits' loads in flight at once on many SMs,
+// instead of one CTA reading every split of the tile.
+constexpr int kMergeThreads = 256;
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_tc_kernel(const __grid_constant__ Args a) {
+  griddep_entry();
+  const Header* hdr = reinterpret_cast<const Header*>(a.ws + a.L.header);
+  const int u = blockIdx.x;
+  const int U = hdr->Utc;
+  const WorkItem ri = reinterpret_cast<const WorkItem*>(a.ws + a.L.work_tc)[u];
+  if (u >= U || ri.nsplit == 1) return;
+  const int s = ri.local % ri.nsplit;
+  const int rest = ri.local / ri.nsplit;
+  const int g = rest % a.Hkv;
+  const int rt = rest / a.Hkv;
+  const int vr0 = rt * kTcRows;
+  const int Mu = min(kTcRows, a.group * (ri.e - ri.b) - vr0);
+  const int per = (Mu + ri.nsplit - 1) / ri.nsplit;
+  const int r0 = min(Mu, s * per), r1 = min(Mu, r0 + per);
+  if (r0 >= r1) return;
+  const int gidx = ri.ubase + (rt * a.Hkv + g) * ri.nsplit;  // unit of split 0
+  merge_splits<D, kTcRows>(a, reinterpret_cast<const float*>(a.ws + a.L.ml_tc),
+                           reinterpret_cast<const float*>(a.ws + a.L.o_tc), gidx, ri.nsplit, r0, r1,
+                           vr0, ri.cu + ri.b, g, threadIdx.x, kMergeThreads);
 }
 
 // cuTensorMapEncodeTiled from the driver, fetched through the runtime (no
@@ -840,6 +1337,18 @@ sv_status launch(const Args& a, cudaStream_t stream) {
   if (sv::launch(plan_kernel, 1, 1024, plan_smem, stream, a) != cudaSuccess) return SV_ERR_CUDA;
   if (sv::launch(attend_kernel<D>, a.L.ucap, kThreads, smem, stream, a, tmK, tmV) != cudaSuccess)
     return SV_ERR_CUDA;
+  if constexpr (D == 128) {
+    if (a.L.ucap_tc > 0) {
+      static PerDevice smem_set_tc;
+      if (smem_limit_once(smem_set_tc, attend_tc_kernel<D>, tcu::kSmem) != cudaSuccess)
+        return SV_ERR_CUDA;
+      if (sv::launch(attend_tc_kernel<D>, a.L.ucap_tc, tcu::kThreads, tcu::kSmem, stream, a, tmK,
+                     tmV) != cudaSuccess)
+        return SV_ERR_CUDA;
+      if (sv::launch(merge_tc_kernel<D>, a.L.ucap_tc, kMergeThreads, 0, stream, a) != cudaSuccess)
+        return SV_ERR_CUDA;
+    }
+  }
   return SV_OK;
 }
 
@@ -869,7 +1378,7 @@ extern "C" size_t sv_tree_attend_workspace(const sv_batch* bt, const sv_paged_kv
   if (check_attend_args(bt, kv, n_q_heads) != SV_OK) return 0;
   const int group = n_q_heads / kv->n_kv_heads;
   return attn::layout(bt->n_req, bt->total_rows, group, kv->n_kv_heads, kv->head_dim,
-                      kv->max_blocks_per_req).total;
+                      kv->max_blocks_per_req, bt->max_rows_per_req).total;
 }
 
 namespace sv {
@@ -906,7 +1415,7 @@ sv_status tree_attend(const sv_paged_kv* kv, const sv_batch* bt, const void* q, 
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.ws = static_cast<uint8_t*>(ws);
   a.L = layout(bt->n_req, bt->total_rows, group, kv->n_kv_heads, kv->head_dim,
-               kv->max_blocks_per_req);
+               kv->max_blocks_per_req, bt->max_rows_per_req);
   a.dev_status = dev_status;
   a.chunk = chunk;
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
@@ -920,7 +1429,7 @@ extern "C" sv_status sv_tree_attend(const sv_paged_kv* kv, const sv_batch* bt, c
                                     int32_t n_q_heads, float softmax_scale, void* out, void* ws,
                                     size_t ws_bytes, int32_t* dev_status, void* stream) {
   SV_TRACE("sv_tree_attend");
-  const attn::ChunkPlan none{-1, 0, nullptr, nullptr, nullptr, nullptr};
+  const attn::ChunkPlan none{-1, 0, nullptr, nullptr, nullptr, nullptr, nullptr};
   return attn::tree_attend(kv, bt, q, n_q_heads, softmax_scale, out, ws, ws_bytes, dev_status,
                            static_cast<cudaStream_t>(stream), none);
 }
