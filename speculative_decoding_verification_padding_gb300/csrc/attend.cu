@@ -433,7 +433,7 @@ __device__ __forceinline__ void merge_splits(const Args& a, const float* ml_all,
     // loads of consecutive splits are independent and overlap
     float Mx = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 8
     for (int sp = 0; sp < nsplit; ++sp) {
       const size_t row = (size_t)(gidx + sp) * TILE + vr;
       const float2 ml2 = __ldcg(reinterpret_cast<const float2*>(ml_all + row * 2));
@@ -886,17 +886,21 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Units of 128 virtual rows (the dense tiles of draft trees and long chains:
 // query rows x GQA group >= 128 per KV head) run on the fifth-generation
 // tensor cores with the accumulators in tensor memory:
-//   S = Q K^T (M 128 x N 64 tokens x K 128) and O += P V (M 128 x N 128 x
-//   K 64 tokens) per 64-token stage, both tcgen05.mma from shared-memory
-//   descriptors, issued by one thread;
+//   S = Q K^T (M 128 x N 64 tokens x K 128, Q and K from shared memory) and
+//   O += P V (M 128 x N 128 x K 64 tokens, P from tensor memory, V from
+//   shared memory as an MN-major operand) per 64-token stage, tcgen05.mma
+//   issued by one thread;
 //   warps 0-3: thread t owns virtual row t (TMEM lane t): it loads S from
-//     tensor memory, masks, keeps the running max and sum, writes P (bf16)
-//     over the stage's K tile (128-byte swizzled, K-major), and rescales the
-//     O accumulator in tensor memory only when its max grows by more than
-//     2^8 (P stays below 256: exact in fp32, within bf16's range);
+//     tensor memory, masks, keeps the running max and sum, and writes P
+//     (bf16, two per column) back over the first half of S's columns; it
+//     rescales the O accumulator in tensor memory only when its max grows
+//     by more than 2^8 (P stays below 256: exact in fp32, within bf16's
+//     range);
 //   warp 4: tensor-memory allocation and the TMA loads of K and V pages into
 //     a 2-slot ring (each slot K 16 KB then V 16 KB, 64-element halves of d
-//     as 8-row swizzle atoms, the layout both MMAs read);
+//     as 8-row swizzle atoms, the layout both MMAs read).  K and V of a slot
+//     are refilled separately: K of stage s + 2 as soon as QK^T of stage s
+//     has run, V once PV of stage s has;
 //   warp 5: the MMA thread (QK^T of stage s + 1 is issued before PV of stage
 //     s, so the tensor cores work while the softmax warps do).
 // Two CTAs per SM (97 KB of shared memory and 256 TMEM columns each).
@@ -954,11 +958,13 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int s_tbl[kTcMaxPages];
   __shared__ int s_par[kMaxRows];
-  __shared__ __align__(8) unsigned long long s_full[2], s_empty[2], s_sfull[2], s_pfull[2], s_odone,
-      s_drain;
+  // per slot: K landed / K free (QK^T done), V landed / V free (PV done);
+  // per S buffer: S ready, P written; PV done; drain of the MMA thread
+  __shared__ __align__(8) unsigned long long s_kfull[2], s_kfree[2], s_vfull[2], s_vfree[2],
+      s_sfull[2], s_pfull[2], s_odone, s_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_issued[2];  // last stage the producer issued into each slot (-1: none)
+  __shared__ int s_issued[4];  // last stage issued into K slot 0, 1, V slot 0, 1 (-1: none)
   const Header* hdr = reinterpret_cast<const Header*>(a.ws + a.L.header);
   const int u = blockIdx.x;
   const int U = hdr->Utc;
@@ -991,10 +997,12 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
     for (int j = tid; j < ri.rows; j += kThreads) s_par[j] = a.bt.parent[cu + j];
   if (tid == 0) {
     s_abort = 0;
-    s_issued[0] = s_issued[1] = -1;
+    for (int k = 0; k < 4; ++k) s_issued[k] = -1;
     for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&s_full[k]), 1);
-      mbar_init(smem_u32(&s_empty[k]), 1);
+      mbar_init(smem_u32(&s_kfull[k]), 1);
+      mbar_init(smem_u32(&s_kfree[k]), 1);
+      mbar_init(smem_u32(&s_vfull[k]), 1);
+      mbar_init(smem_u32(&s_vfree[k]), 1);
       mbar_init(smem_u32(&s_sfull[k]), 1);
       mbar_init(smem_u32(&s_pfull[k]), 128);
     }
@@ -1029,16 +1037,12 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
 
   if (warp == 4) {
     // ---------------------------------------------------------- producer --
+    // K of stage st after QK^T of stage st - 2, V after its PV: in the order
+    // K(st), V(st), K(st + 1), ... no wait is longer than the MMA order
+    // makes it anyway.
     if (lane == 0) {
       for (int st = 0; st < n_stage; ++st) {
         const int slot = st & 1;
-        if (st >= 2 &&
-            !mbar_wait_bounded(smem_u32(&s_empty[slot]), (uint32_t)(((st - 2) >> 1) & 1))) {
-          s_abort = 1;
-          break;
-        }
-        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
-        const uint32_t bar = smem_u32(&s_full[slot]);
         int bids[4];
         uint32_t bytes = 0;
 #pragma unroll
@@ -1050,21 +1054,32 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
             bid = -1;
           }
           bids[p] = bid;
-          if (bid >= 0) bytes += 4u * 2048u;
+          if (bid >= 0) bytes += 2u * 2048u;
         }
-        mbar_arrive_expect_tx(bar, bytes);
         const uint32_t kdst = ring + slot * kSlotBytes;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          if (bids[p] < 0) continue;
-          const int y = (bids[p] * a.Hkv + g) * kBlockSize;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tma_load_2d(kdst + h * kHalf + p * 2048, &tmK, 64 * h, y, bar);
-            tma_load_2d(kdst + 2 * kHalf + h * kHalf + p * 2048, &tmV, 64 * h, y, bar);
+        for (int half = 0; half < 2; ++half) {  // 0: K, 1: V
+          unsigned long long* freeb = half ? s_vfree : s_kfree;
+          unsigned long long* fullb = half ? s_vfull : s_kfull;
+          if (st >= 2 &&
+              !mbar_wait_bounded(smem_u32(&freeb[slot]), (uint32_t)(((st - 2) >> 1) & 1))) {
+            s_abort = 1;
+            break;
           }
+          if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+          const uint32_t bar = smem_u32(&fullb[slot]);
+          mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            if (bids[p] < 0) continue;
+            const int y = (bids[p] * a.Hkv + g) * kBlockSize;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(kdst + half * 2 * kHalf + h * kHalf + p * 2048, half ? &tmV : &tmK,
+                          64 * h, y, bar);
+          }
+          s_issued[2 * half + slot] = st;
         }
-        s_issued[slot] = st;
+        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
       }
     }
   } else if (warp == 5) {
@@ -1072,26 +1087,33 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc5::idesc_bf16_f32(kTcRows, kTok, false);
       constexpr uint32_t idesc_pv = tc5::idesc_bf16_f32(kTcRows, D, true);
-      // O += P V of stage j (P over the stage's K tile, V MN-major)
+      // O += P V of stage j: P (bf16) over the first 32 columns of S buffer
+      // j & 1 in tensor memory, V MN-major in shared memory
       auto pv = [&](int j) -> bool {
         const int slot = j & 1;
-        if (!mbar_wait_bounded(smem_u32(&s_pfull[slot]), (uint32_t)((j >> 1) & 1))) return false;
+        if (!mbar_wait_bounded(smem_u32(&s_pfull[slot]), (uint32_t)((j >> 1) & 1)) ||
+            !mbar_wait_bounded(smem_u32(&s_vfull[slot]), (uint32_t)((j >> 1) & 1)))
+          return false;
         tc5::fence_after_sync();
         const uint32_t sb = ring + slot * kSlotBytes;
+        const uint32_t ptm = tmem + (uint32_t)(slot * kTok);
 #pragma unroll
         for (int ks = 0; ks < kTok / 16; ++ks) {
-          const uint64_t ad = tc5::sw128_desc(sb + ks * 32, 16, 1024);
           const uint64_t bd = tc5::sw128_desc(sb + 2 * kHalf + ks * 2048, kHalf, 1024);
-          tc5::mma_bf16(tmem + kColO, ad, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+          tc5::mma_bf16_ts(tmem + kColO, ptm + ks * 8, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        tc5::commit(smem_u32(&s_empty[slot]));
+        tc5::commit(smem_u32(&s_vfree[slot]));
         tc5::commit(smem_u32(&s_odone));
         return true;
       };
       bool ok = true;
       for (int st = 0; st < n_stage && ok; ++st) {
         const int slot = st & 1;
-        if (!mbar_wait_bounded(smem_u32(&s_full[slot]), (uint32_t)((st >> 1) & 1)) ||
+        // K of stage st has landed, and PV of stage st - 2 -- which read its
+        // P from the S buffer this QK^T overwrites -- has completed
+        if (!mbar_wait_bounded(smem_u32(&s_kfull[slot]), (uint32_t)((st >> 1) & 1)) ||
+            (st >= 2 &&
+             !mbar_wait_bounded(smem_u32(&s_vfree[slot]), (uint32_t)(((st - 2) >> 1) & 1))) ||
             *reinterpret_cast<volatile int*>(&s_abort)) {
           ok = false;
           break;
@@ -1105,6 +1127,7 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
           tc5::mma_bf16(tmem + (uint32_t)(slot * kTok), ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
         }
         tc5::commit(smem_u32(&s_sfull[slot]));
+        tc5::commit(smem_u32(&s_kfree[slot]));
         if (st >= 1) ok = pv(st - 1);
       }
       if (ok && n_stage > 0) ok = pv(n_stage - 1);
@@ -1191,6 +1214,12 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
       // pages not loaded): zero their V rows so that P = 0 meets V = 0.
       const uint32_t sb = ring + slot * kSlotBytes;
       if (t0 + kTok > tok_end) {
+        // V of this stage must have landed before its tail is overwritten
+        const bool gv = mbar_wait_bounded(smem_u32(&s_vfull[slot]), (uint32_t)((st >> 1) & 1));
+        if (!__all_sync(0xffffffffu, gv)) {
+          ok = false;
+          break;
+        }
         const int first = max(0, tok_end - t0);
         for (int xx = tid; xx < (kTok - first) * 16; xx += 128) {
           const int t = first + (xx >> 4), c = xx & 15;
@@ -1198,14 +1227,10 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
           *reinterpret_cast<int4*>(base_ptr + (sb - base) + off) = make_int4(0, 0, 0, 0);
         }
       }
-      // P row t over the stage's K tile: 64 tokens = one 128-byte swizzled row
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t off = (uint32_t)(tid * 128 + ((c ^ (tid & 7)) << 4));
-        *reinterpret_cast<int4*>(base_ptr + (sb - base) + off) =
-            make_int4((int)pk[4 * c], (int)pk[4 * c + 1], (int)pk[4 * c + 2], (int)pk[4 * c + 3]);
-      }
-      fence_proxy_async_smem();
+      // P of row t (64 tokens, two bf16 per 32-bit column) over the first 32
+      // columns of the S buffer just read
+      tc5::tmem_st_x32(tmem + lane_base + (uint32_t)(slot * kTok), pk);
+      fence_proxy_async_smem();  // the zeroed V rows, for the tensor cores
       tc5::fence_before_sync();
       mbar_arrive(smem_u32(&s_pfull[slot]));
     }
@@ -1257,9 +1282,10 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
     // copies still in flight land before the CTA leaves (bounded waits)
     if (tid == 0) {
       flag(a.dev_status, SV_DEV_TIMEOUT);
-      for (int k = 0; k < 2; ++k)
+      for (int k = 0; k < 4; ++k)
         if (s_issued[k] >= 0)
-          mbar_wait_bounded(smem_u32(&s_full[k]), (uint32_t)((s_issued[k] >> 1) & 1));
+          mbar_wait_bounded(smem_u32(k < 2 ? &s_kfull[k] : &s_vfull[k - 2]),
+                            (uint32_t)((s_issued[k] >> 1) & 1));
     }
     __syncthreads();
   }
