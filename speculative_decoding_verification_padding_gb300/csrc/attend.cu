@@ -60,6 +60,12 @@ constexpr int kUnitsPerSM = 8;
 // of a few microseconds and a merge share), nor below twice that when the
 // work still gives every SM such a unit.
 constexpr int kMinPagesPerSplit = 32;
+// Calls with at most this many requests are latency-bound: splits go down to
+// kSmallPagesPerSplit pages and a separate kernel merges them, every unit of
+// a split group taking a slice of its rows (in-kernel, the group's last CTA
+// would merge every split alone).
+constexpr int kSmallBatch = 4;
+constexpr int kSmallPagesPerSplit = 8;
 constexpr int kMaxPagesPerSplit = 1024;  // block ids of a unit staged in shared memory
 
 struct ReqInfo {
@@ -107,6 +113,7 @@ struct Layout {
   int ucap, ucap_tc;
   int nsm;          // SMs of the device the call runs on
   int unit_target;  // units the planner aims for: kUnitsPerSM per SM
+  int small;        // at most kSmallBatch requests: small splits, merge kernel
 };
 
 // Units are at most W / P + Hkv * (row tiles): P >= W / unit_target unless it
@@ -131,7 +138,9 @@ inline Layout layout(int R, int total_rows, int group, int Hkv, int D, int max_b
   Layout L;
   size_t off = 0;
   L.nsm = sizing_sms();
-  L.unit_target = L.nsm * kUnitsPerSM;
+  L.small = R <= kSmallBatch ? 1 : 0;
+  // small batches aim for one wave (two units per SM), the rest for four
+  L.unit_target = L.nsm * (L.small ? 2 : kUnitsPerSM);
   L.ucap = unit_cap(R, total_rows, group, Hkv, max_blocks, L.unit_target);
   L.ucap_tc = unit_cap_tc(R, total_rows, group, Hkv, D, max_rows, max_blocks, L.nsm);
   L.header = off; off += align256(sizeof(Header));
@@ -266,9 +275,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
     // only requests the first chunk found valid (one with bad parents stops
     // there)
     if (w.ok && !(chunked && a.chunk.index > 0)) {
-      for (int j = 0; j < w.rows; ++j) {
-        const int p = a.bt.parent[cu + j];
-        badp |= (j == 0) ? (p != -1) : (p < 0 || p >= j);
+      for (int j0 = 0; j0 < w.rows; j0 += 8) {  // eight loads in flight, then the checks
+        int pp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pp[k] = j0 + k < w.rows ? a.bt.parent[cu + j0 + k] : 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int j = j0 + k;
+          if (j < w.rows) badp |= (j == 0) ? (pp[k] != -1) : (pp[k] < 0 || pp[k] >= j);
+        }
       }
     }
     bool valid = w.ok && !badp;
@@ -331,8 +346,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   }
   const unsigned long long target = (unsigned long long)a.L.unit_target;
   int P = (int)min((unsigned long long)kMaxPagesPerSplit, (W + target - 1) / target);
-  const int Pmin = W >= (unsigned long long)a.L.nsm * 2 * kMinPagesPerSplit ? 2 * kMinPagesPerSplit
-                                                                            : kMinPagesPerSplit;
+  const int Pmin = a.L.small ? kSmallPagesPerSplit
+                 : W >= (unsigned long long)a.L.nsm * 2 * kMinPagesPerSplit ? 2 * kMinPagesPerSplit
+                                                                         : kMinPagesPerSplit;
   if (P < Pmin) P = Pmin;
   // Work list offsets (exclusive scan of units per request); in chunk mode
   // also the accept's list of requests with a non-empty window, in request
@@ -429,24 +445,31 @@ __device__ __forceinline__ void merge_splits(const Args& a, const float* ml_all,
   const int group = a.group;
   for (int x = tid; x < (r1 - r0) * kQuads; x += nthreads) {
     const int vr = r0 + x / kQuads, c4 = x % kQuads;
-    // one online pass over the splits (running max, rescaled sums); the
-    // loads of consecutive splits are independent and overlap
+    // one online pass over the splits (running max, rescaled sums), eight
+    // splits' loads issued before any of them is merged
     float Mx = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const size_t row = (size_t)(gidx + sp) * TILE + vr;
-      const float2 ml2 = __ldcg(reinterpret_cast<const float2*>(ml_all + row * 2));
-      const float4 o4 = __ldcg(reinterpret_cast<const float4*>(op_all + row * D) + c4);
-      const float nm = fmaxf(Mx, ml2.x);
-      if (nm == -INFINITY) continue;
-      const float s_old = exp2f(Mx - nm), s_new = exp2f(ml2.x - nm);
-      L = L * s_old + ml2.y * s_new;
-      acc.x = acc.x * s_old + o4.x * s_new;
-      acc.y = acc.y * s_old + o4.y * s_new;
-      acc.z = acc.z * s_old + o4.z * s_new;
-      acc.w = acc.w * s_old + o4.w * s_new;
-      Mx = nm;
+    for (int sp0 = 0; sp0 < nsplit; sp0 += 8) {
+      float2 ml2[8];
+      float4 o4[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const size_t row = (size_t)(gidx + min(sp0 + k, nsplit - 1)) * TILE + vr;
+        ml2[k] = __ldcg(reinterpret_cast<const float2*>(ml_all + row * 2));
+        o4[k] = __ldcg(reinterpret_cast<const float4*>(op_all + row * D) + c4);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float nm = fmaxf(Mx, ml2[k].x);
+        if (sp0 + k >= nsplit || nm == -INFINITY) continue;
+        const float s_old = exp2f(Mx - nm), s_new = exp2f(ml2[k].x - nm);
+        L = L * s_old + ml2[k].y * s_new;
+        acc.x = acc.x * s_old + o4[k].x * s_new;
+        acc.y = acc.y * s_old + o4[k].y * s_new;
+        acc.z = acc.z * s_old + o4[k].z * s_new;
+        acc.w = acc.w * s_old + o4[k].w * s_new;
+        Mx = nm;
+      }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const int vgl = vr0 + vr;
@@ -866,6 +889,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         *reinterpret_cast<float2*>(op + (size_t)vl_b * D + dn * 8 + 2 * tq) = make_float2(f.o[dn][2], f.o[dn][3]);
     }
   }
+  if (a.L.small) return;  // merge_kernel combines the splits
   __threadfence();
   __syncthreads();
   const int gidx = ri.ubase + (rt * a.Hkv + g) * ri.nsplit;  // unit of split 0
@@ -896,11 +920,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 //     rescales the O accumulator in tensor memory only when its max grows
 //     by more than 2^8 (P stays below 256: exact in fp32, within bf16's
 //     range);
-//   warp 4: tensor-memory allocation and the TMA loads of K and V pages into
-//     a 2-slot ring (each slot K 16 KB then V 16 KB, 64-element halves of d
-//     as 8-row swizzle atoms, the layout both MMAs read).  K and V of a slot
-//     are refilled separately: K of stage s + 2 as soon as QK^T of stage s
-//     has run, V once PV of stage s has;
+//   warps 4 and 6: the TMA loads of K (warp 4, which also allocates the
+//     tensor memory) and of V (warp 6) pages into a 2-slot ring (each slot K
+//     16 KB then V 16 KB, 64-element halves of d as 8-row swizzle atoms, the
+//     layout both MMAs read).  K and V of a slot are refilled on their own
+//     schedules: K of stage s + 2 as soon as QK^T of stage s has run, V once
+//     PV of stage s has;
 //   warp 5: the MMA thread (QK^T of stage s + 1 is issued before PV of stage
 //     s, so the tensor cores work while the softmax warps do).
 // Two CTAs per SM (97 KB of shared memory and 256 TMEM columns each).
@@ -908,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // copies and MMAs land and frees its tensor memory before it returns.
 namespace tcu {
 constexpr int kTok = 64;                      // tokens per stage
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kQBytes = kTcRows * 256;        // Q: two halves of d, 128 rows x 128 B each
 constexpr int kHalf = kTok * 128;             // one 64-element half of d for 64 tokens
 constexpr int kSlotBytes = 4 * kHalf;         // K (two halves), then V (two halves)
@@ -1035,12 +1060,12 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
   tc5::fence_after_sync();
   const uint32_t tmem = s_tmem;
 
-  if (warp == 4) {
-    // ---------------------------------------------------------- producer --
-    // K of stage st after QK^T of stage st - 2, V after its PV: in the order
-    // K(st), V(st), K(st + 1), ... no wait is longer than the MMA order
-    // makes it anyway.
+  if (warp == 4 || warp == 6) {
+    // --------------------------------------------------------- producers --
+    // Warp 4 loads K, warp 6 V: K of stage st once QK^T of stage st - 2 has
+    // run, V once its PV has, each on its own schedule.
     if (lane == 0) {
+      const int half = warp == 6 ? 1 : 0;  // 0: K, 1: V
       for (int st = 0; st < n_stage; ++st) {
         const int slot = st & 1;
         int bids[4];
@@ -1057,7 +1082,7 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
           if (bid >= 0) bytes += 2u * 2048u;
         }
         const uint32_t kdst = ring + slot * kSlotBytes;
-        for (int half = 0; half < 2; ++half) {  // 0: K, 1: V
+        {
           unsigned long long* freeb = half ? s_vfree : s_kfree;
           unsigned long long* fullb = half ? s_vfull : s_kfull;
           if (st >= 2 &&
@@ -1158,23 +1183,23 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
         break;
       }
       tc5::fence_after_sync();
+      // S of this row (64 keys), scaled to the log2 domain in place
       uint32_t sv[kTok];
       tc5::tmem_ld_x64(tmem + lane_base + (uint32_t)(slot * kTok), sv);
       const int t0 = (blk0 + 4 * st) * kBlockSize;
-      float x[kTok];
 #pragma unroll
-      for (int j = 0; j < kTok; ++j) x[j] = __uint_as_float(sv[j]) * a.scale_log2;
+      for (int j = 0; j < kTok; ++j) sv[j] = __float_as_uint(__uint_as_float(sv[j]) * a.scale_log2);
       if (t0 + kTok > ctx || t0 + kTok > tok_end) {
         // Keys of this stage the row sees, as one 64-bit word: the context,
         // then the staged slots of its ancestors-or-self, none past tok_end.
         const unsigned long long vis = stage_visible(t0, ctx, tok_end, mk0, mk1);
 #pragma unroll
         for (int j = 0; j < kTok; ++j)
-          if (!((vis >> j) & 1ull)) x[j] = -INFINITY;
+          if (!((vis >> j) & 1ull)) sv[j] = __float_as_uint(-INFINITY);
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kTok; ++j) mx = fmaxf(mx, x[j]);
+      for (int j = 0; j < kTok; ++j) mx = fmaxf(mx, __uint_as_float(sv[j]));
       // a new reference max only when the row max passes it by 2^8
       const bool grow = mx > m_ref + 8.f;
       if (__any_sync(0xffffffffu, grow)) {
@@ -1205,7 +1230,7 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
       uint32_t pk[kTok / 2];
 #pragma unroll
       for (int j = 0; j < kTok; j += 2) {
-        const float p0 = ex2(x[j] - mb), p1 = ex2(x[j + 1] - mb);
+        const float p0 = ex2(__uint_as_float(sv[j]) - mb), p1 = ex2(__uint_as_float(sv[j + 1]) - mb);
         rs += p0 + p1;
         pk[j / 2] = pack_bf16(p0, p1);
       }
@@ -1292,32 +1317,35 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
   if (warp == 4) tc5::tmem_dealloc(tmem, kTmemCols);
 }
 
-// After the tcgen05 kernel: the units of a split group merge the group's
-// partials together, unit s of the group taking rows [s, s + 1) x
-// ceil(rows / nsplit) -- all splits' loads in flight at once on many SMs,
-// instead of one CTA reading every split of the tile.
+// After an attention kernel whose splits only wrote partials (the tcgen05
+// kernel always, the mma.sync kernel for small batches): the units of a split
+// group merge the group's partials together, unit s of the group taking rows
+// [s, s + 1) x ceil(rows / nsplit) -- all splits' loads in flight at once on
+// many SMs, instead of one CTA reading every split of the tile.
+// TC: the tcgen05 work list (128-row tiles), else the mma.sync one (64).
 constexpr int kMergeThreads = 256;
-template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_tc_kernel(const __grid_constant__ Args a) {
+template <int D, bool TC>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ Args a) {
   griddep_entry();
+  constexpr int TILE = TC ? kTcRows : kTileRows;
   const Header* hdr = reinterpret_cast<const Header*>(a.ws + a.L.header);
   const int u = blockIdx.x;
-  const int U = hdr->Utc;
-  const WorkItem ri = reinterpret_cast<const WorkItem*>(a.ws + a.L.work_tc)[u];
+  const int U = TC ? hdr->Utc : hdr->U;
+  const WorkItem ri = reinterpret_cast<const WorkItem*>(a.ws + (TC ? a.L.work_tc : a.L.work))[u];
   if (u >= U || ri.nsplit == 1) return;
   const int s = ri.local % ri.nsplit;
   const int rest = ri.local / ri.nsplit;
   const int g = rest % a.Hkv;
   const int rt = rest / a.Hkv;
-  const int vr0 = rt * kTcRows;
-  const int Mu = min(kTcRows, a.group * (ri.e - ri.b) - vr0);
+  const int vr0 = rt * TILE;
+  const int Mu = min(TILE, a.group * (ri.e - ri.b) - vr0);
   const int per = (Mu + ri.nsplit - 1) / ri.nsplit;
   const int r0 = min(Mu, s * per), r1 = min(Mu, r0 + per);
   if (r0 >= r1) return;
   const int gidx = ri.ubase + (rt * a.Hkv + g) * ri.nsplit;  // unit of split 0
-  merge_splits<D, kTcRows>(a, reinterpret_cast<const float*>(a.ws + a.L.ml_tc),
-                           reinterpret_cast<const float*>(a.ws + a.L.o_tc), gidx, ri.nsplit, r0, r1,
-                           vr0, ri.cu + ri.b, g, threadIdx.x, kMergeThreads);
+  merge_splits<D, TILE>(a, reinterpret_cast<const float*>(a.ws + (TC ? a.L.ml_tc : a.L.ml)),
+                        reinterpret_cast<const float*>(a.ws + (TC ? a.L.o_tc : a.L.o)), gidx,
+                        ri.nsplit, r0, r1, vr0, ri.cu + ri.b, g, threadIdx.x, kMergeThreads);
 }
 
 // cuTensorMapEncodeTiled from the driver, fetched through the runtime (no
@@ -1363,6 +1391,9 @@ sv_status launch(const Args& a, cudaStream_t stream) {
   if (sv::launch(plan_kernel, 1, 1024, plan_smem, stream, a) != cudaSuccess) return SV_ERR_CUDA;
   if (sv::launch(attend_kernel<D>, a.L.ucap, kThreads, smem, stream, a, tmK, tmV) != cudaSuccess)
     return SV_ERR_CUDA;
+  if (a.L.small &&
+      sv::launch(merge_kernel<D, false>, a.L.ucap, kMergeThreads, 0, stream, a) != cudaSuccess)
+    return SV_ERR_CUDA;
   if constexpr (D == 128) {
     if (a.L.ucap_tc > 0) {
       static PerDevice smem_set_tc;
@@ -1371,7 +1402,8 @@ sv_status launch(const Args& a, cudaStream_t stream) {
       if (sv::launch(attend_tc_kernel<D>, a.L.ucap_tc, tcu::kThreads, tcu::kSmem, stream, a, tmK,
                      tmV) != cudaSuccess)
         return SV_ERR_CUDA;
-      if (sv::launch(merge_tc_kernel<D>, a.L.ucap_tc, kMergeThreads, 0, stream, a) != cudaSuccess)
+      if (sv::launch(merge_kernel<D, true>, a.L.ucap_tc, kMergeThreads, 0, stream, a) !=
+          cudaSuccess)
         return SV_ERR_CUDA;
     }
   }
