@@ -638,10 +638,13 @@ def main():
     tree = 1 if (T > 0 and w.max_rows > 2) else 0
     tc = 1 if (w.cfg.head_dim == 128 and
                w.cfg.n_q_heads // w.cfg.n_kv_heads * w.max_rows >= 128) else 0
+    # attention: plan, [tcgen05 kernel], mma.sync kernel, [one merge launch when
+    # the tcgen05 kernel ran or the batch is small (<= 4 requests)]
+    att = 2 + tc + (1 if (tc or w.n_req <= 4) else 0)
     if mode == "chunked":
-        launches_per_step = n_launch * (2 + tc + 2) + race + (tree if chunk > 2 else 0)
+        launches_per_step = n_launch * (att + 2) + race + (tree if chunk > 2 else 0)
     else:
-        launches_per_step = 2 + tc + 2 + tree + race + (1 if mode == "budget" else 0)
+        launches_per_step = att + 2 + tree + race + (1 if mode == "budget" else 0)
     value = rows_all / t_step
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -1261,8 +1261,12 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
     }
     // The last PV has landed: O row t, normalised, to the output or to the
     // split partials.
+    // Every MMA has completed once the MMA thread's drain barrier completes
+    // its only phase.  (The PV barrier would not do: a parity wait names one
+    // phase only while the barrier is at most one phase from it, and here
+    // the last PV may or may not have landed already.)
     if (ok && n_stage > 0) {
-      const bool g3 = mbar_wait_bounded(smem_u32(&s_odone), (uint32_t)((n_stage - 1) & 1));
+      const bool g3 = mbar_wait_bounded(smem_u32(&s_drain), 0u);
       if (!__all_sync(0xffffffffu, g3)) ok = false;
     }
     if (!ok) {
@@ -1322,14 +1326,14 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
 // group merge the group's partials together, unit s of the group taking rows
 // [s, s + 1) x ceil(rows / nsplit) -- all splits' loads in flight at once on
 // many SMs, instead of one CTA reading every split of the tile.
-// TC: the tcgen05 work list (128-row tiles), else the mma.sync one (64).
+// One launch serves both lists: CTAs [0, n_small) take the mma.sync list
+// (64-row tiles; n_small = 0 unless small batches), the rest the tcgen05 list
+// (128-row tiles).
 constexpr int kMergeThreads = 256;
 template <int D, bool TC>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ Args a) {
-  griddep_entry();
+__device__ __forceinline__ void merge_unit(const Args& a, int u) {
   constexpr int TILE = TC ? kTcRows : kTileRows;
   const Header* hdr = reinterpret_cast<const Header*>(a.ws + a.L.header);
-  const int u = blockIdx.x;
   const int U = TC ? hdr->Utc : hdr->U;
   const WorkItem ri = reinterpret_cast<const WorkItem*>(a.ws + (TC ? a.L.work_tc : a.L.work))[u];
   if (u >= U || ri.nsplit == 1) return;
@@ -1346,6 +1350,17 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   merge_splits<D, TILE>(a, reinterpret_cast<const float*>(a.ws + (TC ? a.L.ml_tc : a.L.ml)),
                         reinterpret_cast<const float*>(a.ws + (TC ? a.L.o_tc : a.L.o)), gidx,
                         ri.nsplit, r0, r1, vr0, ri.cu + ri.b, g, threadIdx.x, kMergeThreads);
+}
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ Args a,
+                                                              int n_small) {
+  griddep_entry();
+  const int u = blockIdx.x;
+  if (u < n_small) {
+    merge_unit<D, false>(a, u);
+  } else if constexpr (D == 128) {
+    merge_unit<D, true>(a, u - n_small);
+  }
 }
 
 // cuTensorMapEncodeTiled from the driver, fetched through the runtime (no
@@ -1389,24 +1404,27 @@ sv_status launch(const Args& a, cudaStream_t stream) {
   const size_t plan_smem =
       a.bt.n_req <= kPlanSmemRequests ? sizeof(ReqInfo) * (size_t)a.bt.n_req : 0;
   if (sv::launch(plan_kernel, 1, 1024, plan_smem, stream, a) != cudaSuccess) return SV_ERR_CUDA;
-  if (sv::launch(attend_kernel<D>, a.L.ucap, kThreads, smem, stream, a, tmK, tmV) != cudaSuccess)
-    return SV_ERR_CUDA;
-  if (a.L.small &&
-      sv::launch(merge_kernel<D, false>, a.L.ucap, kMergeThreads, 0, stream, a) != cudaSuccess)
-    return SV_ERR_CUDA;
+  // the tensor-core units first (the long ones when there are any), then the
+  // mma.sync units, then one merge launch for every split group
+  int ucap_tc = 0;
   if constexpr (D == 128) {
-    if (a.L.ucap_tc > 0) {
+    ucap_tc = a.L.ucap_tc;
+    if (ucap_tc > 0) {
       static PerDevice smem_set_tc;
       if (smem_limit_once(smem_set_tc, attend_tc_kernel<D>, tcu::kSmem) != cudaSuccess)
         return SV_ERR_CUDA;
-      if (sv::launch(attend_tc_kernel<D>, a.L.ucap_tc, tcu::kThreads, tcu::kSmem, stream, a, tmK,
+      if (sv::launch(attend_tc_kernel<D>, ucap_tc, tcu::kThreads, tcu::kSmem, stream, a, tmK,
                      tmV) != cudaSuccess)
-        return SV_ERR_CUDA;
-      if (sv::launch(merge_kernel<D, true>, a.L.ucap_tc, kMergeThreads, 0, stream, a) !=
-          cudaSuccess)
         return SV_ERR_CUDA;
     }
   }
+  if (sv::launch(attend_kernel<D>, a.L.ucap, kThreads, smem, stream, a, tmK, tmV) != cudaSuccess)
+    return SV_ERR_CUDA;
+  const int n_small = a.L.small ? a.L.ucap : 0;
+  if (n_small + ucap_tc > 0 &&
+      sv::launch(merge_kernel<D>, n_small + ucap_tc, kMergeThreads, 0, stream, a, n_small) !=
+          cudaSuccess)
+    return SV_ERR_CUDA;
   return SV_OK;
 }
 
