@@ -283,7 +283,7 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm, Com
     if (!w.ok && lane == 0) flag(a.dev_status, SV_DEV_BAD_WINDOW);
     return kSkipped;
   }
-  const int cu = a.bt.cu_rows[i];
+  const int cu = w.cu;  // loaded with the window (a reload would follow the job store)
   const int V = a.V;
   bool chain = true, badp = false, badt = false;
   h.blk = -1;

@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   WorkItem* work = reinterpret_cast<WorkItem*>(a.ws + a.L.work);
   WorkItem* work_tc = reinterpret_cast<WorkItem*>(a.ws + a.L.work_tc);
   if (U > 0 || Utc > 0)
-    for (int i = warp; i < R; i += 32) {
+    for (int i = warp; i < R; i += (int)(blockDim.x >> 5)) {
       const ReqInfo ri = info[i];
       const int n = ri.nrt * a.Hkv * ri.nsplit;
       if (n == 0 || (ri.tc ? Utc : U) == 0) continue;
@@ -1403,7 +1403,11 @@ sv_status launch(const Args& a, cudaStream_t stream) {
     return SV_ERR_CUDA;
   const size_t plan_smem =
       a.bt.n_req <= kPlanSmemRequests ? sizeof(ReqInfo) * (size_t)a.bt.n_req : 0;
-  if (sv::launch(plan_kernel, 1, 1024, plan_smem, stream, a) != cudaSuccess) return SV_ERR_CUDA;
+  // one thread per request (its block-wide scans and barriers cost less with
+  // fewer warps), at least four warps to write the work items, at most 1024
+  const int plan_threads = min(1024, max(128, (a.bt.n_req + 31) / 32 * 32));
+  if (sv::launch(plan_kernel, 1, plan_threads, plan_smem, stream, a) != cudaSuccess)
+    return SV_ERR_CUDA;
   // the tensor-core units first (the long ones when there are any), then the
   // mma.sync units, then one merge launch for every split group
   int ucap_tc = 0;

@@ -37,12 +37,14 @@ __device__ __forceinline__ int find_segment(const int32_t* cu, int n, int x) {
 // Rows of request i handled by this call: [b, e) inside the chain end lim.
 struct Window {
   int rows, lim, b, e;
+  int cu;  // first packed row of the request
   bool ok;
 };
 
 __device__ __forceinline__ Window window_of(const sv_batch& bt, int i) {
   Window w;
   const int c0 = bt.cu_rows[i], c1 = bt.cu_rows[i + 1];
+  w.cu = c0;
   w.rows = c1 - c0;
   w.ok = w.rows >= 1 && w.rows <= bt.max_rows_per_req && w.rows <= kMaxRows && c0 >= 0 &&
          c1 <= bt.total_rows;
