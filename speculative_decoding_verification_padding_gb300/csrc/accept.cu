@@ -195,6 +195,8 @@ __device__ __forceinline__ bool live(const Args& a, const Window& w, int i) {
 struct DecideSmem {
   float mp[kMaxRows], lp[kMaxRows], mq[kMaxRows], lq[kMaxRows];
   int am[kMaxRows], len[kMaxRows], child[kMaxRows], par[kMaxRows], tok[kMaxRows];
+  int dep[kMaxRows];          // greedy tree: depth of each node
+  unsigned key[kMaxRows];     // greedy tree: best (1 + descent) << 8 | (255 - child)
 };
 
 // Merge the slice partials of n0 target rows r0.. (type 0) and n1 draft rows
@@ -202,6 +204,8 @@ struct DecideSmem {
 // spread over the warp: up to 32 at a time, each on a group of G lanes (the
 // largest power of two that fits), every lane merging slices sub, sub + G, ...
 // of its pair, then log2(G) shuffle rounds inside the group.
+// kLoads: partial loads in flight per lane (fewer where registers are scarce).
+template <int kLoads = 32>
 __device__ __forceinline__ void merge_pairs(const Args& a, int nch, int r0, int n0, int n1,
                                             float* m0, float* lv0, float* m1, float* lv1) {
   const int lane = threadIdx.x & 31;
@@ -219,18 +223,18 @@ __device__ __forceinline__ void merge_pairs(const Args& a, int nch, int r0, int 
     float m = -INFINITY, lv = 0.f;
     int am = 0x7fffffff;
     if (live) {
-      // 16 loads in flight per lane, then the merges
+      // kLoads loads in flight per lane, then the merges
       const StatPart* pr = parts + ((size_t)row * 2 + type) * nch;
       const float2 ident = make_float2(-INFINITY, T > 0.f ? 0.f : __int_as_float(0x7fffffff));
-      for (int c0 = sub; c0 < nch; c0 += 16 * G) {
-        float2 v[16];
+      for (int c0 = sub; c0 < nch; c0 += kLoads * G) {
+        float2 v[kLoads];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < kLoads; ++k) {
           const int c = c0 + k * G;
           v[k] = c < nch ? __ldcg(reinterpret_cast<const float2*>(pr + c)) : ident;
         }
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < kLoads; ++k) {
           if (T > 0.f) merge_ml(m, lv, v[k].x, v[k].y);
           else merge_am(m, am, v[k].x, __float_as_int(v[k].y));
         }
@@ -371,27 +375,70 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm, Com
         if (next < 0 && w.e == w.lim && len == w.lim - 1) next = sm.am[w.lim - 1];
       }
     } else {
-      // tree: longest valid path, lower node index on ties (bottom-up)
-      for (int n = w.rows - 1; n >= 0; --n) {
-        int best = 0, bc = -1;
-        for (int c = n + 1 + lane; c < w.rows; c += 32) {
-          if (sm.par[c] == n && sm.tok[c] == sm.am[n]) {
-            const int cand = 1 + sm.len[c];
-            if (cand > best || (cand == best && bc >= 0 && c < bc)) { best = cand; bc = c; }
-          }
-        }
+      // tree: longest valid path, lower node index on ties.  Every node n
+      // gets len[n] = max over children c whose token is the argmax of row n
+      // of 1 + len[c] (0 without one) and child[n] = the lowest such c of
+      // that length, computed level by level from the deepest: a child
+      // offers (1 + len[c]) << 8 | (255 - c) to its parent by an atomic max
+      // (rows <= 128, so the low byte orders the indices).  Depths by
+      // pointer jumping: 7 rounds cover 128 levels.
+      const int rows = w.rows;
+      int jmp[4], dd[4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const int b2 = __shfl_xor_sync(0xffffffffu, best, o);
-          const int c2 = __shfl_xor_sync(0xffffffffu, bc, o);
-          if (b2 > best || (b2 == best && c2 >= 0 && (bc < 0 || c2 < bc))) { best = b2; bc = c2; }
+      for (int t = 0; t < 4; ++t) {
+        const int c = lane + 32 * t;
+        jmp[t] = c < rows && c > 0 ? sm.par[c] : 0;
+        dd[t] = c < rows && c > 0 ? 1 : 0;
+        if (c < rows) {
+          sm.dep[c] = dd[t];
+          sm.child[c] = jmp[t];  // jump pointers, replaced below
+          sm.key[c] = 0u;
         }
-        if (lane == 0) {
-          sm.len[n] = best;
-          sm.child[n] = bc;
+      }
+      __syncwarp();
+      for (int round = 0; round < 7; ++round) {
+        int nj[4], nd[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          nj[t] = jmp[t] ? sm.child[jmp[t]] : 0;
+          nd[t] = dd[t] + (jmp[t] ? sm.dep[jmp[t]] : 0);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int c = lane + 32 * t;
+          jmp[t] = nj[t];
+          dd[t] = nd[t];
+          if (c < rows) {
+            sm.child[c] = nj[t];
+            sm.dep[c] = nd[t];
+          }
         }
         __syncwarp();
       }
+      int maxd = 0;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) maxd = max(maxd, dd[t]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) maxd = max(maxd, __shfl_xor_sync(0xffffffffu, maxd, o));
+      for (int level = maxd; level >= 1; --level) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int c = lane + 32 * t;
+          if (c < rows && dd[t] == level) {
+            const int p = sm.par[c];
+            if (sm.tok[c] == sm.am[p])
+              atomicMax(&sm.key[p], ((1u + (sm.key[c] >> 8)) << 8) | (unsigned)(255 - c));
+          }
+        }
+        __syncwarp();
+      }
+      for (int n = lane; n < rows; n += 32) {
+        const unsigned k = sm.key[n];
+        sm.len[n] = (int)(k >> 8);
+        sm.child[n] = k ? 255 - (int)(k & 255u) : -1;
+      }
+      __syncwarp();
       if (lane == 0) {
         int n = 0, k = 0;
         while (sm.child[n] >= 0) {
@@ -787,13 +834,29 @@ __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
           m &= m - 1;
           const unsigned long long sr = __shfl_sync(0xffffffffu, srow, j);
           const unsigned long long dr = __shfl_sync(0xffffffffu, drow, j);
-          for (int x = lane; x < per_slot; x += 32) {
-            const int tensor = x / (c.Hkv * cpr), rem = x % (c.Hkv * cpr);
-            const int g = rem / cpr, q = rem % cpr;
-            __nv_bfloat16* base = tensor ? c.v : c.k;
-            const int4 val =
-                reinterpret_cast<const int4*>(base + (sr + (size_t)g * kBlockSize) * c.D)[q];
-            reinterpret_cast<int4*>(base + (dr + (size_t)g * kBlockSize) * c.D)[q] = val;
+          // eight 16-byte loads of the slot in flight per lane, then their stores
+          for (int x0 = 0; x0 < per_slot; x0 += 32 * 8) {
+            int4 val[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const int x = x0 + 32 * t + lane;
+              if (x < per_slot) {
+                const int tensor = x / (c.Hkv * cpr), rem = x % (c.Hkv * cpr);
+                const int g = rem / cpr, q = rem % cpr;
+                const __nv_bfloat16* base = tensor ? c.v : c.k;
+                val[t] = reinterpret_cast<const int4*>(base + (sr + (size_t)g * kBlockSize) * c.D)[q];
+              }
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const int x = x0 + 32 * t + lane;
+              if (x < per_slot) {
+                const int tensor = x / (c.Hkv * cpr), rem = x % (c.Hkv * cpr);
+                const int g = rem / cpr, q = rem % cpr;
+                __nv_bfloat16* base = tensor ? c.v : c.k;
+                reinterpret_cast<int4*>(base + (dr + (size_t)g * kBlockSize) * c.D)[q] = val[t];
+              }
+            }
           }
           __syncwarp();
         }
@@ -940,7 +1003,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
         cnt += __popc(m);
       }
       if (lane == 0) s_nk = cnt;
-      merge_pairs(a, nch, cu + n, 1, cnt > 0 ? 1 : 0, &s_st[0], &s_st[1], &s_st[2], &s_st[3]);
+      merge_pairs<16>(a, nch, cu + n, 1, cnt > 0 ? 1 : 0, &s_st[0], &s_st[1], &s_st[2], &s_st[3]);
     }
     __syncthreads();
     const int nk = s_nk;
