@@ -682,7 +682,7 @@ def main():
 
 
 # Revision tag of the attention kernel the stored ncu traffic belongs to.
-KERNEL_REV = "attend-tma-v3"
+KERNEL_REV = "attend-tma-v4"
 
 if __name__ == "__main__":
     main()
