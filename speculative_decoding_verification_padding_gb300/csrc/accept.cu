@@ -59,7 +59,8 @@ struct Job {
 
 struct RacePart {
   float key;
-  int idx;
+  int idx;   // the slice's best group
+  int tok;   // the entry drawn inside that group
 };
 
 constexpr int kStatThreads = 256;
@@ -70,6 +71,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Slices per row (stats) and per request (race): about 32 warps per SM in
 // flight, slices of at least 2 KB.
 constexpr int kMaxSlices = 64;  // vocabulary slices per row at most
+constexpr long kKeepL2Bytes = 48L << 20;  // logits of a call the statistics keep in L2
 
 inline int stats_chunks(int rows_bound, int V, int nsm) {
   const int maxc = max(1, min(kMaxSlices, V / 512));
@@ -162,6 +164,8 @@ struct Args {
   int use_list;   // the requests come from the active list (chunked steps)
   const int4* act4;  // with the list: (request, first row, rows, draft rows) per entry
   int commit;     // fused KV commit (sv_accept_commit)
+  int keep_l2;    // the statistics load the logits to stay in L2 (small
+                  // calls: the decision and the race read them again)
   CommitArgs kv;
 };
 
@@ -252,6 +256,41 @@ __device__ __forceinline__ void merge_pairs(const Args& a, int nch, int r0, int 
       else { m1[p - n0] = m; lv1[p - n0] = out_lv; }
     }
   }
+}
+
+// a + b as s + e exactly (Knuth's two-sum; IEEE operations, no contraction).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// The acceptance ratio min(1, p / q) of a drafted token with x = logit / T
+// (xp target, xq draft) and row statistics (m, l): p = exp(xp - mp) / lp,
+// q = exp(xq - mq) / lq, so p / q = exp((xp - mp) - (xq - mq)) * lq / lp.
+// The exponent is formed exactly (two-sums) and one expf is taken, so the
+// ratio carries a few 1e-7 of relative error besides that of the fp32
+// normalisers -- inside the 1e-6 band where a decision counts as ambiguous.
+// Everything stays in fp32: double precision runs at a small fraction of the
+// fp32 rate on this GPU, and the dependent fp64 chain of the former form
+// cost microseconds per decision.  q that would vanish in double (q below
+// the smallest denormal) gives ratio 1, as the definition's q > 0 test does.
+// p and q themselves (row statistics output) are formed in fp32.
+__device__ __forceinline__ float accept_ratio(float xp, float xq, float mp, float lp, float mq,
+                                              float lq, float* p_out, float* q_out) {
+  if (p_out) {
+    *p_out = __fdiv_rn(expf(__fsub_rn(xp, mp)), lp);
+    *q_out = __fdiv_rn(expf(__fsub_rn(xq, mq)), lq);
+  }
+  float s1, e1, s2, e2, h, l;
+  two_sum(xq, -mq, s2, e2);
+  if (s2 - logf(lq) < -745.13f) return 1.f;  // also xq = -inf
+  two_sum(xp, -mp, s1, e1);
+  if (s1 == -INFINITY) return 0.f;          // p = 0
+  two_sum(s1, -s2, h, l);
+  l = __fadd_rn(l, __fsub_rn(e1, e2));
+  const float r = __fdiv_rn(__fmul_rn(expf(h) * (1.f + l), lq), lp);
+  return fminf(1.f, r);
 }
 
 // The decision for request i, by one warp, once all its row partials exist.
@@ -483,20 +522,18 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm, Com
   // Lane j - b - 1 evaluates draft j's ratio and draws its uniform; the scan
   // then reads them by shuffle.
   const float T = a.T;
-  double ratio = 1.0;
+  float ratio = 1.f;
   float u_lane = 0.f;
   {
     const int j = w.b + 1 + lane;
     if (lane < nd) {
       u_lane = accept_u(a.seed, i, j);
-      const float xp = xp_raw / T;
-      const float xq = xq_raw / T;
-      const double p = exp((double)xp - (double)sm.mp[j - 1]) / (double)sm.lp[j - 1];
-      const double q = exp((double)xq - (double)sm.mq[j - 1]) / (double)sm.lq[j - 1];
-      ratio = q > 0.0 ? fmin(1.0, p / q) : 1.0;
+      float p, q;
+      ratio = accept_ratio(xp_raw / T, xq_raw / T, sm.mp[j - 1], sm.lp[j - 1], sm.mq[j - 1],
+                           sm.lq[j - 1], rs ? &p : nullptr, &q);
       if (rs) {
-        rs[(size_t)(cu + j) * 4 + 2] = (float)p;
-        rs[(size_t)(cu + j) * 4 + 3] = (float)q;
+        rs[(size_t)(cu + j) * 4 + 2] = p;
+        rs[(size_t)(cu + j) * 4 + 3] = q;
       }
     }
   }
@@ -506,22 +543,23 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm, Com
   jb.c = 1.f;
   for (int k = 0; k < nd; ++k) {
     const int j = w.b + 1 + k;
-    const double rk = __shfl_sync(0xffffffffu, ratio, k & 31);
+    const float rk = __shfl_sync(0xffffffffu, ratio, k & 31);
     const float uk = __shfl_sync(0xffffffffu, u_lane, k & 31);
     if (k >= 32) {  // windows longer than a warp: evaluate the rest serially
       const int x = sm.tok[j];
       const size_t off = (size_t)(cu + j - 1) * V + x;
-      const double p = exp((double)(a.target[off] / T) - (double)sm.mp[j - 1]) / (double)sm.lp[j - 1];
-      const double q = exp((double)(a.draft[off] / T) - (double)sm.mq[j - 1]) / (double)sm.lq[j - 1];
-      ratio = q > 0.0 ? fmin(1.0, p / q) : 1.0;
+      float p, q;
+      ratio = accept_ratio(a.target[off] / T, a.draft[off] / T, sm.mp[j - 1], sm.lp[j - 1],
+                           sm.mq[j - 1], sm.lq[j - 1], rs ? &p : nullptr, &q);
       if (rs && lane == 0) {
-        rs[(size_t)(cu + j) * 4 + 2] = (float)p;
-        rs[(size_t)(cu + j) * 4 + 3] = (float)q;
+        rs[(size_t)(cu + j) * 4 + 2] = p;
+        rs[(size_t)(cu + j) * 4 + 3] = q;
       }
     }
-    const double r_j = k >= 32 ? ratio : rk;
-    const double u = (double)(k >= 32 ? accept_u(a.seed, i, j) : uk);
-    if (fabs(u - r_j) < 1e-6) amb = true;
+    const float r_j = k >= 32 ? ratio : rk;
+    const float u = k >= 32 ? accept_u(a.seed, i, j) : uk;
+    // u and r_j lie in [0, 1]: their difference is exact when it is small
+    if (fabsf(u - r_j) < 1e-6f) amb = true;
     if (u < r_j) {
       len = j;
       if (lane == 0) nodes[j] = j;
@@ -560,7 +598,8 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm, Com
 // Warp-granular: every warp owns one slice of one row at a time and reduces
 // it with shuffles into one partial (no warp waits for another); the
 // decision kernel merges the partials.
-template <bool VEC>
+// KEEP: the logits are loaded to stay in L2 (small calls), else streamed.
+template <bool VEC, bool KEEP>
 __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
   griddep_entry();
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
@@ -650,7 +689,8 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
 #pragma unroll
           for (int k = 0; k < kDepth; ++k) {
             const int v = v0 + 128 * k;
-            x[k] = v < hi ? __ldcs(p4 + (v >> 2)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            x[k] = v < hi ? (KEEP ? __ldg(p4 + (v >> 2)) : __ldcs(p4 + (v >> 2)))
+                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
           }
           float mx = -INFINITY;
 #pragma unroll
@@ -693,7 +733,8 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
 #pragma unroll
           for (int k = 0; k < kDepth; ++k) {
             const int v = v0 + 128 * k;
-            x[k] = v < hi ? __ldcs(p4 + (v >> 2)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            x[k] = v < hi ? (KEEP ? __ldg(p4 + (v >> 2)) : __ldcs(p4 + (v >> 2)))
+                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
           }
 #pragma unroll
           for (int k = 0; k < kDepth; ++k) {
@@ -778,11 +819,18 @@ __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
                                                const CommitHint* hint) {
   const int lane = threadIdx.x & 31;
   const CommitArgs& c = a.kv;
+  // A call with one request needs no ticket: its warp releases at once (the
+  // free count's load goes out first).
+  const bool alone = a.bt.n_req == 1;
+  const int fc_alone = alone ? *c.free_count : 0;
+  const bool chain_hint = final && hint && hint->chain;
   int2 span = make_int2(0, 0);
-  if (final && hint && hint->chain) {
+  int ctx_span = 0;  // cache length the span was computed from
+  if (chain_hint) {
     // A chain the decision just decided: its path is 0..al (nothing moves);
     // the same rules as commit_check, on the values the decision holds.
     const int rows = hint->rows, ctx = hint->ctx, al = hint->al;
+    ctx_span = ctx;
     int bad = 0;
     if (rows < 1 || rows > a.bt.max_rows_per_req || al < 0 || al > rows - 1) {
       bad = SV_DEV_BAD_WINDOW;
@@ -803,6 +851,7 @@ __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
     const int rows = a.bt.cu_rows[i + 1] - a.bt.cu_rows[i];
     const int ctx = c.cache_lens[i];
     const int al = a.accepted_len[i];
+    ctx_span = ctx;
     const int32_t* path = a.accepted_nodes + (size_t)i * a.bt.max_rows_per_req;
     const int32_t* table = c.tables + (size_t)i * c.max_blocks;
     const int bad = commit_check(a, rows, ctx, al, path, table);
@@ -866,16 +915,44 @@ __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
       if (lane == 0) c.cache_lens[i] = ctx + 1 + al;
     }
   }
+  if (alone) {
+    // The span (at most nine blocks: rows <= 128) with its block ids in
+    // registers: a decided chain's from the decision's own loads (lane k
+    // holds the block of slot ctx + k), else one load per lane.
+    const int n = span.y - span.x;
+    int32_t* table = c.tables + (size_t)i * c.max_blocks;
+    int blk = -1;
+    if (chain_hint) {
+      const int kt = max(0, (span.x + lane) * kBlockSize - ctx_span);
+      const int b = __shfl_sync(0xffffffffu, hint->blk, min(kt, 31));
+      if (lane < n) blk = b;
+    } else if (lane < n) {
+      blk = table[span.x + lane];
+    }
+    const bool has = lane < n && blk >= 0;
+    const unsigned m = __ballot_sync(0xffffffffu, has);
+    const int nfree = __popc(m);
+    if (nfree == 0) return;
+    if ((long)fc_alone + nfree <= c.capacity) {
+      if (has) {
+        c.free_list[fc_alone + __popc(m & ((1u << lane) - 1u))] = blk;
+        table[span.x + lane] = -1;
+      }
+      if (lane == 0) *c.free_count = fc_alone + nfree;
+    } else if (lane == 0) {
+      flag(a.dev_status, SV_DEV_POOL_OVERFLOW);
+    }
+    return;
+  }
   int last = 0;
   if (lane == 0) {
     reinterpret_cast<int2*>(a.ws + a.L.cspan)[i] = span;
-    __threadfence();
-    last = atomicAdd(reinterpret_cast<int*>(a.ws + a.L.ctick), 1) == a.bt.n_req - 1;
+    last = ticket_add(reinterpret_cast<int*>(a.ws + a.L.ctick), 1) == a.bt.n_req - 1;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   // Every request is done: release in (request, table index) order.
-  __threadfence();
+  __syncwarp();
   const int R = a.bt.n_req;
   const int2* spans = reinterpret_cast<const int2*>(a.ws + a.L.cspan);
   const int fc0 = *c.free_count;
@@ -1110,6 +1187,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
 __device__ __forceinline__ void race_take(float& best, int& bi, float key, int v) {
   if (key > best || (key == best && v < bi)) { best = key; bi = v; }
 }
+// The same, carrying the entry drawn inside the group along.
+__device__ __forceinline__ void race_take(float& best, int& bi, int& tok, float key, int v, int t) {
+  if (key > best || (key == best && v < bi)) { best = key; bi = v; tok = t; }
+}
 
 constexpr int kRaceBlock = 512;  // entries of 128 groups: one counter per lane
 
@@ -1142,13 +1223,26 @@ __device__ __forceinline__ float sum4(float4 w) { return ((w.x + w.y) + w.z) + w
 
 // Running best (W, E) of a lane: group g beats it iff W_g E_b > W_b E_g,
 // lower index on ties.
-__device__ __forceinline__ void race_keep(float wg, float E, int g, float& bw, float& bE, int& bi) {
+__device__ __forceinline__ bool race_keep(float wg, float E, int g, float& bw, float& bE, int& bi) {
   const float lhs = wg * bE, rhs = bw * E;
   if (lhs > rhs || (lhs == rhs && g < bi)) {
     bw = wg;
     bE = E;
     bi = g;
+    return true;
   }
+  return false;
+}
+
+// Step 2 of the draw: the entry of group g (weights w, invalid entries 0)
+// whose running sum first exceeds t = u W, with u from pick_u; at the very
+// top of the range, the last positive entry.
+__device__ __forceinline__ int pick_in_group(uint64_t seed, int i, int pos, int g, float4 w) {
+  const float s1 = w.x, s2 = s1 + w.y, s3 = s2 + w.z, W = s3 + w.w;
+  const float t = pick_u(seed, i, pos, g) * W;
+  int k = t < s1 ? 0 : t < s2 ? 1 : t < s3 ? 2 : t < W ? 3 : -1;
+  if (k < 0) k = w.w > 0.f ? 3 : w.z > 0.f ? 2 : w.y > 0.f ? 1 : 0;
+  return 4 * g + k;
 }
 
 // Shared-memory ring of the vectorised race: per warp kRaceStages blocks in
@@ -1251,6 +1345,7 @@ __global__ void __launch_bounds__(kRaceThreads, 3) race_kernel(Args a) {
     int* kbest = reinterpret_cast<int*>(a.ws + a.L.race_tickets) + R + i;
     float bw = -1.f, bE = 1.f, K = 0.f;
     int bi = 0x7fffffff;
+    float4 bwv = make_float4(0.f, 0.f, 0.f, 0.f);  // weights of this lane's best group
     int kg_bits = 0;
     for (int b = 0; b < nb; ++b) {
       const int base = lo + b * kRaceBlock;
@@ -1307,9 +1402,9 @@ __global__ void __launch_bounds__(kRaceThreads, 3) race_kernel(Args a) {
             xq = make_float4(lq[v], nk > 1 ? lq[v + 1] : 0.f, nk > 2 ? lq[v + 2] : 0.f,
                              nk > 3 ? lq[v + 3] : 0.f);
         }
-        const float4 pk = group_p(rw, xk, nk);
-        const float Wg = resid ? sum4(group_w(rw, pk, xq, nk)) : sum4(pk);
-        race_keep(Wg, -logf(race_u(wk)), base / 4 + 32 * k + lane, bw, bE, bi);
+        const float4 w4 = group_w(rw, group_p(rw, xk, nk), xq, nk);
+        if (race_keep(sum4(w4), -logf(race_u(wk)), base / 4 + 32 * k + lane, bw, bE, bi))
+          bwv = w4;
       };
       unsigned todo = 0;  // groups of this lane still to key exactly
       if (K == 0.f) {
@@ -1359,55 +1454,59 @@ __global__ void __launch_bounds__(kRaceThreads, 3) race_kernel(Args a) {
       }
     }
     if (timed_out) break;
+    // The warp's best group, and its entry drawn by the lane that holds it
+    // (the same weights the last warp would compute from the logits).
     float best = bi == 0x7fffffff ? -1.f : bw / bE;
+    const int own = bi;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
       const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
       race_take(best, bi, b2, i2);
     }
+    const bool holder = bi != 0x7fffffff && own == bi;
+    const int tok_own = holder ? pick_in_group(a.seed, i, jb.pos, bi, bwv) : -1;
+    const unsigned hm = __ballot_sync(0xffffffffu, holder);
+    const int tok = __shfl_sync(0xffffffffu, tok_own, hm ? __ffs(hm) - 1 : 0);
     RacePart* parts = reinterpret_cast<RacePart*>(a.ws + a.L.race) + (size_t)i * nch;
     int* ticket = reinterpret_cast<int*>(a.ws + a.L.race_tickets) + i;
     int last = 0;
     if (lane == 0) {
       parts[c].key = best;
       parts[c].idx = bi;
-      __threadfence();
-      last = atomicAdd(ticket, 1) == nch - 1;
+      parts[c].tok = tok;
+      last = ticket_add(ticket, 1) == nch - 1;
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
-      // last slice of request i: the winning group, then its entry
-      __threadfence();
+      // last slice of request i: the winning group (its entry drawn already),
+      // eight slices' loads in flight per lane
+      __syncwarp();
       float bk = -1.f;
-      int g = 0x7fffffff;
-      for (int k = lane; k < nch; k += 32) race_take(bk, g, __ldcg(&parts[k].key), __ldcg(&parts[k].idx));
+      int g = 0x7fffffff, tk = -1;
+      for (int k0 = lane; k0 < nch; k0 += 32 * 8) {
+        float kk[8];
+        int gg[8], tt[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int k = k0 + 32 * j;
+          kk[j] = k < nch ? __ldcg(&parts[k].key) : -1.f;
+          gg[j] = k < nch ? __ldcg(&parts[k].idx) : 0x7fffffff;
+          tt[j] = k < nch ? __ldcg(&parts[k].tok) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) race_take(bk, g, tk, kk[j], gg[j], tt[j]);
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float b2 = __shfl_xor_sync(0xffffffffu, bk, o);
         const int i2 = __shfl_xor_sync(0xffffffffu, g, o);
-        race_take(bk, g, b2, i2);
+        const int t2 = __shfl_xor_sync(0xffffffffu, tk, o);
+        race_take(bk, g, tk, b2, i2, t2);
       }
-      const bool found = g >= 0 && g < (V + 3) / 4;  // every non-empty slice finds one
-      const int v0 = found ? 4 * g : 0;
-      const int n = found ? min(4, V - v0) : 0;
-      if (lane == 0 && n > 0) {
-        const float4 xp = make_float4(lp[v0], n > 1 ? lp[v0 + 1] : 0.f, n > 2 ? lp[v0 + 2] : 0.f,
-                                      n > 3 ? lp[v0 + 3] : 0.f);
-        float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (resid)
-          xq = make_float4(lq[v0], n > 1 ? lq[v0 + 1] : 0.f, n > 2 ? lq[v0 + 2] : 0.f,
-                           n > 3 ? lq[v0 + 3] : 0.f);
-        const float4 w = group_w(rw, group_p(rw, xp, n), xq, n);
-        const float s1 = w.x, s2 = s1 + w.y, s3 = s2 + w.z, W = s3 + w.w;
-        const float t = pick_u(a.seed, i, jb.pos, g) * W;
-        int k = t < s1 ? 0 : t < s2 ? 1 : t < s3 ? 2 : t < W ? 3 : -1;
-        if (k < 0)  // t at the very top of the range: the last positive entry
-          k = w.w > 0.f ? 3 : w.z > 0.f ? 2 : w.y > 0.f ? 1 : 0;
-        a.next_token[i] = v0 + k;
-        *ticket = 0;
-      } else if (lane == 0) {
-        a.next_token[i] = -1;  // no group (empty vocabulary slice set)
+      if (lane == 0) {
+        // every non-empty slice finds a group; none: an empty vocabulary set
+        a.next_token[i] = (g >= 0 && g < (V + 3) / 4) ? tk : -1;
         *ticket = 0;
       }
     }
@@ -1511,15 +1610,19 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
     a.kv.capacity = commit_pool->capacity;
   }
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
+  // Logits of a small call (up to kKeepL2Bytes) are loaded so that they stay
+  // in L2 for the decision and the race; larger ones stream past it.
+  const long stat_rows = min((long)bt->total_rows, (long)bt->n_req * a.L.maxw);
+  a.keep_l2 = stat_rows * vocab * 4L * (temperature > 0.f ? 2 : 1) <= kKeepL2Bytes ? 1 : 0;
   const bool vec = vec_ok(vocab, target_logits, draft_logits);
   a.use_list = chunk_step ? 1 : 0;
   a.act4 = chunk_step ? act4 : nullptr;
   const long items = (long)bt->n_req * a.L.maxw * (temperature > 0.f ? 2 : 1) * a.L.nch_cap;
   const long warps = kStatThreads / 32;
   const unsigned gs = (unsigned)max(1L, min((items + warps - 1) / warps, (long)a.L.nsm * 4));
-  if (sv::launch(vec ? stats_kernel<true> : stats_kernel<false>, gs, kStatThreads, 0, s, a) !=
-      cudaSuccess)
-    return SV_ERR_CUDA;
+  auto stats = a.keep_l2 ? (vec ? stats_kernel<true, true> : stats_kernel<false, true>)
+                         : (vec ? stats_kernel<true, false> : stats_kernel<false, false>);
+  if (sv::launch(stats, gs, kStatThreads, 0, s, a) != cudaSuccess) return SV_ERR_CUDA;
   const unsigned gd = (unsigned)max(1, min((bt->n_req + kDecideWarps - 1) / kDecideWarps, a.L.nsm * 8));
   if (sv::launch(decide_kernel, gd, kDecideWarps * 32, 0, s, a) != cudaSuccess) return SV_ERR_CUDA;
   if (temperature > 0.f && bt->max_rows_per_req > 2 &&

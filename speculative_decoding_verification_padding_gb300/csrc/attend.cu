@@ -429,6 +429,169 @@ __global__ void __launch_bounds__(1024) plan_kernel(Args a) {
   }
 }
 
+// ------------------------------------------------------------ small plan --
+// One-pass calls with at most kSmallBatch requests are planned by a single
+// warp (the rules of plan_kernel, without its block-wide scans and barriers):
+// lane r loads request r's window and cache length while lane 0 checks the
+// packed total, then the warp checks every request's parents with all loads
+// in flight, and shuffles give the work, the split sizes and the list
+// offsets.  Two dependent round trips in all.
+struct SmallPlan {
+  int U, P, Utc, Ptc;
+  int ubase[kSmallBatch], nsplit[kSmallBatch], nrt[kSmallBatch], tc[kSmallBatch];
+  int b[kSmallBatch], e[kSmallBatch], ctx[kSmallBatch], nblk[kSmallBatch];
+  int cu[kSmallBatch], rows[kSmallBatch];
+};
+
+__device__ __forceinline__ void small_plan_warp(const Args& a, SmallPlan& sp, bool report) {
+  const unsigned kAll = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int R = a.bt.n_req;  // 1 .. kSmallBatch
+  Window w{};
+  int ctx = 0;
+  if (lane < R) {
+    w = window_of(a.bt, lane);
+    ctx = a.cache_lens[lane];
+  }
+  if (report && lane == 0 && (a.bt.cu_rows[0] != 0 || a.bt.cu_rows[R] != a.bt.total_rows))
+    flag(a.dev_status, SV_DEV_BAD_WINDOW);
+  // parents of every request with a valid window, all loads in flight at once
+  // (a valid window has at most kMaxRows = 128 rows: four per lane)
+  int pv[kSmallBatch][4];
+  int wrows[kSmallBatch];
+  bool wok[kSmallBatch];
+#pragma unroll
+  for (int r = 0; r < kSmallBatch; ++r) {
+    wrows[r] = __shfl_sync(kAll, w.rows, r);
+    const int okr = __shfl_sync(kAll, (int)w.ok, r);
+    wok[r] = r < R && okr != 0;
+    const int cu = __shfl_sync(kAll, w.cu, r);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = lane + 32 * k;
+      pv[r][k] = (wok[r] && j < wrows[r]) ? a.bt.parent[cu + j] : 0;
+    }
+  }
+  int badp_mask = 0;
+#pragma unroll
+  for (int r = 0; r < kSmallBatch; ++r) {
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = lane + 32 * k;
+      if (wok[r] && j < wrows[r]) bad |= (j == 0) ? (pv[r][k] != -1) : (pv[r][k] < 0 || pv[r][k] >= j);
+    }
+    if (__any_sync(kAll, bad)) badp_mask |= 1 << r;
+  }
+  // lane r: request r's rule checks, row tiles and pages
+  bool valid = false, tc = false;
+  int nrt = 0, nblk = 0;
+  if (lane < R) {
+    const bool badp = (badp_mask >> lane) & 1;
+    bool v = w.ok && !badp;
+    if (report && !w.ok) flag(a.dev_status, SV_DEV_BAD_WINDOW);
+    if (report && badp) flag(a.dev_status, SV_DEV_BAD_PARENT);
+    if (v && (ctx < 0 || (long)ctx + w.rows > (long)a.max_blocks * kBlockSize)) {
+      v = false;
+      if (report) flag(a.dev_status, SV_DEV_BAD_LENGTH);
+    }
+    const int nw = v ? max(0, w.e - w.b) : 0;
+    tc = a.L.ucap_tc > 0 && a.group * nw >= kTcMinRows;
+    nrt = tc ? (a.group * nw + kTcRows - 1) / kTcRows : (a.group * nw + kTileRows - 1) / kTileRows;
+    nblk = nw ? (ctx + w.e + kBlockSize - 1) / kBlockSize : 0;
+    valid = v && nw > 0;
+  }
+  unsigned long long W = (!tc) ? (unsigned long long)nrt * a.Hkv * nblk : 0ull;
+  unsigned long long Wtc = tc ? (unsigned long long)nrt * a.Hkv * nblk : 0ull;
+  int Rtc = tc ? nrt * a.Hkv : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    W += __shfl_xor_sync(kAll, W, o);
+    Wtc += __shfl_xor_sync(kAll, Wtc, o);
+    Rtc += __shfl_xor_sync(kAll, Rtc, o);
+  }
+  int Ptc = 0;
+  if (Wtc) {
+    const long avail = max(1L, 2L * a.L.nsm - Rtc);
+    Ptc = (int)min((unsigned long long)kTcMaxPages, (Wtc + avail - 1) / avail);
+    Ptc = max(Ptc, kTcMinPages);
+  }
+  const unsigned long long target = (unsigned long long)a.L.unit_target;
+  int P = (int)min((unsigned long long)kMaxPagesPerSplit, (W + target - 1) / target);
+  if (P < kSmallPagesPerSplit) P = kSmallPagesPerSplit;
+  const int Pi = tc ? Ptc : P;
+  const int nsplit = valid ? (nblk + Pi - 1) / Pi : 0;
+  const int units = nrt * a.Hkv * nsplit;
+  // exclusive prefix of the units within each list (lanes 0 .. R-1)
+  int x = tc ? 0 : units, xt = tc ? units : 0;
+#pragma unroll
+  for (int o = 1; o < kSmallBatch; o <<= 1) {
+    const int y = __shfl_up_sync(kAll, x, o), yt = __shfl_up_sync(kAll, xt, o);
+    if (lane >= o) { x += y; xt += yt; }
+  }
+  int U = __shfl_sync(kAll, x, R - 1), Utc = __shfl_sync(kAll, xt, R - 1);
+  if (U > a.L.ucap || Utc > a.L.ucap_tc) {  // cannot happen with the workspace's bounds
+    U = Utc = 0;
+    if (report && lane == 0) flag(a.dev_status, SV_DEV_BAD_LENGTH);
+  }
+  if (lane < R) {
+    sp.ubase[lane] = tc ? xt - units : x - units;
+    sp.nsplit[lane] = nsplit;
+    sp.nrt[lane] = nrt;
+    sp.tc[lane] = tc ? 1 : 0;
+    sp.b[lane] = w.b;
+    sp.e[lane] = w.e;
+    sp.ctx[lane] = ctx;
+    sp.nblk[lane] = nblk;
+    sp.cu[lane] = w.cu;
+    sp.rows[lane] = w.rows;
+  }
+  if (lane == 0) {
+    sp.U = U;
+    sp.P = P;
+    sp.Utc = Utc;
+    sp.Ptc = Ptc;
+  }
+}
+
+__global__ void __launch_bounds__(32) plan_small_kernel(Args a) {
+  griddep_entry();
+  __shared__ SmallPlan sp;
+  small_plan_warp(a, sp, true);
+  __syncwarp();
+  const int lane = threadIdx.x;
+  Header* hdr = reinterpret_cast<Header*>(a.ws + a.L.header);
+  WorkItem* work = reinterpret_cast<WorkItem*>(a.ws + a.L.work);
+  WorkItem* work_tc = reinterpret_cast<WorkItem*>(a.ws + a.L.work_tc);
+  for (int r = 0; r < a.bt.n_req; ++r) {
+    const int n = sp.nrt[r] * a.Hkv * sp.nsplit[r];
+    if (n == 0 || (sp.tc[r] ? sp.Utc : sp.U) == 0) continue;
+    WorkItem* list = sp.tc[r] ? work_tc : work;
+    for (int x = lane; x < n; x += 32) {
+      WorkItem it;
+      it.i = r;
+      it.local = x;
+      it.nsplit = sp.nsplit[r];
+      it.nblk = sp.nblk[r];
+      it.ctx = sp.ctx[r];
+      it.b = sp.b[r];
+      it.e = sp.e[r];
+      it.ubase = sp.ubase[r];
+      it.cu = sp.cu[r];
+      it.rows = sp.rows[r];
+      it.P = sp.tc[r] ? sp.Ptc : sp.P;
+      it.pad = 0;
+      list[sp.ubase[r] + x] = it;
+    }
+  }
+  if (lane == 0) {
+    hdr->U = sp.U;
+    hdr->P = sp.P;
+    hdr->Utc = sp.Utc;
+    hdr->Ptc = sp.Ptc;
+  }
+}
+
 // ---------------------------------------------------------------- attend --
 
 // The last CTA of a (request, row tile, KV head) group merges the (m, l, O)
@@ -442,35 +605,68 @@ __device__ __forceinline__ void merge_splits(const Args& a, const float* ml_all,
                                              int r1, int vr0, int row0, int g, int tid,
                                              int nthreads) {
   constexpr int kQuads = D / 4;
+  constexpr int kLoads = 8;  // splits' loads a lane issues before merging any
   const int group = a.group;
-  for (int x = tid; x < (r1 - r0) * kQuads; x += nthreads) {
-    const int vr = r0 + x / kQuads, c4 = x % kQuads;
-    // one online pass over the splits (running max, rescaled sums), eight
-    // splits' loads issued before any of them is merged
+  // SL adjacent lanes share one output quad, lane s of them merging splits
+  // s, s + SL, ...: with SL * kLoads >= nsplit every split of the quad is in
+  // flight at once; the SL partial states then merge by shuffles.  The trip
+  // count is the same for every thread (nthreads is a multiple of 32 and
+  // every thread of the block calls this), so whole warps shuffle.
+  int SL = 1;
+  while (SL < 32 && SL * kLoads < nsplit) SL <<= 1;
+  const int items = (r1 - r0) * kQuads * SL;
+  for (int x0 = 0; x0 < items; x0 += nthreads) {
+    const int x = x0 + tid;
+    const bool live = x < items;
+    const int sl = x % SL, q = x / SL;
+    const int vr = r0 + q / kQuads, c4 = q % kQuads;
+    // one online pass (running max, rescaled sums) over this lane's splits
     float Mx = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sp0 = 0; sp0 < nsplit; sp0 += 8) {
-      float2 ml2[8];
-      float4 o4[8];
+    if (live) {
+      for (int sp0 = sl; sp0 < nsplit; sp0 += kLoads * SL) {
+        float2 ml2[kLoads];
+        float4 o4[kLoads];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const size_t row = (size_t)(gidx + min(sp0 + k, nsplit - 1)) * TILE + vr;
-        ml2[k] = __ldcg(reinterpret_cast<const float2*>(ml_all + row * 2));
-        o4[k] = __ldcg(reinterpret_cast<const float4*>(op_all + row * D) + c4);
+        for (int k = 0; k < kLoads; ++k) {
+          const size_t row = (size_t)(gidx + min(sp0 + k * SL, nsplit - 1)) * TILE + vr;
+          ml2[k] = __ldcg(reinterpret_cast<const float2*>(ml_all + row * 2));
+          o4[k] = __ldcg(reinterpret_cast<const float4*>(op_all + row * D) + c4);
+        }
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k) {
+          const float nm = fmaxf(Mx, ml2[k].x);
+          if (sp0 + k * SL >= nsplit || nm == -INFINITY) continue;
+          const float s_old = exp2f(Mx - nm), s_new = exp2f(ml2[k].x - nm);
+          L = L * s_old + ml2[k].y * s_new;
+          acc.x = acc.x * s_old + o4[k].x * s_new;
+          acc.y = acc.y * s_old + o4[k].y * s_new;
+          acc.z = acc.z * s_old + o4[k].z * s_new;
+          acc.w = acc.w * s_old + o4[k].w * s_new;
+          Mx = nm;
+        }
       }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float nm = fmaxf(Mx, ml2[k].x);
-        if (sp0 + k >= nsplit || nm == -INFINITY) continue;
-        const float s_old = exp2f(Mx - nm), s_new = exp2f(ml2[k].x - nm);
-        L = L * s_old + ml2[k].y * s_new;
-        acc.x = acc.x * s_old + o4[k].x * s_new;
-        acc.y = acc.y * s_old + o4[k].y * s_new;
-        acc.z = acc.z * s_old + o4[k].z * s_new;
-        acc.w = acc.w * s_old + o4[k].w * s_new;
+    }
+    for (int o = SL >> 1; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, Mx, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, L, o);
+      float4 a2;
+      a2.x = __shfl_xor_sync(0xffffffffu, acc.x, o);
+      a2.y = __shfl_xor_sync(0xffffffffu, acc.y, o);
+      a2.z = __shfl_xor_sync(0xffffffffu, acc.z, o);
+      a2.w = __shfl_xor_sync(0xffffffffu, acc.w, o);
+      const float nm = fmaxf(Mx, m2);
+      if (nm != -INFINITY) {
+        const float s_old = exp2f(Mx - nm), s_new = exp2f(m2 - nm);
+        L = L * s_old + l2 * s_new;
+        acc.x = acc.x * s_old + a2.x * s_new;
+        acc.y = acc.y * s_old + a2.y * s_new;
+        acc.z = acc.z * s_old + a2.z * s_new;
+        acc.w = acc.w * s_old + a2.w * s_new;
         Mx = nm;
       }
     }
+    if (!live || sl != 0) continue;
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const int vgl = vr0 + vr;
     const int prow = row0 + vgl / group;
@@ -1406,7 +1602,10 @@ sv_status launch(const Args& a, cudaStream_t stream) {
   // one thread per request (its block-wide scans and barriers cost less with
   // fewer warps), at least four warps to write the work items, at most 1024
   const int plan_threads = min(1024, max(128, (a.bt.n_req + 31) / 32 * 32));
-  if (sv::launch(plan_kernel, 1, plan_threads, plan_smem, stream, a) != cudaSuccess)
+  // small one-pass calls: the one-warp planner
+  const bool warp_plan = a.L.small && a.chunk.index < 0;
+  if ((warp_plan ? sv::launch(plan_small_kernel, 1, 32, 0, stream, a)
+                 : sv::launch(plan_kernel, 1, plan_threads, plan_smem, stream, a)) != cudaSuccess)
     return SV_ERR_CUDA;
   // the tensor-core units first (the long ones when there are any), then the
   // mma.sync units, then one merge launch for every split group

@@ -305,6 +305,21 @@ __device__ __forceinline__ void griddep_entry() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
+// ---------------------------------------------------------------- tickets --
+// The warp that finishes its part of a shared job publishes its results and
+// takes a ticket with a release-acquire add at device scope: the writes it
+// made before are visible to whoever takes a later ticket, and the writes
+// published before earlier tickets are visible to it.  The taker's lanes then
+// order their reads after the ticket with __syncwarp() (lane 0 took it).
+__device__ __forceinline__ int ticket_add(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------ host side --
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 

@@ -39,13 +39,23 @@ class DeviceStep:
         f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
 
         self.batch = api.Batch(i32(w.cu_rows), i32(w.parent), i32(w.tokens), w.max_rows)
-        self.kv = api.PagedKV(bf16(w.k_cache), bf16(w.v_cache), i32(w.block_tables), i32(w.cache_lens))
-        self.pool = api.BlockPool(i32(w.free_list), i32(np.array([w.free_count])))
-        # pristine copies of the mutable cache state, restored before each step
-        self._tables0 = self.kv.block_tables.clone()
-        self._lens0 = self.kv.cache_lens.clone()
-        self._free0 = self.pool.free_list.clone()
-        self._fc0 = self.pool.free_count.clone()
+        # The mutable cache state (block tables, cache lengths, free list and
+        # count) lives in one buffer, each part on a 256-byte boundary, so that
+        # restoring it before a step is a single copy.
+        parts = [np.asarray(w.block_tables, dtype=np.int32), np.asarray(w.cache_lens, dtype=np.int32),
+                 np.asarray(w.free_list, dtype=np.int32), np.array([w.free_count], dtype=np.int32)]
+        offs, n = [], 0
+        for a in parts:
+            offs.append(n)
+            n += (a.size + 63) // 64 * 64
+        host = np.zeros(max(n, 64), dtype=np.int32)
+        for a, o in zip(parts, offs):
+            host[o:o + a.size] = a.ravel()
+        self._state = i32(host)
+        self._state0 = self._state.clone()  # pristine copy, restored before each step
+        view = lambda k: self._state[offs[k]:offs[k] + parts[k].size].view(parts[k].shape)
+        self.kv = api.PagedKV(bf16(w.k_cache), bf16(w.v_cache), view(0), view(1))
+        self.pool = api.BlockPool(view(2), view(3))
         self.q = bf16(w.q)
         self.target = f32(w.target_logits)
         self.draft = f32(w.draft_logits) if self.T > 0 else None
@@ -75,10 +85,7 @@ class DeviceStep:
 
     # ---------------------------------------------------------------------
     def restore_cache_state(self):
-        self.kv.block_tables.copy_(self._tables0)
-        self.kv.cache_lens.copy_(self._lens0)
-        self.pool.free_list.copy_(self._free0)
-        self.pool.free_count.copy_(self._fc0)
+        self._state.copy_(self._state0)
 
     def attend(self, batch=None):
         api.sv_tree_attend(self.kv, batch or self.batch, self.q, self.Hq, self.scale, self.out,
