@@ -1383,8 +1383,9 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
       uint32_t sv[kTok];
       tc5::tmem_ld_x64(tmem + lane_base + (uint32_t)(slot * kTok), sv);
       const int t0 = (blk0 + 4 * st) * kBlockSize;
-#pragma unroll
-      for (int j = 0; j < kTok; ++j) sv[j] = __float_as_uint(__uint_as_float(sv[j]) * a.scale_log2);
+      // S stays unscaled: its max scales after (the scale is positive) and the
+      // scale enters each exponent through one fma
+      const float sc = a.scale_log2;
       if (t0 + kTok > ctx || t0 + kTok > tok_end) {
         // Keys of this stage the row sees, as one 64-bit word: the context,
         // then the staged slots of its ancestors-or-self, none past tok_end.
@@ -1396,6 +1397,7 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
       float mx = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kTok; ++j) mx = fmaxf(mx, __uint_as_float(sv[j]));
+      mx *= sc;
       // a new reference max only when the row max passes it by 2^8
       const bool grow = mx > m_ref + 8.f;
       if (__any_sync(0xffffffffu, grow)) {
@@ -1422,15 +1424,17 @@ __global__ void __launch_bounds__(tcu::kThreads, 2)
         m_ref = m_new;
       }
       const float mb = m_ref == -INFINITY ? 0.f : m_ref;
-      float rs = 0.f;
+      float rs0 = 0.f, rs1 = 0.f;  // two running sums: half the dependent adds
       uint32_t pk[kTok / 2];
 #pragma unroll
       for (int j = 0; j < kTok; j += 2) {
-        const float p0 = ex2(__uint_as_float(sv[j]) - mb), p1 = ex2(__uint_as_float(sv[j + 1]) - mb);
-        rs += p0 + p1;
+        const float p0 = ex2(fmaf(__uint_as_float(sv[j]), sc, -mb));
+        const float p1 = ex2(fmaf(__uint_as_float(sv[j + 1]), sc, -mb));
+        rs0 += p0;
+        rs1 += p1;
         pk[j / 2] = pack_bf16(p0, p1);
       }
-      l += rs;
+      l += rs0 + rs1;
       // Slots past the last key may hold anything (unwritten cache slots, or
       // pages not loaded): zero their V rows so that P = 0 meets V = 0.
       const uint32_t sb = ring + slot * kSlotBytes;

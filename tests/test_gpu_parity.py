@@ -224,6 +224,10 @@ def test_commit_matches_oracle(name, T, kw):
     ("batch64", 0.7, dict(n_req=48, ctx_scale=0.02, vocab=2048, draft_sigma=0.5)),
     ("batch64", 0.0, dict(n_req=48, ctx_scale=0.02, vocab=2048, draft_sigma=0.1)),
     ("tree70b", 0.0, dict(ctx_scale=0.01, vocab=512, draft_sigma=0.05)),
+    # several trees: one CTA per request shares the merge and the K/V moves
+    # (up to eight requests), and the per-warp decision beyond that
+    ("tree70b", 0.0, dict(n_req=5, ctx_scale=0.01, vocab=512, draft_sigma=0.05)),
+    ("tree70b", 0.0, dict(n_req=11, ctx_scale=0.01, vocab=512, draft_sigma=0.05)),
     ("tree70b", 1.0, dict(n_req=3, ctx_scale=0.01, vocab=2048, draft_sigma=0.3)),
     ("batch256", 1.0, dict(n_req=200, ctx_scale=0.01, vocab=1024)),
 ])
