@@ -815,8 +815,9 @@ __device__ __forceinline__ int commit_check(const Args& a, int rows, int ctx, in
 // decided for the request, which is only counted.  The lanes look up the
 // moves of 32 path positions at once (chains move nothing); the moves
 // themselves run in ascending k, every lane copying part of the slot.
+// pairs: two moves at a time (more registers; the decision kernel has them).
 __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
-                                               const CommitHint* hint) {
+                                               const CommitHint* hint, bool pairs = false) {
   const int lane = threadIdx.x & 31;
   const CommitArgs& c = a.kv;
   // A call with one request needs no ticket: its warp releases at once (the
@@ -876,34 +877,42 @@ __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
           }
         }
         // A slot written at step k is never the source of a later step
-        // (path[k'] >= k' > k), so ascending k reads every source first.
+        // (path[k'] >= k' > k), so ascending k reads every source first.  Two
+        // moves go at once (both sources read, then both destinations
+        // written): the second move's destination can only be the first's
+        // source, which is read before it is written.
         unsigned m = __ballot_sync(0xffffffffu, mv);
+        auto slot_int4 = [&](unsigned long long row, int x) {
+          const int tensor = x / (c.Hkv * cpr), rem = x % (c.Hkv * cpr);
+          const int g = rem / cpr, q = rem % cpr;
+          return reinterpret_cast<int4*>((tensor ? c.v : c.k) + (row + (size_t)g * kBlockSize) * c.D) + q;
+        };
         while (m) {
           const int j = __ffs(m) - 1;
           m &= m - 1;
+          const int j2 = (pairs && m && per_slot <= 32 * 8) ? __ffs(m) - 1 : -1;
+          if (j2 >= 0) m &= m - 1;
           const unsigned long long sr = __shfl_sync(0xffffffffu, srow, j);
           const unsigned long long dr = __shfl_sync(0xffffffffu, drow, j);
-          // eight 16-byte loads of the slot in flight per lane, then their stores
+          const unsigned long long sr2 = __shfl_sync(0xffffffffu, srow, j2 >= 0 ? j2 : j);
+          const unsigned long long dr2 = __shfl_sync(0xffffffffu, drow, j2 >= 0 ? j2 : j);
+          // eight 16-byte loads of each slot in flight per lane, then the stores
           for (int x0 = 0; x0 < per_slot; x0 += 32 * 8) {
-            int4 val[8];
+            int4 val[8], val2[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
               const int x = x0 + 32 * t + lane;
               if (x < per_slot) {
-                const int tensor = x / (c.Hkv * cpr), rem = x % (c.Hkv * cpr);
-                const int g = rem / cpr, q = rem % cpr;
-                const __nv_bfloat16* base = tensor ? c.v : c.k;
-                val[t] = reinterpret_cast<const int4*>(base + (sr + (size_t)g * kBlockSize) * c.D)[q];
+                val[t] = *slot_int4(sr, x);
+                if (j2 >= 0) val2[t] = *slot_int4(sr2, x);
               }
             }
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
               const int x = x0 + 32 * t + lane;
               if (x < per_slot) {
-                const int tensor = x / (c.Hkv * cpr), rem = x % (c.Hkv * cpr);
-                const int g = rem / cpr, q = rem % cpr;
-                __nv_bfloat16* base = tensor ? c.v : c.k;
-                reinterpret_cast<int4*>(base + (dr + (size_t)g * kBlockSize) * c.D)[q] = val[t];
+                *slot_int4(dr, x) = val[t];
+                if (j2 >= 0) *slot_int4(dr2, x) = val2[t];
               }
             }
           }
@@ -1026,7 +1035,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32, 1) decide_kernel(Args a) {
           now = a.done[i] != 0;
         }
       }
-      if (now) commit_request(a, i, outcome == kFinal, outcome == kFinal ? &hint : nullptr);
+      if (now) commit_request(a, i, outcome == kFinal, outcome == kFinal ? &hint : nullptr, true);
     }
   }
 }

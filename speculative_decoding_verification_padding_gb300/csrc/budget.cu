@@ -143,12 +143,25 @@ __global__ void __launch_bounds__(kThreads) budget_kernel(Args a) {
     __syncthreads();
     for (int e = tid; e < n; e += kThreads) atomicAdd(&hist[(kin[e] >> shift) & 255u], 1);
     __syncthreads();
-    if (tid == 0) {
-      int run = 0;
-      for (int d = 0; d < 256; ++d) {
-        const int t = hist[d];
-        hist[d] = run;
-        run += t;
+    if (warp == 0) {
+      // exclusive scan of the 256 digit counts: eight per lane, then the warp
+      int v[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[j] = hist[lane * 8 + j];
+        sum += v[j];
+      }
+      int x = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      int run = x - sum;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        hist[lane * 8 + j] = run;
+        run += v[j];
       }
     }
     __syncthreads();
@@ -192,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) budget_kernel(Args a) {
   unsigned long long local = 0ull;
   for (int e = e0; e < e1; ++e) {
     const float S = __uint_as_float(~kin[e]);
-    local += (unsigned long long)((double)S * 1099511627776.0);  // trunc(S * 2^40)
+    local += __float2ull_rz(S * 0x1p40f);  // trunc(S * 2^40): the product is exact in fp32
   }
   unsigned long long x = local;
 #pragma unroll
@@ -222,7 +235,7 @@ __global__ void __launch_bounds__(kThreads) budget_kernel(Args a) {
   }
   for (int e = e0; e < e1; ++e) {
     const float S = __uint_as_float(~kin[e]);
-    run += (unsigned long long)((double)S * 1099511627776.0);
+    run += __float2ull_rz(S * 0x1p40f);
     const int m = e + 1;
     if (m > m_hi) break;
     const double th = (double)(tau0 + run) * 0x1p-40 * (double)a.sps[R + m];
