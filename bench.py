@@ -614,7 +614,7 @@ def main():
     # rows make a dense tile that the KV bytes cannot keep busy (the tree
     # workload, about 175 flops per byte), HBM elsewhere.
     att_flops = sum(attend_flops(w, ch) for ch in sched)
-    kernel_name = "sv_tree_attend (plan + TMA split-KV attention with fused merge)"
+    kernel_name = "sv_tree_attend (planner, split-KV attention kernels, split merge)"
     if w.cfg.gamma and w.cfg.gamma[0] == "tree":
         tf_peak, tf_src = bf16_peak_tflops()
         achieved = att_flops / t_att / 1e12
@@ -682,7 +682,7 @@ def main():
 
 
 # Revision tag of the attention kernel the stored ncu traffic belongs to.
-KERNEL_REV = "attend-tma-v4"
+KERNEL_REV = "attend-tma-v5"
 
 if __name__ == "__main__":
     main()
