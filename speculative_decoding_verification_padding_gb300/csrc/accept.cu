@@ -29,10 +29,11 @@
 //                    among groups of four entries, then the entry inside the
 //                    winning group; each warp streams its slice of target
 //                    logits through a shared-memory ring (bulk copies) and
-//                    prunes groups that cannot win; the warp that brings a
-//                    request's last slice (atomic ticket) reduces the slice
-//                    winners and picks the entry.  A chunked step runs it
-//                    once, after its last chunk.
+//                    prunes groups that cannot win, and draws the entry
+//                    inside its own best group; the warp that brings a
+//                    request's last slice (release-acquire ticket) reduces
+//                    the slice winners and writes the winner's entry.  A
+//                    chunked step runs it once, after its last chunk.
 
 #include <math.h>
 
@@ -679,7 +680,7 @@ __global__ void __launch_bounds__(kStatThreads, 4) stats_kernel(Args a) {
     if (T > 0.f) {
       // x = logit / T; exp(x - m) as 2^((x - m) log2 e).  These only build
       // the normaliser: the decision recomputes its own x with an exact
-      // division and exp in fp64.
+      // division and its ratio from an exactly formed exponent.
       if (VEC) {
         // kDepth 128-entry groups per round: all loads first (entries past
         // the slice read as -inf), then one max and at most one rescale.

@@ -6,16 +6,22 @@
 // draft tokens of a request); [FASER] operations notes (the attention kernel
 // must accept a chunk of the rows); [SSD] section details (PagedAttention).
 //
-// Two kernels on one stream:
-//   plan   (1 CTA)   validates parents / windows / lengths (one warp per
-//                    request) and builds a length-weighted split-KV work list:
-//                    the keys of each (request, KV head, 64-row query tile)
-//                    are cut into splits of P pages so that about kUnitTarget
-//                    units exist (P at least 32 pages, 64 when the work still
-//                    fills every SM); every unit gets a self-contained 48-byte
-//                    work item; clears the per-group merge tickets.  An empty
-//                    call (no keys anywhere) only publishes a zero count.
-//   attend (1 CTA per unit, 4 warps, 2 CTAs per SM)
+// Launches, on one stream:
+//   plan   (1 CTA, one thread per request; one warp for one-pass calls of
+//                    at most four requests) validates parents / windows /
+//                    lengths and builds length-weighted split-KV work lists:
+//                    the keys of each (request, KV head, query tile) are cut
+//                    into splits of P pages so that about kUnitsPerSM units
+//                    per SM exist (P at least 32 pages, 64 when the work still
+//                    fills every SM; small batches aim for one wave and go
+//                    down to 8 pages); every unit gets a self-contained 48-byte
+//                    work item; clears the per-group merge tickets.  Requests
+//                    with at least 128 virtual rows per KV head go to the
+//                    tcgen05 list, the others to the mma.sync list.  An empty
+//                    call (no keys anywhere) only publishes zero counts.
+//   attend_tc (the tcgen05 list, when a request can reach 128 virtual rows;
+//                    described with its kernel below).
+//   attend (mma.sync list; 1 CTA per unit, 4 warps, 2 CTAs per SM)
 //                    the query rows of the whole GQA group (row x head packed
 //                    as "virtual rows") share every KV page.  Pages stream
 //                    through a 3-stage ring of 64-token stages: lane 0 of
@@ -24,18 +30,21 @@
 //                    16-row box per half page) that complete on an mbarrier
 //                    per slot (thread 0 arms it with the stage's bytes); the
 //                    warps wait on it with a bounded spin, and one block
-//                    barrier per stage frees the slot.  A warp owns a 16-row m-tile and a
-//                    slice of each stage's tokens: with one m-tile the four
-//                    warps take 16 tokens each, with two they take 32, with
-//                    three or four every warp sees the whole stage.  QK^T and
-//                    PV run on mma.sync m16n8k16 bf16 -> fp32 with an online
-//                    softmax in the log2 domain; the ancestor mask (built per
-//                    CTA from the parent links held in shared memory) is
-//                    applied only where staged draft slots lie.  Warps that
-//                    shared an m-tile merge through shared memory.  A unit
-//                    that covers all keys of its rows writes bf16 output
-//                    directly; otherwise it writes (m, l, O) partials and the
-//                    last CTA of the group (atomic ticket) merges all splits.
+//                    barrier per stage frees the slot.  A warp owns a 16-row
+//                    m-tile and a slice of each stage's tokens: with one m-tile
+//                    the four warps take 16 tokens each, with two they take
+//                    32, with three or four every warp sees the whole stage.
+//                    QK^T and PV run on mma.sync m16n8k16 bf16 -> fp32 with an
+//                    online softmax in the log2 domain; the ancestor mask
+//                    (built per CTA from the parent links held in shared
+//                    memory) is applied only where staged draft slots lie.
+//                    Warps that shared an m-tile merge through shared memory.
+//                    A unit that covers all keys of its rows writes bf16
+//                    output directly; otherwise it writes (m, l, O) partials
+//                    and the last CTA of the group (atomic ticket) merges all
+//                    splits -- or, in small batches, the merge launch does.
+//   merge (when the tcgen05 kernel ran or the batch is small) the units of
+//                    each split group merge its partials together.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
