@@ -607,14 +607,14 @@ __global__ void __launch_bounds__(32) plan_small_kernel(Args a) {
 // partials of all the group's splits -- m in the log2 domain, O unnormalised
 // -- in one online pass per (virtual row, 4 columns) and writes bf16 rows.
 // ml_all / op_all: partials of TILE rows per unit; gidx: the group's split-0
-// unit; row0: packed row of the window's first row.
-template <int D, int TILE>
+// unit; row0: packed row of the window's first row; kLoads: the splits' loads
+// a lane issues before merging any.
+template <int D, int TILE, int kLoads = 8>
 __device__ __forceinline__ void merge_splits(const Args& a, const float* ml_all,
                                              const float* op_all, int gidx, int nsplit, int r0,
                                              int r1, int vr0, int row0, int g, int tid,
                                              int nthreads) {
   constexpr int kQuads = D / 4;
-  constexpr int kLoads = 8;  // splits' loads a lane issues before merging any
   const int group = a.group;
   // SL adjacent lanes share one output quad, lane s of them merging splits
   // s, s + SL, ...: with SL * kLoads >= nsplit every split of the quad is in
@@ -1107,7 +1107,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  merge_splits<D, kTileRows>(a, ml_all, op_all, gidx, ri.nsplit, 0, Mu, vr0, cu + ri.b, g, tid,
+  // the group's last CTA merges alone: sixteen splits' loads in flight per
+  // lane halve its rounds (the main loop's registers are free by now)
+  merge_splits<D, kTileRows, 16>(a, ml_all, op_all, gidx, ri.nsplit, 0, Mu, vr0, cu + ri.b, g, tid,
                              kThreads);
 }
 
