@@ -6,7 +6,8 @@ contexts log-normal (ln 4096, 1) clipped to [512, 32768], paged bf16 KV
 (16-token blocks, shuffled tables), vocab 128256 fp32 logits, sampling at
 T = 0.7, chunked verification in chunks of 2 with early pruning, each
 request's KV committed in the chunk that stops it.  Other workloads: tiny,
-chain8b, tree70b (one pass), batch256 (budget-selected).
+chain8b, tree70b (one pass; tree70b_t1 the same tree sampled at T = 1),
+batch256 (budget-selected).
 
 One step = restore the block tables / lengths / free list the previous
 step's commit changed, then the workload's calls:
@@ -21,7 +22,7 @@ Inputs larger than L2 are timed back to back; smaller ones step by step with
 an L2 flush (a 512 MB write) between steps, outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload batch64|tiny|chain8b|tree70b|batch256]
+                  [--workload batch64|tiny|chain8b|tree70b|tree70b_t1|batch256]
 
 For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of
 the step (the path has no exchange step); the line reports the sum over
@@ -66,7 +67,18 @@ WORKLOAD_TEXT = {
     "batch256": ("batch256: 256 requests, 40 q / 8 kv heads, d 128, context U{1024..8192}, 4 drafts, "
                  "vocab 151936, survival c ~ Beta(4,2), budget by argmax tau*SPS(B) with "
                  "SPS(B)=1000/(1+B/512), then attention + T=1 accept + commit on the selected prefixes"),
+    "tree70b_t1": ("tree70b_t1: the tree70b step with T=1 tree sampling (siblings drawn from q, "
+                   "children tried in index order against the parent's residual), KV commit of "
+                   "the accepted path"),
 }
+
+# Workloads that are a configuration with one setting changed.
+VARIANTS = {"tree70b_t1": ("tree70b", {"temperature": 1.0})}
+
+
+def make_named_workload(wl, name, **kw):
+    base, over = VARIANTS.get(name, (name, {}))
+    return wl.make_workload(wl.config(base), **over, **kw)
 
 
 # ----------------------------------------------------------------- clocks --
@@ -298,7 +310,7 @@ def run_reference(args, rank):
     from speculative_decoding_verification_padding_gb300 import workloads as wl
     import oracle
     oracle.build()
-    w = wl.make_workload(wl.config(args.workload))
+    w = make_named_workload(wl, args.workload)
     mode = mode_of(w.cfg)
     threads = os.cpu_count() or 1
     dt1, _ = time_oracle(w, mode, [0], threads)
@@ -367,7 +379,7 @@ def main():
     dev = f"cuda:{local_rank}"
     reps = Replicas.from_env("nccl", device=dev)
 
-    w = wl.make_workload(wl.config(args.workload),
+    w = make_named_workload(wl, args.workload,
                          ctx_scale=args.ctx_scale if args.profile_steps else 1.0, sps=args.sps)
     s = DeviceStep(w, device=dev)
     mode, chunk, T = s.mode, s.chunk, s.T
