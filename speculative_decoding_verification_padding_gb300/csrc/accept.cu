@@ -277,21 +277,26 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 // cost microseconds per decision.  q that would vanish in double (q below
 // the smallest denormal) gives ratio 1, as the definition's q > 0 test does.
 // p and q themselves (row statistics output) are formed in fp32.
+// p / q itself (unclamped), by the same exact exponent: +inf stands for a q
+// that vanishes in double, 0 for p = 0.
+__device__ __forceinline__ float pq_ratio(float xp, float xq, float mp, float lp, float mq,
+                                          float lq) {
+  float s1, e1, s2, e2, h, l;
+  two_sum(xq, -mq, s2, e2);
+  if (s2 - logf(lq) < -745.13f) return INFINITY;  // also xq = -inf
+  two_sum(xp, -mp, s1, e1);
+  if (s1 == -INFINITY) return 0.f;                // p = 0
+  two_sum(s1, -s2, h, l);
+  l = __fadd_rn(l, __fsub_rn(e1, e2));
+  return __fdiv_rn(__fmul_rn(expf(h) * (1.f + l), lq), lp);
+}
 __device__ __forceinline__ float accept_ratio(float xp, float xq, float mp, float lp, float mq,
                                               float lq, float* p_out, float* q_out) {
   if (p_out) {
     *p_out = __fdiv_rn(expf(__fsub_rn(xp, mp)), lp);
     *q_out = __fdiv_rn(expf(__fsub_rn(xq, mq)), lq);
   }
-  float s1, e1, s2, e2, h, l;
-  two_sum(xq, -mq, s2, e2);
-  if (s2 - logf(lq) < -745.13f) return 1.f;  // also xq = -inf
-  two_sum(xp, -mp, s1, e1);
-  if (s1 == -INFINITY) return 0.f;          // p = 0
-  two_sum(s1, -s2, h, l);
-  l = __fadd_rn(l, __fsub_rn(e1, e2));
-  const float r = __fdiv_rn(__fmul_rn(expf(h) * (1.f + l), lq), lp);
-  return fminf(1.f, r);
+  return fminf(1.f, pq_ratio(xp, xq, mp, lp, mq, lq));
 }
 
 // The decision for request i, by one warp, once all its row partials exist.
@@ -1072,6 +1077,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
   const int nch = stats_slices(a.L, n_slots(a, act), 2, a.use_list != 0, a.bt.total_rows);
   const float T = a.T, rT = 1.f / T;
   const int V = a.V;
+  const bool vec =
+      (V & 3) == 0 && ((((uintptr_t)a.target) | ((uintptr_t)a.draft)) & 15) == 0;
   const int cu = a.bt.cu_rows[i];
   const int rows = a.bt.cu_rows[i + 1] - cu;  // checked by the decision kernel
   int32_t* nodes = a.accepted_nodes + (size_t)i * a.bt.max_rows_per_req;
@@ -1100,16 +1107,20 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
     }
     const float* lp = a.target + (size_t)(cu + n) * V;
     const float* lq = a.draft + (size_t)(cu + n) * V;
-    double c = 0.0, S = 1.0;
+    double c = 0.0, S = 1.0, inv_S = 1.0;
     bool moved = false, vanished = false;
     for (int t = 0; t < nk; ++t) {
       const int ch = s_kids[t];
       if (tid == 0) {
         const int x = a.bt.tokens[cu + ch];
-        const double p = exp((double)(lp[x] / T) - (double)s_st[0]) / (double)s_st[1];
-        const double q = exp((double)(lq[x] / T) - (double)s_st[2]) / (double)s_st[3];
-        const double pres = fmax(0.0, p - c * q) / S;
-        const double ratio = q > 0.0 ? fmin(1.0, pres / q) : 1.0;
+        // pres / q = max(0, p - c q) / (S q) = max(0, p/q - c) / S, with p/q
+        // from the exact exponent in fp32 (as on chains; fp64 runs at a
+        // small fraction of the fp32 rate on this GPU) and 1 / S taken once
+        // per pass.  q that vanishes gives ratio 1, as the definition's
+        // q > 0 test does; p = 0 gives 0.
+        const float r_pq = pq_ratio(lp[x] / T, lq[x] / T, s_st[0], s_st[1], s_st[2], s_st[3]);
+        const double ratio =
+            r_pq == INFINITY ? 1.0 : fmin(1.0, fmax(0.0, (double)r_pq - c) * inv_S);
         const double u = (double)accept_u(a.seed, i, ch);
         if (fabs(u - ratio) < 1e-6) amb = true;
         s_dec = u < ratio ? 1 : 0;
@@ -1129,13 +1140,39 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
       const float mpb = s_st[0] * kLog2e, mqb = s_st[2] * kLog2e;
       const float inv_lp = 1.f / s_st[1], cq = (float)c / s_st[3];
       float sum = 0.f, comp = 0.f;
-      for (int v = tid; v < V; v += kTreeThreads) {
-        const float pv = ex2(fmaf(div_by(lp[v], T, rT), kLog2e, -mpb)) * inv_lp;
-        const float qv = ex2(fmaf(div_by(lq[v], T, rT), kLog2e, -mqb)) * cq;
+      auto add = [&](float xp, float xq) {  // Kahan step of max(0, p_v - c q_v)
+        const float pv = ex2(fmaf(div_by(xp, T, rT), kLog2e, -mpb)) * inv_lp;
+        const float qv = ex2(fmaf(div_by(xq, T, rT), kLog2e, -mqb)) * cq;
         const float y = fmaxf(pv - qv, 0.f) - comp;
         const float tsum = sum + y;
         comp = (tsum - sum) - y;
         sum = tsum;
+      };
+      if (vec) {
+        // 128-bit loads, four of each row in flight per thread (entries past
+        // the row read as -inf logits: p = 0 adds nothing)
+        const float4* p4 = reinterpret_cast<const float4*>(lp);
+        const float4* q4 = reinterpret_cast<const float4*>(lq);
+        const int n4 = V >> 2;
+        const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int v0 = tid; v0 < n4; v0 += 4 * kTreeThreads) {
+          float4 xp[4], xq[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int v = v0 + k * kTreeThreads;
+            xp[k] = v < n4 ? __ldg(p4 + v) : none;
+            xq[k] = v < n4 ? __ldg(q4 + v) : none;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            add(xp[k].x, xq[k].x);
+            add(xp[k].y, xq[k].y);
+            add(xp[k].z, xq[k].z);
+            add(xp[k].w, xq[k].w);
+          }
+        }
+      } else {
+        for (int v = tid; v < V; v += kTreeThreads) add(lp[v], lq[v]);
       }
       double d = (double)sum - (double)comp;
 #pragma unroll
@@ -1154,6 +1191,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
         vanished = true;
         break;
       }
+      inv_S = 1.0 / S;
     }
     if (moved) continue;
     out.mode = vanished ? 2 : 1;
