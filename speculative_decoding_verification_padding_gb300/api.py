@@ -39,6 +39,44 @@ def _stream(stream) -> int:
     return int(stream)
 
 
+# The current stream's handle for a device index, without building a Stream
+# object (a few microseconds less per call on the launch path).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _current_stream(device_index: int) -> int:
+    if _raw_stream is not None:
+        return _raw_stream(device_index)
+    return torch.cuda.current_stream(device_index).cuda_stream
+
+
+def _call(name: str, args: tuple, stream):
+    N.check(getattr(N.lib(), name)(*args, _stream(stream)), name)
+
+
+class BoundCall:
+    """One library call with its arguments marshalled once: the dtypes
+    checked, the structs built and the device pointers taken.  Calling it
+    enqueues the call on the current stream of the bound tensors' device (or
+    on `stream`).  The tensors it was bound to must stay allocated, and the
+    Batch / PagedKV / BlockPool objects must keep the same tensors: the
+    call reads their pointers as they were when it was bound."""
+
+    __slots__ = ("_f", "_name", "_args", "_dev")
+
+    def __init__(self, name: str, args: tuple, device: torch.device):
+        self._f = getattr(N.lib(), name)
+        self._name = name
+        self._args = args  # ctypes byref objects keep their structs alive
+        self._dev = device.index if device.index is not None else torch.cuda.current_device()
+
+    def __call__(self, stream=None):
+        st = _current_stream(self._dev) if stream is None else _stream(stream)
+        status = self._f(*self._args, st)
+        if status != N.SV_OK:
+            N.check(status, self._name)
+
+
 @dataclass
 class Batch:
     """sv_batch: packed draft chains / trees (int32 device tensors)."""
@@ -109,15 +147,28 @@ def sv_tree_attend_workspace(batch: Batch, kv: PagedKV, n_q_heads: int) -> int:
     return N.lib().sv_tree_attend_workspace(ctypes.byref(b), ctypes.byref(k), n_q_heads)
 
 
-def sv_tree_attend(kv: PagedKV, batch: Batch, q: torch.Tensor, n_q_heads: int,
-                   softmax_scale: float, out: torch.Tensor, ws: torch.Tensor,
-                   dev_status: Optional[torch.Tensor] = None, stream=None):
+def _tree_attend_args(kv, batch, q, n_q_heads, softmax_scale, out, ws, dev_status):
     _expect(q, torch.bfloat16, "q")
     _expect(out, torch.bfloat16, "out")
     b, k = batch.c(), kv.c()
-    N.check(N.lib().sv_tree_attend(ctypes.byref(k), ctypes.byref(b), _ptr(q), n_q_heads,
-                                   softmax_scale, _ptr(out), _ptr(ws), ws.numel(),
-                                   _ptr(dev_status), _stream(stream)), "sv_tree_attend")
+    return (ctypes.byref(k), ctypes.byref(b), _ptr(q), n_q_heads, softmax_scale, _ptr(out),
+            _ptr(ws), ws.numel(), _ptr(dev_status))
+
+
+def sv_tree_attend(kv: PagedKV, batch: Batch, q: torch.Tensor, n_q_heads: int,
+                   softmax_scale: float, out: torch.Tensor, ws: torch.Tensor,
+                   dev_status: Optional[torch.Tensor] = None, stream=None):
+    _call("sv_tree_attend",
+          _tree_attend_args(kv, batch, q, n_q_heads, softmax_scale, out, ws, dev_status), stream)
+
+
+def bind_tree_attend(kv: PagedKV, batch: Batch, q: torch.Tensor, n_q_heads: int,
+                     softmax_scale: float, out: torch.Tensor, ws: torch.Tensor,
+                     dev_status: Optional[torch.Tensor] = None) -> BoundCall:
+    """sv_tree_attend with its arguments marshalled once (see BoundCall)."""
+    return BoundCall("sv_tree_attend",
+                     _tree_attend_args(kv, batch, q, n_q_heads, softmax_scale, out, ws,
+                                       dev_status), q.device)
 
 
 def sv_accept_workspace(batch: Batch, vocab: int) -> int:
@@ -130,16 +181,36 @@ def sv_accept(batch: Batch, target_logits: torch.Tensor, draft_logits: Optional[
               accepted_nodes: torch.Tensor, next_token: torch.Tensor, ambiguous: torch.Tensor,
               done: Optional[torch.Tensor], row_stats: Optional[torch.Tensor], ws: torch.Tensor,
               dev_status: Optional[torch.Tensor] = None, stream=None):
+    _call("sv_accept",
+          _accept_args(batch, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
+                       accepted_nodes, next_token, ambiguous, done, row_stats, ws, dev_status),
+          stream)
+
+
+def _accept_args(batch, target_logits, draft_logits, vocab, temperature, seed, accepted_len,
+                 accepted_nodes, next_token, ambiguous, done, row_stats, ws, dev_status):
     _expect(target_logits, torch.float32, "target_logits")
     _expect(draft_logits, torch.float32, "draft_logits")
     _expect(ambiguous, torch.uint8, "ambiguous")
     _expect(row_stats, torch.float32, "row_stats")
     b = batch.c()
-    N.check(N.lib().sv_accept(ctypes.byref(b), _ptr(target_logits), _ptr(draft_logits), vocab,
-                              temperature, seed & 0xFFFFFFFFFFFFFFFF, _ptr(accepted_len),
-                              _ptr(accepted_nodes), _ptr(next_token), _ptr(ambiguous), _ptr(done),
-                              _ptr(row_stats), _ptr(ws), ws.numel(), _ptr(dev_status),
-                              _stream(stream)), "sv_accept")
+    return (ctypes.byref(b), _ptr(target_logits), _ptr(draft_logits), vocab, temperature,
+            seed & 0xFFFFFFFFFFFFFFFF, _ptr(accepted_len), _ptr(accepted_nodes),
+            _ptr(next_token), _ptr(ambiguous), _ptr(done), _ptr(row_stats), _ptr(ws), ws.numel(),
+            _ptr(dev_status))
+
+
+def bind_accept(batch: Batch, target_logits: torch.Tensor,
+                draft_logits: Optional[torch.Tensor], vocab: int, temperature: float, seed: int,
+                accepted_len: torch.Tensor, accepted_nodes: torch.Tensor,
+                next_token: torch.Tensor, ambiguous: torch.Tensor, done: Optional[torch.Tensor],
+                row_stats: Optional[torch.Tensor], ws: torch.Tensor,
+                dev_status: Optional[torch.Tensor] = None) -> BoundCall:
+    """sv_accept with its arguments marshalled once (see BoundCall)."""
+    return BoundCall("sv_accept",
+                     _accept_args(batch, target_logits, draft_logits, vocab, temperature, seed,
+                                  accepted_len, accepted_nodes, next_token, ambiguous, done,
+                                  row_stats, ws, dev_status), target_logits.device)
 
 
 def sv_accept_static(batch: Batch, target_logits: torch.Tensor,
@@ -184,17 +255,39 @@ def sv_accept_commit(batch: Batch, target_logits: torch.Tensor,
                      done: Optional[torch.Tensor], row_stats: Optional[torch.Tensor],
                      kv: PagedKV, pool: BlockPool, ws: torch.Tensor,
                      dev_status: Optional[torch.Tensor] = None, stream=None):
+    _call("sv_accept_commit",
+          _accept_commit_args(batch, target_logits, draft_logits, vocab, temperature, seed,
+                              accepted_len, accepted_nodes, next_token, ambiguous, done,
+                              row_stats, kv, pool, ws, dev_status), stream)
+
+
+def _accept_commit_args(batch, target_logits, draft_logits, vocab, temperature, seed,
+                        accepted_len, accepted_nodes, next_token, ambiguous, done, row_stats, kv,
+                        pool, ws, dev_status):
     _expect(target_logits, torch.float32, "target_logits")
     _expect(draft_logits, torch.float32, "draft_logits")
     _expect(ambiguous, torch.uint8, "ambiguous")
     _expect(row_stats, torch.float32, "row_stats")
     b, k, p = batch.c(), kv.c(), pool.c()
-    N.check(N.lib().sv_accept_commit(ctypes.byref(b), _ptr(target_logits), _ptr(draft_logits),
-                                     vocab, temperature, seed & 0xFFFFFFFFFFFFFFFF,
-                                     _ptr(accepted_len), _ptr(accepted_nodes), _ptr(next_token),
-                                     _ptr(ambiguous), _ptr(done), _ptr(row_stats),
-                                     ctypes.byref(k), ctypes.byref(p), _ptr(ws), ws.numel(),
-                                     _ptr(dev_status), _stream(stream)), "sv_accept_commit")
+    return (ctypes.byref(b), _ptr(target_logits), _ptr(draft_logits), vocab, temperature,
+            seed & 0xFFFFFFFFFFFFFFFF, _ptr(accepted_len), _ptr(accepted_nodes),
+            _ptr(next_token), _ptr(ambiguous), _ptr(done), _ptr(row_stats), ctypes.byref(k),
+            ctypes.byref(p), _ptr(ws), ws.numel(), _ptr(dev_status))
+
+
+def bind_accept_commit(batch: Batch, target_logits: torch.Tensor,
+                       draft_logits: Optional[torch.Tensor], vocab: int, temperature: float,
+                       seed: int, accepted_len: torch.Tensor, accepted_nodes: torch.Tensor,
+                       next_token: torch.Tensor, ambiguous: torch.Tensor,
+                       done: Optional[torch.Tensor], row_stats: Optional[torch.Tensor],
+                       kv: PagedKV, pool: BlockPool, ws: torch.Tensor,
+                       dev_status: Optional[torch.Tensor] = None) -> BoundCall:
+    """sv_accept_commit with its arguments marshalled once (see BoundCall)."""
+    return BoundCall("sv_accept_commit",
+                     _accept_commit_args(batch, target_logits, draft_logits, vocab, temperature,
+                                         seed, accepted_len, accepted_nodes, next_token,
+                                         ambiguous, done, row_stats, kv, pool, ws, dev_status),
+                     target_logits.device)
 
 
 def sv_select_budget_workspace(n_req: int, gamma_max: int) -> int:
@@ -209,10 +302,25 @@ def sv_select_budget(cond_survival: torch.Tensor, gamma: Optional[torch.Tensor],
     _expect(sps, torch.float32, "sps")
     _expect(best_theta, torch.float64, "best_theta")
     R, gmax = cond_survival.shape
-    N.check(N.lib().sv_select_budget(R, gmax, _ptr(cond_survival), _ptr(gamma), _ptr(sps),
-                                     sps.shape[0] - 1, _ptr(verify_len), _ptr(best_B),
-                                     _ptr(best_theta), _ptr(ws), 0 if ws is None else ws.numel(),
-                                     _ptr(dev_status), _stream(stream)), "sv_select_budget")
+    _call("sv_select_budget",
+          (R, gmax, _ptr(cond_survival), _ptr(gamma), _ptr(sps), sps.shape[0] - 1,
+           _ptr(verify_len), _ptr(best_B), _ptr(best_theta), _ptr(ws),
+           0 if ws is None else ws.numel(), _ptr(dev_status)), stream)
+
+
+def bind_select_budget(cond_survival: torch.Tensor, gamma: Optional[torch.Tensor],
+                       sps: torch.Tensor, verify_len: torch.Tensor, best_B: torch.Tensor,
+                       best_theta: torch.Tensor, ws: Optional[torch.Tensor] = None,
+                       dev_status: Optional[torch.Tensor] = None) -> BoundCall:
+    """sv_select_budget with its arguments marshalled once (see BoundCall)."""
+    _expect(cond_survival, torch.float32, "cond_survival")
+    _expect(sps, torch.float32, "sps")
+    _expect(best_theta, torch.float64, "best_theta")
+    R, gmax = cond_survival.shape
+    return BoundCall("sv_select_budget",
+                     (R, gmax, _ptr(cond_survival), _ptr(gamma), _ptr(sps), sps.shape[0] - 1,
+                      _ptr(verify_len), _ptr(best_B), _ptr(best_theta), _ptr(ws),
+                      0 if ws is None else ws.numel(), _ptr(dev_status)), cond_survival.device)
 
 
 def sv_adapt_gamma(accepted_len: torch.Tensor, verified: torch.Tensor, state: torch.Tensor,
@@ -276,13 +384,12 @@ def sv_verify_chunked(kv: PagedKV, batch: Batch, q: torch.Tensor, n_q_heads: int
                       ambiguous: torch.Tensor, done: torch.Tensor, ws: torch.Tensor,
                       dev_status: Optional[torch.Tensor] = None, stream=None):
     b, k = batch.c(), kv.c()
-    N.check(N.lib().sv_verify_chunked(ctypes.byref(k), ctypes.byref(b), _ptr(q), n_q_heads,
-                                      softmax_scale, _ptr(out), _ptr(target_logits),
-                                      _ptr(draft_logits), vocab, temperature,
-                                      seed & 0xFFFFFFFFFFFFFFFF, chunk_size, _ptr(accepted_len),
-                                      _ptr(accepted_nodes), _ptr(next_token), _ptr(ambiguous),
-                                      _ptr(done), _ptr(ws), ws.numel(), _ptr(dev_status),
-                                      _stream(stream)), "sv_verify_chunked")
+    _call("sv_verify_chunked",
+          (ctypes.byref(k), ctypes.byref(b), _ptr(q), n_q_heads, softmax_scale, _ptr(out),
+           _ptr(target_logits), _ptr(draft_logits), vocab, temperature,
+           seed & 0xFFFFFFFFFFFFFFFF, chunk_size, _ptr(accepted_len), _ptr(accepted_nodes),
+           _ptr(next_token), _ptr(ambiguous), _ptr(done), _ptr(ws), ws.numel(),
+           _ptr(dev_status)), stream)
 
 
 def sv_verify_chunked_commit(kv: PagedKV, batch: Batch, q: torch.Tensor, n_q_heads: int,
@@ -293,13 +400,36 @@ def sv_verify_chunked_commit(kv: PagedKV, batch: Batch, q: torch.Tensor, n_q_hea
                              next_token: torch.Tensor, ambiguous: torch.Tensor,
                              done: torch.Tensor, pool: BlockPool, ws: torch.Tensor,
                              dev_status: Optional[torch.Tensor] = None, stream=None):
+    _call("sv_verify_chunked_commit",
+          _chunked_commit_args(kv, batch, q, n_q_heads, softmax_scale, out, target_logits,
+                               draft_logits, vocab, temperature, seed, chunk_size, accepted_len,
+                               accepted_nodes, next_token, ambiguous, done, pool, ws,
+                               dev_status), stream)
+
+
+def _chunked_commit_args(kv, batch, q, n_q_heads, softmax_scale, out, target_logits,
+                         draft_logits, vocab, temperature, seed, chunk_size, accepted_len,
+                         accepted_nodes, next_token, ambiguous, done, pool, ws, dev_status):
     b, k, p = batch.c(), kv.c(), pool.c()
-    N.check(N.lib().sv_verify_chunked_commit(ctypes.byref(k), ctypes.byref(b), _ptr(q), n_q_heads,
-                                             softmax_scale, _ptr(out), _ptr(target_logits),
-                                             _ptr(draft_logits), vocab, temperature,
-                                             seed & 0xFFFFFFFFFFFFFFFF, chunk_size,
-                                             _ptr(accepted_len), _ptr(accepted_nodes),
-                                             _ptr(next_token), _ptr(ambiguous), _ptr(done),
-                                             ctypes.byref(p), _ptr(ws), ws.numel(),
-                                             _ptr(dev_status), _stream(stream)),
-            "sv_verify_chunked_commit")
+    return (ctypes.byref(k), ctypes.byref(b), _ptr(q), n_q_heads, softmax_scale, _ptr(out),
+            _ptr(target_logits), _ptr(draft_logits), vocab, temperature,
+            seed & 0xFFFFFFFFFFFFFFFF, chunk_size, _ptr(accepted_len), _ptr(accepted_nodes),
+            _ptr(next_token), _ptr(ambiguous), _ptr(done), ctypes.byref(p), _ptr(ws), ws.numel(),
+            _ptr(dev_status))
+
+
+def bind_verify_chunked_commit(kv: PagedKV, batch: Batch, q: torch.Tensor, n_q_heads: int,
+                               softmax_scale: float, out: torch.Tensor,
+                               target_logits: torch.Tensor,
+                               draft_logits: Optional[torch.Tensor], vocab: int,
+                               temperature: float, seed: int, chunk_size: int,
+                               accepted_len: torch.Tensor, accepted_nodes: torch.Tensor,
+                               next_token: torch.Tensor, ambiguous: torch.Tensor,
+                               done: torch.Tensor, pool: BlockPool, ws: torch.Tensor,
+                               dev_status: Optional[torch.Tensor] = None) -> BoundCall:
+    """sv_verify_chunked_commit with its arguments marshalled once (see BoundCall)."""
+    return BoundCall("sv_verify_chunked_commit",
+                     _chunked_commit_args(kv, batch, q, n_q_heads, softmax_scale, out,
+                                          target_logits, draft_logits, vocab, temperature, seed,
+                                          chunk_size, accepted_len, accepted_nodes, next_token,
+                                          ambiguous, done, pool, ws, dev_status), q.device)

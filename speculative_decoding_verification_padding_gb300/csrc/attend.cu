@@ -49,6 +49,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "sv_attend_internal.h"
@@ -72,9 +73,17 @@ constexpr int kMinPagesPerSplit = 32;
 // Calls with at most this many requests are latency-bound: splits go down to
 // kSmallPagesPerSplit pages and a separate kernel merges them, every unit of
 // a split group taking a slice of its rows (in-kernel, the group's last CTA
-// would merge every split alone).
+// would merge every split alone) -- unless the split groups run as clusters
+// (one-pass calls, below).
 constexpr int kSmallBatch = 4;
 constexpr int kSmallPagesPerSplit = 8;
+// One-pass calls of at most kSmallBatch requests run the splits of each
+// (row tile, KV head) group of the mma.sync list as one thread-block cluster
+// of kClusterSplits CTAs (on one GPC, two CTAs per SM fit), which merge their
+// partials through distributed shared memory at the end: no partials in
+// global memory and no merge launch (a one-request 4096-token chain step:
+// 53.3 -> 49.8 us, measured).
+constexpr int kClusterSplits = 16;
 constexpr int kMaxPagesPerSplit = 1024;  // block ids of a unit staged in shared memory
 
 struct ReqInfo {
@@ -120,6 +129,7 @@ struct Layout {
   size_t header, info, work, tickets, ml, o;
   size_t work_tc, ml_tc, o_tc, total;
   int ucap, ucap_tc;
+  int ucap_cl;      // units of a small one-pass call whose split groups are clusters
   int nsm;          // SMs of the device the call runs on
   int unit_target;  // units the planner aims for: kUnitsPerSM per SM
   int small;        // at most kSmallBatch requests: small splits, merge kernel
@@ -152,6 +162,15 @@ inline Layout layout(int R, int total_rows, int group, int Hkv, int D, int max_b
   L.unit_target = L.nsm * (L.small ? 2 : kUnitsPerSM);
   L.ucap = unit_cap(R, total_rows, group, Hkv, max_blocks, L.unit_target);
   L.ucap_tc = unit_cap_tc(R, total_rows, group, Hkv, D, max_rows, max_blocks, L.nsm);
+  L.ucap_cl = 0;
+  if (L.small) {
+    // kClusterSplits units per (row tile, KV head): at most
+    // floor(group * total_rows / 64) + R row tiles (clusters only when no
+    // window can reach the tcgen05 list; the work list holds either plan)
+    const long tiles = (long)group * total_rows / kTileRows + R;
+    L.ucap_cl = L.ucap_tc > 0 ? 0 : (int)((long)Hkv * tiles * kClusterSplits);
+    L.ucap = std::max(L.ucap, L.ucap_cl);
+  }
   L.header = off; off += align256(sizeof(Header));
   L.info = off; off += align256(sizeof(ReqInfo) * (size_t)R);
   L.work = off; off += align256(sizeof(WorkItem) * (size_t)L.ucap);
@@ -180,6 +199,7 @@ struct Args {
   Layout L;
   int32_t* dev_status;
   ChunkPlan chunk;  // chunk.index < 0: windows come from the batch
+  int cl;           // > 0: each split group of the mma.sync list is a cluster of cl CTAs
 };
 
 // ------------------------------------------------------------------ plan --
@@ -449,7 +469,7 @@ struct SmallPlan {
   int U, P, Utc, Ptc;
   int ubase[kSmallBatch], nsplit[kSmallBatch], nrt[kSmallBatch], tc[kSmallBatch];
   int b[kSmallBatch], e[kSmallBatch], ctx[kSmallBatch], nblk[kSmallBatch];
-  int cu[kSmallBatch], rows[kSmallBatch];
+  int cu[kSmallBatch], rows[kSmallBatch], Pr[kSmallBatch];
 };
 
 __device__ __forceinline__ void small_plan_warp(const Args& a, SmallPlan& sp, bool report) {
@@ -528,8 +548,11 @@ __device__ __forceinline__ void small_plan_warp(const Args& a, SmallPlan& sp, bo
   const unsigned long long target = (unsigned long long)a.L.unit_target;
   int P = (int)min((unsigned long long)kMaxPagesPerSplit, (W + target - 1) / target);
   if (P < kSmallPagesPerSplit) P = kSmallPagesPerSplit;
-  const int Pi = tc ? Ptc : P;
-  const int nsplit = valid ? (nblk + Pi - 1) / Pi : 0;
+  // clusters: exactly cl splits of ceil(nblk / cl) pages (the last ones may
+  // hold no page)
+  const bool clu = a.cl > 0 && !tc;
+  const int Pi = tc ? Ptc : clu ? max(1, (nblk + a.cl - 1) / a.cl) : P;
+  const int nsplit = valid ? (clu ? a.cl : (nblk + Pi - 1) / Pi) : 0;
   const int units = nrt * a.Hkv * nsplit;
   // exclusive prefix of the units within each list (lanes 0 .. R-1)
   int x = tc ? 0 : units, xt = tc ? units : 0;
@@ -539,7 +562,7 @@ __device__ __forceinline__ void small_plan_warp(const Args& a, SmallPlan& sp, bo
     if (lane >= o) { x += y; xt += yt; }
   }
   int U = __shfl_sync(kAll, x, R - 1), Utc = __shfl_sync(kAll, xt, R - 1);
-  if (U > a.L.ucap || Utc > a.L.ucap_tc) {  // cannot happen with the workspace's bounds
+  if (U > (a.cl > 0 ? a.L.ucap_cl : a.L.ucap) || Utc > a.L.ucap_tc) {  // cannot happen with the workspace's bounds
     U = Utc = 0;
     if (report && lane == 0) flag(a.dev_status, SV_DEV_BAD_LENGTH);
   }
@@ -554,6 +577,7 @@ __device__ __forceinline__ void small_plan_warp(const Args& a, SmallPlan& sp, bo
     sp.nblk[lane] = nblk;
     sp.cu[lane] = w.cu;
     sp.rows[lane] = w.rows;
+    sp.Pr[lane] = Pi;
   }
   if (lane == 0) {
     sp.U = U;
@@ -588,7 +612,7 @@ __global__ void __launch_bounds__(32) plan_small_kernel(Args a) {
       it.ubase = sp.ubase[r];
       it.cu = sp.cu[r];
       it.rows = sp.rows[r];
-      it.P = sp.tc[r] ? sp.Ptc : sp.P;
+      it.P = sp.Pr[r];
       it.pad = 0;
       list[sp.ubase[r] + x] = it;
     }
@@ -807,7 +831,79 @@ __device__ __forceinline__ void slice_compute(Frag<D>& f, const uint32_t (&qf)[D
   }
 }
 
+// The kClusterSplits CTAs of a split group form one cluster: each leaves its
+// (m, l, O) partial of the tile's rows in its own shared memory (the stage
+// ring, idle by now) and, after a cluster barrier, CTA rank r merges rows
+// r, r + kClusterSplits, ... reading every peer's partial of the row through
+// distributed shared memory (all sixteen loads in flight), then writes bf16
+// rows.  A second barrier keeps each CTA resident until its peers have read
+// it.  Every thread of every CTA of the cluster calls this.
 template <int D>
+__device__ __forceinline__ void cluster_merge(const Args& a, const Frag<D>& f, bool owner,
+                                              bool real_a, bool real_b, int vl_a, int vl_b, int tq,
+                                              uint8_t* ring_ptr, int Mu, int vr0, int row0, int g) {
+  constexpr int kStride = D + 4;  // floats per partial row (spreads the stores over banks)
+  constexpr int kQuads = D / 4;
+  static_assert(kTileRows * kStride * 4 + kTileRows * 8 <= kStages * StageLayout<D>::kStageBytes,
+                "partials fit in the ring");
+  float* po = reinterpret_cast<float*>(ring_ptr);
+  float2* pml = reinterpret_cast<float2*>(ring_ptr + (size_t)kTileRows * kStride * sizeof(float));
+  __syncthreads();  // the ring's exchange area has been read
+  if (owner) {
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+      if (real_a)
+        *reinterpret_cast<float2*>(po + vl_a * kStride + dn * 8 + 2 * tq) = make_float2(f.o[dn][0], f.o[dn][1]);
+      if (real_b)
+        *reinterpret_cast<float2*>(po + vl_b * kStride + dn * 8 + 2 * tq) = make_float2(f.o[dn][2], f.o[dn][3]);
+    }
+    if (tq == 0) {
+      if (real_a) pml[vl_a] = make_float2(f.m_a, f.l_a);
+      if (real_b) pml[vl_b] = make_float2(f.m_b, f.l_b);
+    }
+  }
+  cluster_sync();
+  const int rank = (int)cluster_rank();
+  const int nrow = rank < Mu ? (Mu - rank + kClusterSplits - 1) / kClusterSplits : 0;
+  const uint32_t po_s = smem_u32(po), pml_s = smem_u32(pml);
+  for (int x = threadIdx.x; x < nrow * kQuads; x += blockDim.x) {
+    const int vr = rank + (x / kQuads) * kClusterSplits, c4 = x % kQuads;
+    float2 ml[kClusterSplits];
+    float4 o4[kClusterSplits];
+#pragma unroll
+    for (int q = 0; q < kClusterSplits; ++q) {
+      ml[q] = dsmem_ld2(dsmem_addr(pml_s + (uint32_t)vr * 8u, (uint32_t)q));
+      o4[q] = dsmem_ld4(dsmem_addr(po_s + (uint32_t)(vr * kStride + c4 * 4) * 4u, (uint32_t)q));
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kClusterSplits; ++q) mx = fmaxf(mx, ml[q].x);
+    const float base = mx == -INFINITY ? 0.f : mx;  // m in the log2 domain
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < kClusterSplits; ++q) {
+      const float w = exp2f(ml[q].x - base);  // 0 for a split that saw no key of the row
+      L += w * ml[q].y;
+      acc.x += w * o4[q].x;
+      acc.y += w * o4[q].y;
+      acc.z += w * o4[q].z;
+      acc.w += w * o4[q].w;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int vgl = vr0 + vr;
+    const int prow = row0 + vgl / a.group;
+    const int head = g * a.group + vgl % a.group;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + ((size_t)prow * a.Hq + head) * D + c4 * 4);
+    dst[0] = pack_bf16(acc.x * inv, acc.y * inv);
+    dst[1] = pack_bf16(acc.z * inv, acc.w * inv);
+  }
+  cluster_sync();
+}
+
+// CL: the launch groups each split group's kClusterSplits units into one
+// thread-block cluster (small one-pass calls), which merges at the end.
+template <int D, bool CL>
 __global__ void __launch_bounds__(kThreads, 2)
     attend_kernel(Args a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
@@ -826,7 +922,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   // (it lies inside the workspace: the grid is the workspace's unit bound).
   const int U = hdr->U;
   const WorkItem ri = reinterpret_cast<const WorkItem*>(a.ws + a.L.work)[u];
-  if (u >= U) return;
+  // a cluster leaves as a whole (its CTAs meet at cluster barriers later);
+  // U is a multiple of the cluster size, so this only drops idle clusters
+  if (CL ? (u / kClusterSplits + 1) * kClusterSplits > U : u >= U) return;
   const int P = ri.P;
   const int i = ri.i;
   const int local = ri.local;
@@ -839,7 +937,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int vr0 = rt * kTileRows;
   const int Mu = min(kTileRows, M - vr0);
   const int blk0 = s * P;
-  const int blk1 = min(blk0 + P, ri.nblk);
+  // (a cluster's last splits may be empty)
+  const int blk1 = CL ? max(blk0, min(blk0 + P, ri.nblk)) : min(blk0 + P, ri.nblk);
   const int ctx = ri.ctx;
   const int tok_end = min(ctx + ri.e, blk1 * kBlockSize);
   const int cu = ri.cu;
@@ -1010,7 +1109,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int st = abort_at; st < issued_hi; ++st)
         mbar_wait_bounded(smem_u32(&s_full[st % kStages]), (uint32_t)((st / kStages) & 1));
     __syncthreads();
-    return;
+    if constexpr (!CL) {
+      return;
+    } else {
+      // in a cluster the CTA still meets its peers: it contributes nothing
+      // (the call's status already reports the timeout)
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn) f.o[dn][0] = f.o[dn][1] = f.o[dn][2] = f.o[dn][3] = 0.f;
+      f.m_a = f.m_b = -INFINITY;
+      f.l_a = f.l_b = 0.f;
+    }
   }
 
   // Warps that split the tokens of one m-tile merge through shared memory
@@ -1060,6 +1168,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     f.l_a += __shfl_xor_sync(0xffffffffu, f.l_a, 2);
     f.l_b += __shfl_xor_sync(0xffffffffu, f.l_b, 1);
     f.l_b += __shfl_xor_sync(0xffffffffu, f.l_b, 2);
+  }
+  if constexpr (CL) {
+    cluster_merge<D>(a, f, owner, real_a, real_b, vl_a, vl_b, tq, ring_ptr, Mu, vr0, cu + ri.b, g);
+    return;
   }
 
   if (ri.nsplit == 1) {
@@ -1604,11 +1716,51 @@ static bool make_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Clusters of kClusterSplits CTAs of attend_kernel<D, true> that can be
+// resident at once on the current device (a non-portable cluster size: the
+// kernel opts in), asked once per device; 0 if none fits.
 template <int D>
-sv_status launch(const Args& a, cudaStream_t stream) {
+static int cluster_capacity(size_t smem) {
+  static std::mutex mu;
+  static std::vector<int> cap;  // per device: -1 not asked
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if ((size_t)dev >= cap.size()) cap.resize((size_t)dev + 1, -1);
+  if (cap[(size_t)dev] < 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterSplits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = kClusterSplits;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const bool ok =
+        cudaFuncSetAttribute(attend_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) == cudaSuccess &&
+        cudaFuncSetAttribute(attend_kernel<D, true>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, attend_kernel<D, true>, &cfg) == cudaSuccess;
+    if (!ok) {
+      (void)cudaGetLastError();  // a refused query is an answer, not an error
+      n = 0;
+    }
+    cap[(size_t)dev] = n;
+  }
+  return cap[(size_t)dev];
+}
+
+template <int D>
+sv_status launch(const Args& a_in, cudaStream_t stream) {
+  Args a = a_in;
   const size_t smem = (size_t)kStages * StageLayout<D>::kStageBytes + 1024;
   static PerDevice smem_set;  // the ring is above the 48 KB default
-  if (smem_limit_once(smem_set, attend_kernel<D>, smem) != cudaSuccess) return SV_ERR_CUDA;
+  if (smem_limit_once(smem_set, attend_kernel<D, false>, smem) != cudaSuccess) return SV_ERR_CUDA;
   CUtensorMap tmK, tmV;
   if (!make_map(&tmK, a.k, a.num_blocks, a.Hkv, D) || !make_map(&tmV, a.v, a.num_blocks, a.Hkv, D))
     return SV_ERR_CUDA;
@@ -1617,8 +1769,17 @@ sv_status launch(const Args& a, cudaStream_t stream) {
   // one thread per request (its block-wide scans and barriers cost less with
   // fewer warps), at least four warps to write the work items, at most 1024
   const int plan_threads = min(1024, max(128, (a.bt.n_req + 31) / 32 * 32));
-  // small one-pass calls: the one-warp planner
+  // small one-pass calls: the one-warp planner, and split groups that merge
+  // within a cluster -- when no window can reach the tcgen05 list (a cluster
+  // launch behind the tcgen05 kernel waits for whole GPCs to drain: measured
+  // 4-5 us slower on the draft tree), a split's block ids fit in shared
+  // memory and the device takes such clusters
   const bool warp_plan = a.L.small && a.chunk.index < 0;
+  a.cl = warp_plan && a.L.ucap_tc == 0 &&
+                 (a.max_blocks + kClusterSplits - 1) / kClusterSplits <= kMaxPagesPerSplit &&
+                 cluster_capacity<D>(smem) > 0
+             ? kClusterSplits
+             : 0;
   if ((warp_plan ? sv::launch(plan_small_kernel, 1, 32, 0, stream, a)
                  : sv::launch(plan_kernel, 1, plan_threads, plan_smem, stream, a)) != cudaSuccess)
     return SV_ERR_CUDA;
@@ -1636,9 +1797,12 @@ sv_status launch(const Args& a, cudaStream_t stream) {
         return SV_ERR_CUDA;
     }
   }
-  if (sv::launch(attend_kernel<D>, a.L.ucap, kThreads, smem, stream, a, tmK, tmV) != cudaSuccess)
-    return SV_ERR_CUDA;
-  const int n_small = a.L.small ? a.L.ucap : 0;
+  const cudaError_t e =
+      a.cl > 0 ? sv::launch_cluster(attend_kernel<D, true>, a.L.ucap_cl, kThreads, smem, stream,
+                                    a.cl, a, tmK, tmV)
+               : sv::launch(attend_kernel<D, false>, a.L.ucap, kThreads, smem, stream, a, tmK, tmV);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  const int n_small = a.L.small && a.cl == 0 ? a.L.ucap : 0;
   if (n_small + ucap_tc > 0 &&
       sv::launch(merge_kernel<D>, n_small + ucap_tc, kMergeThreads, 0, stream, a, n_small) !=
           cudaSuccess)
@@ -1712,6 +1876,7 @@ sv_status tree_attend(const sv_paged_kv* kv, const sv_batch* bt, const void* q, 
                kv->max_blocks_per_req, bt->max_rows_per_req);
   a.dev_status = dev_status;
   a.chunk = chunk;
+  a.cl = 0;
   if (ws_bytes < a.L.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   return kv->head_dim == 128 ? launch<128>(a, stream) : launch<64>(a, stream);
 }

@@ -68,6 +68,7 @@ class DeviceStep:
         self.done = torch.zeros(R, dtype=torch.int32, device=dev)
         self.row_stats = None
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._calls = {}
         if cfg.budget:
             self.cond = f32(w.cond_survival)
             self.gamma = i32(w.gamma)
@@ -87,20 +88,45 @@ class DeviceStep:
     def restore_cache_state(self):
         self._state.copy_(self._state0)
 
+    def _bound(self, name, batch, make):
+        """The call `name` on `batch`, its arguments marshalled on first use
+        (the step's tensors never move, so later calls only launch)."""
+        key = (name, id(batch))
+        hit = self._calls.get(key)
+        if hit is None or hit[0] is not batch:
+            hit = (batch, make())  # holding the batch keeps its id unique
+            self._calls[key] = hit
+        return hit[1]
+
     def attend(self, batch=None):
-        api.sv_tree_attend(self.kv, batch or self.batch, self.q, self.Hq, self.scale, self.out,
-                           self.ws, self.dev_status)
+        b = batch or self.batch
+        self._bound("attend", b, lambda: api.bind_tree_attend(
+            self.kv, b, self.q, self.Hq, self.scale, self.out, self.ws, self.dev_status))()
 
     def accept(self, batch=None, row_stats=None):
-        api.sv_accept(batch or self.batch, self.target, self.draft, self.V, self.T, self.w.seed,
-                      self.accepted_len, self.accepted_nodes, self.next_token, self.ambiguous,
-                      self.done, row_stats, self.ws, self.dev_status)
+        b = batch or self.batch
+        if row_stats is not None:
+            api.sv_accept(b, self.target, self.draft, self.V, self.T, self.w.seed,
+                          self.accepted_len, self.accepted_nodes, self.next_token,
+                          self.ambiguous, self.done, row_stats, self.ws, self.dev_status)
+            return
+        self._bound("accept", b, lambda: api.bind_accept(
+            b, self.target, self.draft, self.V, self.T, self.w.seed, self.accepted_len,
+            self.accepted_nodes, self.next_token, self.ambiguous, self.done, None, self.ws,
+            self.dev_status))()
 
     def accept_commit(self, batch=None, row_stats=None):
-        api.sv_accept_commit(batch or self.batch, self.target, self.draft, self.V, self.T,
-                             self.w.seed, self.accepted_len, self.accepted_nodes,
-                             self.next_token, self.ambiguous, self.done, row_stats, self.kv,
-                             self.pool, self.ws, self.dev_status)
+        b = batch or self.batch
+        if row_stats is not None:
+            api.sv_accept_commit(b, self.target, self.draft, self.V, self.T, self.w.seed,
+                                 self.accepted_len, self.accepted_nodes, self.next_token,
+                                 self.ambiguous, self.done, row_stats, self.kv, self.pool,
+                                 self.ws, self.dev_status)
+            return
+        self._bound("accept_commit", b, lambda: api.bind_accept_commit(
+            b, self.target, self.draft, self.V, self.T, self.w.seed, self.accepted_len,
+            self.accepted_nodes, self.next_token, self.ambiguous, self.done, None, self.kv,
+            self.pool, self.ws, self.dev_status))()
 
     def chunked(self):
         api.sv_verify_chunked(self.kv, self.batch, self.q, self.Hq, self.scale, self.out,
@@ -109,15 +135,15 @@ class DeviceStep:
                               self.ambiguous, self.done, self.ws, self.dev_status)
 
     def chunked_commit(self):
-        api.sv_verify_chunked_commit(self.kv, self.batch, self.q, self.Hq, self.scale, self.out,
-                                     self.target, self.draft, self.V, self.T, self.w.seed,
-                                     self.chunk, self.accepted_len, self.accepted_nodes,
-                                     self.next_token, self.ambiguous, self.done, self.pool,
-                                     self.ws, self.dev_status)
+        self._bound("chunked_commit", self.batch, lambda: api.bind_verify_chunked_commit(
+            self.kv, self.batch, self.q, self.Hq, self.scale, self.out, self.target, self.draft,
+            self.V, self.T, self.w.seed, self.chunk, self.accepted_len, self.accepted_nodes,
+            self.next_token, self.ambiguous, self.done, self.pool, self.ws, self.dev_status))()
 
     def select(self):
-        api.sv_select_budget(self.cond, self.gamma, self.sps, self.verify_len, self.best_B,
-                             self.best_theta, None, self.dev_status)
+        self._bound("select", self.batch, lambda: api.bind_select_budget(
+            self.cond, self.gamma, self.sps, self.verify_len, self.best_B, self.best_theta, None,
+            self.dev_status))()
 
     def commit(self, batch=None):
         api.sv_commit_kv(self.kv, batch or self.batch, self.accepted_len, self.accepted_nodes,

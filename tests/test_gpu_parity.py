@@ -70,6 +70,13 @@ ATTN_CASES = {
     "batch64_small": dict(name="batch64", n_req=64, ctx_scale=0.05, vocab=256),
     "batch256_small": dict(name="batch256", n_req=96, ctx_scale=0.02, vocab=256),
     "ragged_ctx": dict(name="batch64", n_req=9, ctx_scale=0.0007, vocab=64),  # contexts of a few tokens
+    # one-pass calls of at most four requests: every split group is one
+    # thread-block cluster of sixteen CTAs merging through shared memory --
+    # mixed contexts, contexts shorter than sixteen pages (empty splits), a
+    # long context (64-page splits)
+    "cluster_mixed": dict(name="batch64", n_req=4, ctx_scale=0.5, vocab=64),
+    "cluster_short": dict(name="batch64", n_req=3, ctx_scale=0.004, vocab=64),
+    "cluster_long": dict(name="chain8b", ctx_scale=4.0, vocab=64),
 }
 
 
@@ -508,6 +515,8 @@ def _check_commit_against_oracle(s, w, st, vl=None, skip=()):
     ("batch64", 0.7, 3, dict(n_req=40, ctx_scale=0.05, vocab=2048, draft_sigma=0.3)),
     ("tree70b", 0.0, None, dict(ctx_scale=0.01, vocab=512, draft_sigma=0.05)),
     ("tree70b", 1.0, None, dict(n_req=3, ctx_scale=0.01, vocab=2048, draft_sigma=0.3)),
+    # a chunked call of three requests: small splits merged by the merge kernel
+    ("batch64", 0.7, 2, dict(n_req=3, ctx_scale=0.3, vocab=2048, draft_sigma=0.5)),
 ])
 def test_chunked_commit_fused_matches_oracle(name, T, chunk, kw):
     # sv_verify_chunked_commit == oracle chunked verification followed by the
