@@ -51,7 +51,8 @@ struct StatPart {
 };
 
 struct Job {
-  int mode;     // 0 none, 1 residual max(0, p - c q), 2 bonus (p), 3 tree walk pending
+  int mode;     // 0 none, 1 residual max(0, p - c q), 2 bonus (p), 3 tree walk pending;
+                // | 4: the walk's KV commit is pending (the race kernel runs it)
   int row;      // packed row of the target (and draft) logits
   int pos;      // position of the emitted token
   float c;      // residual coefficient (1 after one rejection)
@@ -167,6 +168,9 @@ struct Args {
   int commit;     // fused KV commit (sv_accept_commit)
   int keep_l2;    // the statistics load the logits to stay in L2 (small
                   // calls: the decision and the race read them again)
+  int tree_commit_race;  // one-pass fused commit at T > 0: a tree walk leaves its
+                         // request's commit to the race kernel (job mode bit 2),
+                         // whose last CTA runs it beside the race
   CommitArgs kv;
 };
 
@@ -1058,21 +1062,38 @@ __global__ void __launch_bounds__(kDecideWarps * 32, 1) decide_kernel(Args a) {
 // the remaining siblings are not tried and the token comes from p_n.  The
 // walk ends at a leaf (bonus from p_leaf) or when every child is rejected
 // (a residual job with coefficient c); the race draws the token.
-constexpr int kTreeThreads = 1024;
+//
+// NT threads per CTA, CL CTAs per tree: with CL > 1 the tree's CTAs form one
+// thread-block cluster that shares each vocabulary pass (thread t of CTA r
+// takes the entries of global thread r * NT + t), adds the CTAs' sums in rank
+// order over distributed shared memory, and takes every decision in each CTA
+// alike (the same inputs and operations: the same walk everywhere); rank 0
+// writes the results.
+constexpr int kTreeThreads = 1024;         // one CTA per tree
+constexpr int kTreeClusterThreads = 256;   // CTAs of a tree's cluster
+constexpr int kTreeCluster = 16;
+// The cluster walk when a request may hold more rows than this (a deep tree;
+// chains of draft length <= 16 and small trees keep the single-CTA walk: a
+// cluster launch behind the decision kernel costs a few microseconds even
+// when no request walks, measured in stream order with a cold L2).
+constexpr int kTreeClusterMinRows = 17;
 
-__global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
+template <int NT, int CL>
+__global__ void __launch_bounds__(NT) tree_kernel(Args a) {
   griddep_entry();
-  const int i = blockIdx.x;
+  const int i = blockIdx.x / CL;
+  const int rank = CL > 1 ? (int)cluster_rank() : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Job* job = reinterpret_cast<Job*>(a.ws + a.L.jobs) + i;
   __shared__ int s_mode, s_nk, s_dec;
   __shared__ int s_kids[kMaxRows];
   __shared__ float s_st[4];  // merged max / normaliser of p and of q at the current node
-  __shared__ double s_red[kTreeThreads / 32];
+  __shared__ double s_red[NT / 32];
   __shared__ double s_S;
+  __shared__ double s_part[2];  // this CTA's sum of the current pass (pass parity)
   if (tid == 0) s_mode = job->mode;
   __syncthreads();
-  if (s_mode != 3) return;
+  if (s_mode != 3) return;  // the same for every CTA of the tree
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   const int nch = stats_slices(a.L, n_slots(a, act), 2, a.use_list != 0, a.bt.total_rows);
   const float T = a.T, rT = 1.f / T;
@@ -1085,7 +1106,24 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
   int n = 0, k = 0;
   bool amb = false;
   Job out{};
+  int npass = 0;  // vocabulary passes so far (parity of the cluster's sum slot)
+  // 128-bit loads of each row in flight per thread in a pass (a cluster's
+  // 4096 threads cover a 128256-entry row in one round)
+  constexpr int kPassDepth = CL > 1 ? 8 : 4;
   for (int step = 0; step < kMaxRows; ++step) {  // every move goes to a larger node
+    if (CL > 1 && warp != 0 && vec) {
+      // the rows a pass at this node would stream, into L2 while warp 0
+      // merges the node's statistics and the decisions run (a rejection
+      // then finds them there)
+      // (whole 128-byte lines inside the rows, one per thread of the cluster)
+      const char* pr = reinterpret_cast<const char*>(a.target + (size_t)(cu + n) * V);
+      const char* qr = reinterpret_cast<const char*>(a.draft + (size_t)(cu + n) * V);
+      const int lines = (int)(((long)V * 4) / 128);
+      for (int L = rank * NT + tid; L < lines; L += NT * CL) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(pr + (size_t)L * 128));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + (size_t)L * 128));
+      }
+    }
     if (warp == 0) {
       // children of n in index order, then the merged statistics of row n
       int cnt = 0;
@@ -1111,7 +1149,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
     bool moved = false, vanished = false;
     for (int t = 0; t < nk; ++t) {
       const int ch = s_kids[t];
-      if (tid == 0) {
+      if (tid == 0) {  // (in every CTA of a cluster: the same decision)
         const int x = a.bt.tokens[cu + ch];
         // pres / q = max(0, p - c q) / (S q) = max(0, p/q - c) / S, with p/q
         // from the exact exponent in fp32 (as on chains; fp64 runs at a
@@ -1129,7 +1167,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
       const int dec = s_dec;
       __syncthreads();  // s_dec is rewritten by the next test
       if (dec) {
-        if (tid == 0) nodes[k + 1] = ch;
+        if (tid == 0 && rank == 0) nodes[k + 1] = ch;
         ++k;
         n = ch;
         moved = true;
@@ -1149,22 +1187,22 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
         sum = tsum;
       };
       if (vec) {
-        // 128-bit loads, four of each row in flight per thread (entries past
+        // 128-bit loads, kPassDepth of each row in flight per thread (entries past
         // the row read as -inf logits: p = 0 adds nothing)
         const float4* p4 = reinterpret_cast<const float4*>(lp);
         const float4* q4 = reinterpret_cast<const float4*>(lq);
         const int n4 = V >> 2;
         const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        for (int v0 = tid; v0 < n4; v0 += 4 * kTreeThreads) {
-          float4 xp[4], xq[4];
+        for (int v0 = rank * NT + tid; v0 < n4; v0 += kPassDepth * NT * CL) {
+          float4 xp[kPassDepth], xq[kPassDepth];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int v = v0 + k * kTreeThreads;
+          for (int k = 0; k < kPassDepth; ++k) {
+            const int v = v0 + k * NT * CL;
             xp[k] = v < n4 ? __ldg(p4 + v) : none;
             xq[k] = v < n4 ? __ldg(q4 + v) : none;
           }
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < kPassDepth; ++k) {
             add(xp[k].x, xq[k].x);
             add(xp[k].y, xq[k].y);
             add(xp[k].z, xq[k].z);
@@ -1172,7 +1210,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
           }
         }
       } else {
-        for (int v = tid; v < V; v += kTreeThreads) add(lp[v], lq[v]);
+        for (int v = rank * NT + tid; v < V; v += NT * CL) add(lp[v], lq[v]);
       }
       double d = (double)sum - (double)comp;
 #pragma unroll
@@ -1180,12 +1218,33 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
       if (lane == 0) s_red[warp] = d;
       __syncthreads();
       if (warp == 0) {
-        double e = lane < kTreeThreads / 32 ? s_red[lane] : 0.0;
+        double e = lane < NT / 32 ? s_red[lane] : 0.0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
-        if (lane == 0) s_S = e;
+        if (lane == 0) {
+          if (CL > 1) s_part[npass & 1] = e;
+          else s_S = e;
+        }
+      }
+      if constexpr (CL > 1) {
+        // every CTA's sum of this pass is in place; each CTA adds them in
+        // rank order (the slot of this parity is next written two passes on,
+        // after every CTA has passed the next pass's barrier)
+        cluster_sync();
+        if (tid == 0) {
+          // all the CTAs' sums in flight at once, then added in rank order
+          const uint32_t slot = smem_u32(&s_part[npass & 1]);
+          double v[CL];
+#pragma unroll
+          for (int q = 0; q < CL; ++q) v[q] = dsmem_ld_f64(dsmem_addr(slot, (uint32_t)q));
+          double t = 0.0;
+#pragma unroll
+          for (int q = 0; q < CL; ++q) t += v[q];
+          s_S = t;
+        }
       }
       __syncthreads();
+      ++npass;
       S = s_S;
       if (!(S > 0.0)) {
         vanished = true;
@@ -1198,7 +1257,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
     out.c = (float)c;
     break;
   }
-  if (tid == 0) {
+  if (tid == 0 && rank == 0) {
     out.row = cu + n;
     out.pos = k + 1;
     out.mp = s_st[0];
@@ -1209,16 +1268,19 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(Args a) {
       out.mq = 0.f;
       out.lq = 1.f;
     }
+    if (a.commit && a.tree_commit_race) out.mode |= 4;
     *job = out;
     a.accepted_len[i] = k;
     a.next_token[i] = -1;
     if (amb) a.ambiguous[i] = 1;
     if (a.done) a.done[i] = 1;
   }
-  if (a.commit && warp == 0) {
+  if (a.commit && !a.tree_commit_race && warp == 0 && rank == 0) {
     __syncwarp();  // the path thread 0 wrote is visible to the warp
     commit_request(a, i, true, nullptr);
   }
+  // no CTA leaves while its peers may still read its last pass's sum
+  if constexpr (CL > 1) cluster_sync();
 }
 
 // ------------------------------------------------------------------ race --
@@ -1302,6 +1364,14 @@ constexpr int kRaceStageFloats = 2 * kRaceBlock;
 constexpr size_t kRaceSmem =
     (size_t)kRaceWarps * kRaceStages * (kRaceStageFloats * sizeof(float) + sizeof(uint64_t));
 
+// The race kernel's last CTA: the commits tree walks left to it, one warp
+// per request (kept out of line: the race's own code stays as small as it was)
+__device__ __noinline__ void commit_deferred(const Args& a) {
+  const Job* jobs = reinterpret_cast<const Job*>(a.ws + a.L.jobs);
+  for (int i = (int)(threadIdx.x >> 5); i < a.bt.n_req; i += kRaceWarps)
+    if (jobs[i].mode & 4) commit_request(a, i, true, nullptr);
+}
+
 // Warp-granular like the statistics: a warp scans one slice (whole blocks of
 // 128 groups) of a request's row(s) and arrives on the request's ticket; the
 // last one reduces and picks the entry.  With VEC the warp's logits stream
@@ -1313,6 +1383,13 @@ __global__ void __launch_bounds__(kRaceThreads, 3) race_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t s_race[];
   const int* act = reinterpret_cast<const int*>(a.ws + a.L.act);
   const int R = a.bt.n_req;
+  // the last CTA commits the requests whose tree walk left its commit here
+  // (one warp per request), beside the race of the other CTAs
+  const int ncta = (int)gridDim.x - (a.tree_commit_race ? 1 : 0);
+  if ((int)blockIdx.x >= ncta) {
+    commit_deferred(a);
+    return;
+  }
   const int count = a.race_all ? R : n_slots(a, act);
   const int V = a.V;
   int nch = race_slices(a.L, count, V);
@@ -1335,7 +1412,7 @@ __global__ void __launch_bounds__(kRaceThreads, 3) race_kernel(Args a) {
   }
   uint32_t issued = 0, used = 0;  // blocks this warp has requested / consumed
   bool timed_out = false;
-  const long stride = (long)gridDim.x * kRaceWarps;
+  const long stride = (long)ncta * kRaceWarps;
   for (long item = (long)blockIdx.x * kRaceWarps + wid; item < total && !timed_out;
        item += stride) {
     const int c = (int)(item % nch);
@@ -1345,8 +1422,9 @@ __global__ void __launch_bounds__(kRaceThreads, 3) race_kernel(Args a) {
     // pass cleared every request's), so a non-zero mode here was written by
     // this call.
     const Job jb = reinterpret_cast<const Job*>(a.ws + a.L.jobs)[i];
-    if (jb.mode != 1 && jb.mode != 2) continue;
-    const bool resid = jb.mode == 1;
+    const int md = jb.mode & 3;
+    if (md != 1 && md != 2) continue;
+    const bool resid = md == 1;
     const float* lp = a.target + (size_t)jb.row * V;
     const float* lq = a.draft + (size_t)jb.row * V;
     const float inv_lq = 1.f / jb.lq;
@@ -1597,8 +1675,8 @@ static sv_status launch_race(const Args& a, bool vec, cudaStream_t s) {
     static PerDevice smem_set;  // the ring is above the 48 KB default
     if (smem_limit_once(smem_set, race_kernel<true>, kRaceSmem) != cudaSuccess) return SV_ERR_CUDA;
   }
-  if (sv::launch(vec ? race_kernel<true> : race_kernel<false>, gr, kRaceThreads,
-                 vec ? kRaceSmem : 0, s, a) != cudaSuccess)
+  if (sv::launch(vec ? race_kernel<true> : race_kernel<false>, gr + (a.tree_commit_race ? 1u : 0u),
+                 kRaceThreads, vec ? kRaceSmem : 0, s, a) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;
 }
@@ -1643,6 +1721,9 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
   a.race_all = 0;
   a.clear_jobs = chunk_index == 0 ? 1 : 0;
   a.commit = commit ? 1 : 0;
+  // one-pass calls at T > 0 run the race after the tree walk: it takes the
+  // walks' commits
+  a.tree_commit_race = commit && !chunk_step && temperature > 0.f ? 1 : 0;
   a.kv = CommitArgs{};
   if (commit) {
     a.kv.k = static_cast<__nv_bfloat16*>(commit_kv->k_cache);
@@ -1679,8 +1760,17 @@ sv_status run(const sv_batch* bt, const float* target_logits, const float* draft
     // exit at once.  A tree is verified in one window: in a chunked step only
     // the first chunk, and only when a chunk holds more than a chain's two
     // rows, can take one whole.
-    if (sv::launch(tree_kernel, (unsigned)bt->n_req, kTreeThreads, 0, s, a) != cudaSuccess)
-      return SV_ERR_CUDA;
+    static ClusterFit tree_fit;
+    const bool clu =
+        bt->max_rows_per_req >= kTreeClusterMinRows &&
+        tree_fit.get(tree_kernel<kTreeClusterThreads, kTreeCluster>, kTreeCluster,
+                     kTreeClusterThreads, 0) > 0;
+    const cudaError_t e =
+        clu ? sv::launch_cluster(tree_kernel<kTreeClusterThreads, kTreeCluster>,
+                                 (unsigned)bt->n_req * kTreeCluster, kTreeClusterThreads, 0, s,
+                                 kTreeCluster, a)
+            : sv::launch(tree_kernel<kTreeThreads, 1>, (unsigned)bt->n_req, kTreeThreads, 0, s, a);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
   }
   if (temperature > 0.f && !chunk_step) return launch_race(a, vec, s);
   return SV_OK;

@@ -1716,51 +1716,13 @@ static bool make_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Clusters of kClusterSplits CTAs of attend_kernel<D, true> that can be
-// resident at once on the current device (a non-portable cluster size: the
-// kernel opts in), asked once per device; 0 if none fits.
-template <int D>
-static int cluster_capacity(size_t smem) {
-  static std::mutex mu;
-  static std::vector<int> cap;  // per device: -1 not asked
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  if ((size_t)dev >= cap.size()) cap.resize((size_t)dev + 1, -1);
-  if (cap[(size_t)dev] < 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kClusterSplits);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeClusterDimension;
-    at.val.clusterDim.x = kClusterSplits;
-    at.val.clusterDim.y = 1;
-    at.val.clusterDim.z = 1;
-    cfg.attrs = &at;
-    cfg.numAttrs = 1;
-    int n = 0;
-    const bool ok =
-        cudaFuncSetAttribute(attend_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) == cudaSuccess &&
-        cudaFuncSetAttribute(attend_kernel<D, true>, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                             1) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&n, attend_kernel<D, true>, &cfg) == cudaSuccess;
-    if (!ok) {
-      (void)cudaGetLastError();  // a refused query is an answer, not an error
-      n = 0;
-    }
-    cap[(size_t)dev] = n;
-  }
-  return cap[(size_t)dev];
-}
-
 template <int D>
 sv_status launch(const Args& a_in, cudaStream_t stream) {
   Args a = a_in;
   const size_t smem = (size_t)kStages * StageLayout<D>::kStageBytes + 1024;
   static PerDevice smem_set;  // the ring is above the 48 KB default
   if (smem_limit_once(smem_set, attend_kernel<D, false>, smem) != cudaSuccess) return SV_ERR_CUDA;
+  static ClusterFit cluster_fit;  // sets the cluster kernel's shared-memory limit too
   CUtensorMap tmK, tmV;
   if (!make_map(&tmK, a.k, a.num_blocks, a.Hkv, D) || !make_map(&tmV, a.v, a.num_blocks, a.Hkv, D))
     return SV_ERR_CUDA;
@@ -1777,7 +1739,7 @@ sv_status launch(const Args& a_in, cudaStream_t stream) {
   const bool warp_plan = a.L.small && a.chunk.index < 0;
   a.cl = warp_plan && a.L.ucap_tc == 0 &&
                  (a.max_blocks + kClusterSplits - 1) / kClusterSplits <= kMaxPagesPerSplit &&
-                 cluster_capacity<D>(smem) > 0
+                 cluster_fit.get(attend_kernel<D, true>, kClusterSplits, kThreads, smem) > 0
              ? kClusterSplits
              : 0;
   if ((warp_plan ? sv::launch(plan_small_kernel, 1, 32, 0, stream, a)

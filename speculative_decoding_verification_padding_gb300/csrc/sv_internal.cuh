@@ -244,6 +244,11 @@ __device__ __forceinline__ float2 dsmem_ld2(uint32_t a) {
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
   return v;
 }
+__device__ __forceinline__ double dsmem_ld_f64(uint32_t a) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];\n" : "=d"(v) : "r"(a) : "memory");
+  return v;
+}
 __device__ __forceinline__ float4 dsmem_ld4(uint32_t a) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
@@ -456,6 +461,53 @@ inline cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 bloc
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+// How many clusters of `cluster` CTAs of a kernel (`threads` per CTA,
+// `smem` bytes of dynamic shared memory) can be resident at once on the
+// current device, asked once per device; 0 if none fits or the query is
+// refused.  Sizes above the portable eight are opted into first.
+class ClusterFit {
+ public:
+  template <class K>
+  int get(K kernel, int cluster, int threads, size_t smem) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    std::lock_guard<std::mutex> lock(mu_);
+    if ((size_t)dev >= cap_.size()) cap_.resize((size_t)dev + 1, -1);
+    if (cap_[(size_t)dev] < 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)cluster);
+      cfg.blockDim = dim3((unsigned)threads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = (unsigned)cluster;
+      at.val.clusterDim.y = 1;
+      at.val.clusterDim.z = 1;
+      cfg.attrs = &at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      bool ok = true;
+      if (smem > 48 * 1024)
+        ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem) == cudaSuccess;
+      if (ok && cluster > 8)
+        ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+             cudaSuccess;
+      ok = ok && cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess;
+      if (!ok) {
+        (void)cudaGetLastError();  // a refused query is an answer, not an error
+        n = 0;
+      }
+      cap_[(size_t)dev] = n;
+    }
+    return cap_[(size_t)dev];
+  }
+
+ private:
+  std::mutex mu_;
+  std::vector<int> cap_;  // per device: -1 not asked
+};
 
 // A named NVTX range around the host part of a call (what it enqueues), so
 // that profilers group the call's kernels under the call's name.
