@@ -1110,32 +1110,53 @@ __global__ void __launch_bounds__(NT) tree_kernel(Args a) {
   // 128-bit loads of each row in flight per thread in a pass (a cluster's
   // 4096 threads cover a 128256-entry row in one round)
   constexpr int kPassDepth = CL > 1 ? 8 : 4;
-  for (int step = 0; step < kMaxRows; ++step) {  // every move goes to a larger node
-    if (CL > 1 && warp != 0 && vec) {
-      // the rows a pass at this node would stream, into L2 while warp 0
-      // merges the node's statistics and the decisions run (a rejection
-      // then finds them there)
-      // (whole 128-byte lines inside the rows, one per thread of the cluster)
-      const char* pr = reinterpret_cast<const char*>(a.target + (size_t)(cu + n) * V);
-      const char* qr = reinterpret_cast<const char*>(a.draft + (size_t)(cu + n) * V);
-      const int lines = (int)(((long)V * 4) / 128);
-      for (int L = rank * NT + tid; L < lines; L += NT * CL) {
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(pr + (size_t)L * 128));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + (size_t)L * 128));
+  // Before the first step, every load a step needs, all at once: the merged
+  // statistics of every node (draft ones of the nodes that can be parents,
+  // rows - 1 at most) and, for every non-root node, its parent's link and its
+  // token's target and draft logits at the parent.  A step then only reads
+  // shared memory.  (The decision kernel checked the parents, in [0, r), and
+  // the tokens, in [0, V).)
+  __shared__ float s_mp[kMaxRows], s_lp[kMaxRows], s_mq[kMaxRows], s_lq[kMaxRows];
+  __shared__ float s_xp[kMaxRows], s_xq[kMaxRows];
+  __shared__ int s_par[kMaxRows];
+  {
+    constexpr int kRowsPerWarp = 8;
+    for (int base = warp * kRowsPerWarp; base < rows; base += (NT / 32) * kRowsPerWarp) {
+      const int cnt = min(kRowsPerWarp, rows - base);
+      merge_pairs<16>(a, nch, cu + base, cnt, max(0, min(cnt, rows - 1 - base)), s_mp + base,
+                      s_lp + base, s_mq + base, s_lq + base);
+    }
+    for (int r = tid; r < rows; r += NT) {
+      const int p = r == 0 ? -1 : a.bt.parent[cu + r];
+      s_par[r] = p;
+      if (r > 0) {
+        const int x = a.bt.tokens[cu + r];
+        s_xp[r] = a.target[(size_t)(cu + p) * V + x];
+        s_xq[r] = a.draft[(size_t)(cu + p) * V + x];
       }
     }
+  }
+  __syncthreads();
+  for (int step = 0; step < kMaxRows; ++step) {  // every move goes to a larger node
     if (warp == 0) {
-      // children of n in index order, then the merged statistics of row n
+      // children of n in index order, and the node's statistics
       int cnt = 0;
       for (int base = n + 1; base < rows; base += 32) {
         const int c = base + lane;
-        const bool is = c < rows && a.bt.parent[cu + c] == n;
+        const bool is = c < rows && s_par[c] == n;
         const unsigned m = __ballot_sync(0xffffffffu, is);
         if (is) s_kids[cnt + __popc(m & ((1u << lane) - 1u))] = c;
         cnt += __popc(m);
       }
-      if (lane == 0) s_nk = cnt;
-      merge_pairs<16>(a, nch, cu + n, 1, cnt > 0 ? 1 : 0, &s_st[0], &s_st[1], &s_st[2], &s_st[3]);
+      if (lane == 0) {
+        s_nk = cnt;
+        s_st[0] = s_mp[n];
+        s_st[1] = s_lp[n];
+        if (cnt > 0) {
+          s_st[2] = s_mq[n];
+          s_st[3] = s_lq[n];
+        }
+      }
     }
     __syncthreads();
     const int nk = s_nk;
@@ -1150,13 +1171,12 @@ __global__ void __launch_bounds__(NT) tree_kernel(Args a) {
     for (int t = 0; t < nk; ++t) {
       const int ch = s_kids[t];
       if (tid == 0) {  // (in every CTA of a cluster: the same decision)
-        const int x = a.bt.tokens[cu + ch];
         // pres / q = max(0, p - c q) / (S q) = max(0, p/q - c) / S, with p/q
         // from the exact exponent in fp32 (as on chains; fp64 runs at a
         // small fraction of the fp32 rate on this GPU) and 1 / S taken once
         // per pass.  q that vanishes gives ratio 1, as the definition's
         // q > 0 test does; p = 0 gives 0.
-        const float r_pq = pq_ratio(lp[x] / T, lq[x] / T, s_st[0], s_st[1], s_st[2], s_st[3]);
+        const float r_pq = pq_ratio(s_xp[ch] / T, s_xq[ch] / T, s_st[0], s_st[1], s_st[2], s_st[3]);
         const double ratio =
             r_pq == INFINITY ? 1.0 : fmin(1.0, fmax(0.0, (double)r_pq - c) * inv_S);
         const double u = (double)accept_u(a.seed, i, ch);
