@@ -113,3 +113,23 @@ def test_static_scratch_holds_the_documented_batch(lib):
                     b = N.SvBatch(R, rows, maxr, 1, 1, 1, None, None, None)
                     worst = max(worst, lib.sv_accept_workspace(ctypes.byref(b), V))
     assert worst <= N.SV_ACCEPT_STATIC_SCRATCH_BYTES
+
+
+def test_bound_calls_check_their_arguments_once_when_bound(lib):
+    # api.bind_* marshal a call's arguments when bound: host tensors and wrong
+    # dtypes are refused there, before anything could be enqueued.
+    import torch
+    from speculative_decoding_verification_padding_gb300 import api, _native as N
+    def i32(n):
+        return torch.zeros(n, dtype=torch.int32)
+    b = api.Batch(i32(2), torch.full((1,), -1, dtype=torch.int32), i32(1), 1)
+    kv = api.PagedKV(torch.zeros((1, 1, 16, 64), dtype=torch.bfloat16),
+                     torch.zeros((1, 1, 16, 64), dtype=torch.bfloat16), i32((1, 1)), i32(1))
+    q = torch.zeros((1, 1, 64), dtype=torch.bfloat16)
+    with pytest.raises(N.SpecVerifyError):
+        api.bind_tree_attend(kv, b, q, 1, 0.125, q.clone(), torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(N.SpecVerifyError):
+        api.bind_tree_attend(kv, b, q.float(), 1, 0.125, q.clone(), torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(N.SpecVerifyError):
+        api.bind_select_budget(torch.zeros((1, 4)), None, torch.zeros(11), i32(1), i32(1),
+                               torch.zeros(1, dtype=torch.float32))  # best_theta must be f64

@@ -851,6 +851,29 @@ def test_tree_sampling_batch_of_trees_matches_oracle():
     _compare_accept(res, st, w, "five trees")
 
 
+def test_small_tree_sampling_walks_on_one_cta_and_matches_oracle():
+    # trees of at most 16 rows are walked by a single CTA (deeper ones by a
+    # 16-CTA cluster): both walks against the oracle on the same kind of input
+    import dataclasses
+    n_same = 0
+    for seed in range(6):
+        cfg = dataclasses.replace(wl.config("tree70b"), gamma=("tree", (3, 2, 2), 15), n_req=2)
+        w = wl.make_workload(cfg, ctx_scale=0.01, vocab=2048, temperature=1.0, draft_sigma=0.7,
+                             step_seed=2000 + seed)
+        assert w.max_rows <= 16
+        s = DeviceStep(w, mode="onepass")
+        s.accept()
+        res = s.results()
+        assert res["dev_status"] == 0
+        err, st = oracle.accept(w.batch(), w.target_logits, w.draft_logits, 1.0, w.seed)
+        assert err == 0
+        if st.ambiguous.any() or res["ambiguous"].any():
+            continue
+        _compare_accept(res, st, w, f"small trees seed={seed}")
+        n_same += 1
+    assert n_same >= 4
+
+
 # ------------------------------------------------------- the largest windows --
 # 128 rows per request (the 128-bit ancestor masks' upper word, decision
 # windows longer than a warp, merges of more than 32 row/type pairs).
@@ -1048,3 +1071,25 @@ def test_batch256_full_size_budget_step(batch256_full):
     if amb.any():
         pytest.skip("an ambiguous decision: the commit inputs differ by construction")
     _check_commit_against_oracle(s, w, st, vl=vl)
+
+
+def test_bound_calls_equal_the_plain_calls():
+    # DeviceStep launches through BoundCall objects (arguments marshalled once);
+    # the plain api calls on the same inputs give the same bytes.
+    w = _make("chain8b", ctx_scale=0.25, vocab=2048)
+    s = DeviceStep(w, mode="onepass")
+    s.restore_cache_state()
+    s.attend()
+    s.accept()
+    torch.cuda.synchronize()
+    out_b = s.out.clone()
+    res_b = [t.clone() for t in (s.accepted_len, s.accepted_nodes, s.next_token, s.ambiguous)]
+    s.out.zero_()
+    api.sv_tree_attend(s.kv, s.batch, s.q, s.Hq, s.scale, s.out, s.ws, s.dev_status)
+    api.sv_accept(s.batch, s.target, s.draft, s.V, s.T, s.w.seed, s.accepted_len,
+                  s.accepted_nodes, s.next_token, s.ambiguous, s.done, None, s.ws, s.dev_status)
+    torch.cuda.synchronize()
+    assert s.dev_status.item() == 0
+    assert torch.equal(out_b.view(torch.int16), s.out.view(torch.int16))
+    for a_, b_ in zip(res_b, (s.accepted_len, s.accepted_nodes, s.next_token, s.ambiguous)):
+        assert torch.equal(a_, b_)
