@@ -976,39 +976,52 @@ __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
   const int2* spans = reinterpret_cast<const int2*>(a.ws + a.L.cspan);
   const int fc0 = *c.free_count;
   int carry = 0, pushed = 0;
-  for (int base = 0; base < R; base += 32) {
-    const int r = base + lane;
-    int nfree = 0;
-    int2 sp = make_int2(0, 0);
-    int32_t* table = nullptr;
-    if (r < R) {
-      sp = __ldcg(spans + r);
-      table = c.tables + (size_t)r * c.max_blocks;
-      for (int t = sp.x; t < sp.y; ++t) nfree += __ldcg(table + t) >= 0;
-    }
-    int x = nfree;
+  // 64 requests per round, lane l taking requests l and l + 32: both halves'
+  // spans, then both halves' table entries, are loaded together before the
+  // blocks go to the list in (request, table index) order
+  for (int base = 0; base < R; base += 64) {
+    int nfree[2] = {0, 0};
+    int2 sp[2];
+    const int32_t* table[2];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+    for (int h = 0; h < 2; ++h) {
+      const int r = base + 32 * h + lane;
+      sp[h] = r < R ? __ldcg(spans + r) : make_int2(0, 0);
+      table[h] = c.tables + (size_t)min(r, R - 1) * c.max_blocks;
     }
-    const int total = __shfl_sync(0xffffffffu, x, 31);
-    if (nfree) {
-      const long start = (long)fc0 + carry + x - nfree;
-      if (start + nfree <= c.capacity) {
-        int n = 0;
-        for (int t = sp.x; t < sp.y; ++t) {
-          const int blk = table[t];
-          if (blk < 0) continue;
-          c.free_list[start + n++] = blk;
-          table[t] = -1;
-        }
-        pushed = max(pushed, (int)(start + nfree - fc0));
-      } else {
-        flag(a.dev_status, SV_DEV_POOL_OVERFLOW);
+    const int len = max(sp[0].y - sp[0].x, sp[1].y - sp[1].x);
+    for (int t = 0; t < len; ++t) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (sp[h].x + t < sp[h].y) nfree[h] += __ldcg(table[h] + sp[h].x + t) >= 0;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int x = nfree[h];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
       }
+      const int total = __shfl_sync(0xffffffffu, x, 31);
+      if (nfree[h]) {
+        const long start = (long)fc0 + carry + x - nfree[h];
+        if (start + nfree[h] <= c.capacity) {
+          int32_t* tb = const_cast<int32_t*>(table[h]);
+          int n = 0;
+          for (int t = sp[h].x; t < sp[h].y; ++t) {
+            const int blk = tb[t];
+            if (blk < 0) continue;
+            c.free_list[start + n++] = blk;
+            tb[t] = -1;
+          }
+          pushed = max(pushed, (int)(start + nfree[h] - fc0));
+        } else {
+          flag(a.dev_status, SV_DEV_POOL_OVERFLOW);
+        }
+      }
+      carry += total;
     }
-    carry += total;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) pushed = max(pushed, __shfl_xor_sync(0xffffffffu, pushed, o));
