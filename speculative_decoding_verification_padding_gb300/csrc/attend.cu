@@ -1735,11 +1735,14 @@ sv_status launch(const Args& a_in, cudaStream_t stream) {
   // within a cluster -- when no window can reach the tcgen05 list (a cluster
   // launch behind the tcgen05 kernel waits for whole GPCs to drain: measured
   // 4-5 us slower on the draft tree), a split's block ids fit in shared
-  // memory and the device takes such clusters
+  // memory and every group's cluster can be resident at once (the device's
+  // count of active 16-CTA clusters, 14 on this GPU: a second wave of
+  // clusters would cost a whole split's time)
   const bool warp_plan = a.L.small && a.chunk.index < 0;
   a.cl = warp_plan && a.L.ucap_tc == 0 &&
                  (a.max_blocks + kClusterSplits - 1) / kClusterSplits <= kMaxPagesPerSplit &&
-                 cluster_fit.get(attend_kernel<D, true>, kClusterSplits, kThreads, smem) > 0
+                 cluster_fit.get(attend_kernel<D, true>, kClusterSplits, kThreads, smem) >=
+                     a.L.ucap_cl / kClusterSplits
              ? kClusterSplits
              : 0;
   if ((warp_plan ? sv::launch(plan_small_kernel, 1, 32, 0, stream, a)

@@ -462,19 +462,21 @@ inline cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 bloc
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// How many clusters of `cluster` CTAs of a kernel (`threads` per CTA,
-// `smem` bytes of dynamic shared memory) can be resident at once on the
-// current device, asked once per device; 0 if none fits or the query is
-// refused.  Sizes above the portable eight are opted into first.
+// How many clusters of `cluster` CTAs (1 .. 16) of a kernel (`threads` per
+// CTA, `smem` bytes of dynamic shared memory) can be resident at once on the
+// current device, asked once per device and cluster size; 0 if none fits or
+// the query is refused.  Sizes above the portable eight are opted into first.
 class ClusterFit {
  public:
   template <class K>
   int get(K kernel, int cluster, int threads, size_t smem) {
     int dev = -1;
+    if (cluster < 1 || cluster > 16) return 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
     std::lock_guard<std::mutex> lock(mu_);
-    if ((size_t)dev >= cap_.size()) cap_.resize((size_t)dev + 1, -1);
-    if (cap_[(size_t)dev] < 0) {
+    const size_t key = (size_t)dev * 17 + (size_t)cluster;
+    if (key >= cap_.size()) cap_.resize(key + 1, -1);
+    if (cap_[key] < 0) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)cluster);
       cfg.blockDim = dim3((unsigned)threads);
@@ -499,14 +501,14 @@ class ClusterFit {
         (void)cudaGetLastError();  // a refused query is an answer, not an error
         n = 0;
       }
-      cap_[(size_t)dev] = n;
+      cap_[key] = n;
     }
-    return cap_[(size_t)dev];
+    return cap_[key];
   }
 
  private:
   std::mutex mu_;
-  std::vector<int> cap_;  // per device: -1 not asked
+  std::vector<int> cap_;  // per (device, cluster size): -1 not asked
 };
 
 // A named NVTX range around the host part of a call (what it enqueues), so

@@ -70,24 +70,29 @@ ATTN_CASES = {
     "batch64_small": dict(name="batch64", n_req=64, ctx_scale=0.05, vocab=256),
     "batch256_small": dict(name="batch256", n_req=96, ctx_scale=0.02, vocab=256),
     "ragged_ctx": dict(name="batch64", n_req=9, ctx_scale=0.0007, vocab=64),  # contexts of a few tokens
-    # one-pass calls of at most four requests: every split group is one
-    # thread-block cluster of sixteen CTAs merging through shared memory --
-    # mixed contexts, contexts shorter than sixteen pages (empty splits), a
-    # long context (64-page splits)
-    "cluster_mixed": dict(name="batch64", n_req=4, ctx_scale=0.5, vocab=64),
-    "cluster_short": dict(name="batch64", n_req=3, ctx_scale=0.004, vocab=64),
+    # one-pass calls of at most four requests whose split groups all fit on
+    # the GPU as 16-CTA clusters at once (14 such clusters on a GB300): every
+    # split group is one thread-block cluster merging through shared memory --
+    # mixed contexts (2 KV heads: 12 groups), a context shorter than sixteen
+    # pages (empty splits), a long context (64-page splits)
+    "cluster_mixed": dict(name="batch64", n_req=4, ctx_scale=0.5, vocab=64,
+                          cfg=dict(n_q_heads=8, n_kv_heads=2)),
+    "cluster_short": dict(name="chain8b", ctx_scale=0.01, vocab=64),
     "cluster_long": dict(name="chain8b", ctx_scale=4.0, vocab=64),
+    # more groups than fit at once: the merge kernel instead
+    "small_many_groups": dict(name="batch64", n_req=3, ctx_scale=0.004, vocab=64),
 }
 
 
 def _make(case, **extra):
     kw = dict(ATTN_CASES[case]) if case in ATTN_CASES else {}
     name = kw.pop("name", case)
+    cfg = kw.pop("cfg", {})
     kw.setdefault("vocab", 1024 if name != "tiny" else None)
     if kw["vocab"] is None:
         kw.pop("vocab")
     kw.update(extra)
-    return wl.make_workload(wl.config(name), **kw)
+    return wl.make_workload(wl.config(name, **cfg), **kw)
 
 
 @pytest.mark.parametrize("case", list(ATTN_CASES))
