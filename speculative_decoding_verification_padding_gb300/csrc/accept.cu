@@ -906,23 +906,38 @@ __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
           const unsigned long long dr = __shfl_sync(0xffffffffu, drow, j);
           const unsigned long long sr2 = __shfl_sync(0xffffffffu, srow, j2 >= 0 ? j2 : j);
           const unsigned long long dr2 = __shfl_sync(0xffffffffu, drow, j2 >= 0 ? j2 : j);
-          // eight 16-byte loads of each slot in flight per lane, then the stores
+          // eight 16-byte loads of each slot in flight per lane, then the
+          // stores.  Paired moves (the decision kernel, which has the
+          // registers) go branch-free: a lane past the slot repeats its last
+          // entry, and without a second move sr2 / dr2 repeat sr / dr (the
+          // same value to the same place) -- guarded loads and stores went
+          // out one after another, 6 us more per draft-tree step, measured.
+          // (pairs is a constant at every call.)
           for (int x0 = 0; x0 < per_slot; x0 += 32 * 8) {
             int4 val[8], val2[8];
+            if (pairs) {
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const int x = x0 + 32 * t + lane;
-              if (x < per_slot) {
+              for (int t = 0; t < 8; ++t) {
+                const int x = min(x0 + 32 * t + lane, per_slot - 1);
                 val[t] = *slot_int4(sr, x);
-                if (j2 >= 0) val2[t] = *slot_int4(sr2, x);
+                val2[t] = *slot_int4(sr2, x);
               }
-            }
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const int x = x0 + 32 * t + lane;
-              if (x < per_slot) {
+              for (int t = 0; t < 8; ++t) {
+                const int x = min(x0 + 32 * t + lane, per_slot - 1);
                 *slot_int4(dr, x) = val[t];
-                if (j2 >= 0) *slot_int4(dr2, x) = val2[t];
+                *slot_int4(dr2, x) = val2[t];
+              }
+            } else {
+#pragma unroll
+              for (int t = 0; t < 8; ++t) {
+                const int x = x0 + 32 * t + lane;
+                if (x < per_slot) val[t] = *slot_int4(sr, x);
+              }
+#pragma unroll
+              for (int t = 0; t < 8; ++t) {
+                const int x = x0 + 32 * t + lane;
+                if (x < per_slot) *slot_int4(dr, x) = val[t];
               }
             }
           }
