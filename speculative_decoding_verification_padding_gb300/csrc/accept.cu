@@ -826,8 +826,11 @@ __device__ __forceinline__ int commit_check(const Args& a, int rows, int ctx, in
 // moves of 32 path positions at once (chains move nothing); the moves
 // themselves run in ascending k, every lane copying part of the slot.
 // pairs: two moves at a time (more registers; the decision kernel has them).
+// lean: a single move's loads and stores under guards (fewest registers: the
+// 1024-thread walk has 64 a thread).
 __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
-                                               const CommitHint* hint, bool pairs = false) {
+                                               const CommitHint* hint, bool pairs = false,
+                                               bool lean = false) {
   const int lane = threadIdx.x & 31;
   const CommitArgs& c = a.kv;
   // A call with one request needs no ticket: its warp releases at once (the
@@ -907,12 +910,11 @@ __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
           const unsigned long long sr2 = __shfl_sync(0xffffffffu, srow, j2 >= 0 ? j2 : j);
           const unsigned long long dr2 = __shfl_sync(0xffffffffu, drow, j2 >= 0 ? j2 : j);
           // eight 16-byte loads of each slot in flight per lane, then the
-          // stores.  Paired moves (the decision kernel, which has the
-          // registers) go branch-free: a lane past the slot repeats its last
-          // entry, and without a second move sr2 / dr2 repeat sr / dr (the
-          // same value to the same place) -- guarded loads and stores went
-          // out one after another, 6 us more per draft-tree step, measured.
-          // (pairs is a constant at every call.)
+          // stores, branch-free: a lane past the slot repeats its last entry,
+          // and without a second move sr2 / dr2 repeat sr / dr (the same
+          // value to the same place) -- guarded loads and stores went out one
+          // after another, 6 us more per draft-tree step, measured.  (pairs
+          // and lean are constants at every call.)
           for (int x0 = 0; x0 < per_slot; x0 += 32 * 8) {
             int4 val[8], val2[8];
             if (pairs) {
@@ -928,6 +930,11 @@ __device__ __forceinline__ void commit_request(const Args& a, int i, bool final,
                 *slot_int4(dr, x) = val[t];
                 *slot_int4(dr2, x) = val2[t];
               }
+            } else if (!lean) {
+#pragma unroll
+              for (int t = 0; t < 8; ++t) val[t] = *slot_int4(sr, min(x0 + 32 * t + lane, per_slot - 1));
+#pragma unroll
+              for (int t = 0; t < 8; ++t) *slot_int4(dr, min(x0 + 32 * t + lane, per_slot - 1)) = val[t];
             } else {
 #pragma unroll
               for (int t = 0; t < 8; ++t) {
@@ -1325,7 +1332,7 @@ __global__ void __launch_bounds__(NT) tree_kernel(Args a) {
   }
   if (a.commit && !a.tree_commit_race && warp == 0 && rank == 0) {
     __syncwarp();  // the path thread 0 wrote is visible to the warp
-    commit_request(a, i, true, nullptr);
+    commit_request(a, i, true, nullptr, false, CL == 1);
   }
   // no CTA leaves while its peers may still read its last pass's sum
   if constexpr (CL > 1) cluster_sync();
