@@ -22,7 +22,17 @@
 //                    merges the slice partials of the window rows, then the
 //                    chain scan (or the tree descent) with Philox uniforms;
 //                    writes the path and, for T > 0, a sampling job for the
-//                    emitted token.
+//                    emitted token (a draft tree at T > 0: a walk job).  The
+//                    fused commit moves the path's K/V and releases the rest.
+//   tree   (T > 0 and requests of more than two rows; one thread-block
+//                    cluster of sixteen 256-thread CTAs per tree when a
+//                    request may hold more than 16 rows, else one 1024-thread
+//                    CTA; every CTA without a walk job leaves at once)
+//                    the children of each node tried in index order against
+//                    the parent's residual, one vocabulary pass per rejected
+//                    sibling spread over the cluster; leaves a residual or
+//                    bonus job.  In one-pass fused calls its KV commit is
+//                    left to the race kernel's extra CTA.
 //   race   (warps, grid-stride over request x vocabulary slice)
 //                    the residual / bonus token, w = max(0, p - q) after a
 //                    rejection or p for the bonus token: an exponential race
@@ -33,7 +43,8 @@
 //                    inside its own best group; the warp that brings a
 //                    request's last slice (release-acquire ticket) reduces
 //                    the slice winners and writes the winner's entry.  A
-//                    chunked step runs it once, after its last chunk.
+//                    chunked step runs it once, after its last chunk.  One
+//                    extra CTA runs the KV commits tree walks left to it.
 
 #include <math.h>
 

@@ -43,8 +43,15 @@
 //                    output directly; otherwise it writes (m, l, O) partials
 //                    and the last CTA of the group (atomic ticket) merges all
 //                    splits -- or, in small batches, the merge launch does.
-//   merge (when the tcgen05 kernel ran or the batch is small) the units of
-//                    each split group merge its partials together.
+//                    One-pass calls of at most four requests with no window
+//                    on the tcgen05 list, whose split groups all fit on the
+//                    GPU at once as 16-CTA clusters, launch the same kernel as
+//                    thread-block clusters (attend_kernel<D, true>): each
+//                    group's 16 splits are one cluster, and its CTAs merge
+//                    their partials over distributed shared memory.
+//   merge (when the tcgen05 kernel ran or the batch is small and not
+//                    clustered) the units of each split group merge its
+//                    partials together.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
