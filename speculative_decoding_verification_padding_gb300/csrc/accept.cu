@@ -328,9 +328,7 @@ struct CommitHint {
   bool chain;
 };
 
-// premerged (T = 0): the window rows' partials are merged into sm already.
-__device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm, CommitHint& h,
-                              bool premerged = false) {
+__device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm, CommitHint& h) {
   const int lane = threadIdx.x & 31;
   Job* job = reinterpret_cast<Job*>(a.ws + a.L.jobs) + i;
   if (a.T > 0.f && lane == 0) {
@@ -410,8 +408,7 @@ __device__ int decide_request(const Args& a, int nch, int i, DecideSmem& sm, Com
   float* rs = a.row_stats;
 
   if (a.T == 0.f) {
-    if (!premerged)
-      merge_pairs(a, nch, cu + w.b, w.e - w.b, 0, sm.mp + w.b, sm.lp + w.b, nullptr, nullptr);
+    merge_pairs(a, nch, cu + w.b, w.e - w.b, 0, sm.mp + w.b, sm.lp + w.b, nullptr, nullptr);
     __syncwarp();
     for (int r = w.b + lane; r < w.e; r += 32) {
       const int idx = __float_as_int(sm.lp[r]);
@@ -1078,29 +1075,6 @@ __global__ void __launch_bounds__(kDecideWarps * 32, 1) decide_kernel(Args a) {
   const int count = n_slots(a, act);
   const int nch = stats_slices(a.L, count, a.T > 0.f ? 2 : 1, a.use_list != 0, a.bt.total_rows);
   const int wid = threadIdx.x >> 5;
-  if (!a.use_list && a.T == 0.f && a.bt.n_req == 1) {
-    // One request at T = 0: the CTA's warps merge a share of its rows'
-    // partials each (the argmax merge is exact in any order) before warp 0
-    // decides -- a 65-row tree's merge is one round of loads, not five.
-    if (blockIdx.x != 0) return;
-    const Window w = window_of(a.bt, 0);
-    if (w.ok && live(a, w, 0)) {
-      const int n = w.e - w.b, q = (n + kDecideWarps - 1) / kDecideWarps;
-      const int r0 = w.b + wid * q, cnt = min(n - wid * q, q);
-      if (cnt > 0)
-        merge_pairs(a, nch, w.cu + r0, cnt, 0, s_dec[0].mp + r0, s_dec[0].lp + r0, nullptr,
-                    nullptr);
-    }
-    __syncthreads();
-    if (wid != 0) return;
-    CommitHint hint;
-    const int outcome = decide_request(a, nch, 0, s_dec[0], hint, true);
-    if (a.commit && outcome != kToTree) {
-      __syncwarp();  // the path and state lane 0 wrote are visible to the warp
-      commit_request(a, 0, outcome == kFinal, outcome == kFinal ? &hint : nullptr, true);
-    }
-    return;
-  }
   for (int ai = blockIdx.x * kDecideWarps + wid; ai < count; ai += gridDim.x * kDecideWarps) {
     const int i = req_of(a, act, ai);
     CommitHint hint;
