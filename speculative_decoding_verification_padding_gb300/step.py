@@ -15,6 +15,8 @@ Nothing here computes any part of the step; it only moves memory and calls.
 
 from __future__ import annotations
 
+import copy
+
 import numpy as np
 import torch
 
@@ -174,6 +176,41 @@ class DeviceStep:
         else:
             raise ValueError(self.mode)
 
+    def inputs(self):
+        """The device tensors a step reads that a caller feeds from the host each
+        step, in a fixed order: q, target logits, tokens, parents, row offsets,
+        then the draft logits (T > 0) and the survival inputs (budget mode)."""
+        t = [self.q, self.target, self.batch.tokens, self.batch.parent, self.batch.cu_rows]
+        if self.draft is not None:
+            t.append(self.draft)
+        if self.mode == "budget":
+            t += [self.cond, self.gamma, self.sps]
+        return t
+
+    def outputs(self):
+        """The device tensors a step's caller reads back: the attention output,
+        accepted lengths, accepted nodes and next tokens."""
+        return [self.out, self.accepted_len, self.accepted_nodes, self.next_token]
+
+    def _twin(self):
+        """A step sharing this one's KV cache, pool, outputs and workspace, with
+        input tensors of its own (a second slot for double-buffered uploads)."""
+        t = copy.copy(self)
+        t._calls = {}
+        b = self.batch
+        t.batch = api.Batch(torch.empty_like(b.cu_rows), torch.empty_like(b.parent),
+                            torch.empty_like(b.tokens), b.max_rows)
+        t.q = torch.empty_like(self.q)
+        t.target = torch.empty_like(self.target)
+        t.draft = torch.empty_like(self.draft) if self.draft is not None else None
+        if self.mode == "budget":
+            t.cond = torch.empty_like(self.cond)
+            t.gamma = torch.empty_like(self.gamma)
+            t.sps = torch.empty_like(self.sps)
+            t.batch_sel = api.Batch(t.batch.cu_rows, t.batch.parent, t.batch.tokens,
+                                    b.max_rows, verify_len=self.verify_len)
+        return t
+
     def results(self):
         torch.cuda.synchronize()
         return {
@@ -184,3 +221,66 @@ class DeviceStep:
             "done": self.done.cpu().numpy(),
             "dev_status": int(self.dev_status.item()),
         }
+
+
+class HostPipeline:
+    """Steps of a ``DeviceStep`` fed from pinned host memory, inputs double-buffered.
+
+    Each step's inputs (``DeviceStep.inputs()``) are copied from pinned host
+    tensors into one of two device slots on a copy stream, and its results
+    (``DeviceStep.outputs()``) are copied back to pinned host memory on the
+    current stream right after its kernels.  The upload of step i + 1 goes into
+    the other slot while step i's kernels run, and waits only until step i - 1
+    (the slot's previous user) has finished reading it, so a step costs the
+    larger of its host-link time and its kernels' time rather than their sum.
+    Every step still moves all of its inputs and results across the link.
+    """
+
+    def __init__(self, step: DeviceStep):
+        self.slots = [step, step._twin()]
+        self.copy_stream = torch.cuda.Stream(device=step.device)
+        self.uploaded = [torch.cuda.Event(), torch.cuda.Event()]
+        self.released = [torch.cuda.Event(), torch.cuda.Event()]
+        self.ready = [torch.cuda.Event(), torch.cuda.Event()]
+        self.used = [False, False]
+        self.host_out = [[torch.empty_like(t, device="cpu").pin_memory() for t in step.outputs()]
+                         for _ in range(2)]
+        self.n = 0
+        self.begin()
+
+    def begin(self):
+        """Order the copy stream after everything enqueued so far on the current
+        stream (call once before a run of steps, e.g. at the start of a timed
+        region)."""
+        self.copy_stream.wait_stream(torch.cuda.current_stream())
+
+    def submit(self, host_inputs):
+        """Enqueue one step on ``host_inputs`` (pinned host tensors matching
+        ``DeviceStep.inputs()``) on the current stream.  Returns the slot's pinned host
+        outputs and the event after which they hold this step's results; they
+        stay valid until the step after next is submitted."""
+        k = self.n & 1
+        st, cs = self.slots[k], self.copy_stream
+        main = torch.cuda.current_stream()
+        dst = st.inputs()
+        if len(host_inputs) != len(dst):
+            raise ValueError(f"expected {len(dst)} host inputs, got {len(host_inputs)}")
+        for d, h in zip(dst, host_inputs):
+            if d.shape != h.shape or d.dtype != h.dtype or h.device.type != "cpu":
+                raise ValueError(f"host input {tuple(h.shape)} {h.dtype} on {h.device} does not "
+                                 f"match {tuple(d.shape)} {d.dtype}")
+        self.n += 1
+        if self.used[k]:
+            cs.wait_event(self.released[k])
+        self.used[k] = True
+        with torch.cuda.stream(cs):
+            for d, h in zip(dst, host_inputs):
+                d.copy_(h, non_blocking=True)
+            self.uploaded[k].record(cs)
+        main.wait_event(self.uploaded[k])
+        st.run()
+        self.released[k].record(main)
+        for h, d in zip(self.host_out[k], st.outputs()):
+            h.copy_(d, non_blocking=True)
+        self.ready[k].record(main)
+        return self.host_out[k], self.ready[k]

@@ -19,7 +19,7 @@ import oracle
 from speculative_decoding_verification_padding_gb300 import api, build
 from speculative_decoding_verification_padding_gb300 import sps as sps_mod
 from speculative_decoding_verification_padding_gb300 import workloads as wl
-from speculative_decoding_verification_padding_gb300.step import DeviceStep
+from speculative_decoding_verification_padding_gb300.step import DeviceStep, HostPipeline
 
 pytestmark = pytest.mark.gpu
 
@@ -1098,3 +1098,67 @@ def test_bound_calls_equal_the_plain_calls():
     assert torch.equal(out_b.view(torch.int16), s.out.view(torch.int16))
     for a_, b_ in zip(res_b, (s.accepted_len, s.accepted_nodes, s.next_token, s.ambiguous)):
         assert torch.equal(a_, b_)
+
+
+@pytest.mark.parametrize("case,kw", [
+    ("chain8b", dict(ctx_scale=0.25, vocab=2048)),                # one pass
+    ("batch64", dict(n_req=12, ctx_scale=0.05, vocab=512)),       # chunked
+    ("batch256", dict(n_req=24, ctx_scale=0.02, vocab=256)),      # budget selection
+])
+def test_host_pipeline_steps_equal_plain_steps(case, kw):
+    # Double-buffered uploads: steps alternating between two input sets, each
+    # step's results read only after the next step was submitted (so its upload
+    # overlapped this step's kernels), equal a plain step on the same set.
+    w = _make(case, **kw)
+    s = DeviceStep(w)
+    rng = np.random.default_rng(11)
+    base = [t.cpu().clone() for t in s.inputs()]
+    alt = [t.clone() for t in base]
+    alt[0] = (alt[0].float() * 0.5).to(torch.bfloat16)  # q
+    alt[1] = alt[1] + torch.from_numpy(rng.normal(0, 1.5, tuple(alt[1].shape)).astype(np.float32))
+    sets = [[t.pin_memory() for t in base], [t.pin_memory() for t in alt]]
+    refs = []
+    for ins in sets:
+        for d, h in zip(s.inputs(), ins):
+            d.copy_(h)
+        s.run()
+        torch.cuda.synchronize()
+        assert s.dev_status.item() == 0
+        refs.append([t.cpu().clone() for t in s.outputs()])
+    assert not torch.equal(refs[0][0].view(torch.int16), refs[1][0].view(torch.int16))
+    for d in s.inputs():
+        d.zero_()
+    pipe = HostPipeline(s)
+    pipe.begin()
+    n, got, pending = 7, {}, []
+
+    def take():
+        j, host, ev = pending.pop(0)
+        ev.synchronize()
+        got[j] = [t.clone() for t in host]
+
+    for i in range(n):
+        pending.append((i,) + pipe.submit(sets[i % 2]))
+        if len(pending) == 2:
+            take()
+    take()
+    torch.cuda.synchronize()
+    assert s.dev_status.item() == 0
+    assert sorted(got) == list(range(n))
+    for j in range(n):
+        ref = refs[j % 2]
+        assert torch.equal(got[j][0].view(torch.int16), ref[0].view(torch.int16)), j
+        for a_, b_ in zip(got[j][1:], ref[1:]):
+            assert torch.equal(a_, b_), j
+
+
+def test_host_pipeline_rejects_mismatched_inputs():
+    w = _make("chain8b", ctx_scale=0.05, vocab=256)
+    s = DeviceStep(w)
+    pipe = HostPipeline(s)
+    ins = [t.cpu() for t in s.inputs()]
+    with pytest.raises(ValueError):
+        pipe.submit(ins[:-1])
+    ins[1] = ins[1][:-1]
+    with pytest.raises(ValueError):
+        pipe.submit(ins)
