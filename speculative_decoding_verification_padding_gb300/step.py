@@ -10,6 +10,9 @@ outputs and workspaces with torch, and enqueues the library calls of a step:
   budget    sv_select_budget -> sv_tree_attend -> sv_accept_commit,
             with the selected verify_len feeding the batch
 
+``HostPipeline`` runs such steps on inputs that arrive in pinned host memory,
+double-buffered so that the next step's upload overlaps this step's kernels.
+
 Nothing here computes any part of the step; it only moves memory and calls.
 """
 
