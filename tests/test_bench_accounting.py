@@ -97,3 +97,14 @@ def test_attend_flops_follow_the_definition():
     win = bench.launch_windows(w, "onepass", np.zeros(1, np.int32))
     assert bench.attend_flops(w, win[0]) == want
     assert abs(want / 1e9 - 17.46) < 0.01
+
+
+def test_e2e_reports_the_faster_complete_timing_and_names_it():
+    t, mode = bench.e2e_choice(2.33e-3, 1.78e-3, False)
+    assert t == 1.78e-3 and mode.startswith("double-buffered") and "flush" not in mode
+    t, mode = bench.e2e_choice(0.105e-3, 0.205e-3, True)
+    assert t == 0.105e-3 and mode.startswith("serial") and "flushed between steps" in mode
+    t, mode = bench.e2e_choice(0.279e-3, 0.261e-3, True)
+    assert t == 0.261e-3 and "L2 flushes inside the timed region" in mode
+    t, mode = bench.e2e_choice(1e-3, 1e-3, False)  # a tie goes to the pipeline
+    assert mode.startswith("double-buffered")
